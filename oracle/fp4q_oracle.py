@@ -1,0 +1,603 @@
+"""Plain CPU oracle for block-scaled 4-bit quantisation and the block-scaled GEMM.
+
+TEST INFRASTRUCTURE ONLY. This module is the independent reference the CUDA
+library is checked against. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import it; the library itself never does, and
+this module imports nothing from the library.
+
+Everything here is written for a reader to check by eye against the method:
+numpy arrays, FP32 where the method computes in FP32 (every such step is a
+single IEEE round-to-nearest numpy operation, in the order stated), FP64 for the
+statistics and the GEMM. No blocking, fusion or reordering beyond what each
+definition states.
+
+Sources (page title, section):
+  [UFP4]  "Replanteamiento del Sesgo de Contracción en el Preentrenamiento de LLM
+          en FP4" -- Metodología §1 (shrinkage bias, (l_i - r_i)/2), §2 (uniform
+          E1M2/INT4 grid, RHT on all GEMMs, stochastic rounding), Eficiencia
+          (fused RHT + FP4 quantisation).
+  [NGPT]  "Le Architetture Normalizzate sono Nativamente a 4 Bit" -- Metodologia
+          (NVFP4 on Blackwell; SNR of Y = WX).
+  [TJ2]   "TetraJet-v2: Accurate NVFP4 Training for Large Language Models ..." --
+          Riepilogo Tecnico §2A (NVFP4: 16-element groups, 8-bit scale,
+          stochastic rounding with E[round(x)] = x, transposed weight copy), §2C
+          (RHT on the backward GEMMs).
+  [MXFP4] "Unveiling the Potential of Quantization with MXFP4: Strategies for
+          Quantization Error Reduction" -- Résumé technique §2 points 1-2
+          (MXFP4: 32-element blocks, E8M0 power-of-two scale; NVFP4: 16-element
+          blocks, E4M3 scale), §2A (alpha_max mapped to a power-of-two window).
+  [OCP-MX] OCP Microscaling Formats (MX) v1.0: shared scale exponent
+          floor(log2 amax) - emax_elem, emax_elem = 2 for E2M1.
+  [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1,
+          2, 3", SC'11: the Philox4x32-10 counter-based generator.
+
+Readings where the pages are silent (each is listed with its reason in the
+design notes of the repository):
+  R1 RHT = (1/4) * H16 * diag(sigma), H16 Sylvester (natural order), one sign
+     vector for the whole tensor and both copies, sigma_j = bit j of one Philox
+     word (key = seed, counter = (0, 0, 0, 0xFFFFFFFF)).
+  R2 UFP4 levels in integer units 0..7 (E1M2 value k/4 scaled by 4), Qmax = 7,
+     tensor scale amax / (7 * 448); codes and block scales are identical to the
+     E1M2-unit reading.
+  R3 NVFP4/UFP4 normalisation: r_b = 1 / (s_b * g) once per block, y = v * r_b.
+  R4 zero keeps its sign in the code (sign bit = sign bit of y).
+  R5 stochastic rounding: round up iff u < f, u = (w >> 8) * 2^-24, w one
+     Philox word keyed on (seed) with counter (i / 4, axis, 0) picking word
+     i mod 4; i = index of the element inside the copy being produced.
+  R6 shrinkage bias = mean over elements of (|q| - |y|) / Qmax.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# --------------------------------------------------------------------------- #
+# Element grids                                                               #
+# --------------------------------------------------------------------------- #
+
+#: E2M1 magnitudes indexed by the three low code bits (1 sign, 2 exponent,
+#: 1 mantissa bit) -- [UFP4] Declaración del Problema / Metodología §1.
+E2M1_LEVELS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+#: UFP4 (uniform E1M2 / INT4-like) magnitudes in integer units, reading R2 --
+#: [UFP4] Metodología §2 "Rejilla Uniforme": equal left/right bin widths.
+UFP4_LEVELS = np.arange(8, dtype=np.float64)
+
+FORMATS = ("nvfp4", "mxfp4", "ufp4")
+QMAX = {"nvfp4": 6.0, "mxfp4": 6.0, "ufp4": 7.0}
+BLOCK = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16}
+E4M3_MAX = 448.0
+
+F32 = np.float32
+
+
+def grid_levels(fmt: str) -> np.ndarray:
+    return UFP4_LEVELS if fmt == "ufp4" else E2M1_LEVELS
+
+
+# --------------------------------------------------------------------------- #
+# BF16 -> FP32 widening (exact)                                               #
+# --------------------------------------------------------------------------- #
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """BF16 is the top half of an FP32 word: shift the 16 bits up by 16."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def f32_to_bf16_bits_rne(x: np.ndarray) -> np.ndarray:
+    """Round FP32 to BF16 (nearest, ties to even); NaN stays a quiet NaN."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)).astype(np.uint16)
+    nan = np.isnan(np.asarray(x, dtype=np.float32))
+    return np.where(nan, np.uint16(0x7FC0), r)
+
+
+# --------------------------------------------------------------------------- #
+# Scale formats                                                               #
+# --------------------------------------------------------------------------- #
+
+def e4m3_decode(code) -> np.ndarray:
+    """Value of an FP8 E4M3 (bias 7, no infinities) code 0..126, as FP64.
+
+    Exponent field 0 is subnormal (m * 2^-9); otherwise (1 + m/8) * 2^(e-7).
+    Largest finite value: e = 15, m = 6 -> 448 ([MXFP4] Résumé technique §2, point 2).
+    """
+    c = np.asarray(code, dtype=np.int64) & 0x7F
+    e = c >> 3
+    m = c & 7
+    sub = m * 2.0 ** -9
+    nrm = (1.0 + m / 8.0) * np.exp2((e - 7).astype(np.float64))
+    return np.where(e == 0, sub, nrm)
+
+
+#: all 127 finite non-negative E4M3 values, ascending with the code.
+E4M3_VALUES = e4m3_decode(np.arange(127))
+
+
+def _nearest_even(a: np.ndarray, table: np.ndarray) -> np.ndarray:
+    """Index into an ascending ``table`` nearest to ``a`` (inside the table's
+    range), ties to the even index. ``a`` and ``table`` are FP64 and every
+    difference taken here is exact."""
+    lo = np.searchsorted(table, a, side="right") - 1
+    lo = np.clip(lo, 0, len(table) - 1)
+    hi = np.minimum(lo + 1, len(table) - 1)
+    d_lo = a - table[lo]
+    d_hi = table[hi] - a
+    take_hi = (hi != lo) & ((d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0)))
+    return np.where(take_hi, hi, lo)
+
+
+def e4m3_encode_rne_sat(t) -> np.ndarray:
+    """FP32 t >= 0 -> E4M3 code: nearest value, ties to even code, values above
+    the largest finite value saturate to 448 (no NaN is produced)."""
+    a = np.minimum(np.asarray(t, dtype=np.float64), E4M3_MAX)
+    return _nearest_even(a, E4M3_VALUES).astype(np.uint8)
+
+
+def e8m0_exponent(amax) -> np.ndarray:
+    """MXFP4 shared exponent of a block: floor(log2 amax) - 2 ([OCP-MX];
+    [MXFP4] §2 point 2: power-of-two scale), clamped to the E8M0 range
+    [-127, 127]; amax = 0 gives -127. frexp gives amax = m * 2^ex with m in
+    [0.5, 1), so floor(log2 amax) = ex - 1 (subnormals included)."""
+    a = np.asarray(amax, dtype=np.float64)
+    _, ex = np.frexp(a)
+    e = ex.astype(np.int64) - 1 - 2
+    e = np.where(a == 0.0, -127, e)
+    return np.clip(e, -127, 127)
+
+
+# --------------------------------------------------------------------------- #
+# Philox4x32-10 [PHILOX]                                                      #
+# --------------------------------------------------------------------------- #
+
+PHILOX_M0 = 0xD2511F53
+PHILOX_M1 = 0xCD9E8D57
+PHILOX_W0 = 0x9E3779B9
+PHILOX_W1 = 0xBB67AE85
+_MASK32 = np.uint64(0xFFFFFFFF)
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Ten Philox rounds on a 4x32-bit counter under a 2x32-bit key.
+
+    One round: (hi0, lo0) = M0 * c0 and (hi1, lo1) = M1 * c2 as 64-bit
+    products; the new counter is (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0).
+    Between rounds the key is bumped by the Weyl constants (W0, W1) mod 2^32.
+    Inputs broadcast; returns four uint64 arrays holding 32-bit words.
+    """
+    c0, c1, c2, c3, k0, k1 = np.broadcast_arrays(
+        *[np.asarray(v, dtype=np.uint64) & _MASK32 for v in (c0, c1, c2, c3, k0, k1)])
+    c0, c1, c2, c3, k0, k1 = (v.copy() for v in (c0, c1, c2, c3, k0, k1))
+    m0, m1 = np.uint64(PHILOX_M0), np.uint64(PHILOX_M1)
+    for rnd in range(10):
+        if rnd > 0:
+            k0 = (k0 + np.uint64(PHILOX_W0)) & _MASK32
+            k1 = (k1 + np.uint64(PHILOX_W1)) & _MASK32
+        p0 = m0 * c0
+        p1 = m1 * c2
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _MASK32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _MASK32
+        c0, c1, c2, c3 = hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0
+    return c0, c1, c2, c3
+
+
+def _seed_words(seed: int):
+    s = int(seed) & 0xFFFFFFFFFFFFFFFF
+    return s & 0xFFFFFFFF, s >> 32
+
+
+def rht_signs(seed: int) -> np.ndarray:
+    """Reading R1: sigma_j = -1 iff bit j of word 0 of
+    Philox(key = seed, counter = (0, 0, 0, 0xFFFFFFFF)) is set, j = 0..15."""
+    k0, k1 = _seed_words(seed)
+    w0 = int(philox4x32_10(0, 0, 0, 0xFFFFFFFF, k0, k1)[0])
+    bits = (w0 >> np.arange(16)) & 1
+    return np.where(bits == 1, -1.0, 1.0)
+
+
+def sr_uniforms(index, seed: int, axis: int) -> np.ndarray:
+    """Reading R5: the uniform u in [0, 1) used to round element ``index`` of
+    copy ``axis`` (0 row-wise, 1 column-wise): u = (w >> 8) * 2^-24 with w word
+    (index mod 4) of Philox(key = seed, counter = (index/4 low 32 bits,
+    index/4 high 32 bits, axis, 0))."""
+    idx = np.asarray(index, dtype=np.int64)
+    q = (idx // 4).astype(np.uint64)
+    k0, k1 = _seed_words(seed)
+    words = philox4x32_10(q & _MASK32, q >> np.uint64(32), axis, 0, k0, k1)
+    lane = idx % 4
+    w = np.choose(lane, words)
+    return (w >> np.uint64(8)).astype(np.float64) * 2.0 ** -24
+
+
+# --------------------------------------------------------------------------- #
+# Random Hadamard Transform (16-point)                                        #
+# --------------------------------------------------------------------------- #
+
+def hadamard16() -> np.ndarray:
+    """Sylvester Hadamard matrix, natural order: H[i, j] = (-1)^popcount(i & j)."""
+    i = np.arange(16)[:, None]
+    j = np.arange(16)[None, :]
+    pc = np.vectorize(lambda v: bin(int(v)).count("1"))(i & j)
+    return np.where(pc % 2 == 0, 1.0, -1.0)
+
+
+_H16 = hadamard16()
+
+
+def rht_definition(blocks: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """v = (1/4) * H16 * diag(sigma) * x for every 16-vector on the last axis,
+    as a dense FP64 product rounded once to FP32 ([UFP4] Metodología §1 and
+    Eficiencia; [TJ2] §2C). Input FP32 [..., 16]."""
+    x = np.asarray(blocks, dtype=np.float64) * signs
+    v = 0.25 * np.einsum("ij,...j->...i", _H16, x)
+    return v.astype(np.float32)
+
+
+def rht_butterfly(blocks: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """The same transform as the fast Walsh-Hadamard butterfly in FP32:
+    w = sigma * x (exact), then stages h = 1, 2, 4, 8 replace (w_i, w_{i+h})
+    for every i with bit h clear by (w_i + w_{i+h}, w_i - w_{i+h}), each a
+    single FP32 rounding, and finally v = 0.25 * w (FP32)."""
+    w = (np.asarray(blocks, dtype=np.float32) * signs.astype(np.float32)).astype(np.float32)
+    w = w.copy()
+    for h in (1, 2, 4, 8):
+        idx = np.array([i for i in range(16) if i & h == 0])
+        a = w[..., idx].copy()
+        b = w[..., idx + h].copy()
+        w[..., idx] = a + b
+        w[..., idx + h] = a - b
+    return (w * F32(0.25)).astype(np.float32)
+
+
+def rht_inverse_butterfly(blocks: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    """Transpose of the RHT, R^T = (1/4) diag(sigma) H16: the same FP32
+    butterfly on v, then 0.25 *, then the sign flip."""
+    w = np.asarray(blocks, dtype=np.float32).copy()
+    for h in (1, 2, 4, 8):
+        idx = np.array([i for i in range(16) if i & h == 0])
+        a = w[..., idx].copy()
+        b = w[..., idx + h].copy()
+        w[..., idx] = a + b
+        w[..., idx + h] = a - b
+    return ((w * F32(0.25)) * signs.astype(np.float32)).astype(np.float32)
+
+
+def rht_inverse_definition(blocks: np.ndarray, signs: np.ndarray) -> np.ndarray:
+    x = np.einsum("ij,...j->...i", _H16, np.asarray(blocks, dtype=np.float64))
+    return (0.25 * x * signs).astype(np.float32)
+
+
+# --------------------------------------------------------------------------- #
+# Rounding onto the element grid                                              #
+# --------------------------------------------------------------------------- #
+
+def round_rtne(y: np.ndarray, fmt: str) -> np.ndarray:
+    """RTNE onto the grid ([UFP4] Metodología §1): |y| is clamped to the
+    largest level, then rounded to the nearest level, ties to the level whose
+    code is even. Returns 4-bit codes: sign bit (bit 3) from y's sign bit
+    (reading R4), level index in bits 0-2."""
+    levels = grid_levels(fmt)
+    a = np.minimum(np.abs(np.asarray(y, dtype=np.float64)), levels[-1])
+    k = _nearest_even(a, levels)
+    sign = np.signbit(y).astype(np.uint8)
+    return (sign << 3) | k.astype(np.uint8)
+
+
+def round_sr(y: np.ndarray, fmt: str, u: np.ndarray) -> np.ndarray:
+    """Stochastic rounding ([UFP4] §2; [TJ2] §2A, E[round(x)] = x): with
+    lo <= |y| < hi adjacent levels and f = (|y| - lo) / (hi - lo), round up iff
+    u < f; |y| at or above the top level gives the top level. Sign kept."""
+    levels = grid_levels(fmt)
+    top = levels[-1]
+    a = np.abs(np.asarray(y, dtype=np.float64))
+    at_top = a >= top
+    lo = np.searchsorted(levels, np.minimum(a, top), side="right") - 1
+    hi = np.minimum(lo + 1, 7)
+    gap = np.where(hi > lo, levels[hi] - levels[lo], 1.0)
+    f = np.where(at_top, 0.0, (a - levels[lo]) / gap)
+    up = (~at_top) & (np.asarray(u, dtype=np.float64) < f)
+    k = np.where(at_top, 7, lo + up.astype(np.int64))
+    sign = np.signbit(y).astype(np.uint8)
+    return (sign << 3) | k.astype(np.uint8)
+
+
+def code_value(codes: np.ndarray, fmt: str) -> np.ndarray:
+    """Grid value (FP64) of 4-bit codes."""
+    c = np.asarray(codes, dtype=np.int64)
+    mag = grid_levels(fmt)[c & 7]
+    return np.where(c & 8, -mag, mag)
+
+
+def pack_nibbles(codes: np.ndarray) -> np.ndarray:
+    """Two codes per byte along the last axis: element 2j in bits 0-3,
+    element 2j+1 in bits 4-7."""
+    c = np.asarray(codes, dtype=np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def unpack_nibbles(packed: np.ndarray) -> np.ndarray:
+    p = np.asarray(packed, dtype=np.uint8)
+    out = np.empty(p.shape[:-1] + (p.shape[-1] * 2,), dtype=np.uint8)
+    out[..., 0::2] = p & 0xF
+    out[..., 1::2] = p >> 4
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# Quantisation of one copy                                                    #
+# --------------------------------------------------------------------------- #
+
+def _as_f32_matrix(x) -> np.ndarray:
+    a = np.asarray(x)
+    if a.dtype == np.uint16:
+        return bf16_bits_to_f32(a)
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def transform_copy(m32: np.ndarray, fmt: str, rht: bool, seed: int,
+                   rht_mode: str = "butterfly") -> np.ndarray:
+    """Values v of a copy (rows x cols, blocks along cols), after the optional
+    16-point RHT. MXFP4 applies two 16-point transforms per 32-block."""
+    if not rht:
+        return m32
+    n, k = m32.shape
+    signs = rht_signs(seed)
+    fn = rht_butterfly if rht_mode == "butterfly" else rht_definition
+    return fn(m32.reshape(n, k // 16, 16), signs).reshape(n, k)
+
+
+def tensor_amax(v: np.ndarray) -> np.float32:
+    """A = max |v| over the whole copy (FP32)."""
+    if v.size == 0:
+        return F32(0.0)
+    return F32(np.max(np.abs(v)))
+
+
+def tensor_scale(amax: np.float32, fmt: str) -> np.float32:
+    """NVFP4 per-tensor FP32 scale g = A / (Qmax * 448), one FP32 division
+    by the exact constant 2688 (NVFP4) or 3136 (UFP4, reading R2); MXFP4 has
+    no tensor scale (1.0)."""
+    if fmt == "mxfp4":
+        return F32(1.0)
+    return F32(F32(amax) / F32(QMAX[fmt] * E4M3_MAX))
+
+
+def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = "rtne",
+                  seed: int = 0, axis: int = 0, rht_mode: str = "butterfly",
+                  chunk_rows: int = 256, keep_y: bool = False) -> dict:
+    """Quantise one copy: a rows x cols FP32 matrix whose blocks run along the
+    columns. For the row-wise copy this is X itself; for the column-wise copy it
+    is X^T ([TJ2] §2A: the transposed operand of the weight-gradient GEMM).
+
+    Steps, per block b of ``block`` consecutive values:
+      v   = RHT(x) or x
+      A   = max |v| over the copy;  g = A / (Qmax * 448)           (FP32)
+      a_b = max |v| over the block
+      NVFP4/UFP4: d = Qmax * g (FP32, once); t = a_b / d (FP32);
+                  s_b = E4M3_rne_sat(t); p = s_b * g (FP32);
+                  r_b = 1 / p (FP32; 0 if p = 0, FLT_MAX if it overflows);
+                  y = v * r_b (FP32)                                  (reading R3)
+                  if g = 0 every scale and code is 0.
+      MXFP4:      e_b = floor(log2 a_b) - 2 in [-127, 127]; scale code e_b + 127;
+                  y = v * 2^-e_b (FP32)
+      q   = RTNE(y) or SR(y, u_i)
+    Statistics (FP64): bias = sum(|q| - |y|) / (Qmax * N)   (reading R6)
+                       snr_db = 10 log10(sum v^2 / sum (v - v_hat)^2), v_hat =
+                       q * s_b * g (or q * 2^e_b) exactly in FP64.
+    """
+    if fmt not in FORMATS:
+        raise ValueError(fmt)
+    b = BLOCK[fmt]
+    n, k = m32.shape
+    if k % b:
+        raise ValueError("cols must be a multiple of the block size")
+    qmax = QMAX[fmt]
+    levels_top = grid_levels(fmt)[-1]
+    assert levels_top == qmax
+
+    # Pass 1: the tensor amax over every transformed value of the copy.
+    amax = F32(0.0)
+    for r0 in range(0, n, chunk_rows):
+        v = transform_copy(m32[r0:r0 + chunk_rows], fmt, rht, seed, rht_mode)
+        if v.size:
+            amax = max(amax, tensor_amax(v))
+    g = tensor_scale(amax, fmt)
+    d = F32(F32(qmax) * g)
+
+    codes = np.zeros((n, k), dtype=np.uint8)
+    scales = np.zeros((n, k // b), dtype=np.uint8)
+    ys = np.zeros((n, k), dtype=np.float32) if keep_y else None
+    sum_bias = 0.0
+    sum_abs_bias = 0.0
+    sum_sig2 = 0.0
+    sum_err2 = 0.0
+    for r0 in range(0, n, chunk_rows):
+        v = transform_copy(m32[r0:r0 + chunk_rows], fmt, rht, seed, rht_mode)
+        rows = v.shape[0]
+        vb = v.reshape(rows, k // b, b)
+        a_b = np.max(np.abs(vb), axis=2).astype(np.float32)
+        if fmt == "mxfp4":
+            e_b = e8m0_exponent(a_b)
+            scales[r0:r0 + rows] = (e_b + 127).astype(np.uint8)
+            mult = np.exp2(-e_b.astype(np.float64)).astype(np.float32)
+            y = (vb * mult[..., None]).astype(np.float32)
+            step64 = np.exp2(e_b.astype(np.float64))
+        else:
+            if g == 0.0:
+                s_code = np.zeros_like(a_b, dtype=np.uint8)
+            else:
+                t = (a_b / d).astype(np.float32)
+                s_code = e4m3_encode_rne_sat(t)
+            scales[r0:r0 + rows] = s_code
+            s_val = e4m3_decode(s_code).astype(np.float32)
+            p = (s_val * g).astype(np.float32)
+            with np.errstate(divide="ignore", over="ignore"):
+                r_b = np.where(p == 0.0, F32(0.0), (F32(1.0) / p)).astype(np.float32)
+            r_b = np.where(np.isinf(r_b), np.finfo(np.float32).max, r_b).astype(np.float32)
+            y = (vb * r_b[..., None]).astype(np.float32)
+            step64 = s_val.astype(np.float64) * np.float64(g)
+        y = y.reshape(rows, k)
+        if rounding == "rtne":
+            c = round_rtne(y, fmt)
+        elif rounding == "sr":
+            idx = (np.arange(r0, r0 + rows, dtype=np.int64)[:, None] * k
+                   + np.arange(k, dtype=np.int64)[None, :])
+            c = round_sr(y, fmt, sr_uniforms(idx, seed, axis))
+        else:
+            raise ValueError(rounding)
+        codes[r0:r0 + rows] = c
+        if keep_y:
+            ys[r0:r0 + rows] = y
+        qv = code_value(c, fmt)
+        term = np.abs(qv) - np.abs(y.astype(np.float64))
+        sum_bias += float(np.sum(term))
+        sum_abs_bias += float(np.sum(np.abs(term)))
+        vhat = (qv.reshape(rows, k // b, b) * step64[..., None]).reshape(rows, k)
+        v64 = v.astype(np.float64)
+        sum_sig2 += float(np.sum(v64 * v64))
+        sum_err2 += float(np.sum((v64 - vhat) ** 2))
+
+    nel = n * k
+    out = {
+        "fmt": fmt, "block": b, "rows": n, "cols": k,
+        "codes": pack_nibbles(codes),
+        "scales": scales,
+        "tensor_scale": F32(g),
+        "amax": F32(amax),
+        "stats": stats_from_sums(sum_bias, sum_abs_bias, sum_sig2, sum_err2, nel, qmax),
+    }
+    if keep_y:
+        out["y"] = ys
+    return out
+
+
+def stats_from_sums(sum_bias, sum_abs_bias, sum_sig2, sum_err2, nel, qmax) -> dict:
+    """Shrinkage bias (mean signed error in magnitude, normalised by Qmax;
+    [UFP4] Metodología §1) and quantisation SNR in dB ([UFP4] Resultados;
+    [NGPT] Risultati §1). SNR is +inf when the error energy is 0."""
+    bias = sum_bias / (qmax * nel) if nel else 0.0
+    if sum_err2 == 0.0:
+        snr = float("inf")
+    elif sum_sig2 == 0.0:
+        snr = float("-inf")
+    else:
+        snr = 10.0 * np.log10(sum_sig2 / sum_err2)
+    return {"shrink_bias": bias, "snr_db": float(snr), "sum_sig2": sum_sig2,
+            "sum_err2": sum_err2, "sum_abs_bias": sum_abs_bias, "n": nel,
+            "mean_abs_bias": (sum_abs_bias / (qmax * nel)) if nel else 0.0}
+
+
+def quantize(x, fmt: str, rht: bool = False, rounding: str = "rtne", seed: int = 0,
+             axis: str = "row", rht_mode: str = "butterfly", keep_y: bool = False) -> dict:
+    """Quantise a rows x cols tensor (BF16 bits as uint16, or FP32).
+
+    axis: "row" (blocks along each row), "col" (blocks along each column,
+    emitted as the transposed copy [cols][rows/2]) or "both".
+    Returns {"row": copy, "col": copy} with the requested copies, plus
+    "nonfinite": True when the input held a NaN or an infinity.
+    """
+    m = _as_f32_matrix(x)
+    out = {"nonfinite": bool(not np.all(np.isfinite(m)))}
+    if axis in ("row", "both"):
+        out["row"] = quantize_copy(m, fmt, rht, rounding, seed, 0, rht_mode, keep_y=keep_y)
+    if axis in ("col", "both"):
+        out["col"] = quantize_copy(np.ascontiguousarray(m.T), fmt, rht, rounding, seed, 1,
+                                   rht_mode, keep_y=keep_y)
+    return out
+
+
+# --------------------------------------------------------------------------- #
+# Dequantisation                                                              #
+# --------------------------------------------------------------------------- #
+
+def dequantize(codes_packed: np.ndarray, scales: np.ndarray, g, fmt: str,
+               inverse_rht: bool = False, seed: int = 0) -> np.ndarray:
+    """v_hat = (q * s_b) * g in FP32, two round-to-nearest products in that
+    order (MXFP4: q * 2^e_b); optionally followed by R^T (FP32 butterfly)."""
+    b = BLOCK[fmt]
+    c = unpack_nibbles(codes_packed)
+    n, k = c.shape
+    q = code_value(c, fmt).astype(np.float32).reshape(n, k // b, b)
+    if fmt == "mxfp4":
+        e_b = np.asarray(scales, dtype=np.int64) - 127
+        mult = np.exp2(e_b.astype(np.float64)).astype(np.float32)
+        v = (q * mult[..., None]).astype(np.float32)
+    else:
+        s_val = e4m3_decode(scales).astype(np.float32)
+        v = ((q * s_val[..., None]).astype(np.float32) * F32(g)).astype(np.float32)
+    v = v.reshape(n, k)
+    if inverse_rht:
+        v = rht_inverse_butterfly(v.reshape(n, k // 16, 16), rht_signs(seed)).reshape(n, k)
+    return v
+
+
+def dequantize_f64(codes_packed: np.ndarray, scales: np.ndarray, g, fmt: str,
+                   rows=None) -> np.ndarray:
+    """Exact FP64 value of each element: q * s_b * g (MXFP4: q * 2^e_b)."""
+    b = BLOCK[fmt]
+    cp = codes_packed if rows is None else codes_packed[rows]
+    sc = scales if rows is None else scales[rows]
+    c = unpack_nibbles(cp)
+    n, k = c.shape
+    q = code_value(c, fmt).reshape(n, k // b, b)
+    if fmt == "mxfp4":
+        step = np.exp2((np.asarray(sc, dtype=np.int64) - 127).astype(np.float64))
+    else:
+        step = e4m3_decode(sc) * np.float64(g)
+    return (q * step[..., None]).reshape(n, k)
+
+
+# --------------------------------------------------------------------------- #
+# Block-scaled GEMM                                                           #
+# --------------------------------------------------------------------------- #
+
+def gemm(a_copy: dict, b_copy: dict, rows=None, cols=None) -> np.ndarray:
+    """Y = dequant(A) @ dequant(B)^T in FP64 ([UFP4] Resultados, single-GEMM
+    output; [NGPT] Metodologia, Y = WX), optionally for a subset of output
+    rows (of A) and columns (rows of B)."""
+    fa = a_copy["fmt"]
+    fb = b_copy["fmt"]
+    a = dequantize_f64(a_copy["codes"], a_copy["scales"], a_copy["tensor_scale"], fa, rows)
+    b = dequantize_f64(b_copy["codes"], b_copy["scales"], b_copy["tensor_scale"], fb, cols)
+    return a @ b.T
+
+
+def snr_db(ref: np.ndarray, approx: np.ndarray) -> float:
+    ref = np.asarray(ref, dtype=np.float64)
+    err = ref - np.asarray(approx, dtype=np.float64)
+    e2 = float(np.sum(err * err))
+    return float("inf") if e2 == 0.0 else 10.0 * np.log10(float(np.sum(ref * ref)) / e2)
+
+
+# --------------------------------------------------------------------------- #
+# Tensor-core scale-factor layout                                             #
+# --------------------------------------------------------------------------- #
+
+def mma_scale_offset(r, kb, nkb: int) -> np.ndarray:
+    """Byte offset of scale (row r, block kb) in the 128x4 tiled layout the
+    block-scaled tensor-core MMA reads: tiles of 128 rows x 4 blocks are 512
+    contiguous bytes, tiles ordered with the block index fastest; inside a
+    tile, byte (r % 32) * 16 + ((r % 128) // 32) * 4 + kb % 4. ``nkb`` is the
+    number of blocks per row, padded to a multiple of 4."""
+    r = np.asarray(r, dtype=np.int64)
+    kb = np.asarray(kb, dtype=np.int64)
+    tile = (r // 128) * (nkb // 4) + kb // 4
+    return tile * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + kb % 4
+
+
+def scales_to_mma_layout(scales: np.ndarray) -> np.ndarray:
+    """Linear [rows][nkb] scales -> the tiled layout (rows padded to 128,
+    blocks to 4, padding bytes 0), as a flat uint8 array."""
+    s = np.asarray(scales, dtype=np.uint8)
+    n, nkb = s.shape
+    n_p = -(-n // 128) * 128
+    nkb_p = -(-nkb // 4) * 4
+    out = np.zeros(n_p * nkb_p, dtype=np.uint8)
+    r, kb = np.meshgrid(np.arange(n), np.arange(nkb), indexing="ij")
+    out[mma_scale_offset(r, kb, nkb_p)] = s
+    return out
+
+
+def mma_layout_bytes(rows: int, nkb: int) -> int:
+    return (-(-rows // 128) * 128) * (-(-nkb // 4) * 4)

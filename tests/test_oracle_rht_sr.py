@@ -1,0 +1,155 @@
+"""Pins of the oracle's RHT, Philox and stochastic rounding (no GPU)."""
+import os
+
+import numpy as np
+import pytest
+
+from oracle import fp4q_oracle as o
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---- RHT -------------------------------------------------------------------
+
+def test_hadamard_orthogonal():
+    H = o.hadamard16()
+    assert np.array_equal(H @ H.T, 16.0 * np.eye(16))
+    assert np.array_equal(H, H.T)
+    # Sylvester recursion H_{2n} = [[H_n, H_n], [H_n, -H_n]] from H_1 = [1]
+    S = np.array([[1.0]])
+    for _ in range(4):
+        S = np.block([[S, S], [S, -S]])
+    assert np.array_equal(S, H)
+
+
+def test_rht_unit_vectors_and_norm():
+    s = o.rht_signs(1234)
+    H = o.hadamard16()
+    eye = np.eye(16, dtype=np.float32)
+    v = o.rht_definition(eye, s)           # row j = R e_j
+    assert np.array_equal(v.T.astype(np.float64), 0.25 * H * s[None, :])
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((4096, 16)).astype(np.float32)
+    vx = o.rht_definition(x, s).astype(np.float64)
+    nx = np.linalg.norm(x.astype(np.float64), axis=1)
+    assert np.allclose(np.linalg.norm(vx, axis=1), nx, rtol=1e-6)
+    back = o.rht_inverse_definition(vx.astype(np.float32), s)
+    assert np.allclose(back, x, rtol=0, atol=4e-6 * np.max(np.abs(x)))
+
+
+def test_rht_butterfly_vs_definition():
+    s = o.rht_signs(99)
+    rng = np.random.default_rng(1)
+    # narrow exponent range (BF16 inputs, spread <= 12 binades): butterfly is exact
+    x = o.bf16_bits_to_f32(o.f32_to_bf16_bits_rne(rng.uniform(0.5, 2.0, (20000, 16)).astype(np.float32)))
+    x = x * np.where(rng.random((20000, 16)) < 0.5, -1, 1).astype(np.float32)
+    assert np.array_equal(o.rht_butterfly(x, s), o.rht_definition(x, s))
+    # heavy tails: within 2 FP32 ulp of the definition (a rounded dense product)
+    y = (rng.standard_t(3, (20000, 16)) * np.exp(rng.standard_normal((1, 16)) * 3)).astype(np.float32)
+    y = o.bf16_bits_to_f32(o.f32_to_bf16_bits_rne(y))
+    b = o.rht_butterfly(y, s).astype(np.float64)
+    d = o.rht_definition(y, s).astype(np.float64)
+    ulp = np.spacing(np.abs(d).astype(np.float32)).astype(np.float64)
+    # 2 ulp of the block's largest output bounds the absolute error of each output
+    blockulp = np.max(ulp, axis=1, keepdims=True)
+    assert np.all(np.abs(b - d) <= 2 * blockulp)
+    inv = o.rht_inverse_butterfly(o.rht_butterfly(x, s), s)
+    assert np.allclose(inv, x, rtol=0, atol=1e-6 * 4)
+
+
+def test_rht_signs_are_seeded():
+    a, b = o.rht_signs(1234), o.rht_signs(1235)
+    assert set(np.unique(a)) <= {-1.0, 1.0}
+    assert not np.array_equal(a, b)
+    assert np.array_equal(a, o.rht_signs(1234))
+
+
+def test_rht_cancels_in_a_dot_product():
+    s = o.rht_signs(7)
+    rng = np.random.default_rng(2)
+    a = rng.standard_normal((64, 16))
+    b = rng.standard_normal((64, 16))
+    H = o.hadamard16()
+    R = 0.25 * H * s[None, :]
+    assert np.allclose((a @ R.T) @ (b @ R.T).T, a @ b.T, atol=1e-12)
+
+
+# ---- Philox ----------------------------------------------------------------
+
+def test_philox_known_answers():
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
+    assert len(rows) == 3
+    for r in rows:
+        vals = [int(v, 16) for v in r]
+        out = o.philox4x32_10(*vals[:6])
+        assert [int(v) for v in out] == vals[6:]
+
+
+def test_sr_uniforms_layout():
+    u = o.sr_uniforms(np.arange(8), 1234, 0)
+    k0, k1 = 1234, 0
+    w = o.philox4x32_10(0, 0, 0, 0, k0, k1)
+    w1 = o.philox4x32_10(1, 0, 0, 0, k0, k1)
+    exp = [(int(v) >> 8) * 2.0 ** -24 for v in list(w) + list(w1)]
+    assert np.array_equal(u, np.array(exp))
+    assert np.all((u >= 0) & (u < 1))
+    # axis word changes the stream
+    assert not np.array_equal(u, o.sr_uniforms(np.arange(8), 1234, 1))
+    # uniformity: chi-square over 64 bins for 2^18 draws
+    uu = o.sr_uniforms(np.arange(1 << 18), 42, 0)
+    h, _ = np.histogram(uu, bins=64, range=(0, 1))
+    e = (1 << 18) / 64
+    chi2 = np.sum((h - e) ** 2 / e)
+    assert chi2 < 120  # 63 dof, p ~ 1e-5
+
+
+# ---- stochastic rounding --------------------------------------------------
+
+@pytest.mark.parametrize("fmt,y", [("nvfp4", 0.3), ("nvfp4", 1.2),
+                                   ("nvfp4", 2.7), ("nvfp4", 5.1), ("ufp4", 3.37),
+                                   ("nvfp4", 1e-6), ("ufp4", 6.999)])
+def test_sr_exact_probability(fmt, y):
+    """Enumerate every one of the 2^24 values u takes: the number that round up
+    is ceil(f * 2^24), f = (|y| - lo) / (hi - lo)."""
+    y32 = np.float32(y)
+    levels = o.grid_levels(fmt)
+    lo = levels[levels <= float(y32)].max()
+    hi = levels[levels > float(y32)].min()
+    f = (float(y32) - lo) / (hi - lo)
+    u = np.arange(1 << 24, dtype=np.float64) * 2.0 ** -24
+    c = o.round_sr(np.full(u.shape, y32), fmt, u)
+    ups = int(np.sum(o.code_value(c, fmt) == hi))
+    downs = int(np.sum(o.code_value(c, fmt) == lo))
+    assert ups + downs == (1 << 24)
+    assert ups == int(np.ceil(f * 2 ** 24))
+
+
+def test_sr_on_grid_and_saturation():
+    for fmt in ("nvfp4", "ufp4"):
+        lv = o.grid_levels(fmt).astype(np.float32)
+        u = np.zeros(lv.size)
+        assert np.array_equal(o.code_value(o.round_sr(lv, fmt, u), fmt), lv)
+        u = np.full(lv.size, 1 - 2.0 ** -24)
+        assert np.array_equal(o.code_value(o.round_sr(lv, fmt, u), fmt), lv)
+        big = np.array([lv[-1] * 1.5, -lv[-1] * 3], dtype=np.float32)
+        assert np.array_equal(o.code_value(o.round_sr(big, fmt, np.zeros(2)), fmt),
+                              [lv[-1], -lv[-1]])
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "ufp4"])
+def test_sr_unbiased(fmt):
+    """E[round(y)] = y: the mean over 2^20 independently keyed elements lies
+    within 4 sigma of y."""
+    n = 1 << 20
+    for y in (0.37, 1.61, 2.2, 4.9):
+        if y >= o.QMAX[fmt]:
+            continue
+        u = o.sr_uniforms(np.arange(n), 77, 0)
+        q = o.code_value(o.round_sr(np.full(n, np.float32(y), dtype=np.float32), fmt, u), fmt)
+        levels = o.grid_levels(fmt)
+        lo = levels[levels <= y].max()
+        hi = levels[levels > y].min()
+        p = (np.float32(y) - lo) / (hi - lo)
+        sigma = (hi - lo) * np.sqrt(p * (1 - p) / n)
+        assert abs(q.mean() - np.float32(y)) < 4 * sigma + 1e-12
