@@ -1,0 +1,278 @@
+// C ABI of libfp4q: argument validation on the host, then dispatch to the
+// kernel launchers. Nothing here allocates device memory.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fp4q.h"
+#include "fp4q_device.cuh"
+#include "fp4q_internal.h"
+
+namespace fp4q {
+
+int sm_count() {
+  static std::mutex mu;
+  static std::unordered_map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  std::lock_guard<std::mutex> lk(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  cache[dev] = n;
+  return n;
+}
+
+int cached_occupancy(const void* kernel, int threads, int smem) {
+  static std::mutex mu;
+  struct Key {
+    const void* k; int dev, t, s;
+    bool operator==(const Key& o) const { return k == o.k && dev == o.dev && t == o.t && s == o.s; }
+  };
+  struct Hash {
+    size_t operator()(const Key& x) const {
+      return std::hash<const void*>()(x.k) ^ ((size_t)x.dev << 48) ^ ((size_t)x.t << 20) ^ (size_t)x.s;
+    }
+  };
+  static std::unordered_map<Key, int, Hash> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const Key key{kernel, dev, threads, smem};
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    occ = 1;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = occ;
+  return occ;
+}
+
+}  // namespace fp4q
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int block_for(int fmt) { return fmt == FP4Q_MXFP4 ? 32 : 16; }
+
+int check_format(int fmt, int block) {
+  if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4 && fmt != FP4Q_UFP4) return FP4Q_EINVAL;
+  if (block != block_for(fmt)) return FP4Q_ENOTSUP;
+  return FP4Q_OK;
+}
+
+int check_qtensor(const fp4q_qtensor* q, bool empty = false) {
+  if (!q || !q->tensor_scale) return FP4Q_EINVAL;
+  if (empty) return aligned(q->tensor_scale, 4) ? FP4Q_OK : FP4Q_EINVAL;
+  if (!q->codes || !q->scales) return FP4Q_EINVAL;
+  if (q->scale_layout != FP4Q_SCALES_LINEAR && q->scale_layout != FP4Q_SCALES_MMA) return FP4Q_EINVAL;
+  if (!aligned(q->codes, 16) || !aligned(q->tensor_scale, 4)) return FP4Q_EINVAL;
+  if (q->scale_layout == FP4Q_SCALES_MMA && !aligned(q->scales, 16)) return FP4Q_EINVAL;
+  return FP4Q_OK;
+}
+
+fp4q::QOut to_qout(const fp4q_qtensor* q) {
+  fp4q::QOut o{};
+  if (q) {
+    o.codes = q->codes;
+    o.scales = q->scales;
+    o.tensor_scale = q->tensor_scale;
+    o.scale_layout = q->scale_layout;
+  }
+  return o;
+}
+
+bool needs_padding(int64_t rows, int64_t nkb) { return (rows % 128) != 0 || (nkb % 4) != 0; }
+
+}  // namespace
+
+extern "C" {
+
+size_t fp4q_workspace_size(void) { return (sizeof(fp4q::Workspace) + 255) / 256 * 256; }
+
+int fp4q_workspace_init(void* workspace, void* stream) {
+  if (!workspace || !aligned(workspace, 16)) return FP4Q_EINVAL;
+  if (cudaMemsetAsync(workspace, 0, fp4q_workspace_size(), (cudaStream_t)stream) != cudaSuccess)
+    return FP4Q_ECUDA;
+  return FP4Q_OK;
+}
+
+size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout) {
+  if (rows < 0 || cols < 0 || block <= 0) return 0;
+  const int64_t nkb = cols / block;
+  if (scale_layout == FP4Q_SCALES_MMA) {
+    return (size_t)(((rows + 127) / 128) * 128) * (size_t)(((nkb + 3) / 4) * 4);
+  }
+  return (size_t)rows * (size_t)nkb;
+}
+
+int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block,
+                  int rht, int rounding, uint64_t seed, int axis, const fp4q_qtensor* row_out,
+                  const fp4q_qtensor* col_out, void* workspace, size_t ws_bytes, void* stream) {
+  int rc = check_format(fmt, block);
+  if (rc) return rc;
+  if (dtype != FP4Q_BF16 && dtype != FP4Q_F32) return FP4Q_EINVAL;
+  if (rht != 0 && rht != 1) return FP4Q_EINVAL;
+  if (rounding != FP4Q_RTNE && rounding != FP4Q_SR) return FP4Q_EINVAL;
+  if (axis < 1 || axis > 3) return FP4Q_EINVAL;
+  if (rows < 0 || cols < 0) return FP4Q_EINVAL;
+  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40) || (rows && cols > (int64_t(1) << 46) / rows))
+    return FP4Q_EINVAL;
+  if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
+  if (rows && cols && (!src || !aligned(src, 16))) return FP4Q_EINVAL;
+  const bool empty = rows == 0 || cols == 0;
+  if (axis & FP4Q_ROWWISE) {
+    if ((rc = check_qtensor(row_out, empty))) return rc;
+    if (cols % block) return FP4Q_EINVAL;
+  }
+  if (axis & FP4Q_COLWISE) {
+    if ((rc = check_qtensor(col_out, empty))) return rc;
+    if (rows % block) return FP4Q_EINVAL;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // padding bytes of the tiled scale layout are defined as 0
+  if (!empty && (axis & FP4Q_ROWWISE) && row_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(rows, cols / block)) {
+    if (cudaMemsetAsync(row_out->scales, 0, fp4q_scales_bytes(rows, cols, block, FP4Q_SCALES_MMA), s) != cudaSuccess)
+      return FP4Q_ECUDA;
+  }
+  if (!empty && (axis & FP4Q_COLWISE) && col_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(cols, rows / block)) {
+    if (cudaMemsetAsync(col_out->scales, 0, fp4q_scales_bytes(cols, rows, block, FP4Q_SCALES_MMA), s) != cudaSuccess)
+      return FP4Q_ECUDA;
+  }
+  fp4q::QuantArgs a{};
+  a.src = src;
+  a.dtype = dtype;
+  a.rows = rows;
+  a.cols = cols;
+  a.fmt = fmt;
+  a.rht = rht;
+  a.rounding = rounding;
+  a.seed = seed;
+  a.axis = axis;
+  a.row = to_qout((axis & FP4Q_ROWWISE) ? row_out : nullptr);
+  a.col = to_qout((axis & FP4Q_COLWISE) ? col_out : nullptr);
+  a.ws = workspace;
+  return fp4q::run_quantize(a, s) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+}
+
+int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, int block,
+                    int inverse_rht, uint64_t seed, void* dst, int dst_dtype, void* stream) {
+  int rc = check_format(fmt, block);
+  if (rc) return rc;
+  if ((rc = check_qtensor(q))) return rc;
+  if (inverse_rht != 0 && inverse_rht != 1) return FP4Q_EINVAL;
+  if (dst_dtype != FP4Q_BF16 && dst_dtype != FP4Q_F32) return FP4Q_EINVAL;
+  if (rows < 0 || cols < 0 || cols % block) return FP4Q_EINVAL;
+  if (rows == 0 || cols == 0) return FP4Q_OK;
+  if (!dst || !aligned(dst, 16)) return FP4Q_EINVAL;
+  fp4q::DequantArgs a{};
+  a.q = to_qout(q);
+  a.rows = rows;
+  a.cols = cols;
+  a.fmt = fmt;
+  a.inverse_rht = inverse_rht;
+  a.seed = seed;
+  a.dst = dst;
+  a.dst_dtype = dst_dtype;
+  return fp4q::run_dequantize(a, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+}
+
+int fp4q_stats(const void* workspace, fp4q_stats_t* row_stats, fp4q_stats_t* col_stats,
+               void* stream) {
+  if (!workspace) return FP4Q_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  const fp4q::Workspace* ws = static_cast<const fp4q::Workspace*>(workspace);
+  double sums[2][5];
+  unsigned int copies = 0;
+  if (cudaMemcpyAsync(sums, ws->sums, sizeof(sums), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(&copies, &ws->copies, sizeof(copies), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FP4Q_ECUDA;
+  fp4q_stats_t* out[2] = {row_stats, col_stats};
+  for (int c = 0; c < 2; ++c) {
+    if (!out[c]) continue;
+    fp4q_stats_t st{};
+    if (copies & (1u << c)) {
+      st.sum_bias = sums[c][0];
+      st.sum_sig2 = sums[c][1];
+      st.sum_err2 = sums[c][2];
+      st.n = (int64_t)sums[c][3];
+      const double qmax = sums[c][4];
+      st.shrink_bias = st.n ? st.sum_bias / (qmax * (double)st.n) : 0.0;
+      if (st.sum_err2 == 0.0) st.snr_db = INFINITY;
+      else if (st.sum_sig2 == 0.0) st.snr_db = -INFINITY;
+      else st.snr_db = 10.0 * std::log10(st.sum_sig2 / st.sum_err2);
+    }
+    *out[c] = st;
+  }
+  return FP4Q_OK;
+}
+
+int fp4q_status(void* workspace, void* stream) {
+  if (!workspace) return FP4Q_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  fp4q::Workspace* ws = static_cast<fp4q::Workspace*>(workspace);
+  unsigned int st = 0;
+  if (cudaMemcpyAsync(&st, &ws->status, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(&ws->status, 0, sizeof(st), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FP4Q_ECUDA;
+  if (st & fp4q::kStatusTimeout) return FP4Q_ETIMEOUT;
+  if (st & fp4q::kStatusNonfinite) return FP4Q_ENONFINITE;
+  return FP4Q_OK;
+}
+
+int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+              int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (fmt == FP4Q_UFP4) return FP4Q_ENOTSUP;
+  if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4) return FP4Q_EINVAL;
+  if (fmt == FP4Q_MXFP4) return FP4Q_ENOTSUP;
+  int rc;
+  if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
+  if (A->scale_layout != FP4Q_SCALES_MMA || B->scale_layout != FP4Q_SCALES_MMA) return FP4Q_EINVAL;
+  if (out_dtype != FP4Q_BF16 && out_dtype != FP4Q_F32) return FP4Q_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 256) return FP4Q_EINVAL;
+  if (M > (int64_t(1) << 20) || N > (int64_t(1) << 20) || K > (int64_t(1) << 20)) return FP4Q_EINVAL;
+  if (!Y || !aligned(Y, 16)) return FP4Q_EINVAL;
+  if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
+  fp4q::GemmArgs a{};
+  a.a = to_qout(A);
+  a.b = to_qout(B);
+  a.m = M;
+  a.n = N;
+  a.k = K;
+  a.fmt = fmt;
+  a.y = Y;
+  a.out_dtype = out_dtype;
+  a.ws = workspace;
+  const cudaError_t e = fp4q::run_gemm(a, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported) return FP4Q_ENOTSUP;
+  return e == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+}
+
+const char* fp4q_strerror(int code) {
+  switch (code) {
+    case FP4Q_OK: return "ok";
+    case FP4Q_EINVAL: return "invalid argument";
+    case FP4Q_ENOTSUP: return "not supported";
+    case FP4Q_ECUDA: return "CUDA error";
+    case FP4Q_ENONFINITE: return "non-finite input";
+    case FP4Q_ETIMEOUT: return "bounded wait timed out";
+    default: return "unknown error";
+  }
+}
+
+int fp4q_version(void) { return 100; }
+
+}  // extern "C"

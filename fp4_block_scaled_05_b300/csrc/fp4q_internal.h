@@ -1,0 +1,57 @@
+// Host-side plumbing shared between the C ABI and the kernel launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp4q {
+
+struct QOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tensor_scale;
+  int scale_layout;
+};
+
+struct QuantArgs {
+  const void* src;
+  int dtype;          // 0 BF16, 1 FP32
+  int64_t rows, cols;
+  int fmt;            // 0 NVFP4, 1 MXFP4, 2 UFP4
+  int rht, rounding;  // rounding 0 RTNE, 1 SR
+  uint64_t seed;
+  int axis;           // bit 0 row-wise, bit 1 column-wise
+  QOut row, col;
+  void* ws;
+};
+
+struct DequantArgs {
+  QOut q;
+  int64_t rows, cols;
+  int fmt;
+  int inverse_rht;
+  uint64_t seed;
+  void* dst;
+  int dst_dtype;
+};
+
+struct GemmArgs {
+  QOut a, b;
+  int64_t m, n, k;
+  int fmt;
+  void* y;
+  int out_dtype;      // 0 BF16, 1 FP32
+  void* ws;
+};
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` dynamic bytes (cached).
+int cached_occupancy(const void* kernel, int threads, int smem);
+
+cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s);
+cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
+// Returns cudaErrorNotSupported when no GEMM kernel covers the request.
+cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s);
+
+}  // namespace fp4q

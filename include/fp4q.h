@@ -1,0 +1,229 @@
+/*
+ * fp4q.h -- block-scaled 4-bit quantisation of GEMM operands and the
+ * block-scaled FP4 GEMM, as a C ABI over hand-written sm_103a CUDA kernels.
+ *
+ * Method sources (page title, section):
+ *   [UFP4]  "Replanteamiento del Sesgo de Contraccion en el Preentrenamiento de
+ *           LLM en FP4": Metodologia §1 (E2M1 grid, RTNE, shrinkage bias
+ *           (l_i - r_i)/2, RHT), §2 (uniform E1M2 grid, stochastic rounding,
+ *           RHT on FPROP/DGRAD/WGRAD), Eficiencia (RHT fused into quantisation).
+ *   [TJ2]   "TetraJet-v2: Accurate NVFP4 Training for Large Language Models with
+ *           Oscillation Suppression and Outlier Control": Riepilogo Tecnico §2A
+ *           (NVFP4 16-element groups with an 8-bit scale, stochastic rounding
+ *           E[round(x)] = x, the transposed operand copy), §2C (RHT on dX, dW).
+ *   [MXFP4] "Unveiling the Potential of Quantization with MXFP4: Strategies for
+ *           Quantization Error Reduction": Resume technique §2 points 1-2
+ *           (MXFP4 32-element blocks with E8M0 scales, NVFP4 16-element blocks
+ *           with E4M3 scales), §2B (scale math beside dense tensor-core math).
+ *   [NGPT]  "Le Architetture Normalizzate sono Nativamente a 4 Bit": Metodologia
+ *           (NVFP4 consumed natively by Blackwell tensor cores; SNR of Y = WX).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer named "device" is a CUDA device pointer owned by the caller.
+ *     The library allocates and frees nothing and keeps no state between calls
+ *     other than what the caller's workspace holds.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Work is enqueued asynchronously on it; only fp4q_stats and
+ *     fp4q_status synchronise that stream.
+ *   - Return value: FP4Q_OK (0) or an FP4Q_E* code. Argument errors are
+ *     detected on the host before anything is launched. Device-side conditions
+ *     (non-finite input, a bounded wait that ran out) are recorded in the
+ *     workspace status word and returned by fp4q_status. Nothing traps or
+ *     aborts on the GPU.
+ *   - Element order: rows x cols, row-major. Packed codes hold two 4-bit codes
+ *     per byte, element 2j in bits 0-3 and element 2j+1 in bits 4-7; bit 3 of a
+ *     code is the sign (a value that rounds to zero keeps its sign).
+ */
+#ifndef FP4Q_H
+#define FP4Q_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- enums and error codes ------------------------------------------------ */
+
+typedef enum {
+  FP4Q_NVFP4 = 0, /* E2M1 elements, 16-element blocks, E4M3 block scale, FP32 tensor scale [TJ2 §2A, MXFP4 §2] */
+  FP4Q_MXFP4 = 1, /* E2M1 elements, 32-element blocks, E8M0 (power-of-two) block scale [MXFP4 §2]          */
+  FP4Q_UFP4  = 2  /* uniform E1M2 levels 0..7, 16-element blocks, E4M3 block scale, FP32 tensor scale [UFP4 §2] */
+} fp4q_format;
+
+typedef enum { FP4Q_RTNE = 0, FP4Q_SR = 1 } fp4q_rounding;
+typedef enum { FP4Q_BF16 = 0, FP4Q_F32 = 1 } fp4q_dtype;
+
+enum { FP4Q_ROWWISE = 1, FP4Q_COLWISE = 2 };            /* axis bit mask            */
+enum { FP4Q_SCALES_LINEAR = 0, FP4Q_SCALES_MMA = 1 };   /* block-scale byte layout  */
+
+enum {
+  FP4Q_OK = 0,
+  FP4Q_EINVAL = 1,     /* bad enum, shape, alignment, null pointer or small workspace   */
+  FP4Q_ENOTSUP = 2,    /* valid request this library does not implement                */
+  FP4Q_ECUDA = 3,      /* a CUDA runtime/driver call or a kernel launch failed          */
+  FP4Q_ENONFINITE = 4, /* (status) a NaN or an infinity was read by a quantise kernel   */
+  FP4Q_ETIMEOUT = 5    /* (status) a bounded wait inside a GEMM kernel ran out          */
+};
+
+/* One quantised copy. All pointers are device pointers owned by the caller.
+ *   codes        rows x cols/2 bytes (packed nibbles, row-major).
+ *   scales       FP4Q_SCALES_LINEAR: rows x cols/block bytes, row-major.
+ *                FP4Q_SCALES_MMA: the tiled layout read by the block-scaled
+ *                tensor-core MMA: tiles of 128 rows x 4 blocks stored as 512
+ *                contiguous bytes, tiles ordered block-index fastest; inside a
+ *                tile the scale of (row r, block kb) sits at byte
+ *                (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4. Rows are padded
+ *                to a multiple of 128 and blocks per row to a multiple of 4;
+ *                padding bytes are written as 0. Size: fp4q_scales_bytes().
+ *                NVFP4/UFP4 scales are E4M3 codes; MXFP4 scales are E8M0
+ *                codes (exponent + 127).
+ *   tensor_scale one FP32 (device): g = amax / (Qmax * 448) for NVFP4 (Qmax 6)
+ *                and UFP4 (Qmax 7, levels in integer units), 1.0 for MXFP4.
+ *   scale_layout FP4Q_SCALES_LINEAR or FP4Q_SCALES_MMA.
+ * The value of element (r, c) is level(code) * scale(r, c / block) * g. */
+typedef struct {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tensor_scale;
+  int scale_layout;
+} fp4q_qtensor;
+
+/* Statistics of one quantised copy ([UFP4] Metodologia §1 and Resultados).
+ *   shrink_bias  mean over all n elements of (|q| - |y|) / Qmax, where y is the
+ *                element after normalisation by its block (and tensor) scale and
+ *                q its grid level: the mean signed rounding error in normalised
+ *                magnitude.
+ *   snr_db       10 log10(sum v^2 / sum (v - v_hat)^2), v the (transformed)
+ *                value and v_hat its dequantised value; +inf when no error.
+ *   sum_sig2, sum_err2, sum_bias  the underlying sums (sum_bias in grid units).
+ *   n            element count. */
+typedef struct {
+  double shrink_bias;
+  double snr_db;
+  double sum_sig2;
+  double sum_err2;
+  double sum_bias;
+  int64_t n;
+} fp4q_stats_t;
+
+/* ---- workspace -------------------------------------------------------------- */
+
+/* Bytes of device workspace every call below needs (a fixed size, a few
+ * hundred KB). The workspace holds the tensor amaxes, the statistics, the
+ * cross-block counters and the status word. It must be zero-filled once
+ * before its first use (fp4q_workspace_init); every call leaves its counters
+ * back at zero. Calls that share one workspace must not overlap on the GPU. */
+size_t fp4q_workspace_size(void);
+
+/* Zero-fill a workspace of fp4q_workspace_size() bytes on `stream`. */
+int fp4q_workspace_init(void* workspace, void* stream);
+
+/* Bytes of the scale array of one copy with `rows` rows of `cols` elements in
+ * blocks of `block`, for the given layout. */
+size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout);
+
+/* ---- quantisation ------------------------------------------------------------ */
+
+/* Quantise a rows x cols tensor into block-scaled 4-bit copies.
+ *
+ * Operation (per copy; [UFP4] Metodologia §1-2, Eficiencia; [TJ2] §2A, §2C;
+ * [MXFP4] §2): widen to FP32; if `rht`, apply v = (1/4) H16 diag(sigma) x to
+ * every 16 consecutive elements along the block axis (H16 Sylvester, sigma a
+ * seeded +-1 vector: bit j of word 0 of Philox4x32-10(key = seed, counter =
+ * (0, 0, 0, 0xFFFFFFFF)), one vector for the whole call), as the FP32
+ * butterfly with stages 1, 2, 4, 8 then * 0.25. NVFP4/UFP4: A = max |v| over
+ * the copy, g = A / (Qmax * 448), per block t = a_b / (Qmax * g) rounded to
+ * E4M3 (nearest-even, saturating at 448), r_b = 1 / (s_b * g), y = v * r_b.
+ * MXFP4: e_b = floor(log2 a_b) - 2 clamped to [-127, 127], y = v * 2^-e_b.
+ * y is rounded onto the grid: FP4Q_RTNE nearest level ties to the even code,
+ * values beyond the top level saturate; FP4Q_SR rounds |y| up from its lower
+ * neighbouring level iff u < f, f the fractional position between the two
+ * levels and u = (w >> 8) * 2^-24, w word (i mod 4) of Philox4x32-10(key =
+ * seed, counter = (i/4 low, i/4 high, axis, 0)), i the element's row-major
+ * index inside the copy, axis 0 for the row-wise copy and 1 for the
+ * column-wise copy. Statistics per copy are fused (fp4q_stats).
+ *
+ * Arguments
+ *   src          device, rows x cols elements of `dtype` (FP4Q_BF16 or
+ *                FP4Q_F32), row-major, 16-byte aligned.
+ *   fmt, block   FP4Q_NVFP4/FP4Q_UFP4 with block 16, FP4Q_MXFP4 with block 32
+ *                (else FP4Q_ENOTSUP).
+ *   rht          0 or 1. rounding: FP4Q_RTNE or FP4Q_SR. seed: RHT signs and SR.
+ *   axis         FP4Q_ROWWISE: blocks along rows, copy row_out (rows x cols).
+ *                FP4Q_COLWISE: blocks along columns, emitted transposed into
+ *                col_out (cols x rows: codes cols x rows/2, scales per column).
+ *                Both bits: both copies from one read of src.
+ *   row_out, col_out  host pointers to fp4q_qtensor descriptors of device
+ *                buffers; the one whose axis bit is clear may be NULL. codes
+ *                must be 16-byte aligned; MMA-layout scales 16-byte aligned.
+ *   workspace    device, ws_bytes >= fp4q_workspace_size(), zero-filled once.
+ * Shapes: cols % block == 0 for the row-wise copy, rows % block == 0 for the
+ * column-wise copy; rows or cols 0 is valid (writes g = 0 for NVFP4/UFP4 and
+ * empty statistics). Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
+int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols,
+                  int fmt, int block, int rht, int rounding, uint64_t seed, int axis,
+                  const fp4q_qtensor* row_out, const fp4q_qtensor* col_out,
+                  void* workspace, size_t ws_bytes, void* stream);
+
+/* Dequantise one copy ([UFP4] §2: UFP4 has no tensor-core format and is
+ * consumed through this call): v_hat = (level * s_b) * g in FP32, two
+ * round-to-nearest products in that order (MXFP4: level * 2^e_b); if
+ * `inverse_rht`, apply R^T = (1/4) diag(sigma) H16 per 16-block along the row
+ * (the same FP32 butterfly, then * 0.25, then the sign flip). Writes rows x
+ * cols elements of `dst_dtype` (BF16 rounded to nearest-even, or FP32) to the
+ * device buffer `dst` (16-byte aligned). q is a host pointer to a descriptor of
+ * device buffers laid out as fp4q_quantize wrote them for a copy of rows x
+ * cols. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
+int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, int block,
+                    int inverse_rht, uint64_t seed, void* dst, int dst_dtype, void* stream);
+
+/* Statistics of the last fp4q_quantize call that used `workspace`
+ * ([UFP4] Metodologia §1 shrinkage bias, Resultados SQNR). Synchronises
+ * `stream`, then fills the host structs row_stats / col_stats (either may be
+ * NULL; a copy that was not produced reads n = 0). Errors: FP4Q_EINVAL,
+ * FP4Q_ECUDA. */
+int fp4q_stats(const void* workspace, fp4q_stats_t* row_stats, fp4q_stats_t* col_stats,
+               void* stream);
+
+/* Synchronise `stream`, return the device status recorded in `workspace` since
+ * the previous fp4q_status call (FP4Q_OK, FP4Q_ENONFINITE or FP4Q_ETIMEOUT;
+ * timeout wins) and clear it. FP4Q_ECUDA if the synchronisation failed. */
+int fp4q_status(void* workspace, void* stream);
+
+/* ---- block-scaled GEMM --------------------------------------------------------- */
+
+/* Y = dequant(A) * dequant(B)^T on the tensor cores ([NGPT] Metodologia: NVFP4
+ * consumed natively by Blackwell tensor cores; [MXFP4] §2B: scale factors
+ * applied beside the dense MMA; [UFP4] Resultados: single-GEMM output of the
+ * quantised operands). A is M x K and B is N x K, both row-wise NVFP4 copies
+ * (blocks along K) with FP4Q_SCALES_MMA scales; the K-block products are
+ * accumulated in FP32 by tcgen05 block-scaled MMAs and the result is
+ * multiplied by g_A * g_B. When both operands were quantised with the RHT
+ * along K under the same seed, the transforms cancel (R R^T = I).
+ *   A, B       host pointers to descriptors of device buffers.
+ *   fmt        FP4Q_NVFP4 (FP4Q_UFP4 -> FP4Q_ENOTSUP: no tensor-core format;
+ *              FP4Q_MXFP4 -> FP4Q_ENOTSUP in this version).
+ *   Y          device, M x N row-major, `out_dtype` FP4Q_BF16 (nearest-even)
+ *              or FP4Q_F32, 16-byte aligned.
+ *   workspace  as for fp4q_quantize (the status word records a bounded wait
+ *              that ran out: FP4Q_ETIMEOUT via fp4q_status).
+ * Shapes: M % 128 == 0, N % 128 == 0, K % 256 == 0, all > 0 (else FP4Q_EINVAL).
+ * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
+int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+              int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- misc ----------------------------------------------------------------------- */
+
+/* Static text for an FP4Q_* code. */
+const char* fp4q_strerror(int code);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int fp4q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP4Q_H */

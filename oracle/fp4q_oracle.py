@@ -365,7 +365,7 @@ def tensor_scale(amax: np.float32, fmt: str) -> np.float32:
 
 def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = "rtne",
                   seed: int = 0, axis: int = 0, rht_mode: str = "butterfly",
-                  chunk_rows: int = 256, keep_y: bool = False) -> dict:
+                  chunk_rows: int = 256, keep_y: bool = False, rows_subset=None) -> dict:
     """Quantise one copy: a rows x cols FP32 matrix whose blocks run along the
     columns. For the row-wise copy this is X itself; for the column-wise copy it
     is X^T ([TJ2] §2A: the transposed operand of the weight-gradient GEMM).
@@ -382,6 +382,8 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
       MXFP4:      e_b = floor(log2 a_b) - 2 in [-127, 127]; scale code e_b + 127;
                   y = v * 2^-e_b (FP32)
       q   = RTNE(y) or SR(y, u_i)
+    ``rows_subset`` (row indices of the copy) restricts the codes, scales and
+    statistics to those rows; the tensor amax still covers the whole copy.
     Statistics (FP64): bias = sum(|q| - |y|) / (Qmax * N)   (reading R6)
                        snr_db = 10 log10(sum v^2 / sum (v - v_hat)^2), v_hat =
                        q * s_b * g (or q * 2^e_b) exactly in FP64.
@@ -405,15 +407,18 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
     g = tensor_scale(amax, fmt)
     d = F32(F32(qmax) * g)
 
-    codes = np.zeros((n, k), dtype=np.uint8)
-    scales = np.zeros((n, k // b), dtype=np.uint8)
-    ys = np.zeros((n, k), dtype=np.float32) if keep_y else None
+    sel = np.arange(n) if rows_subset is None else np.asarray(rows_subset, dtype=np.int64)
+    ns = sel.size
+    codes = np.zeros((ns, k), dtype=np.uint8)
+    scales = np.zeros((ns, k // b), dtype=np.uint8)
+    ys = np.zeros((ns, k), dtype=np.float32) if keep_y else None
     sum_bias = 0.0
     sum_abs_bias = 0.0
     sum_sig2 = 0.0
     sum_err2 = 0.0
-    for r0 in range(0, n, chunk_rows):
-        v = transform_copy(m32[r0:r0 + chunk_rows], fmt, rht, seed, rht_mode)
+    for r0 in range(0, ns, chunk_rows):
+        ridx = sel[r0:r0 + chunk_rows]
+        v = transform_copy(m32[ridx], fmt, rht, seed, rht_mode)
         rows = v.shape[0]
         vb = v.reshape(rows, k // b, b)
         a_b = np.max(np.abs(vb), axis=2).astype(np.float32)
@@ -441,8 +446,7 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
         if rounding == "rtne":
             c = round_rtne(y, fmt)
         elif rounding == "sr":
-            idx = (np.arange(r0, r0 + rows, dtype=np.int64)[:, None] * k
-                   + np.arange(k, dtype=np.int64)[None, :])
+            idx = ridx[:, None] * k + np.arange(k, dtype=np.int64)[None, :]
             c = round_sr(y, fmt, sr_uniforms(idx, seed, axis))
         else:
             raise ValueError(rounding)
@@ -458,9 +462,9 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
         sum_sig2 += float(np.sum(v64 * v64))
         sum_err2 += float(np.sum((v64 - vhat) ** 2))
 
-    nel = n * k
+    nel = ns * k
     out = {
-        "fmt": fmt, "block": b, "rows": n, "cols": k,
+        "fmt": fmt, "block": b, "rows": ns, "cols": k, "rows_subset": rows_subset,
         "codes": pack_nibbles(codes),
         "scales": scales,
         "tensor_scale": F32(g),
@@ -489,21 +493,25 @@ def stats_from_sums(sum_bias, sum_abs_bias, sum_sig2, sum_err2, nel, qmax) -> di
 
 
 def quantize(x, fmt: str, rht: bool = False, rounding: str = "rtne", seed: int = 0,
-             axis: str = "row", rht_mode: str = "butterfly", keep_y: bool = False) -> dict:
+             axis: str = "row", rht_mode: str = "butterfly", keep_y: bool = False,
+             rows_subset=None, cols_subset=None) -> dict:
     """Quantise a rows x cols tensor (BF16 bits as uint16, or FP32).
 
     axis: "row" (blocks along each row), "col" (blocks along each column,
     emitted as the transposed copy [cols][rows/2]) or "both".
+    rows_subset / cols_subset restrict the row-wise copy to those rows of x and
+    the column-wise copy to those columns of x (rows of the transposed copy).
     Returns {"row": copy, "col": copy} with the requested copies, plus
     "nonfinite": True when the input held a NaN or an infinity.
     """
     m = _as_f32_matrix(x)
     out = {"nonfinite": bool(not np.all(np.isfinite(m)))}
     if axis in ("row", "both"):
-        out["row"] = quantize_copy(m, fmt, rht, rounding, seed, 0, rht_mode, keep_y=keep_y)
+        out["row"] = quantize_copy(m, fmt, rht, rounding, seed, 0, rht_mode, keep_y=keep_y,
+                                   rows_subset=rows_subset)
     if axis in ("col", "both"):
         out["col"] = quantize_copy(np.ascontiguousarray(m.T), fmt, rht, rounding, seed, 1,
-                                   rht_mode, keep_y=keep_y)
+                                   rht_mode, keep_y=keep_y, rows_subset=cols_subset)
     return out
 
 

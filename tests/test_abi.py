@@ -1,0 +1,68 @@
+"""The C ABI library: builds, loads without a GPU, exports every function the
+header declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp4q.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp4q_[a-z_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    from fp4_block_scaled_05_b300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_api():
+    names = _declared()
+    for n in ("fp4q_quantize", "fp4q_dequantize", "fp4q_stats", "fp4q_gemm",
+              "fp4q_status", "fp4q_workspace_size", "fp4q_strerror"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(so):
+    missing = [n for n in _declared() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_python_binding_uses_the_c_names():
+    import fp4_block_scaled_05_b300 as fq
+    for n in _declared():
+        assert callable(getattr(fq, n)), n
+
+
+def test_host_validation_without_gpu(so):
+    so.fp4q_workspace_size.restype = ctypes.c_size_t
+    ws_size = so.fp4q_workspace_size()
+    assert 1024 <= ws_size <= (1 << 20)
+    so.fp4q_strerror.restype = ctypes.c_char_p
+    assert so.fp4q_strerror(1) == b"invalid argument"
+    assert so.fp4q_version() >= 100
+    so.fp4q_scales_bytes.restype = ctypes.c_size_t
+    so.fp4q_scales_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+    assert so.fp4q_scales_bytes(100, 96, 16, 0) == 600
+    assert so.fp4q_scales_bytes(100, 96, 16, 1) == 128 * 8
+    q = so.fp4q_quantize
+    q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
+    # bad format / block / dtype / axis / workspace size -> EINVAL or ENOTSUP, no launch
+    assert q(fake, 0, 16, 16, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 16, 16, 0, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 16, 16, 1, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
+    assert q(fake, 5, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 4, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, 16, None) == 1
+    assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1  # row_out NULL
+    assert q(fake, 0, -1, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
