@@ -1,5 +1,447 @@
-// Block-scaled FP4 GEMM (placeholder until the tcgen05 kernel lands).
+// Block-scaled NVFP4 GEMM on the 5th-generation tensor cores (sm_103a).
+//
+// Y[M][N] = (sum_k A[m][k] * B[n][k]) * g_A * g_B, with A, B row-wise NVFP4
+// copies (E2M1 codes, one E4M3 scale per 16 elements along K, one FP32 tensor
+// scale each): "Le Architetture Normalizzate sono Nativamente a 4 Bit",
+// Metodologia (NVFP4 consumed natively by Blackwell tensor cores); "Unveiling
+// the Potential of Quantization with MXFP4 ...", Resume technique §2B (scale
+// factors handled beside the dense tensor-core math).
+//
+// Structure (one persistent CTA per SM, 192 threads):
+//   warp 0      TMA producer: per K stage of 256 elements, one 2-D tiled TMA
+//               load (128B swizzle) of the A and B code tiles and 1-D bulk
+//               copies of their scale tiles into a 4-deep shared-memory ring
+//               (mbarrier transaction counts).
+//   warp 1      allocates the 512 TMEM columns; one thread moves each stage's
+//               scale tiles into TMEM (tcgen05.cp 32x128b.warpx4) and issues
+//               four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               (M = 128, N = BN, K = 64) into an FP32 accumulator in TMEM;
+//               tcgen05.commit frees the ring slot and, after the last stage,
+//               hands the accumulator to the epilogue.
+//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, times
+//               g_A * g_B, BF16 (nearest-even) or FP32 stores.
+// Every mbarrier wait is bounded by a global-timer deadline; on expiry the
+// kernel records FP4Q_ETIMEOUT in the workspace, drains what it issued and
+// returns.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fp4q_device.cuh"
 #include "fp4q_internal.h"
+
 namespace fp4q {
-cudaError_t run_gemm(const GemmArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int BM = 128;           // rows of A per tile (= MMA M)
+constexpr int BK_BYTES = 128;     // bytes of codes per row per stage (256 FP4 values)
+constexpr int BK = 256;           // K elements per stage
+constexpr int kThreads = 192;
+constexpr int kTmemCols = 512;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
+
+template <int BN>
+struct Cfg {
+  static constexpr int kStages = 4;
+  static constexpr int kABytes = BM * BK_BYTES;
+  static constexpr int kBBytes = BN * BK_BYTES;
+  static constexpr int kSfaBytes = 2048;                 // 128 rows x 16 scales
+  static constexpr int kSfbBytes = (BN / 128) * 2048;
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kSfaCols = 16;                    // 4 K chunks x 4 TMEM columns
+  static constexpr int kSfbCols = (BN / 128) * 16;
+  static constexpr int kSfStageCols = kSfaCols + kSfbCols;
+  static constexpr int kSfBase = BN;                     // accumulator uses columns [0, BN)
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+};
+
+// ---- small PTX wrappers ------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: false when `abort` is raised or the deadline passes.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t timeout_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 255u) {
+      if (*abort) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > timeout_ns) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05): start >> 4 in bits 0-13, leading
+// byte offset >> 4 in 16-29, stride byte offset >> 4 in 32-45, the fixed
+// value 1 in bits 46-48, swizzle mode in 61-63 (2 = 128-byte swizzle, 0 = none).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swz << 61);
+}
+
+// Instruction descriptor for kind::mxf4nvf4 (dense, K = 64): A and B E2M1
+// (format 1) K-major, scale type UE4M3, N >> 3 in bits 17-22, M >> 4 in 24-28,
+// scale-factor IDs 0.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_nvf4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                            uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+      ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---- the kernel -----------------------------------------------------------------
+template <int BN, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                 const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
+                 const float* __restrict__ g_a, const float* __restrict__ g_b, void* __restrict__ y,
+                 int M, int N, int K, Workspace* ws, uint64_t timeout_ns, int skip_first_stage) {
+  using C = Cfg<BN>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  // bars[0..S): full, bars[S..2S): empty, bars[2S]: tmem_full, bars[2S+1]: tmem_empty, bars[2S+2]: drain
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  const uint32_t tmem_full = bar0 + 8u * (2 * C::kStages);
+  const uint32_t tmem_empty = bar0 + 8u * (2 * C::kStages + 1);
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 2);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 128);
+    mbar_init(drain_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&s_tmem_base)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  const int num_m = M / BM, num_n = N / BN;
+  const int num_tiles = num_m * num_n;
+  const int nk = K / BK;
+  const int64_t sf_row_stride = (int64_t)(K / 64) * 512;   // bytes per 128-row scale tile row
+
+  auto fail = [&]() {
+    if (!s_abort) {
+      s_abort = 1;
+      atomicOr(&ws->status, kStatusTimeout);
+    }
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t pending = 0;    // bit ss: stage ss has copies whose phase may not have completed
+      uint32_t pend_ph = 0;    // bit ss: the parity of that phase
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const int m = t / num_n, n = t % num_n;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          const bool skip = skip_first_stage && t == (int)blockIdx.x && ks == 0;
+          pending &= ~(1u << s);
+          if (!skip) {
+            uint8_t* st = smem + s * C::kStageBytes;
+            const uint32_t fb = full_bar(s);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            tma_load_2d(smem_u32(st), &tmap_a, fb, ks * BK_BYTES, m * BM);
+            tma_load_2d(smem_u32(st + C::kABytes), &tmap_b, fb, ks * BK_BYTES, n * BN);
+            bulk_load(smem_u32(st + C::kABytes + C::kBBytes),
+                      sfa + (int64_t)m * sf_row_stride + (int64_t)ks * 2048, 2048, fb);
+#pragma unroll
+            for (int j = 0; j < BN / 128; ++j)
+              bulk_load(smem_u32(st + C::kABytes + C::kBBytes + C::kSfaBytes + 2048 * j),
+                        sfb + (int64_t)(n * (BN / 128) + j) * sf_row_stride + (int64_t)ks * 2048,
+                        2048, fb);
+            pending |= 1u << s;
+            pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
+          }
+          if (++s == C::kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: the copies of every stage issued here land before the CTA exits
+        const uint64_t t0 = globaltimer();
+        for (int ss = 0; ss < C::kStages; ++ss) {
+          if (!(pending & (1u << ss))) continue;
+          const uint32_t par = (pend_ph >> ss) & 1u;
+          while (!mbar_try_wait(full_bar(ss), par) && globaltimer() - t0 < 50000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+      int s = 0;
+      uint32_t ph = 0, acc_ph = 0;
+      bool ok = true;
+      bool issued_any = false;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(tmem_empty, acc_ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        tc_fence_after();
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(full_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa_s = st + C::kABytes + C::kBBytes;
+          const uint32_t sfb_s = sfa_s + C::kSfaBytes;
+          const uint32_t sf_col = tmem + C::kSfBase + s * C::kSfStageCols;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_cp_sf(sf_col + 4 * j, smem_desc(sfa_s + 512 * j, 128, 128, 0));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tc_cp_sf(sf_col + C::kSfaCols + (BN / 128) * 4 * j + 4 * h,
+                       smem_desc(sfb_s + 2048 * h + 512 * j, 128, 128, 0));
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t da = smem_desc(st + 32 * j, 16, 1024, 2);
+            const uint64_t db = smem_desc(st + C::kABytes + 32 * j, 16, 1024, 2);
+            tc_mma_nvf4(tmem, da, db, idesc, sf_col + 4 * j, sf_col + C::kSfaCols + (BN / 128) * 4 * j,
+                        (ks | j) != 0 ? 1u : 0u);
+          }
+          issued_any = true;
+          tc_commit(empty_bar(s));
+          if (++s == C::kStages) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tmem_full);
+        acc_ph ^= 1u;
+      }
+      if (!ok && issued_any) {
+        // drain: wait (bounded) until every MMA issued so far has completed
+        tc_commit(drain_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 50000000ull) {
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;                    // TMEM lane quadrant this warp may access
+    const float alpha = __fmul_rn(__ldg(g_a), __ldg(g_b));
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const int m = t / num_n, n = t % num_n;
+      if (!mbar_wait(tmem_full, acc_ph, &s_abort, timeout_ns)) { fail(); break; }
+      tc_fence_after();
+      const int row = m * BM + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+        const int col = n * BN + c * 32;
+        if constexpr (OUT_F32) {
+          float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+        } else {
+          uint32_t h[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
+                                                            __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
+            h[i] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) out[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty);
+      acc_ph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---- host side ----------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    } else {
+      cudaGetLastError();
+    }
+  }
+  return fn;
+}
+
+// 2-D map over a rows x (K/2)-byte code matrix; box = `box_rows` rows x 128 bytes.
+bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kbytes, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kbytes};
+  const cuuint32_t box[2] = {(cuuint32_t)BK_BYTES, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int BN, bool OUT_F32>
+cudaError_t launch(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStream_t s) {
+  using C = Cfg<BN>;
+  CUtensorMap ma, mb;
+  if (!make_code_map(&ma, a.a.codes, a.m, a.k / 2, BM) || !make_code_map(&mb, a.b.codes, a.n, a.k / 2, BN))
+    return cudaErrorInvalidValue;
+  auto k = gemm_nvf4_kernel<BN, OUT_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (int)((a.m / BM) * (a.n / BN));
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  k<<<grid, kThreads, C::kSmem, s>>>(ma, mb, a.a.scales, a.b.scales, a.a.tensor_scale, a.b.tensor_scale,
+                                     a.y, (int)a.m, (int)a.n, (int)a.k, static_cast<Workspace*>(a.ws),
+                                     timeout_ns, skip);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t run_gemm_ex(const GemmArgs& a, uint64_t timeout_ns, int skip_first_stage, cudaStream_t s) {
+  if (a.fmt != 0) return cudaErrorNotSupported;
+  const bool f32 = a.out_dtype == 1;
+  if (a.n % 256 == 0) return f32 ? launch<256, true>(a, timeout_ns, skip_first_stage, s)
+                                 : launch<256, false>(a, timeout_ns, skip_first_stage, s);
+  return f32 ? launch<128, true>(a, timeout_ns, skip_first_stage, s)
+             : launch<128, false>(a, timeout_ns, skip_first_stage, s);
+}
+
+cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
+  return run_gemm_ex(a, kDefaultTimeoutNs, 0, s);
+}
+
 }  // namespace fp4q

@@ -53,5 +53,9 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when no GEMM kernel covers the request.
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s);
+// run_gemm with an explicit bound on every wait and, when `skip_first_stage`,
+// the producer withholding the first stage of its first tile (so that the
+// bounded waits run out): the path that exercises the timeout handling.
+cudaError_t run_gemm_ex(const GemmArgs& a, uint64_t timeout_ns, int skip_first_stage, cudaStream_t s);
 
 }  // namespace fp4q

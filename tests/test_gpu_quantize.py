@@ -48,15 +48,18 @@ def check_copy(gq, oq, layout):
     assert ts == np.float32(oq["tensor_scale"]).view(np.uint32)
 
 
-def snr_tolerance_db(snr_db: float) -> float:
+def snr_error_bound(snr_db: float) -> float:
     """The kernel forms each error v - v_hat from FP32 values carrying at most
     three roundings (y = v * r_b, r_b = 1 / p, the product back), so each error
     is off by at most 3 * 2^-24 |v|. With S = sum v^2 / sum e^2 the error energy
-    is then off by a relative 6 * 2^-24 sqrt(S) + 9 * 2^-48 S; 1e-3 dB covers
-    the summation order."""
+    is then off by a relative 6 * 2^-24 sqrt(S) + 9 * 2^-48 S."""
     s = 10.0 ** (snr_db / 10.0)
-    rel = 6 * 2.0 ** -24 * np.sqrt(s) + 9 * 2.0 ** -48 * s
-    return 1e-3 + 10.0 * np.log10(1.0 + rel)
+    return 6 * 2.0 ** -24 * np.sqrt(s) + 9 * 2.0 ** -48 * s
+
+
+def snr_tolerance_db(snr_db: float) -> float:
+    """The bound above in dB, plus 1e-3 dB for the summation order."""
+    return 1e-3 + 10.0 * np.log10(1.0 + snr_error_bound(snr_db))
 
 
 def check_stats(gs, os_):
@@ -65,9 +68,13 @@ def check_stats(gs, os_):
     assert abs(gs["shrink_bias"] - os_["shrink_bias"]) <= tol, (gs, os_)
     if np.isinf(os_["snr_db"]):
         assert np.isinf(gs["snr_db"]) or gs["snr_db"] > 120
-    else:
+    elif snr_error_bound(os_["snr_db"]) < 1.0:
         tol_db = snr_tolerance_db(os_["snr_db"])
         assert abs(gs["snr_db"] - os_["snr_db"]) <= tol_db, (gs["snr_db"], os_["snr_db"], tol_db)
+    else:
+        # the error energy is below what FP32 arithmetic resolves: only the
+        # order of magnitude is meaningful
+        assert gs["snr_db"] > os_["snr_db"] - snr_tolerance_db(os_["snr_db"]) or np.isinf(gs["snr_db"])
 
 
 @pytest.mark.parametrize("layout", ["linear", "mma"])
