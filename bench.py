@@ -1,0 +1,628 @@
+#!/usr/bin/env python
+"""Throughput of the block-scaled FP4 quantisation path and of the NVFP4 GEMM
+on one B300 (or N, one process per GPU, each with its own copy of the work).
+
+Step (the unit the timed loop repeats): the activation-like 8192 x 4096 BF16
+tensor (Student-t nu = 3 times a per-column lognormal scale) quantised three
+ways -- E2M1/NVFP4 without the RHT, E2M1/NVFP4 with the 16-point RHT, uniform
+E1M2/UFP4 with the RHT -- 16-element blocks, RTNE, row-wise, statistics fused;
+then the UFP4 copy dequantised with the inverse RHT back to BF16 (UFP4 has no
+tensor-core format: a consumer dequantises it). Every quantisation is its
+amax pass followed by its quantisation pass, launched through the C ABI
+(fp4q_amax, fp4q_quantize with FP4Q_AMAX_READY) so that each pass can be timed.
+
+  value   algorithmic bytes of the step / step time, GB/s (whole job: all ranks)
+  e2e     the same bytes / the time of the same step through the Python binding
+          with the input in pinned host memory and every output copied back
+  gemm    quantise-then-GEMM at 8192^3 (A, B N(0, 1/8192) BF16 -> NVFP4 with the
+          RHT along K -> tcgen05 block-scaled GEMM -> BF16 Y), GEMM TFLOP/s
+  roofline   of the kernel that takes most of the step's time
+  cpu_baseline  the CPU oracle, as it stands, on a bounded sample of the step
+
+L2: the 64 MiB input fits the 126 MB L2, so a 256 MiB buffer is written between
+timed steps (outside the timed events); the GEMM leg's BF16 inputs (128 MiB
+each) exceed L2.
+
+--impl reference times the CPU oracle on the same step (a bounded sample per
+step) and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "quantize GB/s & % HBM peak; NVFP4 GEMM TFLOPS & % FP4 peak (1×B300)"
+ROWS, COLS = 8192, 4096
+SEED = 1234
+# (format, rht) of the three quantisations of the step
+WAYS = [("nvfp4", False), ("nvfp4", True), ("ufp4", True)]
+GEMM_N = 8192
+FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / BF16 tensor rate
+L2_FLUSH_BYTES = 256 << 20
+
+# algorithmic bytes per element (BF16 input): amax pass reads 2; the quantise
+# pass reads 2 and writes 0.5 of codes + 1/16 of E4M3 scales; the dequantise
+# pass reads 0.5 + 1/16 and writes 2.
+B_AMAX = 2.0
+B_QUANT = 2.0 + 0.5 + 1.0 / 16
+B_DEQ = 0.5 + 1.0 / 16 + 2.0
+STEP_BYTES_PER_EL = len(WAYS) * (B_AMAX + B_QUANT) + B_DEQ
+
+
+def step_bytes(rows: int, cols: int) -> float:
+    return STEP_BYTES_PER_EL * rows * cols
+
+
+def workload_config(extra=None) -> dict:
+    cfg = {"workload": "activation 8192x4096 BF16 (Student-t nu=3 x per-column lognormal), "
+                       "quantised E2M1 / E2M1+RHT16 / UFP4+RHT16, 16-element blocks, RTNE, "
+                       "row-wise, fused stats; UFP4 copy dequantised (inverse RHT) to BF16",
+           "shape": [ROWS, COLS], "input_dtype": "bf16", "seed": SEED,
+           "l2": "256 MiB buffer written between timed steps (input 64 MiB < L2)",
+           "parallelism": "replicas (one independent workload per GPU)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true",
+                   help="skip the CPU oracle leg (profiling runs)")
+    p.add_argument("--no-gemm", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    a = p.parse_args(argv)
+    if a.warmup < 3:
+        p.error("--warmup must be >= 3")
+    if a.steps < 1:
+        p.error("--steps must be >= 1")
+    return a
+
+
+# --------------------------------------------------------------------------- #
+# distributed plumbing (barrier + max over ranks; no data-path collective)     #
+# --------------------------------------------------------------------------- #
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(x: float, device) -> float:
+    """Max of a scalar over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def whole_job(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job throughput: the units every rank processed / the slowest rank's time."""
+    return units_per_rank * world / seconds_max if seconds_max > 0 else float("nan")
+
+
+# --------------------------------------------------------------------------- #
+# clocks during the timed region                                              #
+# --------------------------------------------------------------------------- #
+
+_REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of the SM clock and throttle reasons of one GPU."""
+
+    def __init__(self, gpu_id: str | None):
+        self.proc = None
+        self.err = None
+        if gpu_id is None:
+            self.err = "no GPU id"
+            return
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.err = f"nvidia-smi unavailable: {e}"
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return {"error": self.err}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return parse_clock_lines(out.splitlines())
+
+
+def parse_clock_lines(lines) -> dict:
+    sm, smax, power = [], [], []
+    seen = set()
+    for ln in lines:
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            smax.append(float(f[2]))
+            power.append(float(f[3]))
+        except ValueError:
+            continue
+        for name, val in zip(_REASONS, f[5:9]):
+            if val.lower() == "active":
+                seen.add(name)
+    if not sm:
+        return {"error": "no samples"}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+            "power_w_max": max(power), "reasons": sorted(seen)}
+
+
+def gpu_uuid(device) -> str | None:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[device.index] if vis else str(device.index)
+
+
+# --------------------------------------------------------------------------- #
+# peaks, traffic counters                                                      #
+# --------------------------------------------------------------------------- #
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", 0.0)),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0,
+                "source": "fallback"}
+
+
+def source_digest() -> str:
+    """Digest of the kernel sources: ncu counters apply only to the build they came from."""
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "fp4_block_scaled_05_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:12]
+
+
+def ncu_traffic(kernel: str, units: float) -> float | None:
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    summary, scaled by the elements (or FLOP) a launch processes here; None if
+    the counters were taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("source_digest") != source_digest():
+        return None
+    k = t.get("kernels", {}).get(kernel)
+    if not k:
+        return None
+    return float(k["dram_bytes"]) * units / float(k["units"])
+
+
+# --------------------------------------------------------------------------- #
+# the CPU oracle leg                                                           #
+# --------------------------------------------------------------------------- #
+
+def oracle_step(bits, seed: int = SEED) -> dict:
+    """One step of the path on the CPU oracle (test infrastructure; used only
+    for the baseline timing)."""
+    from oracle import fp4q_oracle as o
+    out = {}
+    for fmt, rht in WAYS:
+        out[(fmt, rht)] = o.quantize(bits, fmt, rht=rht, seed=seed)["row"]
+    u = out[("ufp4", True)]
+    o.dequantize(u["codes"], u["scales"], u["tensor_scale"], "ufp4", True, seed)
+    return out
+
+
+def time_oracle(rows: int, reps: int = 1) -> dict:
+    """CPU seconds and wall seconds of `reps` oracle steps on the first `rows`
+    rows of the activation tensor."""
+    import synth
+    x = synth.activation(ROWS, COLS)[:rows]
+    bits = synth.bf16_bits(x)
+    oracle_step(bits[:16])                       # imports, first-touch
+    c0, w0 = time.process_time(), time.perf_counter()
+    for _ in range(reps):
+        oracle_step(bits)
+    wall = time.perf_counter() - w0
+    cpu = time.process_time() - c0
+    return {"wall": wall, "cpu": cpu, "cores": max(1, round(cpu / wall)) if wall > 0 else 1}
+
+
+def cpu_baseline(sample_rows: int = 4096) -> dict:
+    t = time_oracle(sample_rows)
+    gbs = step_bytes(sample_rows, COLS) / t["wall"] / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": t["cores"], "kind": "oracle",
+            "sample": f"one step on the first {sample_rows} of {ROWS} rows "
+                      f"({sample_rows * COLS} elements; tensor amax over the sample), "
+                      f"{t['wall']:.2f} s wall, numpy"}
+
+
+def reference_arm(args) -> int:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    # each step is a bounded sample sized so the whole run stays near two minutes
+    probe = time_oracle(64)
+    per_row = probe["wall"] / 64
+    budget = 120.0 / (args.steps + args.warmup)
+    rows = int(max(16, min(ROWS, budget / per_row)) // 16 * 16)
+    import synth
+    from oracle import fp4q_oracle  # noqa: F401
+    bits = synth.bf16_bits(synth.activation(ROWS, COLS)[:rows])
+    for _ in range(args.warmup):
+        oracle_step(bits)
+    c0, w0 = time.process_time(), time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(bits)
+    wall = time.perf_counter() - w0
+    cpu = time.process_time() - c0
+    cores = max(1, round(cpu / wall)) if wall > 0 else 1
+    value = step_bytes(rows, COLS) * args.steps / wall / 1e9
+    sample = (f"each step on the first {rows} of {ROWS} rows ({rows * COLS} elements; "
+              f"tensor amax over the sample), numpy")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": workload_config({"sample_rows": rows}),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------- #
+# the GPU legs                                                                 #
+# --------------------------------------------------------------------------- #
+
+class RawCalls:
+    """Pre-marshalled C-ABI calls for the timed loop (the same entry points the
+    binding wraps, without per-call Python bookkeeping)."""
+
+    def __init__(self, fq, x, outs, deq_out, ws, stream: int):
+        import ctypes
+        self.fq = fq
+        self.lib = fq._lib
+        self.ws = ws
+        self.stream = stream
+        self.x = x
+        rows, cols = x.shape
+        self.calls = []
+        for (fmt, rht), q in zip(WAYS, outs):
+            s = q.c_struct()
+            self.calls.append((
+                (x.data_ptr(), 0, rows, cols, fq.FORMATS[fmt], fq.BLOCKS[fmt], int(rht), SEED, 1,
+                 ws.data_ptr(), ws.numel(), stream),
+                (x.data_ptr(), 0, rows, cols, fq.FORMATS[fmt], fq.BLOCKS[fmt], int(rht), 0, SEED,
+                 1 | 4, ctypes.byref(s), None, ws.data_ptr(), ws.numel(), stream),
+                s))
+        u = outs[-1]
+        self.deq_struct = u.c_struct()
+        self.deq_args = (ctypes.byref(self.deq_struct), rows, cols, fq.FORMATS["ufp4"], 16, 1, SEED,
+                         deq_out.data_ptr(), 0, stream)
+
+    def amax(self, i):
+        rc = self.lib.fp4q_amax(*self.calls[i][0])
+        if rc:
+            raise self.fq.FP4QError("fp4q_amax", rc)
+
+    def quant(self, i):
+        rc = self.lib.fp4q_quantize(*self.calls[i][1])
+        if rc:
+            raise self.fq.FP4QError("fp4q_quantize", rc)
+
+    def deq(self):
+        rc = self.lib.fp4q_dequantize(*self.deq_args)
+        if rc:
+            raise self.fq.FP4QError("fp4q_dequantize", rc)
+
+
+def run_main_leg(fq, torch, device, steps, warmup):
+    import synth
+    x = synth.activation(ROWS, COLS).to(device)
+    outs = [fq.alloc_copy(ROWS, COLS, fmt, "linear", device) for fmt, _ in WAYS]
+    deq_out = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=device)
+    ws = fq.workspace(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    raw = RawCalls(fq, x, outs, deq_out, ws, stream.cuda_stream)
+
+    def one_step(ev):
+        for i in range(len(WAYS)):
+            ev[3 * i].record(stream)
+            raw.amax(i)
+            ev[3 * i + 1].record(stream)
+            raw.quant(i)
+            ev[3 * i + 2].record(stream)
+        raw.deq()
+        ev[3 * len(WAYS)].record(stream)
+
+    nev = 3 * len(WAYS) + 1
+    for _ in range(warmup):
+        flush.zero_()
+        one_step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
+    torch.cuda.synchronize(device)
+    if fq.fp4q_status(ws) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(steps)]
+    barrier(device)
+    torch.cuda.synchronize(device)
+    w0 = time.perf_counter()
+    for k in range(steps):
+        flush.zero_()                    # L2 flush, outside the step's events
+        one_step(evs[k])
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - w0
+    barrier(device)
+
+    step_ms, amax_ms, quant_ms, deq_ms = [], [], [], []
+    for ev in evs:
+        step_ms.append(ev[0].elapsed_time(ev[nev - 1]))
+        for i in range(len(WAYS)):
+            amax_ms.append(ev[3 * i].elapsed_time(ev[3 * i + 1]))
+            quant_ms.append(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]))
+        deq_ms.append(ev[3 * len(WAYS) - 1].elapsed_time(ev[nev - 1]))
+    status = fq.fp4q_status(ws)
+    stats = {}
+    for (fmt, rht), q in zip(WAYS, outs):
+        fq.fp4q_amax(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws)
+        fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q,
+                         amax_ready=True)
+        rs, _ = fq.fp4q_stats(ws)
+        stats[f"{fmt}{'+rht' if rht else ''}"] = {"shrink_bias": rs["shrink_bias"],
+                                                  "snr_db": rs["snr_db"]}
+    return {"step_ms_total": sum(step_ms), "wall_s": wall, "amax_ms": amax_ms,
+            "quant_ms": quant_ms, "deq_ms": deq_ms, "status": status, "stats": stats,
+            "launches_per_step": 2 * len(WAYS) + 1}
+
+
+def run_e2e_leg(fq, torch, device, steps, warmup):
+    """The step through the public binding with host buffers: pinned BF16 input
+    copied in, every output (codes, scales, tensor scales, statistics, the
+    dequantised tensor) copied back, inside the timed region."""
+    import synth
+    x_host = synth.activation(ROWS, COLS).pin_memory()
+    x = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=device)
+    outs = [fq.alloc_copy(ROWS, COLS, fmt, "linear", device) for fmt, _ in WAYS]
+    hosts = [(torch.empty_like(q.codes, device="cpu").pin_memory(),
+              torch.empty_like(q.scales, device="cpu").pin_memory(),
+              torch.empty_like(q.tensor_scale, device="cpu").pin_memory()) for q in outs]
+    deq = torch.empty(ROWS, COLS, dtype=torch.bfloat16, device=device)
+    deq_host = torch.empty(ROWS, COLS, dtype=torch.bfloat16).pin_memory()
+    ws = fq.workspace(device)
+    stream = torch.cuda.current_stream(device)
+    h2d = x_host.numel() * 2
+    d2h = sum(c.numel() + s.numel() + 4 for c, s, _ in hosts) + deq_host.numel() * 2
+    stats_bytes = len(WAYS) * (2 * 5 * 8 + 4)     # fp4q_stats reads the sums + copy mask
+    d2h += stats_bytes
+
+    def one_step():
+        x.copy_(x_host, non_blocking=True)
+        for (fmt, rht), q, (hc, hs, ht) in zip(WAYS, outs, hosts):
+            fq.fp4q_amax(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws)
+            fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q,
+                             amax_ready=True)
+            fq.fp4q_stats(ws)
+            hc.copy_(q.codes, non_blocking=True)
+            hs.copy_(q.scales, non_blocking=True)
+            ht.copy_(q.tensor_scale, non_blocking=True)
+        fq.fp4q_dequantize(outs[-1], inverse_rht=True, seed=SEED, out=deq)
+        deq_host.copy_(deq, non_blocking=True)
+
+    for _ in range(warmup):
+        one_step()
+    torch.cuda.synchronize(device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    return {"ms": e0.elapsed_time(e1), "h2d": h2d, "d2h": d2h}
+
+
+def run_gemm_leg(fq, torch, device, steps, warmup):
+    """Quantise-then-GEMM at 8192^3: A, B N(0, 1/8192) BF16 -> NVFP4 (RHT along
+    K, tensor-core scale layout) -> Y = A B^T in BF16."""
+    import synth
+    n = GEMM_N
+    a = synth.gemm_operand("a", n, n).to(device)
+    b = synth.gemm_operand("b", n, n).to(device)
+    qa = fq.alloc_copy(n, n, "nvfp4", "mma", device)
+    qb = fq.alloc_copy(n, n, "nvfp4", "mma", device)
+    y = torch.empty(n, n, dtype=torch.bfloat16, device=device)
+    ws = fq.workspace(device)
+    stream = torch.cuda.current_stream(device)
+
+    def one(ev):
+        ev[0].record(stream)
+        for src, q in ((a, qa), (b, qb)):
+            fq.fp4q_amax(src, fmt="nvfp4", rht=True, seed=SEED, axis="row", ws=ws)
+            fq.fp4q_quantize(src, fmt="nvfp4", rht=True, seed=SEED, axis="row", layout="mma",
+                             ws=ws, row_out=q, amax_ready=True)
+        ev[1].record(stream)
+        fq.fp4q_gemm(qa, qb, out=y, ws=ws)
+        ev[2].record(stream)
+
+    for _ in range(warmup):
+        one([torch.cuda.Event(enable_timing=True) for _ in range(3)])
+    torch.cuda.synchronize(device)
+    if fq.fp4q_status(ws) != 0:
+        raise RuntimeError("device status set during the GEMM warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(device)
+    torch.cuda.synchronize(device)
+    for k in range(steps):
+        one(evs[k])
+    torch.cuda.synchronize(device)
+    barrier(device)
+    q_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    g_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    status = fq.fp4q_status(ws)
+    # SNR of Y against the BF16-input product on a sample of rows (FP64 on the device)
+    rows = torch.arange(0, n, 64, device=device)
+    ref = a[rows].double() @ b.double().T
+    got = y[rows].double()
+    snr = 10 * math.log10(float((ref * ref).sum()) / float(((got - ref) ** 2).sum()))
+    return {"quant_ms": q_ms, "gemm_ms": g_ms, "status": status, "snr_db_vs_bf16": snr}
+
+
+def main(argv=None) -> int:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    import fp4_block_scaled_05_b300 as fq     # fails loudly when libfp4q.so is missing
+
+    peaks = load_peaks()
+    sampler = ClockSampler(gpu_uuid(device))
+    main_r = run_main_leg(fq, torch, device, args.steps, args.warmup)
+    gemm_r = None if args.no_gemm else run_gemm_leg(fq, torch, device, args.steps, args.warmup)
+    e2e_steps = min(args.steps, 100)
+    e2e_r = None if args.no_e2e else run_e2e_leg(fq, torch, device, e2e_steps, args.warmup)
+    clocks = sampler.stop()
+
+    n_el = ROWS * COLS
+    t_step = reduce_max(main_r["step_ms_total"] / 1e3, device)
+    value = whole_job(step_bytes(ROWS, COLS) * args.steps, t_step, world) / 1e9
+    ms_per_step = t_step / args.steps * 1e3
+
+    # per-kernel averages over the timed region
+    kern = {
+        "amax": {"ms": statistics.fmean(main_r["amax_ms"]), "bytes": B_AMAX * n_el,
+                 "launches": len(main_r["amax_ms"]), "ncu_name": "amax_kernel"},
+        "quantize": {"ms": statistics.fmean(main_r["quant_ms"]), "bytes": B_QUANT * n_el,
+                     "launches": len(main_r["quant_ms"]), "ncu_name": "quantize_kernel"},
+        "dequantize": {"ms": statistics.fmean(main_r["deq_ms"]), "bytes": B_DEQ * n_el,
+                       "launches": len(main_r["deq_ms"]), "ncu_name": "dequantize_kernel"},
+    }
+    for k in kern.values():
+        k["gbs"] = k["bytes"] / (k["ms"] / 1e3) / 1e9
+        k["frac"] = k["gbs"] / peaks["hbm_gbs"]
+        k["total_ms"] = k["ms"] * k["launches"]
+    dom_name = max(kern, key=lambda n: kern[n]["total_ms"])
+    dom = kern[dom_name]
+    roofline = {"kernel": dom_name, "bound": "hbm", "achieved": dom["gbs"],
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dom["frac"],
+                "peak_source": f"{peaks['source']} (copy bandwidth)",
+                "traffic": ncu_traffic(dom["ncu_name"], n_el),
+                "algorithmic_bytes_per_launch": dom["bytes"]}
+
+    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": workload_config(),
+            "roofline": roofline,
+            "kernels": {n: {"avg_us": k["ms"] * 1e3, "GB/s": k["gbs"], "frac_hbm": k["frac"],
+                            "launches": k["launches"]} for n, k in kern.items()},
+            "gpu_launches": main_r["launches_per_step"] * args.steps,
+            "stats": main_r["stats"], "device_status": main_r["status"],
+            "wall_s_timed_region": main_r["wall_s"]}
+
+    if e2e_r is not None:
+        t_e2e = reduce_max(e2e_r["ms"] / 1e3, device)
+        line["e2e"] = {"value": whole_job(step_bytes(ROWS, COLS) * e2e_steps, t_e2e, world) / 1e9,
+                       "unit": "GB/s", "h2d_bytes_per_step": e2e_r["h2d"],
+                       "d2h_bytes_per_step": e2e_r["d2h"], "steps": e2e_steps}
+    if gemm_r is not None:
+        flop = 2.0 * GEMM_N ** 3
+        g_avg = statistics.fmean(gemm_r["gemm_ms"])
+        g_max = reduce_max(sum(gemm_r["gemm_ms"]) / 1e3, device)
+        tflops = flop / (g_avg / 1e3) / 1e12
+        fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        q_avg = statistics.fmean(gemm_r["quant_ms"])
+        line["gemm"] = {
+            "workload": "A, B 8192x8192 BF16 N(0,1/8192) -> NVFP4 + RHT16 along K (E4M3 block "
+                        "scales, FP32 tensor scale) -> tcgen05 block-scaled GEMM, FP32 "
+                        "accumulate, BF16 Y = A B^T",
+            "tflops": tflops, "whole_job_tflops": whole_job(flop * args.steps, g_max, world) / 1e12,
+            "avg_us": g_avg * 1e3, "launches": len(gemm_r["gemm_ms"]),
+            "quantize_A_and_B_us": q_avg * 1e3,
+            "quantize_A_and_B_GB/s": 2 * (B_AMAX + B_QUANT) * GEMM_N * GEMM_N / (q_avg / 1e3) / 1e9,
+            "pipeline_tflops": flop / ((g_avg + q_avg) / 1e3) / 1e12,
+            "snr_db_vs_bf16_product": gemm_r["snr_db_vs_bf16"],
+            "device_status": gemm_r["status"],
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": fp4_peak,
+                         "unit": "TFLOP/s", "frac": tflops / fp4_peak,
+                         "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} "
+                                        "(nominal dense FP4/BF16 ratio)",
+                         "traffic": ncu_traffic("gemm_nvf4_kernel", flop)},
+        }
+        line["gpu_launches_gemm_leg"] = 5 * args.steps
+    line["clocks"] = clocks
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

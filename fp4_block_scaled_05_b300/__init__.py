@@ -5,7 +5,7 @@ stream; every step of the computation runs in the library's sm_103a kernels
 through its C ABI (include/fp4q.h). There is no CPU path: if the shared library
 is missing, importing this package fails.
 
-Function names follow the C ABI: fp4q_quantize, fp4q_dequantize, fp4q_stats,
+Function names follow the C ABI: fp4q_amax, fp4q_quantize, fp4q_dequantize, fp4q_stats,
 fp4q_status, fp4q_gemm, fp4q_workspace_size, fp4q_workspace_init,
 fp4q_scales_bytes, fp4q_strerror, fp4q_version.
 """
@@ -58,6 +58,7 @@ _SIGS = {
     "fp4q_workspace_size": ([], _SZ),
     "fp4q_workspace_init": ([_P, _P], _I),
     "fp4q_scales_bytes": ([_I64, _I64, _I, _I], _SZ),
+    "fp4q_amax": ([_P, _I, _I64, _I64, _I, _I, _I, ctypes.c_uint64, _I, _P, _SZ, _P], _I),
     "fp4q_quantize": ([_P, _I, _I64, _I64, _I, _I, _I, _I, ctypes.c_uint64, _I, _QP, _QP, _P, _SZ, _P], _I),
     "fp4q_dequantize": ([_QP, _I64, _I64, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], _I),
     "fp4q_stats": ([_P, _SP, _SP, _P], _I),
@@ -156,15 +157,33 @@ def alloc_copy(rows: int, cols: int, fmt: str, layout: str = "linear", device=No
     return QCopy(codes, scales, ts, fmt, rows, cols, layout)
 
 
-def fp4q_quantize(x: torch.Tensor, fmt: str = "nvfp4", rht: bool = False, rounding: str = "rtne",
-                  seed: int = 0, axis: str = "row", layout: str = "linear", ws: torch.Tensor = None,
-                  row_out: QCopy = None, col_out: QCopy = None):
-    """Quantise a 2-D BF16/FP32 CUDA tensor. Returns (row_copy, col_copy); the
-    copy not requested is None. The column-wise copy is the transposed matrix
-    (cols x rows)."""
+def _check_src(x: torch.Tensor) -> torch.Tensor:
     if x.dim() != 2 or not x.is_cuda or x.dtype not in DTYPES:
         raise ValueError("x must be a 2-D BF16 or FP32 CUDA tensor")
-    x = x.contiguous()
+    return x.contiguous()
+
+
+def fp4q_amax(x: torch.Tensor, fmt: str = "nvfp4", rht: bool = False, seed: int = 0,
+              axis: str = "row", ws: torch.Tensor = None) -> None:
+    """Record the tensor amax of the requested copies of ``x`` in ``ws`` (the
+    first pass of fp4q_quantize); follow with fp4q_quantize(..., amax_ready=True)."""
+    x = _check_src(x)
+    if ws is None:
+        ws = workspace(x.device)
+    rows, cols = x.shape
+    rc = _lib.fp4q_amax(x.data_ptr(), DTYPES[x.dtype], rows, cols, FORMATS[fmt], BLOCKS[fmt],
+                        int(bool(rht)), seed & 0xFFFFFFFFFFFFFFFF, AXES[axis], ws.data_ptr(),
+                        ws.numel(), _stream(x.device))
+    _check("fp4q_amax", rc)
+
+
+def fp4q_quantize(x: torch.Tensor, fmt: str = "nvfp4", rht: bool = False, rounding: str = "rtne",
+                  seed: int = 0, axis: str = "row", layout: str = "linear", ws: torch.Tensor = None,
+                  row_out: QCopy = None, col_out: QCopy = None, amax_ready: bool = False):
+    """Quantise a 2-D BF16/FP32 CUDA tensor. Returns (row_copy, col_copy); the
+    copy not requested is None. The column-wise copy is the transposed matrix
+    (cols x rows). ``amax_ready``: the amax pass already ran (fp4q_amax)."""
+    x = _check_src(x)
     rows, cols = x.shape
     ax = AXES[axis]
     if ws is None:
@@ -176,7 +195,8 @@ def fp4q_quantize(x: torch.Tensor, fmt: str = "nvfp4", rht: bool = False, roundi
     rs = row_out.c_struct() if ax & 1 else None
     cs = col_out.c_struct() if ax & 2 else None
     rc = _lib.fp4q_quantize(x.data_ptr(), DTYPES[x.dtype], rows, cols, FORMATS[fmt], BLOCKS[fmt],
-                            int(bool(rht)), ROUNDING[rounding], seed & 0xFFFFFFFFFFFFFFFF, ax,
+                            int(bool(rht)), ROUNDING[rounding], seed & 0xFFFFFFFFFFFFFFFF,
+                            ax | (4 if amax_ready else 0),
                             ctypes.byref(rs) if rs is not None else None,
                             ctypes.byref(cs) if cs is not None else None,
                             ws.data_ptr(), ws.numel(), _stream(x.device))

@@ -95,6 +95,24 @@ fp4q::QOut to_qout(const fp4q_qtensor* q) {
 
 bool needs_padding(int64_t rows, int64_t nkb) { return (rows % 128) != 0 || (nkb % 4) != 0; }
 
+// Checks shared by fp4q_quantize and fp4q_amax (axis without the flag bits).
+int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block,
+                 int rht, int axis, const void* workspace, size_t ws_bytes) {
+  int rc = check_format(fmt, block);
+  if (rc) return rc;
+  if (dtype != FP4Q_BF16 && dtype != FP4Q_F32) return FP4Q_EINVAL;
+  if (rht != 0 && rht != 1) return FP4Q_EINVAL;
+  if (axis < 1 || axis > 3) return FP4Q_EINVAL;
+  if (rows < 0 || cols < 0) return FP4Q_EINVAL;
+  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40) || (rows && cols > (int64_t(1) << 46) / rows))
+    return FP4Q_EINVAL;
+  if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
+  if (rows && cols && (!src || !aligned(src, 16))) return FP4Q_EINVAL;
+  if ((axis & FP4Q_ROWWISE) && cols % block) return FP4Q_EINVAL;
+  if ((axis & FP4Q_COLWISE) && rows % block) return FP4Q_EINVAL;
+  return FP4Q_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -117,29 +135,36 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout
   return (size_t)rows * (size_t)nkb;
 }
 
+int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block, int rht,
+              uint64_t seed, int axis, void* workspace, size_t ws_bytes, void* stream) {
+  const int rc = check_source(src, dtype, rows, cols, fmt, block, rht, axis, workspace, ws_bytes);
+  if (rc) return rc;
+  if (fmt == FP4Q_MXFP4) return FP4Q_OK;   // power-of-two block scales only: no tensor amax
+  fp4q::QuantArgs a{};
+  a.src = src;
+  a.dtype = dtype;
+  a.rows = rows;
+  a.cols = cols;
+  a.fmt = fmt;
+  a.rht = rht;
+  a.seed = seed;
+  a.axis = axis;
+  a.ws = workspace;
+  return fp4q::run_amax(a, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+}
+
 int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block,
                   int rht, int rounding, uint64_t seed, int axis, const fp4q_qtensor* row_out,
                   const fp4q_qtensor* col_out, void* workspace, size_t ws_bytes, void* stream) {
-  int rc = check_format(fmt, block);
+  if (axis & ~(FP4Q_ROWWISE | FP4Q_COLWISE | FP4Q_AMAX_READY)) return FP4Q_EINVAL;
+  const int amax_ready = (axis & FP4Q_AMAX_READY) ? 1 : 0;
+  axis &= FP4Q_ROWWISE | FP4Q_COLWISE;
+  int rc = check_source(src, dtype, rows, cols, fmt, block, rht, axis, workspace, ws_bytes);
   if (rc) return rc;
-  if (dtype != FP4Q_BF16 && dtype != FP4Q_F32) return FP4Q_EINVAL;
-  if (rht != 0 && rht != 1) return FP4Q_EINVAL;
   if (rounding != FP4Q_RTNE && rounding != FP4Q_SR) return FP4Q_EINVAL;
-  if (axis < 1 || axis > 3) return FP4Q_EINVAL;
-  if (rows < 0 || cols < 0) return FP4Q_EINVAL;
-  if (rows > (int64_t(1) << 40) || cols > (int64_t(1) << 40) || (rows && cols > (int64_t(1) << 46) / rows))
-    return FP4Q_EINVAL;
-  if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
-  if (rows && cols && (!src || !aligned(src, 16))) return FP4Q_EINVAL;
   const bool empty = rows == 0 || cols == 0;
-  if (axis & FP4Q_ROWWISE) {
-    if ((rc = check_qtensor(row_out, empty))) return rc;
-    if (cols % block) return FP4Q_EINVAL;
-  }
-  if (axis & FP4Q_COLWISE) {
-    if ((rc = check_qtensor(col_out, empty))) return rc;
-    if (rows % block) return FP4Q_EINVAL;
-  }
+  if ((axis & FP4Q_ROWWISE) && (rc = check_qtensor(row_out, empty))) return rc;
+  if ((axis & FP4Q_COLWISE) && (rc = check_qtensor(col_out, empty))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   // padding bytes of the tiled scale layout are defined as 0
   if (!empty && (axis & FP4Q_ROWWISE) && row_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(rows, cols / block)) {
@@ -163,6 +188,7 @@ int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols, int fm
   a.row = to_qout((axis & FP4Q_ROWWISE) ? row_out : nullptr);
   a.col = to_qout((axis & FP4Q_COLWISE) ? col_out : nullptr);
   a.ws = workspace;
+  a.amax_ready = amax_ready;
   return fp4q::run_quantize(a, s) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
 }
 

@@ -23,6 +23,7 @@ struct QuantArgs {
   int axis;           // bit 0 row-wise, bit 1 column-wise
   QOut row, col;
   void* ws;
+  int amax_ready;     // 1: the tensor amax already sits in the workspace (skip K1)
 };
 
 struct DequantArgs {
@@ -50,6 +51,8 @@ int sm_count();
 int cached_occupancy(const void* kernel, int threads, int smem);
 
 cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s);
+// K1 alone: the tensor amax of the requested copies, recorded in the workspace.
+cudaError_t run_amax(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when no GEMM kernel covers the request.
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s);

@@ -724,25 +724,47 @@ __global__ void quantize_empty_kernel(int fmt, int axis, float* ts_row, float* t
   if ((axis & 2) && ts_col) *ts_col = g;
 }
 
-cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
-  if (a.rows == 0 || a.cols == 0) {
-    quantize_empty_kernel<<<1, 1, 0, s>>>(a.fmt, a.axis, a.row.tensor_scale, a.col.tensor_scale,
-                                          static_cast<Workspace*>(a.ws));
-    return cudaGetLastError();
-  }
+static Geom make_geom(const QuantArgs& a) {
   Geom g{};
   g.src = a.src;
   g.rows = a.rows;
   g.cols = a.cols;
   g.ntc = (a.cols + TC - 1) / TC;
   g.ntiles = ((a.rows + TR - 1) / TR) * g.ntc;
+  return g;
+}
+
+// Empty input: a zero amax for both copies.
+__global__ void amax_empty_kernel(Workspace* ws) {
+  ws->amax_bits[0] = 0u;
+  ws->amax_bits[1] = 0u;
+}
+
+cudaError_t run_amax(const QuantArgs& a, cudaStream_t s) {
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  if (a.rows == 0 || a.cols == 0) {
+    amax_empty_kernel<<<1, 1, 0, s>>>(ws);
+    return cudaGetLastError();
+  }
+  const Geom g = make_geom(a);
+  return a.dtype == 1 ? dispatch_amax<true>(a.rht, a.axis, g, a.seed, ws, s)
+                      : dispatch_amax<false>(a.rht, a.axis, g, a.seed, ws, s);
+}
+
+cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
+  if (a.rows == 0 || a.cols == 0) {
+    quantize_empty_kernel<<<1, 1, 0, s>>>(a.fmt, a.axis, a.row.tensor_scale, a.col.tensor_scale,
+                                          static_cast<Workspace*>(a.ws));
+    return cudaGetLastError();
+  }
+  const Geom g = make_geom(a);
   const int block = a.fmt == 1 ? 32 : 16;
   const CopyOut r = make_copy(a.row, a.rows, a.cols, block);
   const CopyOut c = make_copy(a.col, a.cols, a.rows, block);
   Workspace* ws = static_cast<Workspace*>(a.ws);
   cudaError_t e = cudaSuccess;
   const bool f32 = a.dtype == 1;
-  if (a.fmt != 1) {
+  if (a.fmt != 1 && !a.amax_ready) {
     e = f32 ? dispatch_amax<true>(a.rht, a.axis, g, a.seed, ws, s)
             : dispatch_amax<false>(a.rht, a.axis, g, a.seed, ws, s);
     if (e != cudaSuccess) return e;

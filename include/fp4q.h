@@ -56,6 +56,10 @@ typedef enum { FP4Q_RTNE = 0, FP4Q_SR = 1 } fp4q_rounding;
 typedef enum { FP4Q_BF16 = 0, FP4Q_F32 = 1 } fp4q_dtype;
 
 enum { FP4Q_ROWWISE = 1, FP4Q_COLWISE = 2 };            /* axis bit mask            */
+/* Flag OR-ed into fp4q_quantize's `axis`: the tensor amax was already recorded
+ * in the workspace by fp4q_amax (same src, shape, fmt, rht, seed and axis
+ * bits), so the call runs the quantisation pass alone. */
+enum { FP4Q_AMAX_READY = 4 };
 enum { FP4Q_SCALES_LINEAR = 0, FP4Q_SCALES_MMA = 1 };   /* block-scale byte layout  */
 
 enum {
@@ -126,6 +130,18 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout
 
 /* ---- quantisation ------------------------------------------------------------ */
 
+/* The first of fp4q_quantize's two passes on its own: the tensor amax A of
+ * each requested copy (max |v| over the copy, v after the RHT when `rht`),
+ * which sets the FP32 tensor scale g = A / (Qmax * 448) of NVFP4 and UFP4
+ * ([TJ2] Riepilogo Tecnico §2A: NVFP4 block scales under a per-tensor scale).
+ * The amaxes are recorded in `workspace`; a following fp4q_quantize call on
+ * the same workspace with FP4Q_AMAX_READY in its `axis` then skips this pass.
+ * Splitting the call lets a caller time or schedule the two passes apart.
+ * MXFP4 has no tensor scale: the call validates its arguments and launches
+ * nothing. Arguments and errors as for fp4q_quantize (no outputs). */
+int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block,
+              int rht, uint64_t seed, int axis, void* workspace, size_t ws_bytes, void* stream);
+
 /* Quantise a rows x cols tensor into block-scaled 4-bit copies.
  *
  * Operation (per copy; [UFP4] Metodologia §1-2, Eficiencia; [TJ2] §2A, §2C;
@@ -154,7 +170,8 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout
  *   axis         FP4Q_ROWWISE: blocks along rows, copy row_out (rows x cols).
  *                FP4Q_COLWISE: blocks along columns, emitted transposed into
  *                col_out (cols x rows: codes cols x rows/2, scales per column).
- *                Both bits: both copies from one read of src.
+ *                Both bits: both copies from one read of src. May also carry
+ *                FP4Q_AMAX_READY (see fp4q_amax).
  *   row_out, col_out  host pointers to fp4q_qtensor descriptors of device
  *                buffers; the one whose axis bit is clear may be NULL. codes
  *                must be 16-byte aligned; MMA-layout scales 16-byte aligned.

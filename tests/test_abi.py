@@ -18,8 +18,8 @@ def _declared():
 
 @pytest.fixture(scope="module")
 def so():
-    from fp4_block_scaled_05_b300 import _build
-    path = _build.build()
+    import __graft_entry__
+    path = __graft_entry__._load_builder().build()
     return ctypes.CDLL(path)
 
 
@@ -66,3 +66,30 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, 16, None) == 1
     assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1  # row_out NULL
     assert q(fake, 0, -1, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+
+
+def test_amax_validation_without_gpu(so):
+    so.fp4q_workspace_size.restype = ctypes.c_size_t
+    ws_size = so.fp4q_workspace_size()
+    a = so.fp4q_amax
+    a.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_size_t, ctypes.c_void_p]
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
+    assert a(fake, 0, 16, 16, 7, 16, 0, 0, 1, fake, ws_size, None) == 1      # format
+    assert a(fake, 0, 16, 16, 0, 32, 0, 0, 1, fake, ws_size, None) == 2      # block
+    assert a(fake, 0, 16, 24, 0, 16, 0, 0, 1, fake, ws_size, None) == 1      # cols % 16
+    assert a(fake, 0, 24, 16, 0, 16, 0, 0, 2, fake, ws_size, None) == 1      # rows % 16
+    assert a(fake, 0, 16, 16, 0, 16, 2, 0, 1, fake, ws_size, None) == 1      # rht flag
+    assert a(fake, 0, 16, 16, 0, 16, 0, 0, 4, fake, ws_size, None) == 1      # no copy requested
+    assert a(fake, 0, 16, 16, 0, 16, 0, 0, 1, fake, 8, None) == 1            # workspace size
+    assert a(None, 0, 16, 16, 0, 16, 0, 0, 1, fake, ws_size, None) == 1      # null source
+    # MXFP4 has no tensor amax: valid arguments launch nothing and succeed
+    assert a(fake, 0, 32, 32, 1, 32, 0, 0, 3, fake, ws_size, None) == 0
+    q = so.fp4q_quantize
+    q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    # unknown flag bits and the ready flag without a copy are rejected
+    assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 9, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 4, None, None, fake, ws_size, None) == 1

@@ -246,3 +246,22 @@ def test_repeated_calls_reuse_workspace(lib):
         check_copy(r, ref["row"], "linear")
         check_copy(c, ref["col"], "linear")
         check_stats(cs, ref["col"]["stats"])
+
+
+@pytest.mark.parametrize("fmt,rht,axis", [("nvfp4", False, "row"), ("nvfp4", True, "both"),
+                                          ("ufp4", True, "col"), ("mxfp4", True, "both")])
+def test_split_amax_then_quantize(lib, fmt, rht, axis):
+    """fp4q_amax followed by fp4q_quantize(amax_ready) equals one fp4q_quantize
+    call and the oracle, byte for byte."""
+    x = _input(fmt, torch.bfloat16, seed=13)
+    xd = x.cuda()
+    lib.fp4q_amax(xd, fmt=fmt, rht=rht, seed=99, axis=axis)
+    r, c = lib.fp4q_quantize(xd, fmt=fmt, rht=rht, seed=99, axis=axis, amax_ready=True)
+    rs, cs = lib.fp4q_stats()
+    ref = o.quantize(_bits(x), fmt, rht=rht, seed=99, axis=axis)
+    if axis in ("row", "both"):
+        check_copy(r, ref["row"], "linear")
+        check_stats(rs, ref["row"]["stats"])
+    if axis in ("col", "both"):
+        check_copy(c, ref["col"], "linear")
+        check_stats(cs, ref["col"]["stats"])
