@@ -6,7 +6,7 @@ through its C ABI (include/fp4q.h). There is no CPU path: if the shared library
 is missing, importing this package fails.
 
 Function names follow the C ABI: fp4q_amax, fp4q_quantize, fp4q_dequantize, fp4q_stats,
-fp4q_status, fp4q_gemm, fp4q_workspace_size, fp4q_workspace_init,
+fp4q_status, fp4q_gemm, fp4q_quantize_noalloc, fp4q_workspace_size, fp4q_workspace_init,
 fp4q_scales_bytes, fp4q_strerror, fp4q_version.
 """
 from __future__ import annotations
@@ -60,6 +60,7 @@ _SIGS = {
     "fp4q_scales_bytes": ([_I64, _I64, _I, _I], _SZ),
     "fp4q_amax": ([_P, _I, _I64, _I64, _I, _I, _I, ctypes.c_uint64, _I, _P, _SZ, _P], _I),
     "fp4q_quantize": ([_P, _I, _I64, _I64, _I, _I, _I, _I, ctypes.c_uint64, _I, _QP, _QP, _P, _SZ, _P], _I),
+    "fp4q_quantize_noalloc": ([_P, _I, _I64, _I64, _I, _I, _I, _I, ctypes.c_uint64, _I, _QP, _QP, _P], _I),
     "fp4q_dequantize": ([_QP, _I64, _I64, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], _I),
     "fp4q_stats": ([_P, _SP, _SP, _P], _I),
     "fp4q_status": ([_P, _P], _I),
@@ -201,6 +202,32 @@ def fp4q_quantize(x: torch.Tensor, fmt: str = "nvfp4", rht: bool = False, roundi
                             ctypes.byref(cs) if cs is not None else None,
                             ws.data_ptr(), ws.numel(), _stream(x.device))
     _check("fp4q_quantize", rc)
+    return (row_out if ax & 1 else None), (col_out if ax & 2 else None)
+
+
+def fp4q_quantize_noalloc(x: torch.Tensor, fmt: str = "nvfp4", rht: bool = False,
+                          rounding: str = "rtne", seed: int = 0, axis: str = "row",
+                          row_out: QCopy = None, col_out: QCopy = None, layout: str = "linear"):
+    """fp4q_quantize for callers that cannot allocate device memory: the C call
+    uses scratch inside the library instead of a workspace (its statistics are
+    not readable). Pass preallocated row_out / col_out to allocate nothing here
+    either. Calls that overlap on the GPU race on that shared scratch."""
+    x = _check_src(x)
+    rows, cols = x.shape
+    ax = AXES[axis]
+    if (ax & 1) and row_out is None:
+        row_out = alloc_copy(rows, cols, fmt, layout, x.device)
+    if (ax & 2) and col_out is None:
+        col_out = alloc_copy(cols, rows, fmt, layout, x.device)
+    rs = row_out.c_struct() if ax & 1 else None
+    cs = col_out.c_struct() if ax & 2 else None
+    rc = _lib.fp4q_quantize_noalloc(x.data_ptr(), DTYPES[x.dtype], rows, cols, FORMATS[fmt],
+                                    BLOCKS[fmt], int(bool(rht)), ROUNDING[rounding],
+                                    seed & 0xFFFFFFFFFFFFFFFF, ax,
+                                    ctypes.byref(rs) if rs is not None else None,
+                                    ctypes.byref(cs) if cs is not None else None,
+                                    _stream(x.device))
+    _check("fp4q_quantize_noalloc", rc)
     return (row_out if ax & 1 else None), (col_out if ax & 2 else None)
 
 

@@ -184,6 +184,34 @@ int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols,
                   const fp4q_qtensor* row_out, const fp4q_qtensor* col_out,
                   void* workspace, size_t ws_bytes, void* stream);
 
+/* fp4q_quantize without a workspace argument, for callers that cannot
+ * allocate device memory: runtimes and plugins that must live inside a memory
+ * pool fixed at start-up, or latency-critical code that cannot afford
+ * cudaMalloc/cudaFree, which may synchronise the whole device. The method
+ * pages have no counterpart: this is a calling convention, not a step of the
+ * method.
+ *
+ * The scratch the two quantisation passes need lives in a 128 KiB array
+ * (`static __device__`) inside the library, which every GPU that loads the
+ * library holds until the process exits. The call itself allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine); the caller still
+ * allocates src and the output buffers. The first call on each device looks
+ * up the array's device address (cudaGetSymbolAddress) with that device
+ * current, so make that first call before any stream capture. Every call
+ * clears the status word and the counters of the array, then runs exactly
+ * what fp4q_quantize runs; the statistics and status it records stay in the
+ * array and are not readable (use fp4q_quantize with a workspace for them).
+ * All calls on a device share the one array: calls that overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.
+ * Arguments, outputs and errors as for fp4q_quantize, except that
+ * FP4Q_AMAX_READY is rejected (FP4Q_EINVAL: there is no workspace to carry
+ * an earlier fp4q_amax result), and FP4Q_EINVAL if the library's scratch
+ * requirement (fp4q_workspace_size()) exceeds the 128 KiB array. */
+int fp4q_quantize_noalloc(const void* src, int dtype, int64_t rows, int64_t cols,
+                          int fmt, int block, int rht, int rounding, uint64_t seed, int axis,
+                          const fp4q_qtensor* row_out, const fp4q_qtensor* col_out,
+                          void* stream);
+
 /* Dequantise one copy ([UFP4] §2: UFP4 has no tensor-core format and is
  * consumed through this call): v_hat = (level * s_b) * g in FP32, two
  * round-to-nearest products in that order (MXFP4: level * 2^e_b); if
