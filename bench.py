@@ -86,6 +86,10 @@ def parse_args(argv=None):
                    help="skip the CPU oracle leg (profiling runs)")
     p.add_argument("--no-gemm", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="instead of the step: the size sweep (R x 4096 BF16 N(0,1), R = 2^8..2^18), "
+                        "MXFP4 vs NVFP4 quantisation GB/s per size, one JSON line per size")
+    p.add_argument("--sweep-max-rows", type=int, default=1 << 18)
     a = p.parse_args(argv)
     if a.warmup < 3:
         p.error("--warmup must be >= 3")
@@ -377,6 +381,7 @@ def run_main_leg(fq, torch, device, steps, warmup):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     raw = RawCalls(fq, x, outs, deq_out, ws, stream.cuda_stream)
+    x_ref = x.clone()
 
     def one_step(ev):
         for i in range(len(WAYS)):
@@ -415,17 +420,25 @@ def run_main_leg(fq, torch, device, steps, warmup):
             quant_ms.append(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]))
         deq_ms.append(ev[3 * len(WAYS) - 1].elapsed_time(ev[nev - 1]))
     status = fq.fp4q_status(ws)
-    stats = {}
+    # self-checks outside the timed region: the input is intact, and the
+    # statistics of a repeated quantisation are identical (no state leaks
+    # from one call into the next)
+    checks = {"input_unchanged": bool(torch.equal(x, x_ref))}
+    stats, repeat_same = {}, True
     for (fmt, rht), q in zip(WAYS, outs):
-        fq.fp4q_amax(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws)
-        fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q,
-                         amax_ready=True)
-        rs, _ = fq.fp4q_stats(ws)
-        stats[f"{fmt}{'+rht' if rht else ''}"] = {"shrink_bias": rs["shrink_bias"],
-                                                  "snr_db": rs["snr_db"]}
+        seen = []
+        for _ in range(2):
+            fq.fp4q_amax(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws)
+            fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q,
+                             amax_ready=True)
+            rs, _ = fq.fp4q_stats(ws)
+            seen.append((rs["shrink_bias"], rs["snr_db"]))
+        repeat_same &= seen[0] == seen[1]
+        stats[f"{fmt}{'+rht' if rht else ''}"] = {"shrink_bias": seen[0][0], "snr_db": seen[0][1]}
+    checks["stats_repeatable"] = bool(repeat_same)
     return {"step_ms_total": sum(step_ms), "wall_s": wall, "amax_ms": amax_ms,
             "quant_ms": quant_ms, "deq_ms": deq_ms, "status": status, "stats": stats,
-            "launches_per_step": 2 * len(WAYS) + 1}
+            "checks": checks, "launches_per_step": 2 * len(WAYS) + 1}
 
 
 def run_e2e_leg(fq, torch, device, steps, warmup):
@@ -523,6 +536,51 @@ def run_gemm_leg(fq, torch, device, steps, warmup):
     return {"quant_ms": q_ms, "gemm_ms": g_ms, "status": status, "snr_db_vs_bf16": snr}
 
 
+def run_sweep(fq, torch, device, args, peaks) -> None:
+    """MXFP4 (32-element E8M0 blocks, one pass) vs NVFP4 (16-element E4M3
+    blocks, amax pass + quantisation pass) on R x 4096 N(0,1) BF16 tensors,
+    RTNE, no RHT, row-wise: time per call and GB/s of algorithmic bytes."""
+    import synth
+    cols = 4096
+    ws = fq.workspace(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    rows_list = [r for r in synth.sweep_rows() if r <= args.sweep_max_rows]
+    x_full = synth.sweep(max(rows_list), cols).to(device)
+    for rows in rows_list:
+        x = x_full[:rows]
+        n = rows * cols
+        out = {}
+        for fmt in ("mxfp4", "nvfp4"):
+            q = fq.alloc_copy(rows, cols, fmt, "linear", device)
+            times = {"amax": [], "quant": []}
+            for k in range(args.warmup + args.steps):
+                flush.zero_()
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
+                fq.fp4q_amax(x, fmt=fmt, ws=ws)
+                e1.record(stream)
+                fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q, amax_ready=True)
+                e2.record(stream)
+                if k >= args.warmup:
+                    times["amax"].append((e0, e1))
+                    times["quant"].append((e1, e2))
+            torch.cuda.synchronize(device)
+            t_a = statistics.median(a.elapsed_time(b) for a, b in times["amax"]) if fmt == "nvfp4" else 0.0
+            t_q = statistics.median(a.elapsed_time(b) for a, b in times["quant"])
+            b_q = (2.0 + 0.5 + (1.0 / 16 if fmt == "nvfp4" else 1.0 / 32)) * n
+            b_a = 2.0 * n if fmt == "nvfp4" else 0.0
+            out[fmt] = {"call_us": (t_a + t_q) * 1e3, "call_GB/s": (b_a + b_q) / ((t_a + t_q) / 1e3) / 1e9,
+                        "quant_us": t_q * 1e3, "quant_GB/s": b_q / (t_q / 1e3) / 1e9,
+                        "quant_frac_hbm": b_q / (t_q / 1e3) / 1e9 / peaks["hbm_gbs"]}
+            if fmt == "nvfp4":
+                out[fmt].update({"amax_us": t_a * 1e3, "amax_GB/s": b_a / (t_a / 1e3) / 1e9})
+            del q
+        print(json.dumps({"sweep": "R x 4096 BF16 N(0,1), RTNE, no RHT, row-wise", "rows": rows,
+                          "elements": n, **out}), flush=True)
+    assert fq.fp4q_status(ws) == 0
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
     if args.impl == "reference":
@@ -540,6 +598,9 @@ def main(argv=None) -> int:
     import fp4_block_scaled_05_b300 as fq     # fails loudly when libfp4q.so is missing
 
     peaks = load_peaks()
+    if args.sweep:
+        run_sweep(fq, torch, device, args, peaks)
+        return 0
     sampler = ClockSampler(gpu_uuid(device))
     main_r = run_main_leg(fq, torch, device, args.steps, args.warmup)
     gemm_r = None if args.no_gemm else run_gemm_leg(fq, torch, device, args.steps, args.warmup)
@@ -582,6 +643,7 @@ def main(argv=None) -> int:
                             "launches": k["launches"]} for n, k in kern.items()},
             "gpu_launches": main_r["launches_per_step"] * args.steps,
             "stats": main_r["stats"], "device_status": main_r["status"],
+            "self_check": main_r["checks"],
             "wall_s_timed_region": main_r["wall_s"]}
 
     if e2e_r is not None:

@@ -5,6 +5,8 @@
 #include <cstring>
 #include <mutex>
 #include <unordered_map>
+#include <vector>
+#include <cstddef>
 
 #include <cuda_runtime.h>
 
@@ -219,22 +221,46 @@ int fp4q_stats(const void* workspace, fp4q_stats_t* row_stats, fp4q_stats_t* col
   if (!workspace) return FP4Q_EINVAL;
   cudaStream_t s = (cudaStream_t)stream;
   const fp4q::Workspace* ws = static_cast<const fp4q::Workspace*>(workspace);
-  double sums[2][5];
-  unsigned int copies = 0;
-  if (cudaMemcpyAsync(sums, ws->sums, sizeof(sums), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(&copies, &ws->copies, sizeof(copies), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+  // the header fields, then the per-CTA partials of each copy, summed here in FP64
+  constexpr size_t kHead = offsetof(fp4q::Workspace, amax_part);
+  unsigned char head[kHead];
+  if (cudaMemcpyAsync(head, ws, kHead, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return FP4Q_ECUDA;
+  struct {
+    unsigned int stat_nparts, copies;
+    float tensor_scale[2], qmax;
+    double n;
+  } h;
+  std::memcpy(&h.stat_nparts, head + offsetof(fp4q::Workspace, stat_nparts), sizeof(unsigned int));
+  std::memcpy(&h.copies, head + offsetof(fp4q::Workspace, copies), sizeof(unsigned int));
+  std::memcpy(h.tensor_scale, head + offsetof(fp4q::Workspace, tensor_scale), 2 * sizeof(float));
+  std::memcpy(&h.qmax, head + offsetof(fp4q::Workspace, qmax), sizeof(float));
+  std::memcpy(&h.n, head + offsetof(fp4q::Workspace, n), sizeof(double));
+  const unsigned int np = h.stat_nparts < (unsigned)fp4q::kMaxCtas ? h.stat_nparts : (unsigned)fp4q::kMaxCtas;
+  std::vector<double> part((size_t)np * 3);
   fp4q_stats_t* out[2] = {row_stats, col_stats};
   for (int c = 0; c < 2; ++c) {
     if (!out[c]) continue;
     fp4q_stats_t st{};
-    if (copies & (1u << c)) {
-      st.sum_bias = sums[c][0];
-      st.sum_sig2 = sums[c][1];
-      st.sum_err2 = sums[c][2];
-      st.n = (int64_t)sums[c][3];
-      const double qmax = sums[c][4];
+    if (h.copies & (1u << c)) {
+      double sum[3] = {0.0, 0.0, 0.0};
+      if (np) {
+        for (int k = 0; k < 3; ++k) {
+          if (cudaMemcpyAsync(part.data() + (size_t)k * np, &ws->stat_part[c][k][0], np * sizeof(double),
+                              cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return FP4Q_ECUDA;
+        }
+        if (cudaStreamSynchronize(s) != cudaSuccess) return FP4Q_ECUDA;
+        for (int k = 0; k < 3; ++k)
+          for (unsigned int i = 0; i < np; ++i) sum[k] += part[(size_t)k * np + i];
+      }
+      const double g = (double)h.tensor_scale[c];
+      st.sum_bias = sum[0];
+      st.sum_sig2 = sum[1] * g * g;
+      st.sum_err2 = sum[2] * g * g;
+      st.n = (int64_t)h.n;
+      const double qmax = (double)h.qmax;
       st.shrink_bias = st.n ? st.sum_bias / (qmax * (double)st.n) : 0.0;
       if (st.sum_err2 == 0.0) st.snr_db = INFINITY;
       else if (st.sum_sig2 == 0.0) st.snr_db = -INFINITY;

@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cfloat>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -18,16 +19,23 @@ constexpr int kMaxCtas = 2048;   // upper bound on the persistent grid of a quan
 constexpr uint32_t kStatusNonfinite = 1u;
 constexpr uint32_t kStatusTimeout = 2u;
 
+// The passes hand their results on through per-CTA partials, so no kernel
+// ends in a serial fold: the amax pass leaves one partial maximum per CTA,
+// which every CTA of the quantisation pass folds at its start; the
+// quantisation pass leaves one partial per CTA of each statistic, which
+// fp4q_stats sums on the host in FP64.
 struct Workspace {
   unsigned int status;          // sticky FP4Q status bits, cleared by fp4q_status
-  unsigned int cnt_amax;        // last-CTA counters (wrap back to 0 by atomicInc)
-  unsigned int cnt_quant;
-  unsigned int copies;          // axis bits produced by the last quantise call
-  unsigned int amax_bits[2];    // tensor amax (FP32 bits) of the row / column copy
-  float tensor_scale[2];        // g of the row / column copy
-  double sums[2][5];            // per copy: sum_bias, sum_sig2, sum_err2, n, Qmax
-  unsigned int amax_part[2][kMaxCtas];
-  double stat_part[2][3][kMaxCtas];
+  unsigned int amax_nparts;     // CTAs of the last amax pass (entries of amax_part)
+  unsigned int stat_nparts;     // CTAs of the last quantisation pass (entries of stat_part)
+  unsigned int copies;          // axis bits produced by the last quantisation pass
+  float tensor_scale[2];        // g of its row / column copy
+  float qmax;                   // its Qmax
+  unsigned int reserved;
+  double n;                     // its elements per copy
+  unsigned int amax_part[2][kMaxCtas];   // per-CTA max |v| (FP32 bits) of the row / column copy
+  double stat_part[2][3][kMaxCtas];      // per-CTA sums: bias (grid units); signal, error
+                                         // (grid units x s^2; MXFP4: absolute)
 };
 
 // ---- Philox4x32-10 (Salmon et al., SC'11) -----------------------------------
@@ -121,5 +129,168 @@ struct Kahan {
   }
   __device__ __forceinline__ double value() const { return (double)s - (double)c; }
 };
+
+// ---- quantisation plumbing shared by the kernel families ---------------------
+
+struct CopyOut {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tensor_scale;
+  int mma;          // scale layout: 1 = tensor-core tiled
+  int64_t ld;       // bytes per row of codes = (elements per row of the copy) / 2
+  int64_t nkb;      // blocks per row of the copy
+  int64_t nkb_p;    // blocks per row padded to 4 (tiled layout)
+};
+
+
+// Per-copy scale constants derived from the tensor amax (NVFP4 / UFP4).
+struct Ctx {
+  float g;       // tensor scale A / (Qmax * 448)
+  float d;       // Qmax * g
+  float inv_g;   // 1 / g (statistics of blocks whose scale rounds to 0)
+};
+
+__device__ __forceinline__ Ctx make_ctx(uint32_t amax_bits, float qmax, float qmax448) {
+  Ctx c;
+  const float a = __uint_as_float(amax_bits);
+  c.g = __fdiv_rn(a, qmax448);
+  c.d = __fmul_rn(qmax, c.g);
+  c.inv_g = (c.g > 0.f) ? __frcp_rn(c.g) : 0.f;
+  return c;
+}
+
+
+// ---------------------------------------------------------------------------
+// CTA reductions and the last-CTA handshake.
+// ---------------------------------------------------------------------------
+template <int kNT>
+__device__ __forceinline__ double cta_sum(double v, double* sh) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  double r = 0.0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kNT / 32; ++w) r += sh[w];
+  }
+  __syncthreads();
+  return r;   // meaningful in thread 0
+}
+
+template <int kNT>
+__device__ __forceinline__ uint32_t cta_max(uint32_t v, uint32_t* sh) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  uint32_t r = 0;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kNT / 32; ++w) r = max(r, sh[w]);
+  }
+  __syncthreads();
+  return r;
+}
+
+// Thread 0 publishes, then every thread learns whether this CTA finished last.
+__device__ __forceinline__ bool arrive_last(unsigned int* counter, bool* s_flag) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int prev = atomicInc(counter, gridDim.x - 1);
+    *s_flag = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  const bool last = *s_flag;
+  if (last) __threadfence();
+  return last;
+}
+
+
+// SR uniform of one Philox word: its top 24 bits times 2^-24 (exact in FP32).
+__device__ __forceinline__ float sr_u(uint32_t w) { return __uint2float_rz(w >> 8) * 5.9604644775390625e-08f; }
+
+// Stochastic rounding of |y| onto the grid: returns the level index and its value.
+template <int FMT>
+__device__ __forceinline__ uint32_t sr_level(float ay, float u, float& qv) {
+  if (FMT == 2) {   // UFP4: integer levels 0..7
+    if (ay >= 7.f) { qv = 7.f; return 7u; }
+    const float lo = truncf(ay);
+    const float f = __fsub_rn(ay, lo);
+    const uint32_t up = (u < f) ? 1u : 0u;
+    qv = __fadd_rn(lo, (float)up);
+    return (uint32_t)lo + up;
+  } else {          // E2M1
+    if (ay >= 6.f) { qv = 6.f; return 7u; }
+    float lo, step;
+    uint32_t idx;
+    if (ay < 2.f) {
+      const float k = truncf(__fmul_rn(ay, 2.f));
+      lo = __fmul_rn(k, 0.5f); step = 0.5f; idx = (uint32_t)k;
+    } else if (ay < 4.f) {
+      lo = truncf(ay); step = 1.f; idx = (uint32_t)lo + 2u;
+    } else {
+      lo = 4.f; step = 2.f; idx = 6u;
+    }
+    const float f = __fdiv_rn(__fsub_rn(ay, lo), step);
+    const uint32_t up = (u < f) ? 1u : 0u;
+    qv = up ? __fadd_rn(lo, step) : lo;
+    return idx + up;
+  }
+}
+
+
+__device__ __forceinline__ void store_scale(const CopyOut& o, int64_t row, int64_t kb, uint32_t sc) {
+  const int64_t off = o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb;
+  o.scales[off] = (uint8_t)sc;
+}
+
+
+
+// Tensor amax (FP32 bits) of copy c, folded from the amax pass's per-CTA
+// partials; every thread of the CTA gets it.
+template <int kNT>
+__device__ __forceinline__ uint32_t fold_amax(const Workspace* ws, int c, uint32_t* sh) {
+  const uint32_t np = __ldcg(&ws->amax_nparts);
+  uint32_t m = 0u;
+  for (uint32_t i = threadIdx.x; i < np; i += kNT) m = max(m, __ldcg(&ws->amax_part[c][i]));
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = m;
+  __syncthreads();
+  uint32_t r = 0u;
+#pragma unroll
+  for (int w = 0; w < kNT / 32; ++w) r = max(r, sh[w]);
+  __syncthreads();
+  return r;
+}
+
+// FP32 sums of K values over the CTA; the results are meaningful in thread 0.
+template <int kNT, int K>
+__device__ __forceinline__ void cta_sums_f32(float (&v)[K], float (*sh)[kNT / 32]) {
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v[k] += __shfl_xor_sync(0xFFFFFFFFu, v[k], o);
+  }
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) sh[k][threadIdx.x >> 5] = v[k];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      float r = 0.f;
+      for (int w = 0; w < kNT / 32; ++w) r += sh[k][w];
+      v[k] = r;
+    }
+  }
+  __syncthreads();
+}
 
 }  // namespace fp4q

@@ -53,6 +53,11 @@ int cached_occupancy(const void* kernel, int threads, int smem);
 cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s);
 // K1 alone: the tensor amax of the requested copies, recorded in the workspace.
 cudaError_t run_amax(const QuantArgs& a, cudaStream_t s);
+// Flat-stream kernels of the row-wise copy (fp4q_rows.cu): the amax pass when
+// there is no RHT or only the row-wise copy is wanted, and the quantisation
+// pass of a row-wise-only request.
+cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s);
+cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when no GEMM kernel covers the request.
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s);

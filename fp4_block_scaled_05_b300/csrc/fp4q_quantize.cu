@@ -49,32 +49,6 @@ struct Geom {
   int64_t ntiles;
 };
 
-struct CopyOut {
-  uint8_t* codes;
-  uint8_t* scales;
-  float* tensor_scale;
-  int mma;          // scale layout: 1 = tensor-core tiled
-  int64_t ld;       // bytes per row of codes = (elements per row of the copy) / 2
-  int64_t nkb;      // blocks per row of the copy
-  int64_t nkb_p;    // blocks per row padded to 4 (tiled layout)
-};
-
-// Per-copy scale constants derived from the tensor amax (NVFP4 / UFP4).
-struct Ctx {
-  float g;       // tensor scale A / (Qmax * 448)
-  float d;       // Qmax * g
-  float inv_g;   // 1 / g (statistics of blocks whose scale rounds to 0)
-};
-
-__device__ __forceinline__ Ctx make_ctx(uint32_t amax_bits, float qmax, float qmax448) {
-  Ctx c;
-  const float a = __uint_as_float(amax_bits);
-  c.g = __fdiv_rn(a, qmax448);
-  c.d = __fmul_rn(qmax, c.g);
-  c.inv_g = (c.g > 0.f) ? __frcp_rn(c.g) : 0.f;
-  return c;
-}
-
 // ---------------------------------------------------------------------------
 // Loading one row segment of 32 elements (the thread's share of a tile row).
 // Returns the number of valid 16-element blocks (0, 1 or 2). Raw data of the
@@ -183,52 +157,6 @@ __device__ __forceinline__ uint32_t absmax_bits(const float* w) {
 }
 
 // ---------------------------------------------------------------------------
-// CTA reductions and the last-CTA handshake.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ double cta_sum(double v, double* sh) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  double r = 0.0;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < NT / 32; ++w) r += sh[w];
-  }
-  __syncthreads();
-  return r;   // meaningful in thread 0
-}
-
-__device__ __forceinline__ uint32_t cta_max(uint32_t v, uint32_t* sh) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) sh[warp] = v;
-  __syncthreads();
-  uint32_t r = 0;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < NT / 32; ++w) r = max(r, sh[w]);
-  }
-  __syncthreads();
-  return r;
-}
-
-// Thread 0 publishes, then every thread learns whether this CTA finished last.
-__device__ __forceinline__ bool arrive_last(unsigned int* counter, bool* s_flag) {
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int prev = atomicInc(counter, gridDim.x - 1);
-    *s_flag = (prev == gridDim.x - 1);
-  }
-  __syncthreads();
-  const bool last = *s_flag;
-  if (last) __threadfence();
-  return last;
-}
-
-// ---------------------------------------------------------------------------
 // K1: tensor amax of the (transformed) copies. Tiles are visited in reverse
 // order so that the quantise pass, which walks forwards, starts on the tiles
 // this pass left in L2 most recently.
@@ -237,7 +165,6 @@ template <bool F32, bool RHT, bool ROWS, bool COLS>
 __global__ void __launch_bounds__(NT, 3) amax_kernel(Geom g, uint64_t seed, Workspace* ws) {
   extern __shared__ __align__(16) uint8_t tile[];
   __shared__ uint32_t sh_max[NT / 32];
-  __shared__ bool s_last;
   const int tid = threadIdx.x;
   const uint32_t smask = RHT ? rht_sign_mask(seed) : 0u;
   constexpr bool kPark = RHT && COLS;
@@ -268,24 +195,12 @@ __global__ void __launch_bounds__(NT, 3) amax_kernel(Geom g, uint64_t seed, Work
     }
   }
   if (!RHT) m_col = m_row;
-  const uint32_t cr = cta_max(m_row, sh_max);
-  const uint32_t cc = cta_max(m_col, sh_max);
+  const uint32_t cr = cta_max<NT>(m_row, sh_max);
+  const uint32_t cc = cta_max<NT>(m_col, sh_max);
   if (tid == 0) {
     ws->amax_part[0][blockIdx.x] = cr;
     ws->amax_part[1][blockIdx.x] = cc;
-  }
-  if (arrive_last(&ws->cnt_amax, &s_last)) {
-    uint32_t a0 = 0, a1 = 0;
-    for (int i = tid; i < (int)gridDim.x; i += NT) {
-      a0 = max(a0, __ldcg(&ws->amax_part[0][i]));
-      a1 = max(a1, __ldcg(&ws->amax_part[1][i]));
-    }
-    a0 = cta_max(a0, sh_max);
-    a1 = cta_max(a1, sh_max);
-    if (tid == 0) {
-      ws->amax_bits[0] = a0;
-      ws->amax_bits[1] = a1;
-    }
+    if (blockIdx.x == 0) ws->amax_nparts = gridDim.x;
   }
 }
 
@@ -296,38 +211,6 @@ struct Acc {
   Kahan bias, sig, err;      // sig / err in units of g^2 (NVFP4, UFP4)
   double sig64 = 0.0, err64 = 0.0;   // MXFP4: absolute
 };
-
-// SR uniform for element k of a run whose Philox words are in `wd`.
-__device__ __forceinline__ float sr_u(uint32_t w) { return __uint2float_rz(w >> 8) * 5.9604644775390625e-08f; }
-
-// Stochastic rounding of |y| onto the grid: returns the level index and its value.
-template <int FMT>
-__device__ __forceinline__ uint32_t sr_level(float ay, float u, float& qv) {
-  if (FMT == 2) {   // UFP4: integer levels 0..7
-    if (ay >= 7.f) { qv = 7.f; return 7u; }
-    const float lo = truncf(ay);
-    const float f = __fsub_rn(ay, lo);
-    const uint32_t up = (u < f) ? 1u : 0u;
-    qv = __fadd_rn(lo, (float)up);
-    return (uint32_t)lo + up;
-  } else {          // E2M1
-    if (ay >= 6.f) { qv = 6.f; return 7u; }
-    float lo, step;
-    uint32_t idx;
-    if (ay < 2.f) {
-      const float k = truncf(__fmul_rn(ay, 2.f));
-      lo = __fmul_rn(k, 0.5f); step = 0.5f; idx = (uint32_t)k;
-    } else if (ay < 4.f) {
-      lo = truncf(ay); step = 1.f; idx = (uint32_t)lo + 2u;
-    } else {
-      lo = 4.f; step = 2.f; idx = 6u;
-    }
-    const float f = __fdiv_rn(__fsub_rn(ay, lo), step);
-    const uint32_t up = (u < f) ? 1u : 0u;
-    qv = up ? __fadd_rn(lo, step) : lo;
-    return idx + up;
-  }
-}
 
 // Quantise one block of N values (N = 16 for NVFP4/UFP4, 32 for MXFP4).
 // v: transformed values; idx0: row-major index of v[0] inside the copy (SR).
@@ -430,11 +313,6 @@ __device__ __forceinline__ uint32_t quant_block(const float* v, const Ctx& cx, u
   return scode;
 }
 
-__device__ __forceinline__ void store_scale(const CopyOut& o, int64_t row, int64_t kb, uint32_t sc) {
-  const int64_t off = o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb;
-  o.scales[off] = (uint8_t)sc;
-}
-
 // ---------------------------------------------------------------------------
 // K2: quantise. FMT 0 = NVFP4, 1 = MXFP4, 2 = UFP4.
 // ---------------------------------------------------------------------------
@@ -443,8 +321,8 @@ __global__ void __launch_bounds__(NT, 3) quantize_kernel(Geom g, uint64_t seed, 
                                                          CopyOut ocol, Workspace* ws) {
   extern __shared__ __align__(16) uint8_t tile[];
   __shared__ double sh_sum[NT / 32];
-  __shared__ bool s_last;
-  constexpr int B = (FMT == 1) ? 32 : 16;
+  __shared__ float sh_f[6][NT / 32];
+  __shared__ uint32_t sh_max[NT / 32];
   constexpr float kQmax = (FMT == 2) ? 7.f : 6.f;
   constexpr float kQmax448 = (FMT == 2) ? 3136.f : 2688.f;
   const int tid = threadIdx.x;
@@ -452,8 +330,8 @@ __global__ void __launch_bounds__(NT, 3) quantize_kernel(Geom g, uint64_t seed, 
 
   Ctx cr{1.f, 0.f, 0.f}, cc{1.f, 0.f, 0.f};
   if constexpr (FMT != 1) {
-    cr = make_ctx(__ldcg(&ws->amax_bits[0]), kQmax, kQmax448);
-    cc = make_ctx(__ldcg(&ws->amax_bits[1]), kQmax, kQmax448);
+    cr = make_ctx(fold_amax<NT>(ws, 0, sh_max), kQmax, kQmax448);
+    cc = make_ctx(fold_amax<NT>(ws, 1, sh_max), kQmax, kQmax448);
   }
   Acc arow, acol;
   uint32_t nonfinite = 0;
@@ -520,50 +398,37 @@ __global__ void __launch_bounds__(NT, 3) quantize_kernel(Geom g, uint64_t seed, 
     }
   }
 
-  // ---- statistics: CTA partials, then the last CTA folds them in order ----
+  // ---- statistics: one partial per CTA (summed on the host by fp4q_stats) ----
   if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
-  double p[2][3];
-  p[0][0] = arow.bias.value();
-  p[0][1] = (FMT == 1) ? arow.sig64 : arow.sig.value();
-  p[0][2] = (FMT == 1) ? arow.err64 : arow.err.value();
-  p[1][0] = acol.bias.value();
-  p[1][1] = (FMT == 1) ? acol.sig64 : acol.sig.value();
-  p[1][2] = (FMT == 1) ? acol.err64 : acol.err.value();
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const double s = cta_sum(p[c][k], sh_sum);
-      if (tid == 0) ws->stat_part[c][k][blockIdx.x] = s;
-    }
-  }
-  if (arrive_last(&ws->cnt_quant, &s_last)) {
-    double f[2][3];
+  if constexpr (FMT == 1) {
+    const double p[2][3] = {{arow.bias.value(), arow.sig64, arow.err64},
+                            {acol.bias.value(), acol.sig64, acol.err64}};
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
       for (int k = 0; k < 3; ++k) {
-        double s = 0.0;
-        for (int i = tid; i < (int)gridDim.x; i += NT) s += __ldcg(&ws->stat_part[c][k][i]);
-        f[c][k] = cta_sum(s, sh_sum);
+        const double v = cta_sum<NT>(p[c][k], sh_sum);
+        if (tid == 0) ws->stat_part[c][k][blockIdx.x] = v;
       }
     }
+  } else {
+    float v[6] = {(float)arow.bias.value(), (float)arow.sig.value(), (float)arow.err.value(),
+                  (float)acol.bias.value(), (float)acol.sig.value(), (float)acol.err.value()};
+    cta_sums_f32<NT, 6>(v, sh_f);
     if (tid == 0) {
-      const double n = (double)g.rows * (double)g.cols;
-      const Ctx* cx[2] = {&cr, &cc};
-      for (int c = 0; c < 2; ++c) {
-        const double g2 = (FMT == 1) ? 1.0 : (double)cx[c]->g * (double)cx[c]->g;
-        ws->sums[c][0] = f[c][0];
-        ws->sums[c][1] = f[c][1] * g2;
-        ws->sums[c][2] = f[c][2] * g2;
-        ws->sums[c][3] = n;
-        ws->sums[c][4] = (double)kQmax;
-        ws->tensor_scale[c] = (FMT == 1) ? 1.f : cx[c]->g;
-      }
-      ws->copies = (ROWS ? 1u : 0u) | (COLS ? 2u : 0u);
-      if (ROWS && orow.tensor_scale) *orow.tensor_scale = (FMT == 1) ? 1.f : cr.g;
-      if (COLS && ocol.tensor_scale) *ocol.tensor_scale = (FMT == 1) ? 1.f : cc.g;
+#pragma unroll
+      for (int k = 0; k < 6; ++k) ws->stat_part[k / 3][k % 3][blockIdx.x] = (double)v[k];
     }
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    ws->stat_nparts = gridDim.x;
+    ws->copies = (ROWS ? 1u : 0u) | (COLS ? 2u : 0u);
+    ws->tensor_scale[0] = (FMT == 1) ? 1.f : cr.g;
+    ws->tensor_scale[1] = (FMT == 1) ? 1.f : cc.g;
+    ws->qmax = kQmax;
+    ws->n = (double)g.rows * (double)g.cols;
+    if (ROWS && orow.tensor_scale) *orow.tensor_scale = (FMT == 1) ? 1.f : cr.g;
+    if (COLS && ocol.tensor_scale) *ocol.tensor_scale = (FMT == 1) ? 1.f : cc.g;
   }
 }
 
@@ -714,12 +579,12 @@ static cudaError_t dispatch_amax(int rht, int axis, const Geom& g, uint64_t seed
 // Empty input: write the tensor scales and empty statistics, nothing else.
 __global__ void quantize_empty_kernel(int fmt, int axis, float* ts_row, float* ts_col, Workspace* ws) {
   const float g = (fmt == 1) ? 1.f : 0.f;
-  for (int c = 0; c < 2; ++c) {
-    for (int k = 0; k < 4; ++k) ws->sums[c][k] = 0.0;
-    ws->sums[c][4] = (fmt == 2) ? 7.0 : 6.0;
-    ws->tensor_scale[c] = g;
-  }
+  ws->stat_nparts = 0u;
   ws->copies = (unsigned)axis;
+  ws->tensor_scale[0] = g;
+  ws->tensor_scale[1] = g;
+  ws->qmax = (fmt == 2) ? 7.f : 6.f;
+  ws->n = 0.0;
   if ((axis & 1) && ts_row) *ts_row = g;
   if ((axis & 2) && ts_col) *ts_col = g;
 }
@@ -736,8 +601,9 @@ static Geom make_geom(const QuantArgs& a) {
 
 // Empty input: a zero amax for both copies.
 __global__ void amax_empty_kernel(Workspace* ws) {
-  ws->amax_bits[0] = 0u;
-  ws->amax_bits[1] = 0u;
+  ws->amax_part[0][0] = 0u;
+  ws->amax_part[1][0] = 0u;
+  ws->amax_nparts = 1u;
 }
 
 cudaError_t run_amax(const QuantArgs& a, cudaStream_t s) {
@@ -746,6 +612,7 @@ cudaError_t run_amax(const QuantArgs& a, cudaStream_t s) {
     amax_empty_kernel<<<1, 1, 0, s>>>(ws);
     return cudaGetLastError();
   }
+  if (!a.rht || a.axis == 1) return run_amax_rows(a, s);
   const Geom g = make_geom(a);
   return a.dtype == 1 ? dispatch_amax<true>(a.rht, a.axis, g, a.seed, ws, s)
                       : dispatch_amax<false>(a.rht, a.axis, g, a.seed, ws, s);
@@ -765,10 +632,10 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   const bool f32 = a.dtype == 1;
   if (a.fmt != 1 && !a.amax_ready) {
-    e = f32 ? dispatch_amax<true>(a.rht, a.axis, g, a.seed, ws, s)
-            : dispatch_amax<false>(a.rht, a.axis, g, a.seed, ws, s);
+    e = run_amax(a, s);
     if (e != cudaSuccess) return e;
   }
+  if (a.axis == 1) return run_quant_rows(a, s);
   const int sr = a.rounding == 1;
   switch (a.fmt) {
     case 0: e = f32 ? dispatch_rs<0, true>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s)

@@ -1,0 +1,870 @@
+// Row-wise block-scaled 4-bit quantisation as a flat stream (sm_103a): the
+// tensor-amax pass and the quantisation pass for the row-wise copy.
+//
+// Method: "Replanteamiento del Sesgo de Contraccion en el Preentrenamiento de
+// LLM en FP4" (Metodologia §1-2: E2M1 / uniform E1M2 grids, RTNE, stochastic
+// rounding, RHT; Eficiencia: RHT fused into the quantisation pass);
+// "TetraJet-v2 ..." (Riepilogo Tecnico §2A: NVFP4 16-element groups with an
+// 8-bit scale under a per-tensor scale, SR); "Unveiling the Potential of
+// Quantization with MXFP4 ..." (Resume technique §2: MXFP4 32-element E8M0
+// blocks, NVFP4 16-element E4M3 blocks).
+//
+// Blocks of the row-wise copy never straddle a row (cols is a multiple of the
+// block), so the copy is a flat stream of blocks: element e of the row-major
+// source is element e of the copy, its codes sit at byte e/2 and its linear
+// scale at e/b. Each CTA of a persistent grid walks chunks of 8192 elements;
+// one thread keeps a ring of bulk (TMA) copies of the CTA's next chunks in
+// flight into shared memory (16 KiB per BF16 chunk, 4 deep), so the loads
+// overlap the arithmetic. A thread quantises 32 consecutive elements of a
+// chunk (two 16-blocks, or one MXFP4 32-block) in registers, using packed
+// FP32x2 operations where the lanes are independent; every value-deciding step
+// is one IEEE round-to-nearest-even operation in the order of the method.
+#include <cfloat>
+#include <cstdint>
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "fp4q_device.cuh"
+#include "fp4q_internal.h"
+#include "fp4q_ptx.cuh"
+
+namespace fp4q {
+namespace {
+
+constexpr int RT = 256;            // threads per CTA
+constexpr int EPT = 32;            // elements per thread per chunk
+constexpr int CH = RT * EPT;       // elements per chunk
+constexpr uint64_t kRingTimeoutNs = 2000000000ull;
+
+template <bool F32>
+struct Ring {
+  static constexpr int kChunkBytes = CH * (F32 ? 4 : 2);
+  static constexpr int kStages = F32 ? 3 : 4;
+  static constexpr int kSmem = kStages * kChunkBytes;
+};
+
+// Division by a fixed divisor d >= 1 for 32-bit numerators (round-up method
+// of Granlund and Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994): q = (t + ((n - t) >> 1)) >> s, t = mulhi(m, n).
+struct FastDiv {
+  uint32_t d, m, s;
+  __device__ __forceinline__ uint32_t div(uint32_t n) const {
+    if (d == 1) return n;
+    const uint32_t t = __umulhi(m, n);
+    return (t + ((n - t) >> 1)) >> s;
+  }
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f{d, 0, 0};
+  if (d <= 1) return f;
+  uint32_t l = 0;
+  while ((uint64_t(1) << l) < d) ++l;
+  f.m = (uint32_t)(((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1);
+  f.s = l - 1;
+  return f;
+}
+
+struct Flat {
+  const uint8_t* src;
+  int64_t n;          // elements
+  int64_t nchunks;
+  FastDiv nkb;        // blocks per row (tiled scale layout)
+  int small;          // 1 when every block index fits in 32 bits
+};
+
+// ---- the ring ------------------------------------------------------------------
+template <bool F32>
+__device__ __forceinline__ void ring_issue(const Flat& f, int64_t chunk, uint8_t* ring, int slot,
+                                           uint32_t bar) {
+  constexpr int es = F32 ? 4 : 2;
+  const int64_t e0 = chunk * CH;
+  const int64_t ne = (f.n - e0 < CH) ? (f.n - e0) : CH;
+  const uint32_t bytes = (uint32_t)(ne * es);        // a multiple of 32: blocks are whole
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_load(smem_u32(ring + slot * Ring<F32>::kChunkBytes), f.src + e0 * es, bytes, bar);
+}
+
+// Thread 0 starts the first copies; every slot's barrier completes one phase per copy.
+template <bool F32>
+__device__ __forceinline__ void ring_start(const Flat& f, uint8_t* ring, uint64_t* full) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Ring<F32>::kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Ring<F32>::kStages; ++s) {
+      const int64_t c = blockIdx.x + (int64_t)s * gridDim.x;
+      if (c < f.nchunks) ring_issue<F32>(f, c, ring, s, smem_u32(&full[s]));
+    }
+  }
+}
+
+// After a timeout: wait (bounded) for the copies still in flight, so none lands
+// after the CTA has exited. `it` is the first iteration not consumed.
+template <bool F32>
+__device__ __forceinline__ void ring_drain(const Flat& f, uint64_t* full, int64_t it) {
+  if (threadIdx.x != 0) return;
+  constexpr int S = Ring<F32>::kStages;
+  const uint64_t t0 = globaltimer();
+  for (int64_t j = it; j < it + S; ++j) {
+    const int64_t c = blockIdx.x + j * gridDim.x;
+    if (c >= f.nchunks) break;
+    const uint32_t bar = smem_u32(&full[j % S]);
+    const uint32_t par = (uint32_t)((j / S) & 1);
+    while (!mbar_try_wait(bar, par) && globaltimer() - t0 < 50000000ull) {
+    }
+  }
+}
+
+// ---- loading a thread's 32 elements as FP32 pairs -------------------------------
+// Q[j] = {v[2j], v[2j+1]}, v the (transformed) values of elements 32t .. 32t+31
+// of the chunk. With the RHT, each 16-block is sign-flipped by sigma, run
+// through the butterfly stages 1, 2, 4, 8 and scaled by 1/4. Stages 1, 2, 4
+// run on lanes {x_i, x_{i+8}} with packed adds; stage 8 pairs the two lanes.
+__device__ __forceinline__ void rht16_pairs(float (&x)[16], f2* Q) {
+  f2 P[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) P[i] = f2_make(x[i], x[i + 8]);
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const f2 a = P[i], b = P[i + h];
+        P[i] = f2_add(a, b);
+        P[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float lo, hi;
+    f2_split(P[i], lo, hi);
+    v[i] = __fadd_rn(lo, hi);
+    v[i + 8] = __fsub_rn(lo, hi);
+  }
+  const f2 quarter = f2_make(0.25f, 0.25f);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) Q[j] = f2_mul(f2_make(v[2 * j], v[2 * j + 1]), quarter);
+}
+
+// Same butterfly without the final 1/4 and with plain scalar outputs (amax pass:
+// max |round(w/4)| = round(max |w| / 4), since the scaling is monotone).
+__device__ __forceinline__ void rht16_unscaled(float (&x)[16]) {
+  f2 P[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) P[i] = f2_make(x[i], x[i + 8]);
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if ((i & h) == 0) {
+        const f2 a = P[i], b = P[i + h];
+        P[i] = f2_add(a, b);
+        P[i + h] = f2_sub(a, b);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float lo, hi;
+    f2_split(P[i], lo, hi);
+    x[i] = __fadd_rn(lo, hi);
+    x[i + 8] = __fsub_rn(lo, hi);
+  }
+}
+
+// Widen 16 elements of the chunk at `p` to FP32, flipping signs by `sign` when
+// RHT (BF16: sign words hold sigma at bits 15 and 31; FP32: one bit per value).
+template <bool F32, bool RHT>
+__device__ __forceinline__ void widen16(const uint8_t* p, const uint32_t (&sgn)[16], float (&x)[16]) {
+  if constexpr (F32) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * k);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[4 * k + i] = __uint_as_float(RHT ? (w[i] ^ sgn[4 * k + i]) : w[i]);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * k);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t s = RHT ? (w[i] ^ sgn[4 * k + i]) : w[i];
+        x[8 * k + 2 * i] = __uint_as_float(s << 16);
+        x[8 * k + 2 * i + 1] = __uint_as_float(s & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+template <bool F32, bool RHT>
+__device__ __forceinline__ void load_block16(const uint8_t* p, const uint32_t (&sgn)[16], f2* Q) {
+  float x[16];
+  widen16<F32, RHT>(p, sgn, x);
+  if constexpr (RHT) {
+    rht16_pairs(x, Q);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) Q[j] = f2_make(x[2 * j], x[2 * j + 1]);
+  }
+}
+
+// Sign words: BF16 -> word i of a 16-block covers elements 2i, 2i+1 (bits 15,
+// 31); FP32 -> one word per element (bit 31).
+template <bool F32>
+__device__ __forceinline__ void make_sign_words(uint32_t smask, uint32_t (&sgn)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if constexpr (F32) {
+      sgn[i] = ((smask >> i) & 1u) << 31;
+    } else {
+      sgn[i] = (i < 8) ? ((((smask >> (2 * i)) & 1u) << 15) | (((smask >> (2 * i + 1)) & 1u) << 31)) : 0u;
+    }
+  }
+}
+
+// ---- per-block quantisation --------------------------------------------------------
+struct Sums {        // per-thread running sums of one copy
+  Kahan bias, sig, err;
+  double sig64 = 0.0, err64 = 0.0;
+};
+
+// Two independent Kahan-compensated FP32 sums, one per lane of a pair.
+struct Kahan2 {
+  f2 s = 0ull, c = 0ull;
+  __device__ __forceinline__ void add(f2 x) {
+    const f2 y = f2_sub(x, c);
+    const f2 t = f2_add(s, y);
+    c = f2_sub(f2_sub(t, s), y);
+    s = t;
+  }
+  __device__ __forceinline__ float value_f() const {   // both lanes together
+    float s0, s1, c0, c1;
+    f2_split(s, s0, s1);
+    f2_split(c, c0, c1);
+    return __fadd_rn(__fsub_rn(s0, c0), __fsub_rn(s1, c1));
+  }
+};
+
+// max(m, |a|, |b|), NaN-propagating.
+__device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
+  float d;
+  asm("{\n\t.reg .f32 x, y;\n\tabs.f32 x, %2;\n\tabs.f32 y, %3;\n\tmax.NaN.f32 %0, %1, x, y;\n\t}"
+      : "=f"(d) : "f"(m), "f"(a), "f"(b));
+  return d;
+}
+
+// Per-CTA constants of the E4M3 block scales (NVFP4/UFP4), for each of the
+// 128 codes: r = 1 / RN(s * g) rounded to nearest (0 when the product is 0,
+// FLT_MAX when it overflows; the NaN code 127 maps to 0) and s^2, s the
+// code's value. A block's normaliser and statistics weight are then one table
+// read instead of a decode, a product and a reciprocal per block.
+__device__ __forceinline__ void fill_scale_table(float2* tab, float g) {
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
+    const float s = (c < 127) ? e4m3_to_f32((uint32_t)c) : 0.f;
+    const float p = __fmul_rn(s, g);
+    float r = (p == 0.f) ? 0.f : __frcp_rn(p);
+    if (r > FLT_MAX) r = FLT_MAX;
+    tab[c] = make_float2(r, __fmul_rn(s, s));
+  }
+}
+
+// t = RN(m / d) for both lanes. With y = RN(1/d) two correction steps
+// q <- RN(q + RN(m - q d) y) give the correctly rounded quotient (Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990); used only when d lies in
+// [2^-38, 2^50], where no step underflows or overflows.
+struct Divider {
+  int fast;
+  float d;
+  f2 nd2, y2;
+  __device__ __forceinline__ void init(float dd) {
+    d = dd;
+    fast = (dd >= 3.637978807091713e-12f && dd <= 1.125899906842624e15f) ? 1 : 0;
+    const float y = fast ? __frcp_rn(dd) : 0.f;
+    nd2 = f2_make(-dd, -dd);
+    y2 = f2_make(y, y);
+  }
+  __device__ __forceinline__ f2 div(f2 m) const {
+    if (fast) {
+      const f2 q0 = f2_mul(m, y2);
+      const f2 q1 = f2_fma(f2_fma(nd2, q0, m), y2, q0);
+      return f2_fma(f2_fma(nd2, q1, m), y2, q1);
+    }
+    float a, b;
+    f2_split(m, a, b);
+    return f2_make(__fdiv_rn(a, d), __fdiv_rn(b, d));
+  }
+};
+
+// One E2M1 byte (nearest-even, saturating) of the pair Y and the rounding
+// errors |q| - |y| of its two lanes.
+__device__ __forceinline__ uint32_t e2m1_pair(f2 Y, f2& D) {
+  float y0, y1;
+  f2_split(Y, y0, y1);
+  uint32_t byte, hq;
+  asm("{\n\t.reg .b8 t;\n\t.reg .b32 m;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %3, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t"
+      "and.b32 m, %0, 0x77;\n\t"
+      "cvt.u8.u32 t, m;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, t;\n\t}"
+      : "=r"(byte), "=r"(hq) : "f"(y0), "f"(y1));
+  D = f2_make(sub_f16_f32((uint16_t)(hq & 0xFFFFu), fabsf(y0)),
+              sub_f16_f32((uint16_t)(hq >> 16), fabsf(y1)));
+  return byte;
+}
+
+// One UFP4 byte: |y| clamped to 7 and rounded to the nearest integer, ties to
+// even (adding 2^23 rounds to an integer in FP32), sign kept in bit 3.
+__device__ __forceinline__ uint32_t ufp4_pair(f2 Y, f2& D) {
+  float y0, y1;
+  f2_split(Y, y0, y1);
+  const float a0 = fabsf(y0), a1 = fabsf(y1);
+  const f2 magic = f2_make(8388608.f, 8388608.f);
+  const f2 T = f2_add(f2_make(fminf(a0, 7.f), fminf(a1, 7.f)), magic);
+  const f2 Qv = f2_sub(T, magic);
+  D = f2_sub(Qv, f2_make(a0, a1));
+  float t0, t1;
+  f2_split(T, t0, t1);
+  return (__float_as_uint(t0) & 7u) | ((__float_as_uint(t1) & 7u) << 4) |
+         ((__float_as_uint(y0) >> 31) << 3) | ((__float_as_uint(y1) >> 31) << 7);
+}
+
+// Stochastic rounding of a pair with the uniforms of words w0, w1.
+template <int FMT>
+__device__ __forceinline__ uint32_t sr_pair(f2 Y, uint32_t w0, uint32_t w1, f2& D) {
+  float y0, y1, q0, q1;
+  f2_split(Y, y0, y1);
+  const uint32_t k0 = sr_level<FMT>(fabsf(y0), sr_u(w0), q0);
+  const uint32_t k1 = sr_level<FMT>(fabsf(y1), sr_u(w1), q1);
+  D = f2_make(__fsub_rn(q0, fabsf(y0)), __fsub_rn(q1, fabsf(y1)));
+  return (k0 | ((__float_as_uint(y0) >> 31) << 3)) | ((k1 | ((__float_as_uint(y1) >> 31) << 3)) << 4);
+}
+
+// Quantise one block of NP pairs (NP = 8: a 16-block, NP = 16: an MXFP4
+// 32-block) whose first element has index e0 in the copy. Writes NP/4 code
+// words and returns the scale code; adds the block's sums to bsum/ssum/esum
+// (NVFP4/UFP4: grid units times s^2; MXFP4: FP64 absolute in sig64/err64).
+template <int FMT, bool SR, int NP>
+__device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint64_t e0, uint64_t seed,
+                                                uint32_t* cw, float& bsum, float& ssum, float& esum,
+                                                Sums& acc, uint32_t& nonfinite) {
+  float m = 0.f;
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    float a, b;
+    f2_split(Q[j], a, b);
+    m = max_abs_nan(m, a);
+    m = max_abs_nan(m, b);
+  }
+  nonfinite |= (__float_as_uint(m) >= 0x7F800000u) ? 1u : 0u;
+  uint32_t scode;
+  float r, s2 = 0.f;
+  int e2 = 0;
+  if constexpr (FMT == 1) {
+    const uint32_t mb = __float_as_uint(m);
+    const uint32_t E = mb >> 23;
+    const int fl = E ? (int)E - 127 : (mb ? (31 - __clz((int)mb)) - 149 : -200);
+    const int e = max(-127, min(127, fl - 2));
+    scode = (uint32_t)(e + 127);
+    r = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 125]
+    e2 = 2 * e;
+  } else {
+    if (cx.g == 0.f) {
+      scode = 0;
+      r = 0.f;
+    } else {
+      scode = f32_to_e4m3(__fdiv_rn(m, cx.d));
+      const float p = __fmul_rn(e4m3_to_f32(scode), cx.g);
+      r = (p == 0.f) ? 0.f : __frcp_rn(p);
+      if (r > FLT_MAX) r = FLT_MAX;
+    }
+    const float s = e4m3_to_f32(scode);
+    s2 = __fmul_rn(s, s);
+  }
+
+  const f2 R = f2_make(r, r);
+  f2 B2 = f2_make(0.f, 0.f), E2 = B2, S2 = B2;
+#pragma unroll
+  for (int j = 0; j < NP / 4; ++j) cw[j] = 0u;
+#pragma unroll
+  for (int j0 = 0; j0 < NP; j0 += 2) {
+    uint4 rw = make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (SR) {   // one Philox call per 4 elements (e0 is a multiple of 16)
+      const uint64_t q = (e0 >> 2) + (uint64_t)(j0 >> 1);
+      rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
+                         (uint32_t)(seed >> 32));
+    }
+#pragma unroll
+    for (int j = j0; j < j0 + 2; ++j) {
+      const f2 Y = f2_mul(Q[j], R);
+      f2 D;
+      uint32_t byte;
+      if constexpr (SR) {
+        byte = (j == j0) ? sr_pair<FMT>(Y, rw.x, rw.y, D) : sr_pair<FMT>(Y, rw.z, rw.w, D);
+      } else if constexpr (FMT == 2) {
+        byte = ufp4_pair(Y, D);
+      } else {
+        byte = e2m1_pair(Y, D);
+      }
+      cw[j >> 2] |= byte << (8 * (j & 3));
+      B2 = f2_add(B2, D);
+      E2 = f2_fma(D, D, E2);
+      S2 = f2_fma(Y, Y, S2);
+    }
+  }
+  float b0, b1, e0f, e1f, s0, s1;
+  f2_split(B2, b0, b1);
+  f2_split(E2, e0f, e1f);
+  f2_split(S2, s0, s1);
+  const float bs = __fadd_rn(b0, b1), es = __fadd_rn(e0f, e1f), ys = __fadd_rn(s0, s1);
+  bsum = __fadd_rn(bsum, bs);
+  if constexpr (FMT == 1) {
+    const double sc = __longlong_as_double((long long)(1023 + e2) << 52);
+    acc.sig64 += (double)ys * sc;
+    acc.err64 += (double)es * sc;
+  } else if (scode == 0 && cx.g > 0.f) {
+    // the scale rounded to 0: every element becomes 0 and its error is v itself
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < NP; ++j) {
+      float a, b;
+      f2_split(Q[j], a, b);
+      const float wa = __fmul_rn(a, cx.inv_g), wb = __fmul_rn(b, cx.inv_g);
+      z = __fmaf_rn(wa, wa, __fmaf_rn(wb, wb, z));
+    }
+    ssum = __fadd_rn(ssum, z);
+    esum = __fadd_rn(esum, z);
+  } else {
+    ssum = __fadd_rn(ssum, __fmul_rn(ys, s2));
+    esum = __fadd_rn(esum, __fmul_rn(es, s2));
+  }
+  return scode;
+}
+
+// Quantise the thread's two consecutive 16-blocks (NVFP4 or UFP4) at `p`,
+// elements e .. e+31 of the copy. The scalar steps of both blocks run in the
+// two lanes of FP32 pairs. Writes four code words and two scale codes; adds
+// the blocks' bias / signal / error sums (grid units, signal and error times
+// s^2) to the lanes of bias2 / sig2 / err2.
+template <int FMT, bool F32, bool RHT, bool SR>
+__device__ __forceinline__ void quant_two16(const uint8_t* p, const uint32_t (&sgn)[16], const Ctx& cx,
+                                            const Divider& dv, const float2* tab, uint64_t e,
+                                            uint64_t seed, uint32_t (&cw)[4], uint32_t (&sc)[2],
+                                            f2& bias2, f2& sig2, f2& err2, uint32_t& nonfinite) {
+  f2 Q[16];
+  float m0 = 0.f, m1 = 0.f;
+  if constexpr (!F32 && !RHT) {
+    uint32_t w[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * k);
+      w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+    }
+    uint32_t a0 = 0u, a1 = 0u;     // block maxima on the BF16 pairs
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      a0 = max_abs_nan_bf16x2(a0, w[k]);
+      a1 = max_abs_nan_bf16x2(a1, w[k + 8]);
+    }
+    m0 = max_abs_nan(bf16lo(a0), bf16hi(a0));
+    m1 = max_abs_nan(bf16lo(a1), bf16hi(a1));
+#pragma unroll
+    for (int j = 0; j < 16; ++j) Q[j] = f2_make(bf16lo(w[j]), bf16hi(w[j]));
+  } else {
+    load_block16<F32, RHT>(p, sgn, Q);
+    load_block16<F32, RHT>(p + 16 * (F32 ? 4 : 2), sgn, Q + 8);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a, b;
+      f2_split(Q[j], a, b);
+      m0 = max3_abs_nan(m0, a, b);
+      f2_split(Q[j + 8], a, b);
+      m1 = max3_abs_nan(m1, a, b);
+    }
+  }
+  nonfinite |= (max(__float_as_uint(m0), __float_as_uint(m1)) >= 0x7F800000u) ? 1u : 0u;
+
+  sc[0] = sc[1] = 0u;
+  if (cx.g > 0.f) {
+    float t0, t1;
+    f2_split(dv.div(f2_make(m0, m1)), t0, t1);
+    uint16_t c2;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c2) : "f"(t1), "f"(t0));
+    sc[0] = c2 & 0xFFu;
+    sc[1] = (uint32_t)c2 >> 8;
+  }
+  const float2 T0 = tab[sc[0]], T1 = tab[sc[1]];
+
+  float bs[2], ys[2], es[2];
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    const f2 R = b ? f2_make(T1.x, T1.x) : f2_make(T0.x, T0.x);
+    f2 B2 = 0ull, E2 = 0ull, S2 = 0ull;
+    cw[2 * b] = 0u;
+    cw[2 * b + 1] = 0u;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; j0 += 2) {
+      uint4 rw = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (SR) {   // one Philox call per 4 elements
+        const uint64_t q = ((e + 16 * b) >> 2) + (uint64_t)(j0 >> 1);
+        rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
+                           (uint32_t)(seed >> 32));
+      }
+#pragma unroll
+      for (int j = j0; j < j0 + 2; ++j) {
+        const f2 Y = f2_mul(Q[8 * b + j], R);
+        f2 D;
+        uint32_t byte;
+        if constexpr (SR) {
+          byte = (j == j0) ? sr_pair<FMT>(Y, rw.x, rw.y, D) : sr_pair<FMT>(Y, rw.z, rw.w, D);
+        } else if constexpr (FMT == 2) {
+          byte = ufp4_pair(Y, D);
+        } else {
+          byte = e2m1_pair(Y, D);
+        }
+        cw[2 * b + (j >> 2)] += byte << (8 * (j & 3));
+        B2 = f2_add(B2, D);
+        E2 = f2_fma(D, D, E2);
+        S2 = f2_fma(Y, Y, S2);
+      }
+    }
+    float x0, x1;
+    f2_split(B2, x0, x1);
+    bs[b] = __fadd_rn(x0, x1);
+    f2_split(E2, x0, x1);
+    es[b] = __fadd_rn(x0, x1);
+    f2_split(S2, x0, x1);
+    ys[b] = __fadd_rn(x0, x1);
+  }
+  bias2 = f2_add(bias2, f2_make(bs[0], bs[1]));
+  const f2 W = f2_make(T0.y, T1.y);
+  sig2 = f2_fma(f2_make(ys[0], ys[1]), W, sig2);
+  err2 = f2_fma(f2_make(es[0], es[1]), W, err2);
+  if (cx.g > 0.f && (sc[0] == 0u || sc[1] == 0u)) {
+    // a scale that rounded to 0: its block's elements become 0 and their
+    // error is the value itself
+    float z[2] = {0.f, 0.f};
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      if (sc[b] == 0u) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          float a, c;
+          f2_split(Q[8 * b + j], a, c);
+          const float wa = __fmul_rn(a, cx.inv_g), wc = __fmul_rn(c, cx.inv_g);
+          z[b] = __fmaf_rn(wa, wa, __fmaf_rn(wc, wc, z[b]));
+        }
+      }
+    }
+    const f2 Z = f2_make(z[0], z[1]);
+    sig2 = f2_add(sig2, Z);
+    err2 = f2_add(err2, Z);
+  }
+}
+
+__device__ __forceinline__ void put_scale(const CopyOut& o, const Flat& f, uint64_t blk, uint32_t sc) {
+  if (!o.mma) {
+    o.scales[blk] = (uint8_t)sc;
+    return;
+  }
+  uint64_t r;
+  if (f.small) {
+    r = f.nkb.div((uint32_t)blk);
+  } else {
+    r = blk / f.nkb.d;
+  }
+  const uint64_t kb = blk - r * f.nkb.d;
+  o.scales[mma_scale_offset((int64_t)r, (int64_t)kb, o.nkb_p)] = (uint8_t)sc;
+}
+
+// ---- K1: tensor amax of the row-wise copy ----------------------------------------
+template <bool F32, bool RHT>
+__global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed, Workspace* ws,
+                                                          uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages];
+  __shared__ uint32_t sh_max[RT / 32];
+  constexpr int S = Ring<F32>::kStages;
+  const int tid = threadIdx.x;
+  uint32_t sgn[16];
+  make_sign_words<F32>(RHT ? rht_sign_mask(seed) : 0u, sgn);
+  ring_start<F32>(f, ring, full);
+
+  float m = 0.f;
+  uint32_t m2 = 0u;      // BF16 pairs without the RHT
+  bool timed_out = false;
+  int64_t it = 0;
+  for (int64_t c = blockIdx.x; c < f.nchunks; ++it, c += gridDim.x) {
+    const int s = (int)(it % S);
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
+    if (ok) {
+      const int64_t e = c * CH + (int64_t)tid * EPT;
+      const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
+      const uint8_t* p = ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2);
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        if (b < nb) {
+          const uint8_t* pb = p + b * 16 * (F32 ? 4 : 2);
+          if constexpr (!RHT && !F32) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint4 u = *reinterpret_cast<const uint4*>(pb + 16 * k);
+              m2 = max_abs_nan_bf16x2(m2, u.x);
+              m2 = max_abs_nan_bf16x2(m2, u.y);
+              m2 = max_abs_nan_bf16x2(m2, u.z);
+              m2 = max_abs_nan_bf16x2(m2, u.w);
+            }
+          } else {
+            float x[16];
+            widen16<F32, RHT>(pb, sgn, x);
+            if (RHT) rht16_unscaled(x);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) m = max3_abs_nan(m, x[i], x[i + 1]);
+          }
+        }
+      }
+    }
+    timed_out = __syncthreads_or(!ok);
+    if (timed_out) break;
+    if (tid == 0) {
+      const int64_t nx = c + (int64_t)S * gridDim.x;
+      if (nx < f.nchunks) ring_issue<F32>(f, nx, ring, s, smem_u32(&full[s]));
+    }
+  }
+  if (timed_out) {
+    ring_drain<F32>(f, full, it);
+    if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
+  }
+  if constexpr (!RHT && !F32) {
+    m = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+    if ((m2 & 0x7FFFu) > 0x7F80u || (m2 >> 16 & 0x7FFFu) > 0x7F80u) m = __uint_as_float(0x7FFFFFFFu);
+  }
+  // with the RHT the maxima above are of |w| = 4 |v|: scaling the maximum once
+  // is exact (or monotone) and gives max |v|
+  const uint32_t cm = cta_max<RT>(__float_as_uint(RHT ? __fmul_rn(m, 0.25f) : m), sh_max);
+  if (tid == 0) {
+    ws->amax_part[0][blockIdx.x] = cm;
+    ws->amax_part[1][blockIdx.x] = cm;
+    if (blockIdx.x == 0) ws->amax_nparts = gridDim.x;
+  }
+}
+
+// ---- K2: quantise the row-wise copy --------------------------------------------------
+template <int FMT, bool F32, bool RHT, bool SR>
+__global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint64_t seed, CopyOut o,
+                                                           Workspace* ws, uint64_t timeout_ns) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages];
+  __shared__ float2 tab[128];
+  __shared__ double sh_sum[RT / 32];
+  __shared__ float sh_f[3][RT / 32];
+  __shared__ uint32_t sh_max[RT / 32];
+  constexpr int S = Ring<F32>::kStages;
+  constexpr int ES = F32 ? 4 : 2;
+  constexpr float kQmax = (FMT == 2) ? 7.f : 6.f;
+  constexpr float kQmax448 = (FMT == 2) ? 3136.f : 2688.f;
+  const int tid = threadIdx.x;
+  uint32_t sgn[16];
+  make_sign_words<F32>(RHT ? rht_sign_mask(seed) : 0u, sgn);
+  ring_start<F32>(f, ring, full);     // the first copies fly while the scales are set up
+  Ctx cx{1.f, 0.f, 0.f};
+  Divider dv{};
+  if constexpr (FMT != 1) {
+    cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
+    dv.init(cx.d);
+    fill_scale_table(tab, cx.g);
+    __syncthreads();
+  }
+
+  Sums acc;
+  Kahan2 kb, ks, ke;
+  uint32_t nonfinite = 0;
+  bool timed_out = false;
+  int64_t it = 0;
+  for (int64_t c = blockIdx.x; c < f.nchunks; ++it, c += gridDim.x) {
+    const int s = (int)(it % S);
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
+    if (ok) {
+      const int64_t e = c * CH + (int64_t)tid * EPT;
+      const int nb16 = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
+      const uint8_t* p = ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES;
+      if constexpr (FMT == 1) {
+        if (nb16 == 2) {
+          float bsum = 0.f, ssum = 0.f, esum = 0.f;
+          f2 Q[16];
+          load_block16<F32, RHT>(p, sgn, Q);
+          load_block16<F32, RHT>(p + 16 * ES, sgn, Q + 8);
+          uint32_t cw[4];
+          const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+                                                        acc, nonfinite);
+          *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          put_scale(o, f, (uint64_t)e / 32, sc);
+          acc.bias.add(bsum);
+        }
+      } else if (nb16 == 2) {
+        uint32_t cw[4], sc[2];
+        f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
+        quant_two16<FMT, F32, RHT, SR>(p, sgn, cx, dv, tab, (uint64_t)e, seed, cw, sc, b2, s2, e2,
+                                       nonfinite);
+        *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        put_scale(o, f, (uint64_t)e / 16, sc[0]);
+        put_scale(o, f, (uint64_t)e / 16 + 1, sc[1]);
+        kb.add(b2);
+        ks.add(s2);
+        ke.add(e2);
+      } else if (nb16 == 1) {
+        // a lone 16-block at the very end of the copy
+        float bsum = 0.f, ssum = 0.f, esum = 0.f;
+        f2 Q[8];
+        load_block16<F32, RHT>(p, sgn, Q);
+        uint32_t cw[2];
+        const uint32_t sc = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+                                                     acc, nonfinite);
+        *reinterpret_cast<uint2*>(o.codes + e / 2) = make_uint2(cw[0], cw[1]);
+        put_scale(o, f, (uint64_t)e / 16, sc);
+        kb.add(f2_make(bsum, 0.f));
+        ks.add(f2_make(ssum, 0.f));
+        ke.add(f2_make(esum, 0.f));
+      }
+    }
+    timed_out = __syncthreads_or(!ok);
+    if (timed_out) break;
+    if (tid == 0) {
+      const int64_t nx = c + (int64_t)S * gridDim.x;
+      if (nx < f.nchunks) ring_issue<F32>(f, nx, ring, s, smem_u32(&full[s]));
+    }
+  }
+  if (timed_out) {
+    ring_drain<F32>(f, full, it);
+    if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
+  }
+
+  // ---- statistics: one partial per CTA (summed on the host by fp4q_stats) ----
+  if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
+  if constexpr (FMT == 1) {
+    const double p[3] = {acc.bias.value(), acc.sig64, acc.err64};
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const double v = cta_sum<RT>(p[k], sh_sum);
+      if (tid == 0) ws->stat_part[0][k][blockIdx.x] = v;
+    }
+  } else {
+    float v[3] = {kb.value_f(), ks.value_f(), ke.value_f()};
+    cta_sums_f32<RT, 3>(v, sh_f);
+    if (tid == 0) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) ws->stat_part[0][k][blockIdx.x] = (double)v[k];
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    ws->stat_nparts = gridDim.x;
+    ws->copies = 1u;
+    ws->tensor_scale[0] = (FMT == 1) ? 1.f : cx.g;
+    ws->qmax = kQmax;
+    ws->n = (double)f.n;
+    if (o.tensor_scale) *o.tensor_scale = (FMT == 1) ? 1.f : cx.g;
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------
+Flat make_flat(const void* src, int64_t rows, int64_t cols, int block) {
+  Flat f{};
+  f.src = static_cast<const uint8_t*>(src);
+  f.n = rows * cols;
+  f.nchunks = (f.n + CH - 1) / CH;
+  const int64_t nkb = cols / block;
+  f.nkb = make_fastdiv((uint32_t)nkb);
+  f.small = (f.n / block < (int64_t(1) << 32) && nkb < (int64_t(1) << 32)) ? 1 : 0;
+  return f;
+}
+
+template <typename K>
+int grid_for(K kernel, int smem, int64_t nchunks) {
+  const int occ = cached_occupancy(reinterpret_cast<const void*>(kernel), RT, smem);
+  int64_t g = (int64_t)sm_count() * (occ > 0 ? occ : 1);
+  if (g > kMaxCtas) g = kMaxCtas;
+  return (int)(nchunks < g ? nchunks : g);
+}
+
+template <typename K>
+cudaError_t prepare(K kernel, int smem) {
+  static_assert(sizeof(K) > 0, "");
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <bool F32, bool RHT>
+cudaError_t launch_amax_rows(const Flat& f, uint64_t seed, Workspace* ws, cudaStream_t s) {
+  auto k = amax_rows_kernel<F32, RHT>;
+  constexpr int smem = Ring<F32>::kSmem;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid_for(k, smem, f.nchunks), RT, smem, s>>>(f, seed, ws, kRingTimeoutNs);
+  return cudaGetLastError();
+}
+
+template <int FMT, bool F32, bool RHT, bool SR>
+cudaError_t launch_quant_rows(const Flat& f, uint64_t seed, const CopyOut& o, Workspace* ws,
+                              cudaStream_t s) {
+  auto k = quant_rows_kernel<FMT, F32, RHT, SR>;
+  constexpr int smem = Ring<F32>::kSmem;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid_for(k, smem, f.nchunks), RT, smem, s>>>(f, seed, o, ws, kRingTimeoutNs);
+  return cudaGetLastError();
+}
+
+template <int FMT, bool F32>
+cudaError_t dispatch_quant_rows(int rht, int sr, const Flat& f, uint64_t seed, const CopyOut& o,
+                                Workspace* ws, cudaStream_t s) {
+  if (rht) return sr ? launch_quant_rows<FMT, F32, true, true>(f, seed, o, ws, s)
+                     : launch_quant_rows<FMT, F32, true, false>(f, seed, o, ws, s);
+  return sr ? launch_quant_rows<FMT, F32, false, true>(f, seed, o, ws, s)
+            : launch_quant_rows<FMT, F32, false, false>(f, seed, o, ws, s);
+}
+
+}  // namespace
+
+cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s) {
+  const Flat f = make_flat(a.src, a.rows, a.cols, a.fmt == 1 ? 32 : 16);
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  if (a.dtype == 1) return a.rht ? launch_amax_rows<true, true>(f, a.seed, ws, s)
+                                 : launch_amax_rows<true, false>(f, a.seed, ws, s);
+  return a.rht ? launch_amax_rows<false, true>(f, a.seed, ws, s)
+               : launch_amax_rows<false, false>(f, a.seed, ws, s);
+}
+
+cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
+  const int block = a.fmt == 1 ? 32 : 16;
+  const Flat f = make_flat(a.src, a.rows, a.cols, block);
+  CopyOut o{};
+  o.codes = a.row.codes;
+  o.scales = a.row.scales;
+  o.tensor_scale = a.row.tensor_scale;
+  o.mma = a.row.scale_layout;
+  o.ld = a.cols / 2;
+  o.nkb = a.cols / block;
+  o.nkb_p = (o.nkb + 3) / 4 * 4;
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  const bool f32 = a.dtype == 1;
+  const int sr = a.rounding == 1;
+  switch (a.fmt) {
+    case 0: return f32 ? dispatch_quant_rows<0, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<0, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 1: return f32 ? dispatch_quant_rows<1, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<1, false>(a.rht, sr, f, a.seed, o, ws, s);
+    default: return f32 ? dispatch_quant_rows<2, true>(a.rht, sr, f, a.seed, o, ws, s)
+                        : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s);
+  }
+}
+
+}  // namespace fp4q

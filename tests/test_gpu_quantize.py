@@ -265,3 +265,58 @@ def test_split_amax_then_quantize(lib, fmt, rht, axis):
     if axis in ("col", "both"):
         check_copy(c, ref["col"], "linear")
         check_stats(cs, ref["col"]["stats"])
+
+
+# ---- the row-wise stream kernels: ragged tails, tiled scales, subnormals ----------
+
+RAGGED = [(1, 16), (3, 48), (207, 272), (129, 8208), (33, 4096 + 32)]
+
+
+@pytest.mark.parametrize("shape", RAGGED)
+@pytest.mark.parametrize("fmt,rht,rounding,layout", [
+    ("nvfp4", False, "rtne", "linear"), ("nvfp4", True, "rtne", "mma"), ("nvfp4", True, "sr", "linear"),
+    ("ufp4", True, "rtne", "mma"), ("ufp4", False, "sr", "linear"),
+    ("mxfp4", False, "rtne", "mma"), ("mxfp4", True, "sr", "linear")])
+def test_rowwise_stream_ragged(lib, shape, fmt, rht, rounding, layout):
+    """Row-wise copies whose element count leaves a partial chunk and, where
+    rows x cols is an odd multiple of 16, a half-filled last thread segment;
+    odd block counts per row exercise the tiled scale layout's row split."""
+    rows, cols = shape
+    if fmt == "mxfp4" and cols % 32:
+        pytest.skip("MXFP4 needs cols % 32 == 0")
+    x = synth.normal_with_outliers(rows, cols, 1.0, 0.01, 20.0, 17)
+    r, _ = lib.fp4q_quantize(x.cuda(), fmt=fmt, rht=rht, rounding=rounding, seed=5, axis="row",
+                             layout=layout)
+    rs, _ = lib.fp4q_stats()
+    assert lib.fp4q_status() == 0
+    ref = o.quantize(_bits(x), fmt, rht=rht, rounding=rounding, seed=5, axis="row")["row"]
+    check_copy(r, ref, layout)
+    check_stats(rs, ref["stats"])
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "ufp4", "mxfp4"])
+@pytest.mark.parametrize("rht", [False, True])
+def test_fp32_subnormal_inputs(lib, fmt, rht):
+    """FP32 inputs in the subnormal range next to normal ones: every packed
+    FP32x2 step must keep subnormals (no flush to zero), as the oracle does."""
+    g = torch.Generator().manual_seed(23)
+    x = torch.randn(64, 256, generator=g) * 1e-39          # mostly subnormal
+    x[:, ::7] *= 1e6                                        # some normal neighbours
+    x[5] = torch.randn(256, generator=g) * 1e-44            # a row of the smallest subnormals
+    x = x.float()
+    r, _ = lib.fp4q_quantize(x.cuda(), fmt=fmt, rht=rht, seed=3, axis="row")
+    rs, _ = lib.fp4q_stats()
+    ref = o.quantize(x.numpy(), fmt, rht=rht, seed=3, axis="row")["row"]
+    check_copy(r, ref, "linear")
+    y = lib.fp4q_dequantize(r, inverse_rht=rht, seed=3)
+    want = o.dequantize(ref["codes"], ref["scales"], ref["tensor_scale"], fmt, inverse_rht=rht, seed=3)
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp4"])
+def test_rowwise_nonfinite_sets_status(lib, fmt):
+    for bad in (float("nan"), float("inf"), float("-inf")):
+        x = torch.randn(40, 256).to(torch.bfloat16)
+        x[17, 3] = bad
+        lib.fp4q_quantize(x.cuda(), fmt=fmt, axis="row", rht=True, seed=1)
+        assert lib.fp4q_status() == 4, bad
