@@ -616,9 +616,9 @@ def main(argv=None) -> int:
     # per-kernel averages over the timed region
     kern = {
         "amax": {"ms": statistics.fmean(main_r["amax_ms"]), "bytes": B_AMAX * n_el,
-                 "launches": len(main_r["amax_ms"]), "ncu_name": "amax_kernel"},
+                 "launches": len(main_r["amax_ms"]), "ncu_name": "amax_rows_kernel"},
         "quantize": {"ms": statistics.fmean(main_r["quant_ms"]), "bytes": B_QUANT * n_el,
-                     "launches": len(main_r["quant_ms"]), "ncu_name": "quantize_kernel"},
+                     "launches": len(main_r["quant_ms"]), "ncu_name": "quant_rows_kernel"},
         "dequantize": {"ms": statistics.fmean(main_r["deq_ms"]), "bytes": B_DEQ * n_el,
                        "launches": len(main_r["deq_ms"]), "ncu_name": "dequantize_kernel"},
     }
