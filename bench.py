@@ -7,9 +7,9 @@ tensor (Student-t nu = 3 times a per-column lognormal scale) quantised three
 ways -- E2M1/NVFP4 without the RHT, E2M1/NVFP4 with the 16-point RHT, uniform
 E1M2/UFP4 with the RHT -- 16-element blocks, RTNE, row-wise, statistics fused;
 then the UFP4 copy dequantised with the inverse RHT back to BF16 (UFP4 has no
-tensor-core format: a consumer dequantises it). Every quantisation is its
-amax pass followed by its quantisation pass, launched through the C ABI
-(fp4q_amax, fp4q_quantize with FP4Q_AMAX_READY) so that each pass can be timed.
+tensor-core format: a consumer dequantises it). Each quantisation is one
+fp4q_quantize call through the C ABI: both passes of the method (the tensor
+amax, then the block scales and codes) in one launch.
 
   value   algorithmic bytes of the step / step time, GB/s (whole job: all ranks)
   e2e     the same bytes / the time of the same step through the Python binding
@@ -51,9 +51,10 @@ GEMM_N = 8192
 FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / BF16 tensor rate
 L2_FLUSH_BYTES = 256 << 20
 
-# algorithmic bytes per element (BF16 input): amax pass reads 2; the quantise
-# pass reads 2 and writes 0.5 of codes + 1/16 of E4M3 scales; the dequantise
-# pass reads 0.5 + 1/16 and writes 2.
+# algorithmic bytes per element (BF16 input): the amax pass reads 2; the
+# quantisation pass reads 2 and writes 0.5 of codes + 1/16 of E4M3 scales (one
+# fp4q_quantize launch does both passes); the dequantise pass reads 0.5 + 1/16
+# and writes 2.
 B_AMAX = 2.0
 B_QUANT = 2.0 + 0.5 + 1.0 / 16
 B_DEQ = 0.5 + 1.0 / 16 + 2.0
@@ -346,23 +347,16 @@ class RawCalls:
         for (fmt, rht), q in zip(WAYS, outs):
             s = q.c_struct()
             self.calls.append((
-                (x.data_ptr(), 0, rows, cols, fq.FORMATS[fmt], fq.BLOCKS[fmt], int(rht), SEED, 1,
-                 ws.data_ptr(), ws.numel(), stream),
                 (x.data_ptr(), 0, rows, cols, fq.FORMATS[fmt], fq.BLOCKS[fmt], int(rht), 0, SEED,
-                 1 | 4, ctypes.byref(s), None, ws.data_ptr(), ws.numel(), stream),
+                 1, ctypes.byref(s), None, ws.data_ptr(), ws.numel(), stream),
                 s))
         u = outs[-1]
         self.deq_struct = u.c_struct()
         self.deq_args = (ctypes.byref(self.deq_struct), rows, cols, fq.FORMATS["ufp4"], 16, 1, SEED,
                          deq_out.data_ptr(), 0, stream)
 
-    def amax(self, i):
-        rc = self.lib.fp4q_amax(*self.calls[i][0])
-        if rc:
-            raise self.fq.FP4QError("fp4q_amax", rc)
-
     def quant(self, i):
-        rc = self.lib.fp4q_quantize(*self.calls[i][1])
+        rc = self.lib.fp4q_quantize(*self.calls[i][0])
         if rc:
             raise self.fq.FP4QError("fp4q_quantize", rc)
 
@@ -384,16 +378,14 @@ def run_main_leg(fq, torch, device, steps, warmup):
     x_ref = x.clone()
 
     def one_step(ev):
+        ev[0].record(stream)
         for i in range(len(WAYS)):
-            ev[3 * i].record(stream)
-            raw.amax(i)
-            ev[3 * i + 1].record(stream)
             raw.quant(i)
-            ev[3 * i + 2].record(stream)
+            ev[i + 1].record(stream)
         raw.deq()
-        ev[3 * len(WAYS)].record(stream)
+        ev[len(WAYS) + 1].record(stream)
 
-    nev = 3 * len(WAYS) + 1
+    nev = len(WAYS) + 2
     for _ in range(warmup):
         flush.zero_()
         one_step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
@@ -412,13 +404,12 @@ def run_main_leg(fq, torch, device, steps, warmup):
     wall = time.perf_counter() - w0
     barrier(device)
 
-    step_ms, amax_ms, quant_ms, deq_ms = [], [], [], []
+    step_ms, quant_ms, deq_ms = [], [], []
     for ev in evs:
         step_ms.append(ev[0].elapsed_time(ev[nev - 1]))
         for i in range(len(WAYS)):
-            amax_ms.append(ev[3 * i].elapsed_time(ev[3 * i + 1]))
-            quant_ms.append(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]))
-        deq_ms.append(ev[3 * len(WAYS) - 1].elapsed_time(ev[nev - 1]))
+            quant_ms.append(ev[i].elapsed_time(ev[i + 1]))
+        deq_ms.append(ev[nev - 2].elapsed_time(ev[nev - 1]))
     status = fq.fp4q_status(ws)
     # self-checks outside the timed region: the input is intact, and the
     # statistics of a repeated quantisation are identical (no state leaks
@@ -428,17 +419,15 @@ def run_main_leg(fq, torch, device, steps, warmup):
     for (fmt, rht), q in zip(WAYS, outs):
         seen = []
         for _ in range(2):
-            fq.fp4q_amax(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws)
-            fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q,
-                             amax_ready=True)
+            fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q)
             rs, _ = fq.fp4q_stats(ws)
             seen.append((rs["shrink_bias"], rs["snr_db"]))
         repeat_same &= seen[0] == seen[1]
         stats[f"{fmt}{'+rht' if rht else ''}"] = {"shrink_bias": seen[0][0], "snr_db": seen[0][1]}
     checks["stats_repeatable"] = bool(repeat_same)
-    return {"step_ms_total": sum(step_ms), "wall_s": wall, "amax_ms": amax_ms,
+    return {"step_ms_total": sum(step_ms), "wall_s": wall,
             "quant_ms": quant_ms, "deq_ms": deq_ms, "status": status, "stats": stats,
-            "checks": checks, "launches_per_step": 2 * len(WAYS) + 1}
+            "checks": checks, "launches_per_step": len(WAYS) + 1}
 
 
 def run_e2e_leg(fq, torch, device, steps, warmup):
@@ -464,9 +453,7 @@ def run_e2e_leg(fq, torch, device, steps, warmup):
     def one_step():
         x.copy_(x_host, non_blocking=True)
         for (fmt, rht), q, (hc, hs, ht) in zip(WAYS, outs, hosts):
-            fq.fp4q_amax(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws)
-            fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q,
-                             amax_ready=True)
+            fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, axis="row", ws=ws, row_out=q)
             fq.fp4q_stats(ws)
             hc.copy_(q.codes, non_blocking=True)
             hs.copy_(q.scales, non_blocking=True)
@@ -506,9 +493,8 @@ def run_gemm_leg(fq, torch, device, steps, warmup):
     def one(ev):
         ev[0].record(stream)
         for src, q in ((a, qa), (b, qb)):
-            fq.fp4q_amax(src, fmt="nvfp4", rht=True, seed=SEED, axis="row", ws=ws)
             fq.fp4q_quantize(src, fmt="nvfp4", rht=True, seed=SEED, axis="row", layout="mma",
-                             ws=ws, row_out=q, amax_ready=True)
+                             ws=ws, row_out=q)
         ev[1].record(stream)
         fq.fp4q_gemm(qa, qb, out=y, ws=ws)
         ev[2].record(stream)
@@ -539,7 +525,9 @@ def run_gemm_leg(fq, torch, device, steps, warmup):
 def run_sweep(fq, torch, device, args, peaks) -> None:
     """MXFP4 (32-element E8M0 blocks, one pass) vs NVFP4 (16-element E4M3
     blocks, amax pass + quantisation pass) on R x 4096 N(0,1) BF16 tensors,
-    RTNE, no RHT, row-wise: time per call and GB/s of algorithmic bytes."""
+    RTNE, no RHT, row-wise: time per call and GB/s of algorithmic bytes. NVFP4
+    is timed as the two-call split (fp4q_amax, then fp4q_quantize with the amax
+    ready) and as the one-launch fp4q_quantize."""
     import synth
     cols = 4096
     ws = fq.workspace(device)
@@ -553,7 +541,7 @@ def run_sweep(fq, torch, device, args, peaks) -> None:
         out = {}
         for fmt in ("mxfp4", "nvfp4"):
             q = fq.alloc_copy(rows, cols, fmt, "linear", device)
-            times = {"amax": [], "quant": []}
+            times = {"amax": [], "quant": [], "one": []}
             for k in range(args.warmup + args.steps):
                 flush.zero_()
                 e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
@@ -562,10 +550,17 @@ def run_sweep(fq, torch, device, args, peaks) -> None:
                 e1.record(stream)
                 fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q, amax_ready=True)
                 e2.record(stream)
+                flush.zero_()
+                e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+                e3.record(stream)
+                fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q)
+                e4.record(stream)
                 if k >= args.warmup:
                     times["amax"].append((e0, e1))
                     times["quant"].append((e1, e2))
+                    times["one"].append((e3, e4))
             torch.cuda.synchronize(device)
+            t_one = statistics.median(a.elapsed_time(b) for a, b in times["one"])
             t_a = statistics.median(a.elapsed_time(b) for a, b in times["amax"]) if fmt == "nvfp4" else 0.0
             t_q = statistics.median(a.elapsed_time(b) for a, b in times["quant"])
             b_q = (2.0 + 0.5 + (1.0 / 16 if fmt == "nvfp4" else 1.0 / 32)) * n
@@ -574,7 +569,9 @@ def run_sweep(fq, torch, device, args, peaks) -> None:
                         "quant_us": t_q * 1e3, "quant_GB/s": b_q / (t_q / 1e3) / 1e9,
                         "quant_frac_hbm": b_q / (t_q / 1e3) / 1e9 / peaks["hbm_gbs"]}
             if fmt == "nvfp4":
-                out[fmt].update({"amax_us": t_a * 1e3, "amax_GB/s": b_a / (t_a / 1e3) / 1e9})
+                out[fmt].update({"amax_us": t_a * 1e3, "amax_GB/s": b_a / (t_a / 1e3) / 1e9,
+                                 "one_launch_us": t_one * 1e3,
+                                 "one_launch_GB/s": (b_a + b_q) / (t_one / 1e3) / 1e9})
             del q
         print(json.dumps({"sweep": "R x 4096 BF16 N(0,1), RTNE, no RHT, row-wise", "rows": rows,
                           "elements": n, **out}), flush=True)
@@ -615,12 +612,10 @@ def main(argv=None) -> int:
 
     # per-kernel averages over the timed region
     kern = {
-        "amax": {"ms": statistics.fmean(main_r["amax_ms"]), "bytes": B_AMAX * n_el,
-                 "launches": len(main_r["amax_ms"]), "ncu_name": "amax_rows_kernel"},
-        "quantize": {"ms": statistics.fmean(main_r["quant_ms"]), "bytes": B_QUANT * n_el,
-                     "launches": len(main_r["quant_ms"]), "ncu_name": "quant_rows_kernel"},
+        "quantize": {"ms": statistics.fmean(main_r["quant_ms"]), "bytes": (B_AMAX + B_QUANT) * n_el,
+                     "launches": len(main_r["quant_ms"]), "ncu_name": "quant_fused_kernel"},
         "dequantize": {"ms": statistics.fmean(main_r["deq_ms"]), "bytes": B_DEQ * n_el,
-                       "launches": len(main_r["deq_ms"]), "ncu_name": "dequantize_kernel"},
+                       "launches": len(main_r["deq_ms"]), "ncu_name": "dequant_rows_kernel"},
     }
     for k in kern.values():
         k["gbs"] = k["bytes"] / (k["ms"] / 1e3) / 1e9
@@ -675,7 +670,7 @@ def main(argv=None) -> int:
                                         "(nominal dense FP4/BF16 ratio)",
                          "traffic": ncu_traffic("gemm_nvf4_kernel", flop)},
         }
-        line["gpu_launches_gemm_leg"] = 5 * args.steps
+        line["gpu_launches_gemm_leg"] = 3 * args.steps
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -31,8 +31,10 @@ struct Workspace {
   unsigned int copies;          // axis bits produced by the last quantisation pass
   float tensor_scale[2];        // g of its row / column copy
   float qmax;                   // its Qmax
-  unsigned int reserved;
+  unsigned int gbar_count;      // grid barrier of the one-launch quantiser: arrivals (wraps to 0)
   double n;                     // its elements per copy
+  unsigned int gbar_gen;        // grid barrier: generation, bumped by the last arrival
+  unsigned int reserved;
   unsigned int amax_part[2][kMaxCtas];   // per-CTA max |v| (FP32 bits) of the row / column copy
   double stat_part[2][3][kMaxCtas];      // per-CTA sums: bias (grid units); signal, error
                                          // (grid units x s^2; MXFP4: absolute)
@@ -291,6 +293,40 @@ __device__ __forceinline__ void cta_sums_f32(float (&v)[K], float (*sh)[kNT / 32
     }
   }
   __syncthreads();
+}
+
+
+// Barrier over every CTA of a co-resident (cooperatively launched) grid,
+// through the workspace: the last CTA to arrive bumps the generation the
+// others poll. Bounded: returns false (every thread) if the wait ran out.
+__device__ __forceinline__ bool grid_barrier(Workspace* ws, uint64_t timeout_ns) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    volatile unsigned int* gen = &ws->gbar_gen;
+    const unsigned int g0 = *gen;
+    __threadfence();
+    const unsigned int prev = atomicInc(&ws->gbar_count, gridDim.x - 1);
+    if (prev == gridDim.x - 1) {
+      __threadfence();
+      atomicAdd(&ws->gbar_gen, 1u);
+    } else {
+      uint64_t t0 = 0;
+      for (uint32_t i = 1; *gen == g0; ++i) {
+        if ((i & 255u) == 0u) {
+          uint64_t now;
+          asm volatile("mov.u64 %0, %globaltimer;" : "=l"(now));
+          if (t0 == 0) t0 = now;
+          else if (now - t0 > timeout_ns) { ok = 0; break; }
+        }
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
 }
 
 }  // namespace fp4q

@@ -58,6 +58,8 @@ cudaError_t run_amax(const QuantArgs& a, cudaStream_t s);
 // pass of a row-wise-only request.
 cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s);
+// Both passes of a row-wise NVFP4/UFP4 request in one cooperative launch.
+cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
 // Returns cudaErrorNotSupported when no GEMM kernel covers the request.
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s);

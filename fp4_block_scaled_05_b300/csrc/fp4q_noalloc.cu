@@ -56,9 +56,10 @@ extern "C" int fp4q_quantize_noalloc(const void* src, int dtype, int64_t rows, i
   void* scratch = nullptr;
   const int rc = scratch_address(&scratch);
   if (rc) return rc;
-  // the status word and the partial counts must start at zero; everything
-  // else in the scratch is written before it is read within one call
-  const size_t head = offsetof(fp4q::Workspace, tensor_scale);
+  // the header (status word, partial counts, grid-barrier state) must start
+  // at zero; everything else in the scratch is written before it is read
+  // within one call
+  const size_t head = offsetof(fp4q::Workspace, amax_part);
   if (cudaMemsetAsync(scratch, 0, head, (cudaStream_t)stream) != cudaSuccess) return FP4Q_ECUDA;
   return fp4q_quantize(src, dtype, rows, cols, fmt, block, rht, rounding, seed, axis, row_out,
                        col_out, scratch, kNoAllocScratchBytes, stream);

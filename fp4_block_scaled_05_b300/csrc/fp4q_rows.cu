@@ -22,6 +22,7 @@
 #include <cfloat>
 #include <cstdint>
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -86,9 +87,11 @@ __device__ __forceinline__ void ring_issue(const Flat& f, int64_t chunk, uint8_t
   bulk_load(smem_u32(ring + slot * Ring<F32>::kChunkBytes), f.src + e0 * es, bytes, bar);
 }
 
-// Thread 0 starts the first copies; every slot's barrier completes one phase per copy.
+// Thread 0 starts the first copies; every slot's barrier completes one phase
+// per copy. `reverse`: the CTA's k-th chunk is counted from the end.
 template <bool F32>
-__device__ __forceinline__ void ring_start(const Flat& f, uint8_t* ring, uint64_t* full) {
+__device__ __forceinline__ void ring_start(const Flat& f, uint8_t* ring, uint64_t* full,
+                                           bool reverse = false) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < Ring<F32>::kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
     fence_mbarrier_init();
@@ -97,7 +100,7 @@ __device__ __forceinline__ void ring_start(const Flat& f, uint8_t* ring, uint64_
   if (threadIdx.x == 0) {
     for (int s = 0; s < Ring<F32>::kStages; ++s) {
       const int64_t c = blockIdx.x + (int64_t)s * gridDim.x;
-      if (c < f.nchunks) ring_issue<F32>(f, c, ring, s, smem_u32(&full[s]));
+      if (c < f.nchunks) ring_issue<F32>(f, reverse ? f.nchunks - 1 - c : c, ring, s, smem_u32(&full[s]));
     }
   }
 }
@@ -311,11 +314,11 @@ __device__ __forceinline__ uint32_t e2m1_pair(f2 Y, f2& D) {
   float y0, y1;
   f2_split(Y, y0, y1);
   uint32_t byte, hq;
-  asm("{\n\t.reg .b8 t;\n\t.reg .b32 m;\n\t"
+  asm("{\n\t.reg .b8 t;\n\t"
       "cvt.rn.satfinite.e2m1x2.f32 t, %3, %2;\n\t"
       "cvt.u32.u8 %0, t;\n\t"
-      "and.b32 m, %0, 0x77;\n\t"
-      "cvt.u8.u32 t, m;\n\t"
+      "and.b32 %1, %0, 0x77;\n\t"
+      "cvt.u8.u32 t, %1;\n\t"
       "cvt.rn.f16x2.e2m1x2 %1, t;\n\t}"
       : "=r"(byte), "=r"(hq) : "f"(y0), "f"(y1));
   D = f2_make(sub_f16_f32((uint16_t)(hq & 0xFFFFu), fabsf(y0)),
@@ -587,6 +590,96 @@ __device__ __forceinline__ void put_scale(const CopyOut& o, const Flat& f, uint6
   o.scales[mma_scale_offset((int64_t)r, (int64_t)kb, o.nkb_p)] = (uint8_t)sc;
 }
 
+// ---- per-thread work on its 32 elements of a ring slot ---------------------------------
+// Running max |v| of the (up to two) 16-blocks at p: `m` (FP32 values; |w| = 4|v|
+// with the RHT) or `m2` (BF16 pairs, no RHT).
+template <bool F32, bool RHT>
+__device__ __forceinline__ void amax_segment(const uint8_t* p, int nb, const uint32_t (&sgn)[16], float& m,
+                                             uint32_t& m2) {
+#pragma unroll
+  for (int b = 0; b < 2; ++b) {
+    if (b < nb) {
+      const uint8_t* pb = p + b * 16 * (F32 ? 4 : 2);
+      if constexpr (!RHT && !F32) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint4 u = *reinterpret_cast<const uint4*>(pb + 16 * k);
+          m2 = max_abs_nan_bf16x2(m2, u.x);
+          m2 = max_abs_nan_bf16x2(m2, u.y);
+          m2 = max_abs_nan_bf16x2(m2, u.z);
+          m2 = max_abs_nan_bf16x2(m2, u.w);
+        }
+      } else {
+        float x[16];
+        widen16<F32, RHT>(pb, sgn, x);
+        if (RHT) rht16_unscaled(x);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) m = max3_abs_nan(m, x[i], x[i + 1]);
+      }
+    }
+  }
+}
+
+// The thread's max |v| from its running maxima. With the RHT the maxima are of
+// |w| = 4 |v|: scaling the maximum once is exact (or monotone) and gives max |v|.
+template <bool F32, bool RHT>
+__device__ __forceinline__ float amax_result(float m, uint32_t m2) {
+  if constexpr (!RHT && !F32) {
+    m = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+    if ((m2 & 0x7FFFu) > 0x7F80u || (m2 >> 16 & 0x7FFFu) > 0x7F80u) m = __uint_as_float(0x7FFFFFFFu);
+  }
+  return RHT ? __fmul_rn(m, 0.25f) : m;
+}
+
+// Quantise the thread's 32 elements at p (elements e .. e+31 of the copy) and
+// add their statistics to the running sums.
+template <int FMT, bool F32, bool RHT, bool SR>
+__device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const Flat& f, const CopyOut& o,
+                                              const uint32_t (&sgn)[16], const Ctx& cx, const Divider& dv,
+                                              const float2* tab, uint64_t seed, Sums& acc, Kahan2& kb,
+                                              Kahan2& ks, Kahan2& ke, uint32_t& nonfinite) {
+  constexpr int ES = F32 ? 4 : 2;
+  const int nb16 = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
+  if constexpr (FMT == 1) {
+    if (nb16 == 2) {
+      float bsum = 0.f, ssum = 0.f, esum = 0.f;
+      f2 Q[16];
+      load_block16<F32, RHT>(p, sgn, Q);
+      load_block16<F32, RHT>(p + 16 * ES, sgn, Q + 8);
+      uint32_t cw[4];
+      const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+                                                    acc, nonfinite);
+      *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      put_scale(o, f, (uint64_t)e / 32, sc);
+      acc.bias.add(bsum);
+    }
+  } else if (nb16 == 2) {
+    uint32_t cw[4], sc[2];
+    f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
+    quant_two16<FMT, F32, RHT, SR>(p, sgn, cx, dv, tab, (uint64_t)e, seed, cw, sc, b2, s2, e2,
+                                   nonfinite);
+    *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    put_scale(o, f, (uint64_t)e / 16, sc[0]);
+    put_scale(o, f, (uint64_t)e / 16 + 1, sc[1]);
+    kb.add(b2);
+    ks.add(s2);
+    ke.add(e2);
+  } else if (nb16 == 1) {
+    // a lone 16-block at the very end of the copy
+    float bsum = 0.f, ssum = 0.f, esum = 0.f;
+    f2 Q[8];
+    load_block16<F32, RHT>(p, sgn, Q);
+    uint32_t cw[2];
+    const uint32_t sc = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+                                                 acc, nonfinite);
+    *reinterpret_cast<uint2*>(o.codes + e / 2) = make_uint2(cw[0], cw[1]);
+    put_scale(o, f, (uint64_t)e / 16, sc);
+    kb.add(f2_make(bsum, 0.f));
+    ks.add(f2_make(ssum, 0.f));
+    ke.add(f2_make(esum, 0.f));
+  }
+}
+
 // ---- K1: tensor amax of the row-wise copy ----------------------------------------
 template <bool F32, bool RHT>
 __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed, Workspace* ws,
@@ -598,7 +691,9 @@ __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed,
   const int tid = threadIdx.x;
   uint32_t sgn[16];
   make_sign_words<F32>(RHT ? rht_sign_mask(seed) : 0u, sgn);
-  ring_start<F32>(f, ring, full);
+  // chunks are visited from the end of the tensor, so that the quantisation
+  // pass (which walks forward) starts on the chunks this pass left in L2
+  ring_start<F32>(f, ring, full, true);
 
   float m = 0.f;
   uint32_t m2 = 0u;      // BF16 pairs without the RHT
@@ -608,50 +703,22 @@ __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed,
     const int s = (int)(it % S);
     const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
     if (ok) {
-      const int64_t e = c * CH + (int64_t)tid * EPT;
+      const int64_t e = (f.nchunks - 1 - c) * CH + (int64_t)tid * EPT;
       const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
-      const uint8_t* p = ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2);
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        if (b < nb) {
-          const uint8_t* pb = p + b * 16 * (F32 ? 4 : 2);
-          if constexpr (!RHT && !F32) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const uint4 u = *reinterpret_cast<const uint4*>(pb + 16 * k);
-              m2 = max_abs_nan_bf16x2(m2, u.x);
-              m2 = max_abs_nan_bf16x2(m2, u.y);
-              m2 = max_abs_nan_bf16x2(m2, u.z);
-              m2 = max_abs_nan_bf16x2(m2, u.w);
-            }
-          } else {
-            float x[16];
-            widen16<F32, RHT>(pb, sgn, x);
-            if (RHT) rht16_unscaled(x);
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) m = max3_abs_nan(m, x[i], x[i + 1]);
-          }
-        }
-      }
+      amax_segment<F32, RHT>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2), nb, sgn, m, m2);
     }
     timed_out = __syncthreads_or(!ok);
     if (timed_out) break;
     if (tid == 0) {
       const int64_t nx = c + (int64_t)S * gridDim.x;
-      if (nx < f.nchunks) ring_issue<F32>(f, nx, ring, s, smem_u32(&full[s]));
+      if (nx < f.nchunks) ring_issue<F32>(f, f.nchunks - 1 - nx, ring, s, smem_u32(&full[s]));
     }
   }
   if (timed_out) {
     ring_drain<F32>(f, full, it);
     if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
   }
-  if constexpr (!RHT && !F32) {
-    m = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
-    if ((m2 & 0x7FFFu) > 0x7F80u || (m2 >> 16 & 0x7FFFu) > 0x7F80u) m = __uint_as_float(0x7FFFFFFFu);
-  }
-  // with the RHT the maxima above are of |w| = 4 |v|: scaling the maximum once
-  // is exact (or monotone) and gives max |v|
-  const uint32_t cm = cta_max<RT>(__float_as_uint(RHT ? __fmul_rn(m, 0.25f) : m), sh_max);
+  const uint32_t cm = cta_max<RT>(__float_as_uint(amax_result<F32, RHT>(m, m2)), sh_max);
   if (tid == 0) {
     ws->amax_part[0][blockIdx.x] = cm;
     ws->amax_part[1][blockIdx.x] = cm;
@@ -696,46 +763,8 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
     const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
     if (ok) {
       const int64_t e = c * CH + (int64_t)tid * EPT;
-      const int nb16 = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
-      const uint8_t* p = ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES;
-      if constexpr (FMT == 1) {
-        if (nb16 == 2) {
-          float bsum = 0.f, ssum = 0.f, esum = 0.f;
-          f2 Q[16];
-          load_block16<F32, RHT>(p, sgn, Q);
-          load_block16<F32, RHT>(p + 16 * ES, sgn, Q + 8);
-          uint32_t cw[4];
-          const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
-                                                        acc, nonfinite);
-          *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          put_scale(o, f, (uint64_t)e / 32, sc);
-          acc.bias.add(bsum);
-        }
-      } else if (nb16 == 2) {
-        uint32_t cw[4], sc[2];
-        f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
-        quant_two16<FMT, F32, RHT, SR>(p, sgn, cx, dv, tab, (uint64_t)e, seed, cw, sc, b2, s2, e2,
-                                       nonfinite);
-        *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        put_scale(o, f, (uint64_t)e / 16, sc[0]);
-        put_scale(o, f, (uint64_t)e / 16 + 1, sc[1]);
-        kb.add(b2);
-        ks.add(s2);
-        ke.add(e2);
-      } else if (nb16 == 1) {
-        // a lone 16-block at the very end of the copy
-        float bsum = 0.f, ssum = 0.f, esum = 0.f;
-        f2 Q[8];
-        load_block16<F32, RHT>(p, sgn, Q);
-        uint32_t cw[2];
-        const uint32_t sc = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
-                                                     acc, nonfinite);
-        *reinterpret_cast<uint2*>(o.codes + e / 2) = make_uint2(cw[0], cw[1]);
-        put_scale(o, f, (uint64_t)e / 16, sc);
-        kb.add(f2_make(bsum, 0.f));
-        ks.add(f2_make(ssum, 0.f));
-        ke.add(f2_make(esum, 0.f));
-      }
+      quant_segment<FMT, F32, RHT, SR>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, e, f, o, sgn, cx, dv,
+                                       tab, seed, acc, kb, ks, ke, nonfinite);
     }
     timed_out = __syncthreads_or(!ok);
     if (timed_out) break;
@@ -773,6 +802,253 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
     ws->qmax = kQmax;
     ws->n = (double)f.n;
     if (o.tensor_scale) *o.tensor_scale = (FMT == 1) ? 1.f : cx.g;
+  }
+}
+
+// ---- one launch for both passes (NVFP4 / UFP4 row-wise) ------------------------------
+// A cooperatively launched (co-resident) grid streams its chunks twice through
+// one ring: the amax pass, a grid barrier, the fold of the per-CTA maxima, then
+// the quantisation pass. The ring runs on across the barrier, so the second
+// pass's first chunks are already in flight while the first pass finishes.
+template <int FMT, bool F32, bool RHT, bool SR>
+__global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uint64_t seed, CopyOut o,
+                                                                     Workspace* ws, uint64_t timeout_ns) {
+  static_assert(FMT != 1, "MXFP4 has no tensor amax");
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages];
+  __shared__ float2 tab[128];
+  __shared__ float sh_f[3][RT / 32];
+  __shared__ uint32_t sh_max[RT / 32];
+  constexpr int S = Ring<F32>::kStages;
+  constexpr int ES = F32 ? 4 : 2;
+  constexpr float kQmax = (FMT == 2) ? 7.f : 6.f;
+  constexpr float kQmax448 = (FMT == 2) ? 3136.f : 2688.f;
+  const int tid = threadIdx.x;
+  uint32_t sgn[16];
+  make_sign_words<F32>(RHT ? rht_sign_mask(seed) : 0u, sgn);
+  // this CTA's chunks: bid, bid + grid, ...; visited once per pass
+  const int64_t n1 = (f.nchunks - (int64_t)blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const int64_t total = 2 * n1;
+  auto chunk_of = [&](int64_t it) { return (int64_t)blockIdx.x + (it < n1 ? it : it - n1) * gridDim.x; };
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(smem_u32(&full[s]), 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < S && s < total; ++s) ring_issue<F32>(f, chunk_of(s), ring, s, smem_u32(&full[s]));
+  }
+
+  bool timed_out = false;
+  int64_t it = 0;
+  // ---- pass 1: tensor amax ----
+  float m = 0.f;
+  uint32_t m2 = 0u;
+  for (; it < n1; ++it) {
+    const int s = (int)(it % S);
+    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
+    if (ok) {
+      const int64_t e = chunk_of(it) * CH + (int64_t)tid * EPT;
+      const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
+      amax_segment<F32, RHT>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, nb, sgn, m, m2);
+    }
+    timed_out = __syncthreads_or(!ok);
+    if (timed_out) break;
+    if (tid == 0 && it + S < total) ring_issue<F32>(f, chunk_of(it + S), ring, s, smem_u32(&full[s]));
+  }
+
+  Sums acc;
+  Kahan2 kb, ks, ke;
+  uint32_t nonfinite = 0;
+  Ctx cx{1.f, 0.f, 0.f};
+  if (!timed_out) {
+    const uint32_t cm = cta_max<RT>(__float_as_uint(amax_result<F32, RHT>(m, m2)), sh_max);
+    if (tid == 0) {
+      ws->amax_part[0][blockIdx.x] = cm;
+      ws->amax_part[1][blockIdx.x] = cm;
+      if (blockIdx.x == 0) ws->amax_nparts = gridDim.x;
+    }
+    timed_out = !grid_barrier(ws, timeout_ns);
+  }
+  if (!timed_out) {
+    cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
+    Divider dv{};
+    dv.init(cx.d);
+    fill_scale_table(tab, cx.g);
+    __syncthreads();
+    // ---- pass 2: quantise ----
+    for (; it < total; ++it) {
+      const int s = (int)(it % S);
+      const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
+      if (ok) {
+        const int64_t e = chunk_of(it) * CH + (int64_t)tid * EPT;
+        quant_segment<FMT, F32, RHT, SR>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, e, f, o, sgn, cx,
+                                         dv, tab, seed, acc, kb, ks, ke, nonfinite);
+      }
+      timed_out = __syncthreads_or(!ok);
+      if (timed_out) break;
+      if (tid == 0 && it + S < total) ring_issue<F32>(f, chunk_of(it + S), ring, s, smem_u32(&full[s]));
+    }
+  }
+  if (timed_out) {
+    // let the copies still in flight land before the CTA exits
+    if (tid == 0) {
+      const uint64_t t0 = globaltimer();
+      for (int64_t j = it; j < it + S && j < total; ++j) {
+        const uint32_t bar = smem_u32(&full[j % S]);
+        while (!mbar_try_wait(bar, (uint32_t)((j / S) & 1)) && globaltimer() - t0 < 50000000ull) {
+        }
+      }
+      atomicOr(&ws->status, kStatusTimeout);
+    }
+  }
+
+  // ---- statistics: one partial per CTA (summed on the host by fp4q_stats) ----
+  if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
+  float v[3] = {kb.value_f(), ks.value_f(), ke.value_f()};
+  cta_sums_f32<RT, 3>(v, sh_f);
+  if (tid == 0) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) ws->stat_part[0][k][blockIdx.x] = (double)v[k];
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    ws->stat_nparts = gridDim.x;
+    ws->copies = 1u;
+    ws->tensor_scale[0] = cx.g;
+    ws->qmax = kQmax;
+    ws->n = (double)f.n;
+    if (o.tensor_scale) *o.tensor_scale = cx.g;
+  }
+}
+
+// ---- dequantisation of a row-wise copy -------------------------------------------------
+// v_hat = (level * s_b) * g (MXFP4: level * 2^e_b), two round-to-nearest
+// products in that order; optionally the inverse transform (1/4) diag(sigma)
+// H16 on every 16-block: butterfly stages 1, 2, 4, 8, then * 1/4, then the sign
+// flip. A thread converts 32 consecutive elements (one 16-byte load of codes),
+// grid-stride over the copy.
+
+// Two signed levels of one code byte (bits 0-3 -> lo, bits 4-7 -> hi) as FP32.
+template <int FMT>
+__device__ __forceinline__ void levels2(uint32_t byte, float& lo, float& hi) {
+  if constexpr (FMT == 2) {   // UFP4: integer levels, via the 2^23 offset trick (exact)
+    const uint32_t l = byte & 0xFu, h = (byte >> 4) & 0xFu;
+    const f2 m = f2_sub(f2_make(__uint_as_float(0x4B000000u | (l & 7u)), __uint_as_float(0x4B000000u | (h & 7u))),
+                        f2_make(8388608.f, 8388608.f));
+    float a, b;
+    f2_split(m, a, b);
+    lo = __uint_as_float(__float_as_uint(a) ^ ((l & 8u) << 28));
+    hi = __uint_as_float(__float_as_uint(b) ^ ((h & 8u) << 28));
+  } else {                    // E2M1 through the hardware conversion (exact in FP16)
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "r"(byte));
+    lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+  }
+}
+
+template <int FMT>
+__device__ __forceinline__ float block_scale_value(uint32_t sc) {
+  if constexpr (FMT == 1) {   // E8M0: 2^(sc - 127); code 0 is 2^-127 (subnormal)
+    return sc ? __uint_as_float(sc << 23) : __uint_as_float(0x00400000u);
+  } else {
+    return e4m3_to_f32(sc);
+  }
+}
+
+// Dequantise one 16-block: `w0`, `w1` its code words, `sv` its scale value.
+// Writes 16 values at `out` (BF16 or FP32).
+template <int FMT, bool OUT_F32, bool IRHT>
+__device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float g, const uint32_t (&sgn)[16],
+                                      void* out) {
+  float q[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) levels2<FMT>(((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu, q[2 * j], q[2 * j + 1]);
+  float v[16];
+  {
+    const f2 S = f2_make(sv, sv), G = f2_make(g, g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f2 r = f2_mul(f2_make(q[2 * j], q[2 * j + 1]), S);
+      if (FMT != 1) r = f2_mul(r, G);
+      f2_split(r, v[2 * j], v[2 * j + 1]);
+    }
+  }
+  if constexpr (IRHT) {
+    // R^T = (1/4) diag(sigma) H16: the forward butterfly (stages 1, 2, 4, 8, then
+    // * 1/4) without its sign flip, then the sign flip
+    f2 Q[8];
+    rht16_pairs(v, Q);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float a, b;
+      f2_split(Q[j], a, b);
+      v[2 * j] = __uint_as_float(__float_as_uint(a) ^ sgn[2 * j]);
+      v[2 * j + 1] = __uint_as_float(__float_as_uint(b) ^ sgn[2 * j + 1]);
+    }
+  }
+  if constexpr (OUT_F32) {
+    float4* o = reinterpret_cast<float4*>(out);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) o[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  } else {
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+      h[k] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    uint4* o = reinterpret_cast<uint4*>(out);
+    o[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    o[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
+__device__ __forceinline__ uint32_t get_scale(const CopyOut& q, const Flat& f, uint64_t blk) {
+  if (!q.mma) return __ldg(q.scales + blk);
+  const uint64_t r = f.small ? (uint64_t)f.nkb.div((uint32_t)blk) : blk / f.nkb.d;
+  const uint64_t kb = blk - r * f.nkb.d;
+  return __ldg(q.scales + mma_scale_offset((int64_t)r, (int64_t)kb, q.nkb_p));
+}
+
+template <int FMT, bool OUT_F32, bool IRHT>
+__global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, uint64_t seed, void* dst) {
+  uint32_t sgn[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) sgn[i] = 0u;
+  if constexpr (IRHT) {
+    const uint32_t m = rht_sign_mask(seed);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sgn[i] = ((m >> i) & 1u) << 31;
+  }
+  constexpr int B = (FMT == 1) ? 32 : 16;
+  constexpr int ES = OUT_F32 ? 4 : 2;
+  const float g = (FMT == 1) ? 1.f : __ldg(q.tensor_scale);
+  const int64_t nseg = (f.n + 31) / 32;
+  uint8_t* out = static_cast<uint8_t*>(dst);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t sgi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; sgi < nseg; sgi += stride) {
+    const int64_t e = sgi * 32;
+    // the next segment's codes are loaded ahead, so two loads are in flight
+    const int64_t e2 = e + stride * 32;
+    if (e2 + 32 <= f.n) asm volatile("prefetch.global.L2 [%0];" ::"l"(q.codes + e2 / 2));
+    if (f.n - e >= 32) {
+      const uint4 cw = __ldg(reinterpret_cast<const uint4*>(q.codes + e / 2));
+      if constexpr (B == 32) {
+        const float sv = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 32));
+        deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, sv, g, sgn, out + e * ES);
+        deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, sv, g, sgn, out + (e + 16) * ES);
+      } else {
+        const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16));
+        const float s1 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16 + 1));
+        deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, g, sgn, out + e * ES);
+        deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, s1, g, sgn, out + (e + 16) * ES);
+      }
+    } else {   // a lone 16-block at the very end (16-element formats only)
+      const uint2 cw = __ldg(reinterpret_cast<const uint2*>(q.codes + e / 2));
+      const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / B));
+      deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, g, sgn, out + e * ES);
+    }
   }
 }
 
@@ -834,6 +1110,51 @@ cudaError_t dispatch_quant_rows(int rht, int sr, const Flat& f, uint64_t seed, c
 
 }  // namespace
 
+template <int FMT>
+cudaError_t launch_dequant_rows(const Flat& f, const CopyOut& q, int irht, uint64_t seed, void* dst,
+                                int f32, cudaStream_t s) {
+  const int64_t nseg = (f.n + 31) / 32;
+  int64_t grid = (nseg + 255) / 256;
+  const int64_t gmax = (int64_t)sm_count() * 8;
+  if (grid > gmax) grid = gmax;
+  if (grid < 1) grid = 1;
+  if (f32) {
+    if (irht) dequant_rows_kernel<FMT, true, true><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
+    else dequant_rows_kernel<FMT, true, false><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
+  } else {
+    if (irht) dequant_rows_kernel<FMT, false, true><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
+    else dequant_rows_kernel<FMT, false, false><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
+  }
+  return cudaGetLastError();
+}
+
+template <int FMT, bool F32, bool RHT, bool SR>
+cudaError_t launch_quant_fused(const Flat& f, uint64_t seed, const CopyOut& o, Workspace* ws,
+                               cudaStream_t s) {
+  auto k = quant_fused_kernel<FMT, F32, RHT, SR>;
+  constexpr int smem = Ring<F32>::kSmem;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  const int grid = grid_for(k, smem, f.nchunks);    // at most the co-resident CTAs
+  Flat fa = f;
+  uint64_t sd = seed, to = kRingTimeoutNs;
+  CopyOut oa = o;
+  Workspace* wa = ws;
+  void* args[] = {&fa, &sd, &oa, &wa, &to};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k), dim3(grid), dim3(RT), args, smem, s);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+template <int FMT, bool F32>
+cudaError_t dispatch_quant_fused(int rht, int sr, const Flat& f, uint64_t seed, const CopyOut& o,
+                                 Workspace* ws, cudaStream_t s) {
+  if (rht) return sr ? launch_quant_fused<FMT, F32, true, true>(f, seed, o, ws, s)
+                     : launch_quant_fused<FMT, F32, true, false>(f, seed, o, ws, s);
+  return sr ? launch_quant_fused<FMT, F32, false, true>(f, seed, o, ws, s)
+            : launch_quant_fused<FMT, F32, false, false>(f, seed, o, ws, s);
+}
+
 cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s) {
   const Flat f = make_flat(a.src, a.rows, a.cols, a.fmt == 1 ? 32 : 16);
   Workspace* ws = static_cast<Workspace*>(a.ws);
@@ -865,6 +1186,43 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
     default: return f32 ? dispatch_quant_rows<2, true>(a.rht, sr, f, a.seed, o, ws, s)
                         : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s);
   }
+}
+
+cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s) {
+  const int block = a.fmt == 1 ? 32 : 16;
+  const Flat f = make_flat(a.q.codes, a.rows, a.cols, block);
+  CopyOut q{};
+  q.codes = a.q.codes;
+  q.scales = a.q.scales;
+  q.tensor_scale = a.q.tensor_scale;
+  q.mma = a.q.scale_layout;
+  q.ld = a.cols / 2;
+  q.nkb = a.cols / block;
+  q.nkb_p = (q.nkb + 3) / 4 * 4;
+  switch (a.fmt) {
+    case 0: return launch_dequant_rows<0>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 1: return launch_dequant_rows<1>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    default: return launch_dequant_rows<2>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+  }
+}
+
+cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s) {
+  const Flat f = make_flat(a.src, a.rows, a.cols, 16);
+  CopyOut o{};
+  o.codes = a.row.codes;
+  o.scales = a.row.scales;
+  o.tensor_scale = a.row.tensor_scale;
+  o.mma = a.row.scale_layout;
+  o.ld = a.cols / 2;
+  o.nkb = a.cols / 16;
+  o.nkb_p = (o.nkb + 3) / 4 * 4;
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  const bool f32 = a.dtype == 1;
+  const int sr = a.rounding == 1;
+  if (a.fmt == 0) return f32 ? dispatch_quant_fused<0, true>(a.rht, sr, f, a.seed, o, ws, s)
+                             : dispatch_quant_fused<0, false>(a.rht, sr, f, a.seed, o, ws, s);
+  return f32 ? dispatch_quant_fused<2, true>(a.rht, sr, f, a.seed, o, ws, s)
+             : dispatch_quant_fused<2, false>(a.rht, sr, f, a.seed, o, ws, s);
 }
 
 }  // namespace fp4q

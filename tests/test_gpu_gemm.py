@@ -46,7 +46,8 @@ def _rand_copy(rng, rows, k, kexp_lo, kexp_hi):
 
 
 @pytest.mark.parametrize("variant", ["unit", "a_scales", "b_scales", "both"])
-@pytest.mark.parametrize("shape", [(128, 256, 256), (128, 128, 512), (256, 512, 768)])
+@pytest.mark.parametrize("shape", [(128, 256, 256), (128, 128, 512), (256, 512, 768), (512, 256, 512),
+                                   (1024, 512, 256)])
 def test_gemm_exact_power_of_two(lib, variant, shape):
     M, N, K = shape
     rng = np.random.default_rng(M + N + K)
@@ -65,7 +66,8 @@ def test_gemm_exact_power_of_two(lib, variant, shape):
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("shape", [(256, 512, 1024), (384, 128, 512), (128, 384, 2048)])
+@pytest.mark.parametrize("shape", [(256, 512, 1024), (384, 128, 512), (128, 384, 2048), (512, 512, 1024),
+                                   (1024, 256, 512), (512, 384, 768)])
 def test_quantize_then_gemm(lib, shape, out_dtype):
     M, N, K = shape
     a = synth.gemm_operand("a", M, K)
