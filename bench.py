@@ -7,9 +7,11 @@ tensor (Student-t nu = 3 times a per-column lognormal scale) quantised three
 ways -- E2M1/NVFP4 without the RHT, E2M1/NVFP4 with the 16-point RHT, uniform
 E1M2/UFP4 with the RHT -- 16-element blocks, RTNE, row-wise, statistics fused;
 then the UFP4 copy dequantised with the inverse RHT back to BF16 (UFP4 has no
-tensor-core format: a consumer dequantises it). Each quantisation is one
-fp4q_quantize call through the C ABI: both passes of the method (the tensor
-amax, then the block scales and codes) in one launch.
+tensor-core format: a consumer dequantises it). Each quantisation is the two
+passes of the method through the C ABI -- fp4q_amax (the tensor amax), then
+fp4q_quantize with FP4Q_AMAX_READY (block scales, codes, statistics) -- which
+is exactly what fp4q_quantize launches at this size, split so that each pass
+is timed on its own.
 
   value   algorithmic bytes of the step / step time, GB/s (whole job: all ranks)
   e2e     the same bytes / the time of the same step through the Python binding
@@ -52,9 +54,8 @@ FP4_OVER_BF16 = 13.5 / 2.25        # nominal dense FP4 / BF16 tensor rate
 L2_FLUSH_BYTES = 256 << 20
 
 # algorithmic bytes per element (BF16 input): the amax pass reads 2; the
-# quantisation pass reads 2 and writes 0.5 of codes + 1/16 of E4M3 scales (one
-# fp4q_quantize launch does both passes); the dequantise pass reads 0.5 + 1/16
-# and writes 2.
+# quantisation pass reads 2 and writes 0.5 of codes + 1/16 of E4M3 scales; the
+# dequantise pass reads 0.5 + 1/16 and writes 2.
 B_AMAX = 2.0
 B_QUANT = 2.0 + 0.5 + 1.0 / 16
 B_DEQ = 0.5 + 1.0 / 16 + 2.0
@@ -347,16 +348,23 @@ class RawCalls:
         for (fmt, rht), q in zip(WAYS, outs):
             s = q.c_struct()
             self.calls.append((
+                (x.data_ptr(), 0, rows, cols, fq.FORMATS[fmt], fq.BLOCKS[fmt], int(rht), SEED, 1,
+                 ws.data_ptr(), ws.numel(), stream),
                 (x.data_ptr(), 0, rows, cols, fq.FORMATS[fmt], fq.BLOCKS[fmt], int(rht), 0, SEED,
-                 1, ctypes.byref(s), None, ws.data_ptr(), ws.numel(), stream),
+                 1 | 4, ctypes.byref(s), None, ws.data_ptr(), ws.numel(), stream),
                 s))
         u = outs[-1]
         self.deq_struct = u.c_struct()
         self.deq_args = (ctypes.byref(self.deq_struct), rows, cols, fq.FORMATS["ufp4"], 16, 1, SEED,
                          deq_out.data_ptr(), 0, stream)
 
+    def amax(self, i):
+        rc = self.lib.fp4q_amax(*self.calls[i][0])
+        if rc:
+            raise self.fq.FP4QError("fp4q_amax", rc)
+
     def quant(self, i):
-        rc = self.lib.fp4q_quantize(*self.calls[i][0])
+        rc = self.lib.fp4q_quantize(*self.calls[i][1])
         if rc:
             raise self.fq.FP4QError("fp4q_quantize", rc)
 
@@ -380,12 +388,14 @@ def run_main_leg(fq, torch, device, steps, warmup):
     def one_step(ev):
         ev[0].record(stream)
         for i in range(len(WAYS)):
+            raw.amax(i)
+            ev[2 * i + 1].record(stream)
             raw.quant(i)
-            ev[i + 1].record(stream)
+            ev[2 * i + 2].record(stream)
         raw.deq()
-        ev[len(WAYS) + 1].record(stream)
+        ev[2 * len(WAYS) + 1].record(stream)
 
-    nev = len(WAYS) + 2
+    nev = 2 * len(WAYS) + 2
     for _ in range(warmup):
         flush.zero_()
         one_step([torch.cuda.Event(enable_timing=True) for _ in range(nev)])
@@ -404,11 +414,12 @@ def run_main_leg(fq, torch, device, steps, warmup):
     wall = time.perf_counter() - w0
     barrier(device)
 
-    step_ms, quant_ms, deq_ms = [], [], []
+    step_ms, amax_ms, quant_ms, deq_ms = [], [], [], []
     for ev in evs:
         step_ms.append(ev[0].elapsed_time(ev[nev - 1]))
         for i in range(len(WAYS)):
-            quant_ms.append(ev[i].elapsed_time(ev[i + 1]))
+            amax_ms.append(ev[2 * i].elapsed_time(ev[2 * i + 1]))
+            quant_ms.append(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]))
         deq_ms.append(ev[nev - 2].elapsed_time(ev[nev - 1]))
     status = fq.fp4q_status(ws)
     # self-checks outside the timed region: the input is intact, and the
@@ -425,9 +436,9 @@ def run_main_leg(fq, torch, device, steps, warmup):
         repeat_same &= seen[0] == seen[1]
         stats[f"{fmt}{'+rht' if rht else ''}"] = {"shrink_bias": seen[0][0], "snr_db": seen[0][1]}
     checks["stats_repeatable"] = bool(repeat_same)
-    return {"step_ms_total": sum(step_ms), "wall_s": wall,
+    return {"step_ms_total": sum(step_ms), "wall_s": wall, "amax_ms": amax_ms,
             "quant_ms": quant_ms, "deq_ms": deq_ms, "status": status, "stats": stats,
-            "checks": checks, "launches_per_step": len(WAYS) + 1}
+            "checks": checks, "launches_per_step": 2 * len(WAYS) + 1}
 
 
 def run_e2e_leg(fq, torch, device, steps, warmup):
@@ -578,6 +589,38 @@ def run_sweep(fq, torch, device, args, peaks) -> None:
     assert fq.fp4q_status(ws) == 0
 
 
+def run_grad_leg(fq, torch, device, steps, warmup):
+    """The gradient-like workload: 4096 x 14336 and 14336 x 4096 BF16, N(0, 1e-6)
+    with 0.1% x100 outliers, NVFP4 with the 16-point RHT and Philox stochastic
+    rounding (seed 1234), row-wise and column-wise (transposed) copies from one
+    read: time per fp4q_quantize call."""
+    import synth
+    out = {}
+    for which in ("a", "b"):
+        x = synth.gradient(which).to(device)
+        rows, cols = x.shape
+        r = fq.alloc_copy(rows, cols, "nvfp4", "linear", device)
+        c = fq.alloc_copy(cols, rows, "nvfp4", "linear", device)
+        ws = fq.workspace(device)
+        stream = torch.cuda.current_stream(device)
+        evs = []
+        for k in range(warmup + steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fq.fp4q_quantize(x, fmt="nvfp4", rht=True, rounding="sr", seed=SEED, axis="both", ws=ws,
+                             row_out=r, col_out=c)
+            e1.record(stream)
+            if k >= warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+        us = statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+        n = rows * cols
+        byts = (B_AMAX + 2.0 + 2 * (0.5 + 1.0 / 16)) * n
+        out[f"{rows}x{cols}"] = {"us": us, "GB/s": byts / (us * 1e-6) / 1e9,
+                                 "status": fq.fp4q_status(ws)}
+    return out
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
     if args.impl == "reference":
@@ -601,6 +644,7 @@ def main(argv=None) -> int:
     sampler = ClockSampler(gpu_uuid(device))
     main_r = run_main_leg(fq, torch, device, args.steps, args.warmup)
     gemm_r = None if args.no_gemm else run_gemm_leg(fq, torch, device, args.steps, args.warmup)
+    grad_r = run_grad_leg(fq, torch, device, min(args.steps, 50), args.warmup)
     e2e_steps = min(args.steps, 100)
     e2e_r = None if args.no_e2e else run_e2e_leg(fq, torch, device, e2e_steps, args.warmup)
     clocks = sampler.stop()
@@ -612,8 +656,10 @@ def main(argv=None) -> int:
 
     # per-kernel averages over the timed region
     kern = {
-        "quantize": {"ms": statistics.fmean(main_r["quant_ms"]), "bytes": (B_AMAX + B_QUANT) * n_el,
-                     "launches": len(main_r["quant_ms"]), "ncu_name": "quant_fused_kernel"},
+        "amax": {"ms": statistics.fmean(main_r["amax_ms"]), "bytes": B_AMAX * n_el,
+                 "launches": len(main_r["amax_ms"]), "ncu_name": "amax_rows_kernel"},
+        "quantize": {"ms": statistics.fmean(main_r["quant_ms"]), "bytes": B_QUANT * n_el,
+                     "launches": len(main_r["quant_ms"]), "ncu_name": "quant_rows_kernel"},
         "dequantize": {"ms": statistics.fmean(main_r["deq_ms"]), "bytes": B_DEQ * n_el,
                        "launches": len(main_r["deq_ms"]), "ncu_name": "dequant_rows_kernel"},
     }
@@ -671,6 +717,10 @@ def main(argv=None) -> int:
                          "traffic": ncu_traffic("gemm_nvf4_kernel", flop)},
         }
         line["gpu_launches_gemm_leg"] = 3 * args.steps
+    line["gradient_leg"] = {
+        "workload": "4096x14336 and 14336x4096 BF16 N(0,1e-6) with 0.1% x100, NVFP4 + RHT16 + Philox "
+                    "SR (seed 1234), row-wise and column-wise copies from one read",
+        "bytes_per_element": B_AMAX + 2.0 + 2 * (0.5 + 1.0 / 16), **grad_r}
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -6,7 +6,7 @@ through its C ABI (include/fp4q.h). There is no CPU path: if the shared library
 is missing, importing this package fails.
 
 Function names follow the C ABI: fp4q_amax, fp4q_quantize, fp4q_dequantize, fp4q_stats,
-fp4q_status, fp4q_gemm, fp4q_quantize_noalloc, fp4q_workspace_size, fp4q_workspace_init,
+fp4q_status, fp4q_gemm, fp4q_gemm_selftest_timeout, fp4q_quantize_noalloc, fp4q_workspace_size, fp4q_workspace_init,
 fp4q_scales_bytes, fp4q_strerror, fp4q_version.
 """
 from __future__ import annotations
@@ -65,6 +65,7 @@ _SIGS = {
     "fp4q_stats": ([_P, _SP, _SP, _P], _I),
     "fp4q_status": ([_P, _P], _I),
     "fp4q_gemm": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
+    "fp4q_gemm_selftest_timeout": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, ctypes.c_uint64, _P], _I),
     "fp4q_strerror": ([_I], ctypes.c_char_p),
     "fp4q_version": ([], _I),
 }
@@ -282,6 +283,22 @@ def fp4q_gemm(a: QCopy, b: QCopy, out_dtype=torch.bfloat16, out: torch.Tensor = 
                         out.data_ptr(), DTYPES[out.dtype], ws.data_ptr(), ws.numel(),
                         _stream(out.device))
     _check("fp4q_gemm", rc)
+    return out
+
+
+def fp4q_gemm_selftest_timeout(a: QCopy, b: QCopy, timeout_ns: int, out: torch.Tensor = None,
+                               ws: torch.Tensor = None) -> torch.Tensor:
+    """Test hook: the GEMM with one stage withheld and every wait bounded by
+    ``timeout_ns``; afterwards fp4q_status(ws) reads 5 (FP4Q_ETIMEOUT)."""
+    if ws is None:
+        ws = workspace(a.codes.device)
+    if out is None:
+        out = torch.empty(a.rows, b.rows, dtype=torch.bfloat16, device=a.codes.device)
+    sa, sb = a.c_struct(), b.c_struct()
+    rc = _lib.fp4q_gemm_selftest_timeout(ctypes.byref(sa), ctypes.byref(sb), a.rows, b.rows, a.cols,
+                                         FORMATS[a.fmt], out.data_ptr(), DTYPES[out.dtype], ws.data_ptr(),
+                                         ws.numel(), int(timeout_ns), _stream(out.device))
+    _check("fp4q_gemm_selftest_timeout", rc)
     return out
 
 

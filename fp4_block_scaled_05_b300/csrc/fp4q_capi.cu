@@ -285,8 +285,11 @@ int fp4q_status(void* workspace, void* stream) {
   return FP4Q_OK;
 }
 
-int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
-              int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+
+int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K, int fmt,
+                void* Y, int out_dtype, void* workspace, size_t ws_bytes, uint64_t timeout_ns, int skip,
+                void* stream) {
   if (fmt == FP4Q_UFP4) return FP4Q_ENOTSUP;
   if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4) return FP4Q_EINVAL;
   if (fmt == FP4Q_MXFP4) return FP4Q_ENOTSUP;
@@ -308,9 +311,24 @@ int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N
   a.y = Y;
   a.out_dtype = out_dtype;
   a.ws = workspace;
-  const cudaError_t e = fp4q::run_gemm(a, (cudaStream_t)stream);
+  const cudaError_t e = timeout_ns ? fp4q::run_gemm_ex(a, timeout_ns, skip, (cudaStream_t)stream)
+                                   : fp4q::run_gemm(a, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return FP4Q_ENOTSUP;
   return e == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+}
+
+}  // namespace
+
+int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+              int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  return gemm_common(A, B, M, N, K, fmt, Y, out_dtype, workspace, ws_bytes, 0, 0, stream);
+}
+
+int fp4q_gemm_selftest_timeout(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N,
+                               int64_t K, int fmt, void* Y, int out_dtype, void* workspace,
+                               size_t ws_bytes, uint64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000000ull || timeout_ns > 10000000000ull) return FP4Q_EINVAL;
+  return gemm_common(A, B, M, N, K, fmt, Y, out_dtype, workspace, ws_bytes, timeout_ns, 1, stream);
 }
 
 const char* fp4q_strerror(int code) {

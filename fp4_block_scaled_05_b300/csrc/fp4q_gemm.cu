@@ -258,7 +258,7 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         const int m = (gi / num_n) * CL + (int)rank, n = gi % num_n;
         for (int ks = 0; ks < nk; ++ks) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
-          const bool skip = skip_first_stage && gi == cid && ks == 0 && rank == 0;
+          const bool skip = skip_first_stage && blockIdx.x == 0 && gi == cid && ks == 0;
           pending &= ~(1u << s);
           if (!skip) {
             uint8_t* st = smem + s * C::kStageBytes;

@@ -259,6 +259,18 @@ int fp4q_status(void* workspace, void* stream);
 int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
               int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* Test hook for the device-side failure path (not a step of the method): runs
+ * fp4q_gemm with the producer of the first CTA withholding the first stage of
+ * its first tile and every wait bounded by `timeout_ns`, so the waits that
+ * depend on that stage run out. The kernel records FP4Q_ETIMEOUT in the
+ * workspace status word, lets the copies it issued land, frees its Tensor
+ * Memory and returns; nothing traps, and the CUDA context stays usable (the
+ * output Y is then incomplete). Arguments as fp4q_gemm; 1 ms <= timeout_ns
+ * <= 10 s (else FP4Q_EINVAL). */
+int fp4q_gemm_selftest_timeout(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N,
+                               int64_t K, int fmt, void* Y, int out_dtype, void* workspace,
+                               size_t ws_bytes, uint64_t timeout_ns, void* stream);
+
 /* ---- misc ----------------------------------------------------------------------- */
 
 /* Static text for an FP4Q_* code. */

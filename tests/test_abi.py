@@ -93,3 +93,16 @@ def test_amax_validation_without_gpu(so):
     # unknown flag bits and the ready flag without a copy are rejected
     assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 9, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 4, None, None, fake, ws_size, None) == 1
+
+
+def test_gemm_selftest_validation_without_gpu(so):
+    so.fp4q_workspace_size.restype = ctypes.c_size_t
+    f = so.fp4q_gemm_selftest_timeout
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                  ctypes.c_uint64, ctypes.c_void_p]
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the calls below fail validation first
+    ws = so.fp4q_workspace_size()
+    assert f(fake, fake, 128, 128, 256, 0, fake, 0, fake, ws, 100, None) == 1           # bound too short
+    assert f(fake, fake, 128, 128, 256, 0, fake, 0, fake, ws, 10**11, None) == 1        # bound too long
+    assert f(fake, fake, 128, 128, 256, 2, fake, 0, fake, ws, 10**7, None) == 2         # UFP4 GEMM

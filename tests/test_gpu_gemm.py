@@ -114,3 +114,23 @@ def test_gemm_full_size_sampled(lib):
     assert 15.0 < snr < 40.0, snr
     assert lib.fp4q_status() == 0
     del ref
+
+
+def test_bounded_wait_runs_out_without_fault(lib):
+    """Failure detection on the device: the first CTA's producer withholds one
+    stage, the waits that depend on it run out after 20 ms, the kernel records
+    FP4Q_ETIMEOUT and returns; the context stays usable and the next GEMM on
+    it is correct."""
+    a = synth.gemm_operand("a", 256, 512)
+    b = synth.gemm_operand("b", 256, 512)
+    qa, _ = lib.fp4q_quantize(a.cuda(), fmt="nvfp4", layout="mma")
+    qb, _ = lib.fp4q_quantize(b.cuda(), fmt="nvfp4", layout="mma")
+    assert lib.fp4q_status() == 0
+    lib.fp4q_gemm_selftest_timeout(qa, qb, 20_000_000)
+    assert lib.fp4q_status() == 5          # FP4Q_ETIMEOUT, read and cleared
+    assert lib.fp4q_status() == 0
+    y = lib.fp4q_gemm(qa, qb, out_dtype=torch.float32)
+    assert lib.fp4q_status() == 0
+    ra = o.quantize(_bits(a), "nvfp4")["row"]
+    rb = o.quantize(_bits(b), "nvfp4")["row"]
+    assert _rel(y.cpu().numpy(), o.gemm(ra, rb)) < 1e-5
