@@ -60,6 +60,42 @@ int cached_occupancy(const void* kernel, int threads, int smem) {
   return occ;
 }
 
+namespace {
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    } else {
+      cudaGetLastError();
+    }
+  });
+  return fn;
+}
+}  // namespace
+
+bool encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                     uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  const cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace fp4q
 
 namespace {
@@ -110,6 +146,7 @@ int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt
     return FP4Q_EINVAL;
   if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
   if (rows && cols && (!src || !aligned(src, 16))) return FP4Q_EINVAL;
+  if (cols % 16) return FP4Q_EINVAL;     // source rows start on 32-byte boundaries
   if ((axis & FP4Q_ROWWISE) && cols % block) return FP4Q_EINVAL;
   if ((axis & FP4Q_COLWISE) && rows % block) return FP4Q_EINVAL;
   return FP4Q_OK;

@@ -214,36 +214,6 @@ __device__ __forceinline__ bool arrive_last(unsigned int* counter, bool* s_flag)
 // SR uniform of one Philox word: its top 24 bits times 2^-24 (exact in FP32).
 __device__ __forceinline__ float sr_u(uint32_t w) { return __uint2float_rz(w >> 8) * 5.9604644775390625e-08f; }
 
-// Stochastic rounding of |y| onto the grid: returns the level index and its value.
-template <int FMT>
-__device__ __forceinline__ uint32_t sr_level(float ay, float u, float& qv) {
-  if (FMT == 2) {   // UFP4: integer levels 0..7
-    if (ay >= 7.f) { qv = 7.f; return 7u; }
-    const float lo = truncf(ay);
-    const float f = __fsub_rn(ay, lo);
-    const uint32_t up = (u < f) ? 1u : 0u;
-    qv = __fadd_rn(lo, (float)up);
-    return (uint32_t)lo + up;
-  } else {          // E2M1
-    if (ay >= 6.f) { qv = 6.f; return 7u; }
-    float lo, step;
-    uint32_t idx;
-    if (ay < 2.f) {
-      const float k = truncf(__fmul_rn(ay, 2.f));
-      lo = __fmul_rn(k, 0.5f); step = 0.5f; idx = (uint32_t)k;
-    } else if (ay < 4.f) {
-      lo = truncf(ay); step = 1.f; idx = (uint32_t)lo + 2u;
-    } else {
-      lo = 4.f; step = 2.f; idx = 6u;
-    }
-    const float f = __fdiv_rn(__fsub_rn(ay, lo), step);
-    const uint32_t up = (u < f) ? 1u : 0u;
-    qv = up ? __fadd_rn(lo, step) : lo;
-    return idx + up;
-  }
-}
-
-
 __device__ __forceinline__ void store_scale(const CopyOut& o, int64_t row, int64_t kb, uint32_t sc) {
   const int64_t off = o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb;
   o.scales[off] = (uint8_t)sc;

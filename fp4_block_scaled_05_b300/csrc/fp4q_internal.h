@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fp4q {
@@ -49,6 +50,12 @@ struct GemmArgs {
 int sm_count();
 // Resident CTAs per SM of `kernel` at `threads` threads and `smem` dynamic bytes (cached).
 int cached_occupancy(const void* kernel, int threads, int smem);
+// A 2-D TMA map (128-byte swizzle, zero fill outside the tensor) over `outer`
+// rows of `inner` elements of type `dt`, rows `pitch_bytes` apart, with a box
+// of box_inner x box_outer elements. False if the driver's encoder is missing
+// or rejects the arguments.
+bool encode_tiled_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                     uint64_t outer, uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer);
 
 cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s);
 // K1 alone: the tensor amax of the requested copies, recorded in the workspace.
@@ -58,6 +65,9 @@ cudaError_t run_amax(const QuantArgs& a, cudaStream_t s);
 // pass of a row-wise-only request.
 cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s);
+// Requests with the column-wise copy (rows and cols multiples of 16).
+cudaError_t run_amax_tiles(const QuantArgs& a, cudaStream_t s);
+cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s);
 // Both passes of a row-wise NVFP4/UFP4 request in one cooperative launch.
 cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);

@@ -1,6 +1,5 @@
-// Block-scaled 4-bit quantisation kernels (sm_103a) for requests with a
-// column-wise (transposed) copy: tensor amax, then fused RHT + scale + round +
-// pack + statistics for the row-wise and the transposed copy from one read.
+// Dispatch of the block-scaled 4-bit quantisation (sm_103a): which kernels one
+// fp4q_amax / fp4q_quantize call launches.
 //
 // Method: "Replanteamiento del Sesgo de Contraccion en el Preentrenamiento de
 // LLM en FP4" (Metodologia §1-2: E2M1 / uniform E1M2 grids, RTNE, stochastic
@@ -10,21 +9,17 @@
 // the Potential of Quantization with MXFP4 ..." (Resume technique §2: MXFP4
 // 32-element E8M0 blocks, NVFP4 16-element E4M3 blocks).
 //
-// Design: a persistent grid of 256-thread CTAs walks 64 x 128 tiles of the
-// input. Each thread loads 32 consecutive elements of one row with 16-byte
-// vector loads (a warp reads 8 rows x 256 B), runs the row-wise blocks in
-// registers, and parks the raw tile in shared memory (rows padded by 16 B so
-// both the row-wise stores and the column reads are conflict-free). After one
-// barrier each thread reads two adjacent columns x 16 rows (one 4-byte word per
-// row, a warp covering 128 contiguous bytes) and runs the column-wise blocks.
-// The two copies therefore cost one read of the input. Per-CTA partial sums
-// are combined by the last CTA to finish (atomicInc on a wrapping counter), in
-// a fixed order, so results do not depend on scheduling.
-#include <cfloat>
+// Paths (all kernels in fp4q_rows.cu):
+//  * row-wise copy only: the tensor is a flat stream of 8192-element chunks
+//    (amax_rows_kernel, quant_rows_kernel), or one cooperative launch of both
+//    passes for NVFP4 / UFP4 tensors below 2^25 elements (quant_fused_kernel);
+//  * any request with the column-wise copy: 64 x 128 tiles through a shared-
+//    memory ring, one read of the source serving both copies
+//    (amax_tiles_kernel when the RHT makes the two copies' amax differ,
+//    quant_tiles_kernel).
+// MXFP4 has no tensor scale, so it skips the amax pass.
 #include <cstdint>
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "fp4q_device.cuh"
@@ -32,476 +27,7 @@
 
 namespace fp4q {
 
-constexpr int TR = 64;    // tile rows
-constexpr int TC = 128;   // tile cols
-constexpr int NT = 256;   // threads per CTA
-
-template <bool F32>
-struct TileSmem {
-  static constexpr int kRowBytes = TC * (F32 ? 4 : 2) + 16;
-  static constexpr int kBytes = TR * kRowBytes;
-};
-
-struct Geom {
-  const void* src;
-  int64_t rows, cols;
-  int64_t ntc;      // tiles along the columns
-  int64_t ntiles;
-};
-
-// ---------------------------------------------------------------------------
-// Loading one row segment of 32 elements (the thread's share of a tile row).
-// Returns the number of valid 16-element blocks (0, 1 or 2). Raw data of the
-// segment (zeros where invalid) is copied into the shared tile when `park`.
-// ---------------------------------------------------------------------------
-template <bool F32>
-__device__ __forceinline__ int load_row_segment(const Geom& g, int64_t r0, int64_t c0, int tid,
-                                                float (&v)[32], uint8_t* tile, bool park) {
-  const int rr = tid >> 2, sg = tid & 3;
-  const int64_t r = r0 + rr;
-  const int64_t c = c0 + 32 * sg;
-  int nvalid = 0;
-  if (r < g.rows && c < g.cols) nvalid = (g.cols - c >= 32) ? 2 : 1;
-  if constexpr (!F32) {
-    uint4 w[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                  make_uint4(0, 0, 0, 0)};
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(g.src) +
-                                                    r * g.cols + c);
-    if (nvalid >= 1) { w[0] = __ldg(p + 0); w[1] = __ldg(p + 1); }
-    if (nvalid == 2) { w[2] = __ldg(p + 2); w[3] = __ldg(p + 3); }
-    if (park) {
-      uint4* s = reinterpret_cast<uint4*>(tile + rr * TileSmem<false>::kRowBytes + 64 * sg);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) s[i] = w[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[8 * i + 0] = bf16lo(w[i].x); v[8 * i + 1] = bf16hi(w[i].x);
-      v[8 * i + 2] = bf16lo(w[i].y); v[8 * i + 3] = bf16hi(w[i].y);
-      v[8 * i + 4] = bf16lo(w[i].z); v[8 * i + 5] = bf16hi(w[i].z);
-      v[8 * i + 6] = bf16lo(w[i].w); v[8 * i + 7] = bf16hi(w[i].w);
-    }
-  } else {
-    float4 w[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(g.src) +
-                                                      r * g.cols + c);
-    if (nvalid >= 1) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) w[i] = __ldg(p + i);
-    }
-    if (nvalid == 2) {
-#pragma unroll
-      for (int i = 4; i < 8; ++i) w[i] = __ldg(p + i);
-    }
-    if (park) {
-      float4* s = reinterpret_cast<float4*>(tile + rr * TileSmem<true>::kRowBytes + 128 * sg);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) s[i] = w[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[4 * i + 0] = w[i].x; v[4 * i + 1] = w[i].y; v[4 * i + 2] = w[i].z; v[4 * i + 3] = w[i].w;
-    }
-  }
-  return nvalid;
-}
-
-// Two adjacent columns x 16 rows of the parked tile (column-wise 16-blocks).
-template <bool F32>
-__device__ __forceinline__ void read_col_pair(const uint8_t* tile, int row0, int pair,
-                                              float (&a)[16], float (&b)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    if constexpr (F32) {
-      const float2 f = *reinterpret_cast<const float2*>(tile + (row0 + i) * TileSmem<true>::kRowBytes + 8 * pair);
-      a[i] = f.x; b[i] = f.y;
-    } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(tile + (row0 + i) * TileSmem<false>::kRowBytes + 4 * pair);
-      a[i] = bf16lo(w); b[i] = bf16hi(w);
-    }
-  }
-}
-
-// One column x 32 rows of the parked tile (column-wise MXFP4 blocks).
-template <bool F32>
-__device__ __forceinline__ void read_col32(const uint8_t* tile, int row0, int col, float (&a)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    if constexpr (F32) {
-      a[i] = *reinterpret_cast<const float*>(tile + (row0 + i) * TileSmem<true>::kRowBytes + 4 * col);
-    } else {
-      const uint32_t h = *reinterpret_cast<const uint16_t*>(tile + (row0 + i) * TileSmem<false>::kRowBytes + 2 * col);
-      a[i] = __uint_as_float(h << 16);
-    }
-  }
-}
-
-// Sign flip by sigma then the 16-point butterfly, on every 16 values of w.
-template <int N>
-__device__ __forceinline__ void rht_inplace(float* w, uint32_t smask) {
-#pragma unroll
-  for (int i = 0; i < N; ++i)
-    w[i] = __uint_as_float(__float_as_uint(w[i]) ^ (((smask >> (i & 15)) & 1u) << 31));
-#pragma unroll
-  for (int j = 0; j < N; j += 16) fwht16_quarter(w + j);
-}
-
-template <int N>
-__device__ __forceinline__ uint32_t absmax_bits(const float* w) {
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < N; ++i) m = max(m, __float_as_uint(w[i]) & 0x7FFFFFFFu);
-  return m;
-}
-
-// ---------------------------------------------------------------------------
-// K1: tensor amax of the (transformed) copies. Tiles are visited in reverse
-// order so that the quantise pass, which walks forwards, starts on the tiles
-// this pass left in L2 most recently.
-// ---------------------------------------------------------------------------
-template <bool F32, bool RHT, bool ROWS, bool COLS>
-__global__ void __launch_bounds__(NT, 3) amax_kernel(Geom g, uint64_t seed, Workspace* ws) {
-  extern __shared__ __align__(16) uint8_t tile[];
-  __shared__ uint32_t sh_max[NT / 32];
-  const int tid = threadIdx.x;
-  const uint32_t smask = RHT ? rht_sign_mask(seed) : 0u;
-  constexpr bool kPark = RHT && COLS;
-  uint32_t m_row = 0, m_col = 0;
-
-  for (int64_t t = g.ntiles - 1 - blockIdx.x; t >= 0; t -= gridDim.x) {
-    const int64_t r0 = (t / g.ntc) * TR, c0 = (t % g.ntc) * TC;
-    float v[32];
-    // invalid parts of the segment are loaded as zeros, which leave the max unchanged
-    load_row_segment<F32>(g, r0, c0, tid, v, tile, kPark);
-    if (ROWS || !RHT) {
-      if (RHT) rht_inplace<32>(v, smask);
-      m_row = max(m_row, absmax_bits<32>(v));
-    }
-    if constexpr (kPark) {
-      __syncthreads();
-      const int pair = tid & 63, cb = tid >> 6;
-      const int64_t rb = r0 + 16 * cb, col = c0 + 2 * pair;
-      if (rb < g.rows && col < g.cols) {
-        float a[16], b[16];
-        read_col_pair<F32>(tile, 16 * cb, pair, a, b);
-        rht_inplace<16>(a, smask);
-        rht_inplace<16>(b, smask);
-        m_col = max(m_col, absmax_bits<16>(a));
-        if (col + 1 < g.cols) m_col = max(m_col, absmax_bits<16>(b));
-      }
-      __syncthreads();
-    }
-  }
-  if (!RHT) m_col = m_row;
-  const uint32_t cr = cta_max<NT>(m_row, sh_max);
-  const uint32_t cc = cta_max<NT>(m_col, sh_max);
-  if (tid == 0) {
-    ws->amax_part[0][blockIdx.x] = cr;
-    ws->amax_part[1][blockIdx.x] = cc;
-    if (blockIdx.x == 0) ws->amax_nparts = gridDim.x;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Per-block quantisation.
-// ---------------------------------------------------------------------------
-struct Acc {
-  Kahan bias, sig, err;      // sig / err in units of g^2 (NVFP4, UFP4)
-  double sig64 = 0.0, err64 = 0.0;   // MXFP4: absolute
-};
-
-// Quantise one block of N values (N = 16 for NVFP4/UFP4, 32 for MXFP4).
-// v: transformed values; idx0: row-major index of v[0] inside the copy (SR).
-// Writes N/2 bytes of packed codes to `codes` (registers) and returns the
-// scale code.
-template <int FMT, bool SR, int N>
-__device__ __forceinline__ uint32_t quant_block(const float* v, const Ctx& cx, uint64_t idx0,
-                                                uint32_t axis, uint64_t seed, uint32_t* codes,
-                                                Acc& acc, uint32_t& nonfinite) {
-  const uint32_t mb = absmax_bits<N>(v);
-  nonfinite |= (mb >= 0x7F800000u) ? 1u : 0u;
-  const float ab = __uint_as_float(mb);
-  uint32_t scode;
-  float r;        // y = v * r
-  float s2;       // scale^2 used for the statistics
-  int e2 = 0;     // MXFP4: 2 * e_b
-  if constexpr (FMT == 1) {
-    // floor(log2 a_b) from the exponent bits; subnormals via the leading-zero count
-    const uint32_t E = mb >> 23;
-    int fl = E ? (int)E - 127 : (mb ? (31 - __clz((int)mb)) - 149 : -200);
-    int e = max(-127, min(127, fl - 2));
-    scode = (uint32_t)(e + 127);
-    r = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 125]
-    s2 = 0.f;
-    e2 = 2 * e;
-  } else {
-    if (cx.g == 0.f) {
-      scode = 0; r = 0.f;
-    } else {
-      const float t = __fdiv_rn(ab, cx.d);
-      scode = f32_to_e4m3(t);
-      const float s = e4m3_to_f32(scode);
-      const float p = __fmul_rn(s, cx.g);
-      r = (p == 0.f) ? 0.f : __frcp_rn(p);
-      if (r > FLT_MAX) r = FLT_MAX;
-    }
-    const float s = e4m3_to_f32(scode);
-    s2 = __fmul_rn(s, s);
-  }
-
-  float bsum = 0.f, ysum = 0.f, esum = 0.f;
-#pragma unroll
-  for (int j = 0; j < N / 8; ++j) codes[j] = 0u;
-#pragma unroll
-  for (int i4 = 0; i4 < N; i4 += 4) {
-    // SR: one Philox call per 4 elements (idx0 is a multiple of 4)
-    uint4 rw = make_uint4(0u, 0u, 0u, 0u);
-    if constexpr (SR) {
-      const uint64_t q = (idx0 >> 2) + (uint64_t)(i4 >> 2);
-      rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
-    }
-#pragma unroll
-    for (int i = i4; i < i4 + 4; i += 2) {
-      const float y0 = __fmul_rn(v[i], r), y1 = __fmul_rn(v[i + 1], r);
-      float q0, q1;
-      uint32_t byte;
-      if constexpr (SR) {
-        const uint32_t w0 = (i == i4) ? rw.x : rw.z, w1 = (i == i4) ? rw.y : rw.w;
-        const uint32_t k0 = sr_level<FMT>(fabsf(y0), sr_u(w0), q0);
-        const uint32_t k1 = sr_level<FMT>(fabsf(y1), sr_u(w1), q1);
-        byte = (k0 | ((__float_as_uint(y0) >> 31) << 3)) |
-               ((k1 | ((__float_as_uint(y1) >> 31) << 3)) << 4);
-      } else if constexpr (FMT == 2) {
-        const float a0 = fminf(fabsf(y0), 7.f), a1 = fminf(fabsf(y1), 7.f);
-        const uint32_t k0 = __float2uint_rn(a0), k1 = __float2uint_rn(a1);
-        q0 = (float)k0; q1 = (float)k1;
-        byte = (k0 | ((__float_as_uint(y0) >> 31) << 3)) |
-               ((k1 | ((__float_as_uint(y1) >> 31) << 3)) << 4);
-      } else {
-        byte = e2m1x2(y0, y1);
-        e2m1x2_abs(byte, q0, q1);
-      }
-      codes[i / 8] |= byte << (8 * ((i / 2) & 3));
-      const float d0 = __fsub_rn(q0, fabsf(y0)), d1 = __fsub_rn(q1, fabsf(y1));
-      bsum = __fadd_rn(bsum, __fadd_rn(d0, d1));
-      esum = __fmaf_rn(d0, d0, __fmaf_rn(d1, d1, esum));
-      ysum = __fmaf_rn(y0, y0, __fmaf_rn(y1, y1, ysum));
-    }
-  }
-  acc.bias.add(bsum);
-  if constexpr (FMT == 1) {
-    const double sc = __longlong_as_double((long long)(1023 + e2) << 52);
-    acc.sig64 += (double)ysum * sc;
-    acc.err64 += (double)esum * sc;
-  } else if (scode == 0 && cx.g > 0.f) {
-    // scale rounded to 0: every element becomes 0, its error is v itself
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-      const float w = __fmul_rn(v[i], cx.inv_g);
-      z = __fmaf_rn(w, w, z);
-    }
-    acc.sig.add(z);
-    acc.err.add(z);
-  } else {
-    acc.sig.add(__fmul_rn(ysum, s2));
-    acc.err.add(__fmul_rn(esum, s2));
-  }
-  return scode;
-}
-
-// ---------------------------------------------------------------------------
-// K2: quantise. FMT 0 = NVFP4, 1 = MXFP4, 2 = UFP4.
-// ---------------------------------------------------------------------------
-template <int FMT, bool F32, bool RHT, bool SR, bool ROWS, bool COLS>
-__global__ void __launch_bounds__(NT, 3) quantize_kernel(Geom g, uint64_t seed, CopyOut orow,
-                                                         CopyOut ocol, Workspace* ws) {
-  extern __shared__ __align__(16) uint8_t tile[];
-  __shared__ double sh_sum[NT / 32];
-  __shared__ float sh_f[6][NT / 32];
-  __shared__ uint32_t sh_max[NT / 32];
-  constexpr float kQmax = (FMT == 2) ? 7.f : 6.f;
-  constexpr float kQmax448 = (FMT == 2) ? 3136.f : 2688.f;
-  const int tid = threadIdx.x;
-  const uint32_t smask = RHT ? rht_sign_mask(seed) : 0u;
-
-  Ctx cr{1.f, 0.f, 0.f}, cc{1.f, 0.f, 0.f};
-  if constexpr (FMT != 1) {
-    cr = make_ctx(fold_amax<NT>(ws, 0, sh_max), kQmax, kQmax448);
-    cc = make_ctx(fold_amax<NT>(ws, 1, sh_max), kQmax, kQmax448);
-  }
-  Acc arow, acol;
-  uint32_t nonfinite = 0;
-
-  for (int64_t t = blockIdx.x; t < g.ntiles; t += gridDim.x) {
-    const int64_t r0 = (t / g.ntc) * TR, c0 = (t % g.ntc) * TC;
-    float v[32];
-    const int nv = load_row_segment<F32>(g, r0, c0, tid, v, tile, COLS);
-    if constexpr (ROWS) {
-      if (nv > 0) {
-        if (RHT) rht_inplace<32>(v, smask);
-        const int64_t r = r0 + (tid >> 2);
-        const int64_t c = c0 + 32 * (tid & 3);
-        uint32_t cw[4];
-        if constexpr (FMT == 1) {
-          const uint32_t sc = quant_block<FMT, SR, 32>(v, cr, (uint64_t)(r * g.cols + c), 0u, seed, cw, arow, nonfinite);
-          *reinterpret_cast<uint4*>(orow.codes + r * orow.ld + c / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          store_scale(orow, r, c / 32, sc);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (j < nv) {
-              const uint32_t sc = quant_block<FMT, SR, 16>(v + 16 * j, cr, (uint64_t)(r * g.cols + c + 16 * j), 0u, seed, cw + 2 * j, arow, nonfinite);
-              *reinterpret_cast<uint2*>(orow.codes + r * orow.ld + (c + 16 * j) / 2) = make_uint2(cw[2 * j], cw[2 * j + 1]);
-              store_scale(orow, r, (c + 16 * j) / 16, sc);
-            }
-          }
-        }
-      }
-    }
-    if constexpr (COLS) {
-      __syncthreads();
-      if constexpr (FMT == 1) {
-        const int col = tid & 127, cb = tid >> 7;
-        const int64_t rb = r0 + 32 * cb, cg = c0 + col;
-        if (rb < g.rows && cg < g.cols) {
-          float a[32];
-          read_col32<F32>(tile, 32 * cb, col, a);
-          if (RHT) rht_inplace<32>(a, smask);
-          uint32_t cw[4];
-          const uint32_t sc = quant_block<FMT, SR, 32>(a, cc, (uint64_t)(cg * g.rows + rb), 1u, seed, cw, acol, nonfinite);
-          *reinterpret_cast<uint4*>(ocol.codes + cg * ocol.ld + rb / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          store_scale(ocol, cg, rb / 32, sc);
-        }
-      } else {
-        const int pair = tid & 63, cb = tid >> 6;
-        const int64_t rb = r0 + 16 * cb, cg = c0 + 2 * pair;
-        if (rb < g.rows && cg < g.cols) {
-          float a[16], b[16];
-          read_col_pair<F32>(tile, 16 * cb, pair, a, b);
-          if (RHT) { rht_inplace<16>(a, smask); rht_inplace<16>(b, smask); }
-          uint32_t cw[2];
-          uint32_t sc = quant_block<FMT, SR, 16>(a, cc, (uint64_t)(cg * g.rows + rb), 1u, seed, cw, acol, nonfinite);
-          *reinterpret_cast<uint2*>(ocol.codes + cg * ocol.ld + rb / 2) = make_uint2(cw[0], cw[1]);
-          store_scale(ocol, cg, rb / 16, sc);
-          if (cg + 1 < g.cols) {
-            sc = quant_block<FMT, SR, 16>(b, cc, (uint64_t)((cg + 1) * g.rows + rb), 1u, seed, cw, acol, nonfinite);
-            *reinterpret_cast<uint2*>(ocol.codes + (cg + 1) * ocol.ld + rb / 2) = make_uint2(cw[0], cw[1]);
-            store_scale(ocol, cg + 1, rb / 16, sc);
-          }
-        }
-      }
-      __syncthreads();
-    }
-  }
-
-  // ---- statistics: one partial per CTA (summed on the host by fp4q_stats) ----
-  if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
-  if constexpr (FMT == 1) {
-    const double p[2][3] = {{arow.bias.value(), arow.sig64, arow.err64},
-                            {acol.bias.value(), acol.sig64, acol.err64}};
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-#pragma unroll
-      for (int k = 0; k < 3; ++k) {
-        const double v = cta_sum<NT>(p[c][k], sh_sum);
-        if (tid == 0) ws->stat_part[c][k][blockIdx.x] = v;
-      }
-    }
-  } else {
-    float v[6] = {(float)arow.bias.value(), (float)arow.sig.value(), (float)arow.err.value(),
-                  (float)acol.bias.value(), (float)acol.sig.value(), (float)acol.err.value()};
-    cta_sums_f32<NT, 6>(v, sh_f);
-    if (tid == 0) {
-#pragma unroll
-      for (int k = 0; k < 6; ++k) ws->stat_part[k / 3][k % 3][blockIdx.x] = (double)v[k];
-    }
-  }
-  if (blockIdx.x == 0 && tid == 0) {
-    ws->stat_nparts = gridDim.x;
-    ws->copies = (ROWS ? 1u : 0u) | (COLS ? 2u : 0u);
-    ws->tensor_scale[0] = (FMT == 1) ? 1.f : cr.g;
-    ws->tensor_scale[1] = (FMT == 1) ? 1.f : cc.g;
-    ws->qmax = kQmax;
-    ws->n = (double)g.rows * (double)g.cols;
-    if (ROWS && orow.tensor_scale) *orow.tensor_scale = (FMT == 1) ? 1.f : cr.g;
-    if (COLS && ocol.tensor_scale) *ocol.tensor_scale = (FMT == 1) ? 1.f : cc.g;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Host launchers.
-// ---------------------------------------------------------------------------
-static CopyOut make_copy(const QOut& o, int64_t crow, int64_t ccol, int block) {
-  CopyOut c{};
-  c.codes = o.codes;
-  c.scales = o.scales;
-  c.tensor_scale = o.tensor_scale;
-  c.mma = o.scale_layout;
-  c.ld = ccol / 2;
-  c.nkb = ccol / block;
-  c.nkb_p = (c.nkb + 3) / 4 * 4;
-  (void)crow;
-  return c;
-}
-
-template <typename K>
-static int grid_for(K kernel, int smem, int64_t ntiles) {
-  const int occ = cached_occupancy(reinterpret_cast<const void*>(kernel), NT, smem);
-  int64_t gmax = (int64_t)sm_count() * (occ > 0 ? occ : 1);
-  if (gmax > kMaxCtas) gmax = kMaxCtas;
-  return (int)(ntiles < gmax ? ntiles : gmax);
-}
-
-template <bool F32, bool RHT, bool ROWS, bool COLS>
-static cudaError_t launch_amax(const Geom& g, uint64_t seed, Workspace* ws, cudaStream_t s) {
-  auto k = amax_kernel<F32, RHT, ROWS, COLS>;
-  const int smem = (RHT && COLS) ? TileSmem<F32>::kBytes : 0;
-  const int grid = grid_for(k, smem, g.ntiles);
-  k<<<grid, NT, smem, s>>>(g, seed, ws);
-  return cudaGetLastError();
-}
-
-template <int FMT, bool F32, bool RHT, bool SR, bool ROWS, bool COLS>
-static cudaError_t launch_quant(const Geom& g, uint64_t seed, const CopyOut& r, const CopyOut& c,
-                                Workspace* ws, cudaStream_t s) {
-  auto k = quantize_kernel<FMT, F32, RHT, SR, ROWS, COLS>;
-  const int smem = COLS ? TileSmem<F32>::kBytes : 0;
-  const int grid = grid_for(k, smem, g.ntiles);
-  k<<<grid, NT, smem, s>>>(g, seed, r, c, ws);
-  return cudaGetLastError();
-}
-
-template <int FMT, bool F32, bool RHT, bool SR>
-static cudaError_t dispatch_axis(int axis, const Geom& g, uint64_t seed, const CopyOut& r,
-                                 const CopyOut& c, Workspace* ws, cudaStream_t s) {
-  if (axis == 1) return launch_quant<FMT, F32, RHT, SR, true, false>(g, seed, r, c, ws, s);
-  if (axis == 2) return launch_quant<FMT, F32, RHT, SR, false, true>(g, seed, r, c, ws, s);
-  return launch_quant<FMT, F32, RHT, SR, true, true>(g, seed, r, c, ws, s);
-}
-
-template <int FMT, bool F32>
-static cudaError_t dispatch_rs(int rht, int sr, int axis, const Geom& g, uint64_t seed,
-                               const CopyOut& r, const CopyOut& c, Workspace* ws, cudaStream_t s) {
-  if (rht) {
-    return sr ? dispatch_axis<FMT, F32, true, true>(axis, g, seed, r, c, ws, s)
-              : dispatch_axis<FMT, F32, true, false>(axis, g, seed, r, c, ws, s);
-  }
-  return sr ? dispatch_axis<FMT, F32, false, true>(axis, g, seed, r, c, ws, s)
-            : dispatch_axis<FMT, F32, false, false>(axis, g, seed, r, c, ws, s);
-}
-
-template <bool F32>
-static cudaError_t dispatch_amax(int rht, int axis, const Geom& g, uint64_t seed, Workspace* ws,
-                                 cudaStream_t s) {
-  if (!rht) return launch_amax<F32, false, true, false>(g, seed, ws, s);
-  if (axis == 1) return launch_amax<F32, true, true, false>(g, seed, ws, s);
-  if (axis == 2) return launch_amax<F32, true, false, true>(g, seed, ws, s);
-  return launch_amax<F32, true, true, true>(g, seed, ws, s);
-}
+namespace {
 
 // Empty input: write the tensor scales and empty statistics, nothing else.
 __global__ void quantize_empty_kernel(int fmt, int axis, float* ts_row, float* ts_col, Workspace* ws) {
@@ -516,16 +42,6 @@ __global__ void quantize_empty_kernel(int fmt, int axis, float* ts_row, float* t
   if ((axis & 2) && ts_col) *ts_col = g;
 }
 
-static Geom make_geom(const QuantArgs& a) {
-  Geom g{};
-  g.src = a.src;
-  g.rows = a.rows;
-  g.cols = a.cols;
-  g.ntc = (a.cols + TC - 1) / TC;
-  g.ntiles = ((a.rows + TR - 1) / TR) * g.ntc;
-  return g;
-}
-
 // Empty input: a zero amax for both copies.
 __global__ void amax_empty_kernel(Workspace* ws) {
   ws->amax_part[0][0] = 0u;
@@ -533,16 +49,17 @@ __global__ void amax_empty_kernel(Workspace* ws) {
   ws->amax_nparts = 1u;
 }
 
+}  // namespace
+
 cudaError_t run_amax(const QuantArgs& a, cudaStream_t s) {
   Workspace* ws = static_cast<Workspace*>(a.ws);
   if (a.rows == 0 || a.cols == 0) {
     amax_empty_kernel<<<1, 1, 0, s>>>(ws);
     return cudaGetLastError();
   }
+  // without the RHT both copies hold the same values, so one flat pass serves both
   if (!a.rht || a.axis == 1) return run_amax_rows(a, s);
-  const Geom g = make_geom(a);
-  return a.dtype == 1 ? dispatch_amax<true>(a.rht, a.axis, g, a.seed, ws, s)
-                      : dispatch_amax<false>(a.rht, a.axis, g, a.seed, ws, s);
+  return run_amax_tiles(a, s);
 }
 
 cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
@@ -551,38 +68,21 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
                                           static_cast<Workspace*>(a.ws));
     return cudaGetLastError();
   }
-  const Geom g = make_geom(a);
-  const int block = a.fmt == 1 ? 32 : 16;
-  const CopyOut r = make_copy(a.row, a.rows, a.cols, block);
-  const CopyOut c = make_copy(a.col, a.cols, a.rows, block);
-  Workspace* ws = static_cast<Workspace*>(a.ws);
-  cudaError_t e = cudaSuccess;
-  const bool f32 = a.dtype == 1;
   // Both passes in one launch pays for tensors up to 2^24 elements (one fixed
   // launch cost less; measured on B300: 12.4 vs 14.4 us at 1M elements) and
   // ties at 2^25; above that the two launches are faster, because the second
   // launch's grid restarts on chunks the amax pass left in L2.
   if (a.fmt != 1 && !a.amax_ready && a.axis == 1 && a.rows * a.cols < (int64_t(1) << 25)) {
     // the two-launch path if a co-resident grid cannot be had
-    e = run_quant_fused(a, s);
+    const cudaError_t e = run_quant_fused(a, s);
     if (e == cudaSuccess) return e;
     cudaGetLastError();
   }
   if (a.fmt != 1 && !a.amax_ready) {
-    e = run_amax(a, s);
+    const cudaError_t e = run_amax(a, s);
     if (e != cudaSuccess) return e;
   }
-  if (a.axis == 1) return run_quant_rows(a, s);
-  const int sr = a.rounding == 1;
-  switch (a.fmt) {
-    case 0: e = f32 ? dispatch_rs<0, true>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s)
-                    : dispatch_rs<0, false>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s); break;
-    case 1: e = f32 ? dispatch_rs<1, true>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s)
-                    : dispatch_rs<1, false>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s); break;
-    default: e = f32 ? dispatch_rs<2, true>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s)
-                     : dispatch_rs<2, false>(a.rht, sr, a.axis, g, a.seed, r, c, ws, s); break;
-  }
-  return e;
+  return a.axis == 1 ? run_quant_rows(a, s) : run_quant_tiles(a, s);
 }
 
 }  // namespace fp4q

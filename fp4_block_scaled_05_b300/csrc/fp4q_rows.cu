@@ -181,14 +181,31 @@ __device__ __forceinline__ void rht16_unscaled(float (&x)[16]) {
   }
 }
 
-// Widen 16 elements of the chunk at `p` to FP32, flipping signs by `sign` when
-// RHT (BF16: sign words hold sigma at bits 15 and 31; FP32: one bit per value).
-template <bool F32, bool RHT>
-__device__ __forceinline__ void widen16(const uint8_t* p, const uint32_t (&sgn)[16], float (&x)[16]) {
+// A thread's 32-element segment in shared memory, read as 16-byte chunks
+// (4 for BF16, 8 for FP32). LinearSeg: the chunks are contiguous. SwzSeg: one
+// row of a TMA box written with the 128-byte swizzle, where chunk c of row r
+// sits at position c ^ (r & 7); `y` holds 16 * (first chunk ^ (r & 7)).
+struct LinearSeg {
+  const uint8_t* p;
+  __device__ __forceinline__ uint4 chunk(int k) const { return *reinterpret_cast<const uint4*>(p + 16 * k); }
+};
+struct SwzSeg {
+  const uint8_t* row;
+  uint32_t y;
+  __device__ __forceinline__ uint4 chunk(int k) const {
+    return *reinterpret_cast<const uint4*>(row + ((16u * (uint32_t)k) ^ y));
+  }
+};
+
+// Widen the 16 elements starting at chunk k0 of `sg` to FP32, flipping signs
+// by `sign` when RHT (BF16: sign words hold sigma at bits 15 and 31; FP32: one
+// bit per value).
+template <bool F32, bool RHT, class Seg>
+__device__ __forceinline__ void widen16(const Seg& sg, int k0, const uint32_t (&sgn)[16], float (&x)[16]) {
   if constexpr (F32) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * k);
+      const uint4 u = sg.chunk(k0 + k);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) x[4 * k + i] = __uint_as_float(RHT ? (w[i] ^ sgn[4 * k + i]) : w[i]);
@@ -196,7 +213,7 @@ __device__ __forceinline__ void widen16(const uint8_t* p, const uint32_t (&sgn)[
   } else {
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-      const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * k);
+      const uint4 u = sg.chunk(k0 + k);
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -208,10 +225,10 @@ __device__ __forceinline__ void widen16(const uint8_t* p, const uint32_t (&sgn)[
   }
 }
 
-template <bool F32, bool RHT>
-__device__ __forceinline__ void load_block16(const uint8_t* p, const uint32_t (&sgn)[16], f2* Q) {
+template <bool F32, bool RHT, class Seg>
+__device__ __forceinline__ void load_block16(const Seg& sg, int k0, const uint32_t (&sgn)[16], f2* Q) {
   float x[16];
-  widen16<F32, RHT>(p, sgn, x);
+  widen16<F32, RHT>(sg, k0, sgn, x);
   if constexpr (RHT) {
     rht16_pairs(x, Q);
   } else {
@@ -342,15 +359,70 @@ __device__ __forceinline__ uint32_t ufp4_pair(f2 Y, f2& D) {
          ((__float_as_uint(y0) >> 31) << 3) | ((__float_as_uint(y1) >> 31) << 7);
 }
 
-// Stochastic rounding of a pair with the uniforms of words w0, w1.
+// ---- stochastic rounding of a pair, without branches ------------------------------
+// The level goes up iff u < f, f = (|y| - lo) / step the exact fraction of the
+// way from the level below to the one above and u = (w >> 8) 2^-24 the
+// element's uniform. Both grids have power-of-two steps, so f is exact; floor
+// is an addition of 2^23 rounded toward zero (exact below 2^23).
+__device__ __forceinline__ f2 f2_add_rz(f2 a, f2 b) {
+  f2 d;
+  asm("add.rz.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// E2M1: with a = min(|y|, 6) and E = max(floor(log2 a), 0) the neighbouring
+// levels are lo and lo + step, step = 2^(E-1) (0.5 below 2, then 1, then 2):
+// t = a / step, lo = floor(t) step. The grid value q is exact and its code
+// (sign of y kept) comes from the nearest-even conversion of the signed q.
+__device__ __forceinline__ uint32_t sr_pair_e2m1(f2 Y, uint32_t w0, uint32_t w1, f2& D) {
+  float y0, y1;
+  f2_split(Y, y0, y1);
+  const float a0 = fminf(fabsf(y0), 6.f), a1 = fminf(fabsf(y1), 6.f);
+  const uint32_t m0 = max(__float_as_uint(a0) >> 23, 127u), m1 = max(__float_as_uint(a1) >> 23, 127u);
+  const f2 T = f2_mul(f2_make(a0, a1),
+                      f2_make(__uint_as_float((255u - m0) << 23), __uint_as_float((255u - m1) << 23)));
+  const f2 magic = f2_make(8388608.f, 8388608.f);
+  const f2 FL = f2_sub(f2_add_rz(T, magic), magic);
+  float t0, t1, l0, l1;
+  f2_split(T, t0, t1);
+  f2_split(FL, l0, l1);
+  const float v0 = (sr_u(w0) < __fsub_rn(t0, l0)) ? __fadd_rn(l0, 1.f) : l0;
+  const float v1 = (sr_u(w1) < __fsub_rn(t1, l1)) ? __fadd_rn(l1, 1.f) : l1;
+  const f2 Q = f2_mul(f2_make(v0, v1),
+                      f2_make(__uint_as_float((m0 - 1u) << 23), __uint_as_float((m1 - 1u) << 23)));
+  D = f2_sub(Q, f2_make(fabsf(y0), fabsf(y1)));
+  float q0, q1;
+  f2_split(Q, q0, q1);
+  uint32_t byte;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(byte) : "f"(copysignf(q0, y0)), "f"(copysignf(q1, y1)));
+  return byte;
+}
+
+// UFP4: integer levels 0..7; with a = min(|y|, 7), lo = floor(a), whose low
+// three bits sit in the mantissa of a + 2^23 (rounded toward zero).
+__device__ __forceinline__ uint32_t sr_pair_ufp4(f2 Y, uint32_t w0, uint32_t w1, f2& D) {
+  float y0, y1;
+  f2_split(Y, y0, y1);
+  const f2 A = f2_make(fminf(fabsf(y0), 7.f), fminf(fabsf(y1), 7.f));
+  const f2 magic = f2_make(8388608.f, 8388608.f);
+  const f2 T = f2_add_rz(A, magic);
+  const f2 L = f2_sub(T, magic);
+  const f2 F = f2_sub(A, L);
+  float l0, l1, f0, f1, t0, t1;
+  f2_split(L, l0, l1);
+  f2_split(F, f0, f1);
+  f2_split(T, t0, t1);
+  const uint32_t u0 = (sr_u(w0) < f0) ? 1u : 0u, u1 = (sr_u(w1) < f1) ? 1u : 0u;
+  D = f2_sub(f2_make(__fadd_rn(l0, (float)u0), __fadd_rn(l1, (float)u1)), f2_make(fabsf(y0), fabsf(y1)));
+  const uint32_t k0 = (__float_as_uint(t0) & 7u) + u0, k1 = (__float_as_uint(t1) & 7u) + u1;
+  return (k0 | ((__float_as_uint(y0) >> 31) << 3)) | ((k1 | ((__float_as_uint(y1) >> 31) << 3)) << 4);
+}
+
 template <int FMT>
 __device__ __forceinline__ uint32_t sr_pair(f2 Y, uint32_t w0, uint32_t w1, f2& D) {
-  float y0, y1, q0, q1;
-  f2_split(Y, y0, y1);
-  const uint32_t k0 = sr_level<FMT>(fabsf(y0), sr_u(w0), q0);
-  const uint32_t k1 = sr_level<FMT>(fabsf(y1), sr_u(w1), q1);
-  D = f2_make(__fsub_rn(q0, fabsf(y0)), __fsub_rn(q1, fabsf(y1)));
-  return (k0 | ((__float_as_uint(y0) >> 31) << 3)) | ((k1 | ((__float_as_uint(y1) >> 31) << 3)) << 4);
+  if constexpr (FMT == 2) return sr_pair_ufp4(Y, w0, w1, D);
+  else return sr_pair_e2m1(Y, w0, w1, D);
 }
 
 // Quantise one block of NP pairs (NP = 8: a 16-block, NP = 16: an MXFP4
@@ -360,7 +432,7 @@ __device__ __forceinline__ uint32_t sr_pair(f2 Y, uint32_t w0, uint32_t w1, f2& 
 template <int FMT, bool SR, int NP>
 __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint64_t e0, uint64_t seed,
                                                 uint32_t* cw, float& bsum, float& ssum, float& esum,
-                                                Sums& acc, uint32_t& nonfinite) {
+                                                Sums& acc, uint32_t& nonfinite, uint32_t axis = 0u) {
   float m = 0.f;
 #pragma unroll
   for (int j = 0; j < NP; ++j) {
@@ -404,7 +476,7 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
     uint4 rw = make_uint4(0u, 0u, 0u, 0u);
     if constexpr (SR) {   // one Philox call per 4 elements (e0 is a multiple of 16)
       const uint64_t q = (e0 >> 2) + (uint64_t)(j0 >> 1);
-      rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
+      rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), (uint32_t)seed,
                          (uint32_t)(seed >> 32));
     }
 #pragma unroll
@@ -459,8 +531,15 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
 // two lanes of FP32 pairs. Writes four code words and two scale codes; adds
 // the blocks' bias / signal / error sums (grid units, signal and error times
 // s^2) to the lanes of bias2 / sig2 / err2.
-template <int FMT, bool F32, bool RHT, bool SR>
-__device__ __forceinline__ void quant_two16(const uint8_t* p, const uint32_t (&sgn)[16], const Ctx& cx,
+template <int FMT, bool SR>
+__device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1, const Ctx& cx,
+                                                 const Divider& dv, const float2* tab, uint64_t e0,
+                                                 uint64_t e1, uint64_t seed, uint32_t axis,
+                                                 uint32_t (&cw)[4], uint32_t (&sc)[2], f2& bias2,
+                                                 f2& sig2, f2& err2, uint32_t& nonfinite);
+
+template <int FMT, bool F32, bool RHT, bool SR, class Seg>
+__device__ __forceinline__ void quant_two16(const Seg& sg, const uint32_t (&sgn)[16], const Ctx& cx,
                                             const Divider& dv, const float2* tab, uint64_t e,
                                             uint64_t seed, uint32_t (&cw)[4], uint32_t (&sc)[2],
                                             f2& bias2, f2& sig2, f2& err2, uint32_t& nonfinite) {
@@ -470,7 +549,7 @@ __device__ __forceinline__ void quant_two16(const uint8_t* p, const uint32_t (&s
     uint32_t w[16];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint4 u = *reinterpret_cast<const uint4*>(p + 16 * k);
+      const uint4 u = sg.chunk(k);
       w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
     }
     uint32_t a0 = 0u, a1 = 0u;     // block maxima on the BF16 pairs
@@ -484,8 +563,8 @@ __device__ __forceinline__ void quant_two16(const uint8_t* p, const uint32_t (&s
 #pragma unroll
     for (int j = 0; j < 16; ++j) Q[j] = f2_make(bf16lo(w[j]), bf16hi(w[j]));
   } else {
-    load_block16<F32, RHT>(p, sgn, Q);
-    load_block16<F32, RHT>(p + 16 * (F32 ? 4 : 2), sgn, Q + 8);
+    load_block16<F32, RHT>(sg, 0, sgn, Q);
+    load_block16<F32, RHT>(sg, F32 ? 4 : 2, sgn, Q + 8);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float a, b;
@@ -495,6 +574,20 @@ __device__ __forceinline__ void quant_two16(const uint8_t* p, const uint32_t (&s
       m1 = max3_abs_nan(m1, a, b);
     }
   }
+  quant_two16_vals<FMT, SR>(Q, m0, m1, cx, dv, tab, e, e + 16, seed, 0u, cw, sc, bias2, sig2, err2,
+                            nonfinite);
+}
+
+// Quantise two 16-blocks given as FP32 pairs (block 0 in Q[0..7], block 1 in
+// Q[8..15], pair j holding elements 2j and 2j+1) with their maxima |v| m0, m1;
+// e0, e1 are the blocks' first element indices in the copy, `axis` the copy
+// (0 row-wise, 1 column-wise) for the SR counter.
+template <int FMT, bool SR>
+__device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1, const Ctx& cx,
+                                                 const Divider& dv, const float2* tab, uint64_t e0,
+                                                 uint64_t e1, uint64_t seed, uint32_t axis,
+                                                 uint32_t (&cw)[4], uint32_t (&sc)[2], f2& bias2,
+                                                 f2& sig2, f2& err2, uint32_t& nonfinite) {
   nonfinite |= (max(__float_as_uint(m0), __float_as_uint(m1)) >= 0x7F800000u) ? 1u : 0u;
 
   sc[0] = sc[1] = 0u;
@@ -519,8 +612,8 @@ __device__ __forceinline__ void quant_two16(const uint8_t* p, const uint32_t (&s
     for (int j0 = 0; j0 < 8; j0 += 2) {
       uint4 rw = make_uint4(0u, 0u, 0u, 0u);
       if constexpr (SR) {   // one Philox call per 4 elements
-        const uint64_t q = ((e + 16 * b) >> 2) + (uint64_t)(j0 >> 1);
-        rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
+        const uint64_t q = ((b ? e1 : e0) >> 2) + (uint64_t)(j0 >> 1);
+        rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), (uint32_t)seed,
                            (uint32_t)(seed >> 32));
       }
 #pragma unroll
@@ -593,17 +686,17 @@ __device__ __forceinline__ void put_scale(const CopyOut& o, const Flat& f, uint6
 // ---- per-thread work on its 32 elements of a ring slot ---------------------------------
 // Running max |v| of the (up to two) 16-blocks at p: `m` (FP32 values; |w| = 4|v|
 // with the RHT) or `m2` (BF16 pairs, no RHT).
-template <bool F32, bool RHT>
-__device__ __forceinline__ void amax_segment(const uint8_t* p, int nb, const uint32_t (&sgn)[16], float& m,
+template <bool F32, bool RHT, class Seg>
+__device__ __forceinline__ void amax_segment(const Seg& sg, int nb, const uint32_t (&sgn)[16], float& m,
                                              uint32_t& m2) {
 #pragma unroll
   for (int b = 0; b < 2; ++b) {
     if (b < nb) {
-      const uint8_t* pb = p + b * 16 * (F32 ? 4 : 2);
+      const int kb = b * (F32 ? 4 : 2);
       if constexpr (!RHT && !F32) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-          const uint4 u = *reinterpret_cast<const uint4*>(pb + 16 * k);
+          const uint4 u = sg.chunk(kb + k);
           m2 = max_abs_nan_bf16x2(m2, u.x);
           m2 = max_abs_nan_bf16x2(m2, u.y);
           m2 = max_abs_nan_bf16x2(m2, u.z);
@@ -611,7 +704,7 @@ __device__ __forceinline__ void amax_segment(const uint8_t* p, int nb, const uin
         }
       } else {
         float x[16];
-        widen16<F32, RHT>(pb, sgn, x);
+        widen16<F32, RHT>(sg, kb, sgn, x);
         if (RHT) rht16_unscaled(x);
 #pragma unroll
         for (int i = 0; i < 16; i += 2) m = max3_abs_nan(m, x[i], x[i + 1]);
@@ -638,14 +731,13 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
                                               const uint32_t (&sgn)[16], const Ctx& cx, const Divider& dv,
                                               const float2* tab, uint64_t seed, Sums& acc, Kahan2& kb,
                                               Kahan2& ks, Kahan2& ke, uint32_t& nonfinite) {
-  constexpr int ES = F32 ? 4 : 2;
   const int nb16 = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
   if constexpr (FMT == 1) {
     if (nb16 == 2) {
       float bsum = 0.f, ssum = 0.f, esum = 0.f;
       f2 Q[16];
-      load_block16<F32, RHT>(p, sgn, Q);
-      load_block16<F32, RHT>(p + 16 * ES, sgn, Q + 8);
+      load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
+      load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
       uint32_t cw[4];
       const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
                                                     acc, nonfinite);
@@ -656,7 +748,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
   } else if (nb16 == 2) {
     uint32_t cw[4], sc[2];
     f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
-    quant_two16<FMT, F32, RHT, SR>(p, sgn, cx, dv, tab, (uint64_t)e, seed, cw, sc, b2, s2, e2,
+    quant_two16<FMT, F32, RHT, SR>(LinearSeg{p}, sgn, cx, dv, tab, (uint64_t)e, seed, cw, sc, b2, s2, e2,
                                    nonfinite);
     *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     put_scale(o, f, (uint64_t)e / 16, sc[0]);
@@ -668,7 +760,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
     // a lone 16-block at the very end of the copy
     float bsum = 0.f, ssum = 0.f, esum = 0.f;
     f2 Q[8];
-    load_block16<F32, RHT>(p, sgn, Q);
+    load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
     uint32_t cw[2];
     const uint32_t sc = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
                                                  acc, nonfinite);
@@ -705,7 +797,8 @@ __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed,
     if (ok) {
       const int64_t e = (f.nchunks - 1 - c) * CH + (int64_t)tid * EPT;
       const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
-      amax_segment<F32, RHT>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2), nb, sgn, m, m2);
+      amax_segment<F32, RHT>(LinearSeg{ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2)}, nb, sgn, m,
+                             m2);
     }
     timed_out = __syncthreads_or(!ok);
     if (timed_out) break;
@@ -805,6 +898,486 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   }
 }
 
+// ---- requests with the transposed (column-wise) copy: tiles through a ring ------------
+// The source is walked in 64 x 128 tiles. Warp 0 brings each tile into a ring
+// slot with 2-D TMA loads, as boxes of 64 rows x 128 bytes (two per tile for
+// BF16, four for FP32) written with the 128-byte swizzle: chunk c (16 bytes)
+// of row r lands at chunk position c ^ (r & 7). With that layout both reading
+// patterns are free of bank conflicts: the row-wise pass (each thread 32
+// consecutive elements of one row, the 8 lanes of a quarter-warp on 8
+// consecutive rows) and the column-wise pass (each thread two adjacent columns
+// x 16 rows, a warp covering one 128-byte box row at a time). One read of the
+// source serves both copies. Rows and cols are multiples of 16; TMA fills the
+// parts of a box outside the tensor with zeros, which no thread reads.
+constexpr int TTR = 64;     // tile rows
+constexpr int TTC = 128;    // tile cols
+constexpr int kBoxBytes = TTR * 128;
+
+template <bool F32>
+struct TileRing {
+  static constexpr int kBoxes = F32 ? 4 : 2;
+  static constexpr int kBoxCols = F32 ? 32 : 64;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStages = F32 ? 3 : 4;
+  static constexpr int kSmem = kStages * kTileBytes + 1024;    // + slack to align the ring to 1024
+};
+
+struct TileGeom {
+  int64_t rows, cols;
+  int64_t ntc;        // tiles along the columns
+  int64_t ntiles;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int32_t x,
+                                            int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Lane 0 of warp 0 fills `slot` with tile t: the byte count (whole boxes, the
+// zero fill included), then one load per box.
+template <bool F32>
+__device__ __forceinline__ void tile_issue(const CUtensorMap* map, const TileGeom& g, int64_t t, uint8_t* slot,
+                                           uint32_t bar) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int32_t r0 = (int32_t)((t / g.ntc) * TTR), c0 = (int32_t)((t % g.ntc) * TTC);
+  mbar_arrive_expect_tx(bar, (uint32_t)TileRing<F32>::kTileBytes);
+#pragma unroll
+  for (int b = 0; b < TileRing<F32>::kBoxes; ++b)
+    tma_load_2d(smem_u32(slot + b * kBoxBytes), map, bar, c0 + b * TileRing<F32>::kBoxCols, r0);
+}
+
+// Ring protocol. full[s]: the slot's loads have landed (one arrival with the
+// byte count, then the loads' transactions). empty[s]: every warp is done
+// reading the slot (one arrival per warp). Warps run ahead of one another by
+// up to kStages - 1 tiles; only warp 0, which refills the slots, waits for the
+// slowest. Every wait is bounded.
+struct TilePipe {
+  uint64_t* full;
+  uint64_t* empty;
+  int64_t next_it;     // warp 0: the next iteration whose tile is to be issued
+};
+
+template <bool F32>
+__device__ __forceinline__ void tile_ring_start(const CUtensorMap* map, const TileGeom& g, uint8_t* ring,
+                                                TilePipe& p) {
+  constexpr int S = TileRing<F32>::kStages;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&p.full[s]), 1);
+      mbar_init(smem_u32(&p.empty[s]), RT / 32);
+    }
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  p.next_it = 0;
+  if (threadIdx.x < 32) {
+    for (int s = 0; s < S; ++s) {
+      const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
+      if (t >= g.ntiles) break;
+      tile_issue<F32>(map, g, t, ring + s * TileRing<F32>::kTileBytes, smem_u32(&p.full[s]));
+      p.next_it = s + 1;
+    }
+  }
+}
+
+// The calling warp is done with iteration `it` (tile t). Warp 0 then waits for
+// the other warps to be done with the slot too and refills it with the tile
+// kStages iterations later. False if that wait ran out.
+template <bool F32>
+__device__ __forceinline__ bool tile_ring_release(const CUtensorMap* map, const TileGeom& g, uint8_t* ring,
+                                                  TilePipe& p, int64_t it, int64_t t, uint64_t timeout_ns) {
+  constexpr int S = TileRing<F32>::kStages;
+  const int s = (int)(it % S);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&p.empty[s]));
+  if (threadIdx.x < 32) {
+    const int64_t nx = t + (int64_t)S * gridDim.x;
+    if (nx < g.ntiles) {
+      if (!mbar_wait_bounded(smem_u32(&p.empty[s]), (uint32_t)((it / S) & 1), timeout_ns)) return false;
+      tile_issue<F32>(map, g, nx, ring + s * TileRing<F32>::kTileBytes, smem_u32(&p.full[s]));
+      p.next_it = it + S + 1;
+    }
+  }
+  return true;
+}
+
+// After a wait ran out: thread 0 waits (50 ms at most) for the loads that may
+// still be in flight, the last kStages issued, so that none lands in shared
+// memory after the CTA has exited.
+template <bool F32>
+__device__ __forceinline__ void tile_ring_drain(const TilePipe& p) {
+  if (threadIdx.x != 0) return;
+  constexpr int S = TileRing<F32>::kStages;
+  const uint64_t t0 = globaltimer();
+  for (int64_t j = max((int64_t)0, p.next_it - S); j < p.next_it; ++j) {
+    const uint32_t bar = smem_u32(&p.full[j % S]);
+    while (!mbar_try_wait(bar, (uint32_t)((j / S) & 1)) && globaltimer() - t0 < 50000000ull) {
+    }
+  }
+}
+
+// The row-wise pass's thread layout: row r of the tile, 32-element segment
+// `seg` of that row (a warp covers 8 rows; a quarter-warp, 8 rows at one seg).
+__device__ __forceinline__ int tile_row_of(int tid) { return (tid & 7) + 8 * (tid >> 5); }
+__device__ __forceinline__ int tile_seg_of(int tid) { return (tid >> 3) & 3; }
+
+// The thread's row segment in a slot: its box and its chunks.
+template <bool F32>
+__device__ __forceinline__ SwzSeg tile_row_seg(const uint8_t* slot, int r, int seg) {
+  const int box = F32 ? seg : (seg >> 1);
+  const uint32_t first = F32 ? 0u : (uint32_t)(seg & 1) * 4u;
+  return SwzSeg{slot + box * kBoxBytes + r * 128, 16u * (first ^ (uint32_t)(r & 7))};
+}
+
+// Byte offset, within a slot, of the byte at `b` (0 .. row bytes - 1) of tile
+// row r, for r = r0 + i with r0 a multiple of 8.
+__device__ __forceinline__ uint32_t tile_byte(int r, uint32_t b, int i) {
+  return (b >> 7) * kBoxBytes + (uint32_t)r * 128u + ((b & 127u) ^ (16u * (uint32_t)(i & 7)));
+}
+
+// Two adjacent columns x 16 rows of a slot as FP32 (sign-flipped by sigma
+// along the column when RHT): a[i] = column 2*pair, b[i] = column 2*pair+1.
+template <bool F32, bool RHT>
+__device__ __forceinline__ void load_col_pair(const uint8_t* slot, int row0, int pair, uint32_t smask,
+                                              float (&a)[16], float (&b)[16]) {
+  const uint32_t bo = (uint32_t)pair * (F32 ? 8u : 4u);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint8_t* q = slot + tile_byte(row0 + i, bo, i);
+    const uint32_t sg = RHT ? (((smask >> i) & 1u) << 31) : 0u;
+    if constexpr (F32) {
+      const uint2 w = *reinterpret_cast<const uint2*>(q);
+      a[i] = __uint_as_float(w.x ^ sg);
+      b[i] = __uint_as_float(w.y ^ sg);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(q);
+      a[i] = __uint_as_float((w << 16) ^ sg);
+      b[i] = __uint_as_float((w & 0xFFFF0000u) ^ sg);
+    }
+  }
+}
+
+// One column x 32 rows (MXFP4 column blocks) as FP32 pairs of consecutive rows.
+template <bool F32, bool RHT>
+__device__ __forceinline__ void load_col32(const uint8_t* slot, int row0, int col, uint32_t smask, f2* Q) {
+  const uint32_t bo = (uint32_t)col * (F32 ? 4u : 2u);
+  float x[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint8_t* q = slot + tile_byte(row0 + i, bo, i);
+    const uint32_t sg = RHT ? (((smask >> (i & 15)) & 1u) << 31) : 0u;
+    if constexpr (F32) {
+      x[i] = __uint_as_float(*reinterpret_cast<const uint32_t*>(q) ^ sg);
+    } else {
+      x[i] = __uint_as_float(((uint32_t)*reinterpret_cast<const uint16_t*>(q) << 16) ^ sg);
+    }
+  }
+  if constexpr (RHT) {
+    float h0[16], h1[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) { h0[i] = x[i]; h1[i] = x[i + 16]; }
+    rht16_pairs(h0, Q);
+    rht16_pairs(h1, Q + 8);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) Q[j] = f2_make(x[2 * j], x[2 * j + 1]);
+  }
+}
+
+__device__ __forceinline__ void put_scale_rk(const CopyOut& o, int64_t row, int64_t kb, uint32_t sc) {
+  o.scales[o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb] = (uint8_t)sc;
+}
+
+// 16 code bytes of one row of a copy. A row starts on an 8-byte boundary (its
+// length is a multiple of 16 elements); the bytes go out as one 16-byte store
+// where the address allows, else as two 8-byte stores.
+__device__ __forceinline__ void store_codes16(uint8_t* p, const uint32_t (&cw)[4]) {
+  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+    *reinterpret_cast<uint4*>(p) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  } else {
+    *reinterpret_cast<uint2*>(p) = make_uint2(cw[0], cw[1]);
+    *reinterpret_cast<uint2*>(p + 8) = make_uint2(cw[2], cw[3]);
+  }
+}
+
+// Per-copy state of the quantisation pass.
+struct CopyState {
+  Ctx cx;
+  Divider dv;
+  Sums acc;
+  Kahan2 kb, ks, ke;
+};
+
+// ---- K1 for tiles: tensor amax of the row-wise and the column-wise copy (RHT) --------
+template <bool F32, bool ROWS>
+__global__ void __launch_bounds__(RT, 2) amax_tiles_kernel(const __grid_constant__ CUtensorMap tmap, TileGeom g,
+                                                           uint64_t seed, Workspace* ws, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[TileRing<F32>::kStages], empty[TileRing<F32>::kStages];
+  __shared__ uint32_t sh_max[RT / 32];
+  constexpr int S = TileRing<F32>::kStages;
+  uint8_t* ring = align1024(smem_raw);
+  const int tid = threadIdx.x;
+  const uint32_t smask = rht_sign_mask(seed);
+  uint32_t sgn[16];
+  make_sign_words<F32>(smask, sgn);
+  TilePipe pipe{full, empty, 0};
+  tile_ring_start<F32>(&tmap, g, ring, pipe);
+  const int rr = tile_row_of(tid), seg = tile_seg_of(tid);   // row-wise pass
+  const int pair = tid & 63, cb = tid >> 6;                    // column-wise pass
+  float mr = 0.f, mc = 0.f;
+  bool timed_out = false;
+  int64_t it = 0;
+  for (int64_t t = blockIdx.x; t < g.ntiles; ++it, t += gridDim.x) {
+    const int s = (int)(it % S);
+    if (!mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+    {
+      const uint8_t* slot = ring + s * TileRing<F32>::kTileBytes;
+      const int64_t r0 = (t / g.ntc) * TTR, c0 = (t % g.ntc) * TTC;
+      const int vr = (int)min((int64_t)TTR, g.rows - r0), vc = (int)min((int64_t)TTC, g.cols - c0);
+      if constexpr (ROWS) {
+        if (rr < vr && 32 * seg < vc) {
+          uint32_t m2 = 0u;
+          amax_segment<F32, true>(tile_row_seg<F32>(slot, rr, seg), min(2, (vc - 32 * seg) / 16), sgn, mr, m2);
+        }
+      }
+      if (16 * cb < vr && 2 * pair < vc) {
+        float a[16], b[16];
+        load_col_pair<F32, true>(slot, 16 * cb, pair, smask, a, b);
+        rht16_unscaled(a);
+        rht16_unscaled(b);
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          mc = max3_abs_nan(mc, a[i], a[i + 1]);
+          mc = max3_abs_nan(mc, b[i], b[i + 1]);
+        }
+      }
+    }
+    if (!tile_ring_release<F32>(&tmap, g, ring, pipe, it, t, timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+  }
+  if (__syncthreads_or(timed_out)) {
+    tile_ring_drain<F32>(pipe);
+    if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
+  }
+  // maxima of |w| = 4 |v|: one exact (or monotone) scaling gives max |v|
+  const uint32_t cr = cta_max<RT>(__float_as_uint(__fmul_rn(mr, 0.25f)), sh_max);
+  const uint32_t cc = cta_max<RT>(__float_as_uint(__fmul_rn(mc, 0.25f)), sh_max);
+  if (tid == 0) {
+    ws->amax_part[0][blockIdx.x] = cr;
+    ws->amax_part[1][blockIdx.x] = cc;
+    if (blockIdx.x == 0) ws->amax_nparts = gridDim.x;
+  }
+}
+
+// ---- K2 for tiles: quantise the row-wise and/or the column-wise copy ------------------
+template <int FMT, bool F32, bool RHT, bool SR, bool ROWS>
+__global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constant__ CUtensorMap tmap, TileGeom g,
+                                                            uint64_t seed, CopyOut orow, CopyOut ocol,
+                                                            Workspace* ws, uint64_t timeout_ns) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[TileRing<F32>::kStages], empty[TileRing<F32>::kStages];
+  __shared__ float2 tab[2][128];
+  __shared__ double sh_sum[RT / 32];
+  __shared__ float sh_f[6][RT / 32];
+  __shared__ uint32_t sh_max[RT / 32];
+  constexpr int S = TileRing<F32>::kStages;
+  constexpr float kQmax = (FMT == 2) ? 7.f : 6.f;
+  constexpr float kQmax448 = (FMT == 2) ? 3136.f : 2688.f;
+  uint8_t* ring = align1024(smem_raw);
+  const int tid = threadIdx.x;
+  const uint32_t smask = RHT ? rht_sign_mask(seed) : 0u;
+  uint32_t sgn[16];
+  make_sign_words<F32>(smask, sgn);
+  TilePipe pipe{full, empty, 0};
+  tile_ring_start<F32>(&tmap, g, ring, pipe);   // the first loads fly while the scales are set up
+  CopyState cr, cc;
+  cr.cx = Ctx{1.f, 0.f, 0.f};
+  cc.cx = Ctx{1.f, 0.f, 0.f};
+  cr.dv = Divider{};
+  cc.dv = Divider{};
+  if constexpr (FMT != 1) {
+    if (ROWS) {
+      cr.cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
+      cr.dv.init(cr.cx.d);
+      fill_scale_table(tab[0], cr.cx.g);
+    }
+    cc.cx = make_ctx(fold_amax<RT>(ws, 1, sh_max), kQmax, kQmax448);
+    cc.dv.init(cc.cx.d);
+    fill_scale_table(tab[1], cc.cx.g);
+    __syncthreads();
+  }
+  const int rr = tile_row_of(tid), seg = tile_seg_of(tid);
+  uint32_t nonfinite = 0;
+  bool timed_out = false;
+  int64_t it = 0;
+  for (int64_t t = blockIdx.x; t < g.ntiles; ++it, t += gridDim.x) {
+    const int s = (int)(it % S);
+    if (!mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+    {
+      const uint8_t* slot = ring + s * TileRing<F32>::kTileBytes;
+      const int64_t r0 = (t / g.ntc) * TTR, c0 = (t % g.ntc) * TTC;
+      const int vr = (int)min((int64_t)TTR, g.rows - r0), vc = (int)min((int64_t)TTC, g.cols - c0);
+      // ---- row-wise copy: 32 consecutive elements of one tile row per thread ----
+      if constexpr (ROWS) {
+        const int nb16 = (rr < vr) ? max(0, min(2, (vc - 32 * seg) / 16)) : 0;
+        const SwzSeg sg = tile_row_seg<F32>(slot, rr, seg);
+        const int64_t row = r0 + rr, col = c0 + 32 * seg;
+        const int64_t e = row * g.cols + col;
+        if constexpr (FMT == 1) {
+          if (nb16 == 2) {
+            float bsum = 0.f, ssum = 0.f, esum = 0.f;
+            f2 Q[16];
+            load_block16<F32, RHT>(sg, 0, sgn, Q);
+            load_block16<F32, RHT>(sg, F32 ? 4 : 2, sgn, Q + 8);
+            uint32_t cw[4];
+            const uint32_t sc = quant_block<FMT, SR, 16>(Q, cr.cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+                                                          cr.acc, nonfinite, 0u);
+            store_codes16(orow.codes + row * orow.ld + col / 2, cw);
+            put_scale_rk(orow, row, col / 32, sc);
+            cr.acc.bias.add(bsum);
+          }
+        } else if (nb16 == 2) {
+          uint32_t cw[4], sc[2];
+          f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
+          quant_two16<FMT, F32, RHT, SR>(sg, sgn, cr.cx, cr.dv, tab[0], (uint64_t)e, seed, cw, sc, b2, s2, e2,
+                                         nonfinite);
+          store_codes16(orow.codes + row * orow.ld + col / 2, cw);
+          put_scale_rk(orow, row, col / 16, sc[0]);
+          put_scale_rk(orow, row, col / 16 + 1, sc[1]);
+          cr.kb.add(b2);
+          cr.ks.add(s2);
+          cr.ke.add(e2);
+        } else if (nb16 == 1) {
+          float bsum = 0.f, ssum = 0.f, esum = 0.f;
+          f2 Q[8];
+          load_block16<F32, RHT>(sg, 0, sgn, Q);
+          uint32_t cw[2];
+          const uint32_t sc = quant_block<FMT, SR, 8>(Q, cr.cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+                                                       cr.acc, nonfinite, 0u);
+          *reinterpret_cast<uint2*>(orow.codes + row * orow.ld + col / 2) = make_uint2(cw[0], cw[1]);
+          put_scale_rk(orow, row, col / 16, sc);
+          cr.kb.add(f2_make(bsum, 0.f));
+          cr.ks.add(f2_make(ssum, 0.f));
+          cr.ke.add(f2_make(esum, 0.f));
+        }
+      }
+      // ---- column-wise copy: blocks run down the columns; copy row = source column ----
+      if constexpr (FMT == 1) {
+        const int col = tid & 127, cb = tid >> 7;        // one column x 32 rows
+        if (32 * cb < vr && col < vc) {
+          float bsum = 0.f, ssum = 0.f, esum = 0.f;
+          f2 Q[16];
+          load_col32<F32, RHT>(slot, 32 * cb, col, smask, Q);
+          const int64_t crow = c0 + col, ccol = r0 + 32 * cb;
+          uint32_t cw[4];
+          const uint32_t sc = quant_block<FMT, SR, 16>(Q, cc.cx, (uint64_t)(crow * g.rows + ccol), seed, cw,
+                                                        bsum, ssum, esum, cc.acc, nonfinite, 1u);
+          *reinterpret_cast<uint4*>(ocol.codes + crow * ocol.ld + ccol / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          put_scale_rk(ocol, crow, ccol / 32, sc);
+          cc.acc.bias.add(bsum);
+        }
+      } else {
+        const int pair = tid & 63, cb = tid >> 6;         // two columns x 16 rows
+        if (16 * cb < vr && 2 * pair < vc) {
+          float a[16], b[16];
+          load_col_pair<F32, RHT>(slot, 16 * cb, pair, smask, a, b);
+          f2 Q[16];
+          float m0 = 0.f, m1 = 0.f;
+          if constexpr (RHT) {
+            rht16_pairs(a, Q);
+            rht16_pairs(b, Q + 8);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              Q[j] = f2_make(a[2 * j], a[2 * j + 1]);
+              Q[j + 8] = f2_make(b[2 * j], b[2 * j + 1]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float x0, x1;
+            f2_split(Q[j], x0, x1);
+            m0 = max3_abs_nan(m0, x0, x1);
+            f2_split(Q[j + 8], x0, x1);
+            m1 = max3_abs_nan(m1, x0, x1);
+          }
+          const int64_t ca = c0 + 2 * pair, rw = r0 + 16 * cb;
+          uint32_t cw[4], sc[2];
+          f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
+          quant_two16_vals<FMT, SR>(Q, m0, m1, cc.cx, cc.dv, tab[1], (uint64_t)(ca * g.rows + rw),
+                                    (uint64_t)((ca + 1) * g.rows + rw), seed, 1u, cw, sc, b2, s2, e2, nonfinite);
+          *reinterpret_cast<uint2*>(ocol.codes + ca * ocol.ld + rw / 2) = make_uint2(cw[0], cw[1]);
+          *reinterpret_cast<uint2*>(ocol.codes + (ca + 1) * ocol.ld + rw / 2) = make_uint2(cw[2], cw[3]);
+          put_scale_rk(ocol, ca, rw / 16, sc[0]);
+          put_scale_rk(ocol, ca + 1, rw / 16, sc[1]);
+          cc.kb.add(b2);
+          cc.ks.add(s2);
+          cc.ke.add(e2);
+        }
+      }
+    }
+    if (!tile_ring_release<F32>(&tmap, g, ring, pipe, it, t, timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+  }
+  if (__syncthreads_or(timed_out)) {
+    tile_ring_drain<F32>(pipe);
+    if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
+  }
+
+  // ---- statistics: one partial per CTA and copy (summed on the host) ----
+  if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
+  if constexpr (FMT == 1) {
+    const double p[2][3] = {{cr.acc.bias.value(), cr.acc.sig64, cr.acc.err64},
+                            {cc.acc.bias.value(), cc.acc.sig64, cc.acc.err64}};
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const double v = cta_sum<RT>(p[c][k], sh_sum);
+        if (tid == 0) ws->stat_part[c][k][blockIdx.x] = v;
+      }
+    }
+  } else {
+    float v[6] = {cr.kb.value_f(), cr.ks.value_f(), cr.ke.value_f(),
+                  cc.kb.value_f(), cc.ks.value_f(), cc.ke.value_f()};
+    cta_sums_f32<RT, 6>(v, sh_f);
+    if (tid == 0) {
+#pragma unroll
+      for (int k = 0; k < 6; ++k) ws->stat_part[k / 3][k % 3][blockIdx.x] = (double)v[k];
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) {
+    ws->stat_nparts = gridDim.x;
+    ws->copies = (ROWS ? 1u : 0u) | 2u;
+    ws->tensor_scale[0] = (FMT == 1) ? 1.f : cr.cx.g;
+    ws->tensor_scale[1] = (FMT == 1) ? 1.f : cc.cx.g;
+    ws->qmax = kQmax;
+    ws->n = (double)g.rows * (double)g.cols;
+    if (ROWS && orow.tensor_scale) *orow.tensor_scale = (FMT == 1) ? 1.f : cr.cx.g;
+    if (ocol.tensor_scale) *ocol.tensor_scale = (FMT == 1) ? 1.f : cc.cx.g;
+  }
+}
+
 // ---- one launch for both passes (NVFP4 / UFP4 row-wise) ------------------------------
 // A cooperatively launched (co-resident) grid streams its chunks twice through
 // one ring: the amax pass, a grid barrier, the fold of the per-CTA maxima, then
@@ -850,7 +1423,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uin
     if (ok) {
       const int64_t e = chunk_of(it) * CH + (int64_t)tid * EPT;
       const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
-      amax_segment<F32, RHT>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, nb, sgn, m, m2);
+      amax_segment<F32, RHT>(LinearSeg{ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES}, nb, sgn, m, m2);
     }
     timed_out = __syncthreads_or(!ok);
     if (timed_out) break;
@@ -1108,6 +1681,68 @@ cudaError_t dispatch_quant_rows(int rht, int sr, const Flat& f, uint64_t seed, c
             : launch_quant_rows<FMT, F32, false, false>(f, seed, o, ws, s);
 }
 
+template <bool F32, bool ROWS>
+cudaError_t launch_amax_tiles(const CUtensorMap& map, const TileGeom& g, uint64_t seed, Workspace* ws,
+                              cudaStream_t s) {
+  auto k = amax_tiles_kernel<F32, ROWS>;
+  constexpr int smem = TileRing<F32>::kSmem;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid_for(k, smem, g.ntiles), RT, smem, s>>>(map, g, seed, ws, kRingTimeoutNs);
+  return cudaGetLastError();
+}
+
+template <int FMT, bool F32, bool RHT, bool SR>
+cudaError_t launch_quant_tiles(const CUtensorMap& map, const TileGeom& g, uint64_t seed, bool rows,
+                               const CopyOut& r, const CopyOut& c, Workspace* ws, cudaStream_t s) {
+  auto k = rows ? quant_tiles_kernel<FMT, F32, RHT, SR, true> : quant_tiles_kernel<FMT, F32, RHT, SR, false>;
+  constexpr int smem = TileRing<F32>::kSmem;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  k<<<grid_for(k, smem, g.ntiles), RT, smem, s>>>(map, g, seed, r, c, ws, kRingTimeoutNs);
+  return cudaGetLastError();
+}
+
+template <int FMT, bool F32>
+cudaError_t dispatch_quant_tiles(int rht, int sr, const CUtensorMap& m, const TileGeom& g, uint64_t seed,
+                                 bool rows, const CopyOut& r, const CopyOut& c, Workspace* ws, cudaStream_t s) {
+  if (rht) return sr ? launch_quant_tiles<FMT, F32, true, true>(m, g, seed, rows, r, c, ws, s)
+                     : launch_quant_tiles<FMT, F32, true, false>(m, g, seed, rows, r, c, ws, s);
+  return sr ? launch_quant_tiles<FMT, F32, false, true>(m, g, seed, rows, r, c, ws, s)
+            : launch_quant_tiles<FMT, F32, false, false>(m, g, seed, rows, r, c, ws, s);
+}
+
+// The source as a 2-D TMA map whose box is one 64-row x 128-byte box of a tile.
+bool make_tile_map(CUtensorMap* map, const QuantArgs& a) {
+  const bool f32 = a.dtype == 1;
+  return encode_tiled_2d(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.src,
+                         (uint64_t)a.cols, (uint64_t)a.rows, (uint64_t)a.cols * (f32 ? 4u : 2u),
+                         f32 ? (uint32_t)TileRing<true>::kBoxCols : (uint32_t)TileRing<false>::kBoxCols,
+                         (uint32_t)TTR);
+}
+
+TileGeom make_tile_geom(const QuantArgs& a) {
+  TileGeom g;
+  g.rows = a.rows;
+  g.cols = a.cols;
+  g.ntc = (a.cols + TTC - 1) / TTC;
+  g.ntiles = ((a.rows + TTR - 1) / TTR) * g.ntc;
+  return g;
+}
+
+CopyOut tile_copy(const QOut& q, int64_t crows, int64_t ccols, int block) {
+  (void)crows;
+  CopyOut o{};
+  o.codes = q.codes;
+  o.scales = q.scales;
+  o.tensor_scale = q.tensor_scale;
+  o.mma = q.scale_layout;
+  o.ld = ccols / 2;
+  o.nkb = ccols / block;
+  o.nkb_p = (o.nkb + 3) / 4 * 4;
+  return o;
+}
+
 }  // namespace
 
 template <int FMT>
@@ -1223,6 +1858,38 @@ cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s) {
                              : dispatch_quant_fused<0, false>(a.rht, sr, f, a.seed, o, ws, s);
   return f32 ? dispatch_quant_fused<2, true>(a.rht, sr, f, a.seed, o, ws, s)
              : dispatch_quant_fused<2, false>(a.rht, sr, f, a.seed, o, ws, s);
+}
+
+cudaError_t run_amax_tiles(const QuantArgs& a, cudaStream_t s) {
+  CUtensorMap map;
+  if (!make_tile_map(&map, a)) return cudaErrorNotSupported;
+  const TileGeom g = make_tile_geom(a);
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  const bool rows = (a.axis & 1) != 0;
+  if (a.dtype == 1) return rows ? launch_amax_tiles<true, true>(map, g, a.seed, ws, s)
+                                : launch_amax_tiles<true, false>(map, g, a.seed, ws, s);
+  return rows ? launch_amax_tiles<false, true>(map, g, a.seed, ws, s)
+              : launch_amax_tiles<false, false>(map, g, a.seed, ws, s);
+}
+
+cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s) {
+  CUtensorMap map;
+  if (!make_tile_map(&map, a)) return cudaErrorNotSupported;
+  const int block = a.fmt == 1 ? 32 : 16;
+  const TileGeom g = make_tile_geom(a);
+  const CopyOut r = tile_copy(a.row, a.rows, a.cols, block);
+  const CopyOut c = tile_copy(a.col, a.cols, a.rows, block);
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  const bool f32 = a.dtype == 1, rows = (a.axis & 1) != 0;
+  const int sr = a.rounding == 1;
+  switch (a.fmt) {
+    case 0: return f32 ? dispatch_quant_tiles<0, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
+                       : dispatch_quant_tiles<0, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+    case 1: return f32 ? dispatch_quant_tiles<1, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
+                       : dispatch_quant_tiles<1, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+    default: return f32 ? dispatch_quant_tiles<2, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
+                        : dispatch_quant_tiles<2, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+  }
 }
 
 }  // namespace fp4q

@@ -176,7 +176,8 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  *                buffers; the one whose axis bit is clear may be NULL. codes
  *                must be 16-byte aligned; MMA-layout scales 16-byte aligned.
  *   workspace    device, ws_bytes >= fp4q_workspace_size(), zero-filled once.
- * Shapes: cols % block == 0 for the row-wise copy, rows % block == 0 for the
+ * Shapes: cols % 16 == 0 always (rows of src start on 32-byte boundaries),
+ * cols % block == 0 for the row-wise copy, rows % block == 0 for the
  * column-wise copy; rows or cols 0 is valid (writes g = 0 for NVFP4/UFP4 and
  * empty statistics). Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
 int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols,

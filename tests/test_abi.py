@@ -66,6 +66,8 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, 16, None) == 1
     assert q(fake, 0, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1  # row_out NULL
     assert q(fake, 0, -1, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    # column-wise only still needs source rows of a multiple of 16 elements
+    assert q(fake, 0, 32, 100, 0, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
 
 
 def test_amax_validation_without_gpu(so):
@@ -80,6 +82,7 @@ def test_amax_validation_without_gpu(so):
     assert a(fake, 0, 16, 16, 0, 32, 0, 0, 1, fake, ws_size, None) == 2      # block
     assert a(fake, 0, 16, 24, 0, 16, 0, 0, 1, fake, ws_size, None) == 1      # cols % 16
     assert a(fake, 0, 24, 16, 0, 16, 0, 0, 2, fake, ws_size, None) == 1      # rows % 16
+    assert a(fake, 0, 32, 24, 0, 16, 1, 0, 2, fake, ws_size, None) == 1      # cols % 16, column-wise only
     assert a(fake, 0, 16, 16, 0, 16, 2, 0, 1, fake, ws_size, None) == 1      # rht flag
     assert a(fake, 0, 16, 16, 0, 16, 0, 0, 4, fake, ws_size, None) == 1      # no copy requested
     assert a(fake, 0, 16, 16, 0, 16, 0, 0, 1, fake, 8, None) == 1            # workspace size

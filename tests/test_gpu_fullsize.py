@@ -38,3 +38,31 @@ def test_activation_three_ways_full_size(lib, activation, fmt, rht):
         y = lib.fp4q_dequantize(r, inverse_rht=True, seed=SEED)
         want = o.dequantize(ref["codes"], ref["scales"], ref["tensor_scale"], fmt, True, SEED)
         assert np.array_equal(y.cpu().numpy().view(np.uint32), want.view(np.uint32))
+
+
+def _sample(n, tile, k=40):
+    """Indices that include both ends, tile boundaries and a seeded spread."""
+    rng = np.random.default_rng(n)
+    edge = [0, 1, tile - 1, tile, n - tile - 1, n - tile, n - 2, n - 1]
+    return np.unique(np.concatenate([edge, rng.integers(0, n, k)])).astype(np.int64)
+
+
+@pytest.mark.parametrize("which", ["a", "b"])
+def test_gradient_both_copies_full_size(lib, which):
+    """The gradient workload as bench.py times it (NVFP4, RHT, Philox SR, row-wise
+    and column-wise copies from one call), compared on sampled rows of each
+    copy: the tensor amax and scale still come from the whole tensor."""
+    import torch
+    x = synth.gradient(which)
+    rows, cols = x.shape
+    r, c = lib.fp4q_quantize(x.cuda(), fmt="nvfp4", rht=True, rounding="sr", seed=SEED, axis="both")
+    assert lib.fp4q_status() == 0
+    rsel, csel = _sample(rows, 64), _sample(cols, 128)
+    ref = o.quantize(synth.bf16_bits(x), "nvfp4", rht=True, rounding="sr", seed=SEED, axis="both",
+                     rows_subset=rsel, cols_subset=csel)
+    for got, want, sel in ((r, ref["row"], rsel), (c, ref["col"], csel)):
+        idx = torch.from_numpy(sel).cuda()
+        assert np.array_equal(got.codes[idx].cpu().numpy(), want["codes"])
+        assert np.array_equal(got.scales[idx].cpu().numpy(), want["scales"])
+        ts = got.tensor_scale.cpu().numpy().view(np.uint32)[0]
+        assert ts == np.float32(want["tensor_scale"]).view(np.uint32)

@@ -229,6 +229,10 @@ def test_invalid_arguments_rejected(lib):
     y = torch.randn(48, 64, device="cuda").to(torch.bfloat16)     # 48 % 32 != 0
     with pytest.raises(lib.FP4QError):
         lib.fp4q_quantize(y, fmt="mxfp4", axis="col")
+    z = torch.randn(208, 100, device="cuda").to(torch.bfloat16)   # column-wise, 100 % 16 != 0
+    with pytest.raises(lib.FP4QError) as e:
+        lib.fp4q_quantize(z, fmt="nvfp4", axis="col")
+    assert e.value.code == 1
     r, _ = lib.fp4q_quantize(torch.randn(128, 256, device="cuda"), fmt="ufp4", layout="mma")
     with pytest.raises(lib.FP4QError) as e:
         lib.fp4q_gemm(r, r)
