@@ -58,6 +58,18 @@ __device__ __forceinline__ void fence_mbarrier_init() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------------
+// The grid launched after this one on the stream (with programmatic stream
+// serialisation) may start once every CTA of this grid has executed this.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Block until the grid this one depends on has completed and its writes are
+// visible (returns at once when there is no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- bulk copies -------------------------------------------------------------------
 // Global -> shared, completion signalled on `bar` (transaction bytes). `bytes`
 // and both addresses must be multiples of 16.

@@ -87,37 +87,69 @@ __device__ __forceinline__ void ring_issue(const Flat& f, int64_t chunk, uint8_t
   bulk_load(smem_u32(ring + slot * Ring<F32>::kChunkBytes), f.src + e0 * es, bytes, bar);
 }
 
-// Thread 0 starts the first copies; every slot's barrier completes one phase
-// per copy. `reverse`: the CTA's k-th chunk is counted from the end.
+// The same ring with warps decoupled: empty[s] collects one arrival per warp
+// once the warp is done with slot s, and only warp 0, which refills the slot,
+// waits for the slowest; warps run ahead of one another by up to kStages - 1
+// chunks. Every wait is bounded.
+struct FlatPipe {
+  uint64_t* full;
+  uint64_t* empty;
+  int64_t next_it;     // thread 0: the next iteration whose chunk is to be issued
+};
+
 template <bool F32>
-__device__ __forceinline__ void ring_start(const Flat& f, uint8_t* ring, uint64_t* full,
-                                           bool reverse = false) {
+__device__ __forceinline__ void flat_ring_start(const Flat& f, uint8_t* ring, FlatPipe& p, bool reverse) {
+  constexpr int S = Ring<F32>::kStages;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Ring<F32>::kStages; ++s) mbar_init(smem_u32(&full[s]), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&p.full[s]), 1);
+      mbar_init(smem_u32(&p.empty[s]), RT / 32);
+    }
     fence_mbarrier_init();
   }
   __syncthreads();
+  p.next_it = 0;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Ring<F32>::kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       const int64_t c = blockIdx.x + (int64_t)s * gridDim.x;
-      if (c < f.nchunks) ring_issue<F32>(f, reverse ? f.nchunks - 1 - c : c, ring, s, smem_u32(&full[s]));
+      if (c >= f.nchunks) break;
+      ring_issue<F32>(f, reverse ? f.nchunks - 1 - c : c, ring, s, smem_u32(&p.full[s]));
+      p.next_it = s + 1;
     }
   }
 }
 
-// After a timeout: wait (bounded) for the copies still in flight, so none lands
-// after the CTA has exited. `it` is the first iteration not consumed.
+// The calling warp is done with iteration `it` (chunk c of the CTA's walk).
+// False if warp 0's wait for the other warps ran out.
 template <bool F32>
-__device__ __forceinline__ void ring_drain(const Flat& f, uint64_t* full, int64_t it) {
-  if (threadIdx.x != 0) return;
+__device__ __forceinline__ bool flat_ring_release(const Flat& f, uint8_t* ring, FlatPipe& p, int64_t it,
+                                                  int64_t c, bool reverse, uint64_t timeout_ns) {
   constexpr int S = Ring<F32>::kStages;
+  const int s = (int)(it % S);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&p.empty[s]));
+  if (threadIdx.x < 32) {
+    const int64_t nx = c + (int64_t)S * gridDim.x;
+    if (nx < f.nchunks) {
+      if (!mbar_wait_bounded(smem_u32(&p.empty[s]), (uint32_t)((it / S) & 1), timeout_ns)) return false;
+      if (threadIdx.x == 0) {
+        ring_issue<F32>(f, reverse ? f.nchunks - 1 - nx : nx, ring, s, smem_u32(&p.full[s]));
+        p.next_it = it + S + 1;
+      }
+    }
+  }
+  return true;
+}
+
+// After a wait ran out: thread 0 waits (50 ms at most) for the copies that may
+// still be in flight, the last kStages issued.
+template <int S>
+__device__ __forceinline__ void pipe_drain(const uint64_t* full, int64_t next_it) {
+  if (threadIdx.x != 0) return;
   const uint64_t t0 = globaltimer();
-  for (int64_t j = it; j < it + S; ++j) {
-    const int64_t c = blockIdx.x + j * gridDim.x;
-    if (c >= f.nchunks) break;
+  for (int64_t j = max((int64_t)0, next_it - S); j < next_it; ++j) {
     const uint32_t bar = smem_u32(&full[j % S]);
-    const uint32_t par = (uint32_t)((j / S) & 1);
-    while (!mbar_try_wait(bar, par) && globaltimer() - t0 < 50000000ull) {
+    while (!mbar_try_wait(bar, (uint32_t)((j / S) & 1)) && globaltimer() - t0 < 50000000ull) {
     }
   }
 }
@@ -777,7 +809,7 @@ template <bool F32, bool RHT>
 __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed, Workspace* ws,
                                                           uint64_t timeout_ns) {
   extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages];
+  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages], empty[Ring<F32>::kStages];
   __shared__ uint32_t sh_max[RT / 32];
   constexpr int S = Ring<F32>::kStages;
   const int tid = threadIdx.x;
@@ -785,30 +817,36 @@ __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed,
   make_sign_words<F32>(RHT ? rht_sign_mask(seed) : 0u, sgn);
   // chunks are visited from the end of the tensor, so that the quantisation
   // pass (which walks forward) starts on the chunks this pass left in L2
-  ring_start<F32>(f, ring, full, true);
+  FlatPipe pipe{full, empty, 0};
+  flat_ring_start<F32>(f, ring, pipe, true);
 
   float m = 0.f;
   uint32_t m2 = 0u;      // BF16 pairs without the RHT
   bool timed_out = false;
   int64_t it = 0;
   for (int64_t c = blockIdx.x; c < f.nchunks; ++it, c += gridDim.x) {
+    // the CTA's last chunk: the next kernel on the stream may start its prologue
+    if (c + gridDim.x >= f.nchunks) grid_launch_dependents();
     const int s = (int)(it % S);
-    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
-    if (ok) {
-      const int64_t e = (f.nchunks - 1 - c) * CH + (int64_t)tid * EPT;
-      const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
-      amax_segment<F32, RHT>(LinearSeg{ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2)}, nb, sgn, m,
-                             m2);
+    if (!mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns)) {
+      timed_out = true;
+      break;
     }
-    timed_out = __syncthreads_or(!ok);
-    if (timed_out) break;
-    if (tid == 0) {
-      const int64_t nx = c + (int64_t)S * gridDim.x;
-      if (nx < f.nchunks) ring_issue<F32>(f, f.nchunks - 1 - nx, ring, s, smem_u32(&full[s]));
+    const int64_t e = (f.nchunks - 1 - c) * CH + (int64_t)tid * EPT;
+    const int nb = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
+    amax_segment<F32, RHT>(LinearSeg{ring + s * Ring<F32>::kChunkBytes + tid * EPT * (F32 ? 4 : 2)}, nb, sgn, m,
+                           m2);
+    if (!flat_ring_release<F32>(f, ring, pipe, it, c, true, timeout_ns)) {
+      timed_out = true;
+      break;
     }
   }
-  if (timed_out) {
-    ring_drain<F32>(f, full, it);
+  grid_launch_dependents();     // a CTA that left the loop early
+  // the workspace may still be read by the kernel before this one (its
+  // quantisation pass): write only once that kernel has completed
+  grid_dependency_wait();
+  if (__syncthreads_or(timed_out)) {
+    pipe_drain<S>(full, pipe.next_it);
     if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
   }
   const uint32_t cm = cta_max<RT>(__float_as_uint(amax_result<F32, RHT>(m, m2)), sh_max);
@@ -824,7 +862,7 @@ template <int FMT, bool F32, bool RHT, bool SR>
 __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint64_t seed, CopyOut o,
                                                            Workspace* ws, uint64_t timeout_ns) {
   extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages];
+  __shared__ __align__(8) uint64_t full[Ring<F32>::kStages], empty[Ring<F32>::kStages];
   __shared__ float2 tab[128];
   __shared__ double sh_sum[RT / 32];
   __shared__ float sh_f[3][RT / 32];
@@ -836,7 +874,11 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   const int tid = threadIdx.x;
   uint32_t sgn[16];
   make_sign_words<F32>(RHT ? rht_sign_mask(seed) : 0u, sgn);
-  ring_start<F32>(f, ring, full);     // the first copies fly while the scales are set up
+  FlatPipe pipe{full, empty, 0};
+  flat_ring_start<F32>(f, ring, pipe, false);     // the first copies fly while the scales are set up
+  // Launched as a programmatic dependent of the amax pass: everything above
+  // only reads the source; the amax partials are read after this wait.
+  grid_dependency_wait();
   Ctx cx{1.f, 0.f, 0.f};
   Divider dv{};
   if constexpr (FMT != 1) {
@@ -851,6 +893,8 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   uint32_t nonfinite = 0;
   bool timed_out = false;
   int64_t it = 0;
+  // One CTA barrier per chunk (measured faster here than letting warps run
+  // ahead: the quantisation work per chunk is even across warps).
   for (int64_t c = blockIdx.x; c < f.nchunks; ++it, c += gridDim.x) {
     const int s = (int)(it % S);
     const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
@@ -863,11 +907,16 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
     if (timed_out) break;
     if (tid == 0) {
       const int64_t nx = c + (int64_t)S * gridDim.x;
-      if (nx < f.nchunks) ring_issue<F32>(f, nx, ring, s, smem_u32(&full[s]));
+      if (nx < f.nchunks) {
+        ring_issue<F32>(f, nx, ring, s, smem_u32(&full[s]));
+        pipe.next_it = it + S + 1;
+      }
     }
   }
+  // the CTA's last chunk is done: the next kernel on the stream may start
+  grid_launch_dependents();
   if (timed_out) {
-    ring_drain<F32>(f, full, it);
+    pipe_drain<S>(full, pipe.next_it);
     if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
   }
 
@@ -1010,21 +1059,6 @@ __device__ __forceinline__ bool tile_ring_release(const CUtensorMap* map, const 
   return true;
 }
 
-// After a wait ran out: thread 0 waits (50 ms at most) for the loads that may
-// still be in flight, the last kStages issued, so that none lands in shared
-// memory after the CTA has exited.
-template <bool F32>
-__device__ __forceinline__ void tile_ring_drain(const TilePipe& p) {
-  if (threadIdx.x != 0) return;
-  constexpr int S = TileRing<F32>::kStages;
-  const uint64_t t0 = globaltimer();
-  for (int64_t j = max((int64_t)0, p.next_it - S); j < p.next_it; ++j) {
-    const uint32_t bar = smem_u32(&p.full[j % S]);
-    while (!mbar_try_wait(bar, (uint32_t)((j / S) & 1)) && globaltimer() - t0 < 50000000ull) {
-    }
-  }
-}
-
 // The row-wise pass's thread layout: row r of the tile, 32-element segment
 // `seg` of that row (a warp covers 8 rows; a quarter-warp, 8 rows at one seg).
 __device__ __forceinline__ int tile_row_of(int tid) { return (tid & 7) + 8 * (tid >> 5); }
@@ -1138,6 +1172,8 @@ __global__ void __launch_bounds__(RT, 2) amax_tiles_kernel(const __grid_constant
   bool timed_out = false;
   int64_t it = 0;
   for (int64_t t = blockIdx.x; t < g.ntiles; ++it, t += gridDim.x) {
+    // the CTA's last tile: the next kernel on the stream may start its prologue
+    if (t + gridDim.x >= g.ntiles) grid_launch_dependents();
     const int s = (int)(it % S);
     if (!mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns)) {
       timed_out = true;
@@ -1170,8 +1206,12 @@ __global__ void __launch_bounds__(RT, 2) amax_tiles_kernel(const __grid_constant
       break;
     }
   }
+  grid_launch_dependents();     // a CTA that left the loop early
+  // the workspace may still be read by the kernel before this one (its
+  // quantisation pass): write only once that kernel has completed
+  grid_dependency_wait();
   if (__syncthreads_or(timed_out)) {
-    tile_ring_drain<F32>(pipe);
+    pipe_drain<TileRing<F32>::kStages>(pipe.full, pipe.next_it);
     if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
   }
   // maxima of |w| = 4 |v|: one exact (or monotone) scaling gives max |v|
@@ -1205,6 +1245,9 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
   make_sign_words<F32>(smask, sgn);
   TilePipe pipe{full, empty, 0};
   tile_ring_start<F32>(&tmap, g, ring, pipe);   // the first loads fly while the scales are set up
+  // Launched as a programmatic dependent of the amax pass: everything above
+  // only reads the source; the amax partials are read after this wait.
+  grid_dependency_wait();
   CopyState cr, cc;
   cr.cx = Ctx{1.f, 0.f, 0.f};
   cc.cx = Ctx{1.f, 0.f, 0.f};
@@ -1339,8 +1382,10 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
       break;
     }
   }
+  // the CTA's last tile is done: the next kernel on the stream may start
+  grid_launch_dependents();
   if (__syncthreads_or(timed_out)) {
-    tile_ring_drain<F32>(pipe);
+    pipe_drain<TileRing<F32>::kStages>(pipe.full, pipe.next_it);
     if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
   }
 
@@ -1586,6 +1631,9 @@ __device__ __forceinline__ uint32_t get_scale(const CopyOut& q, const Flat& f, u
 
 template <int FMT, bool OUT_F32, bool IRHT>
 __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, uint64_t seed, void* dst) {
+  // launched as a programmatic dependent: the codes may come from the kernel
+  // just before this one
+  grid_dependency_wait();
   uint32_t sgn[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) sgn[i] = 0u;
@@ -1637,6 +1685,26 @@ Flat make_flat(const void* src, int64_t rows, int64_t cols, int block) {
   return f;
 }
 
+// A launch that may begin while the previous kernel on the stream is still
+// running (programmatic stream serialisation); the kernel itself waits for
+// that kernel's results (griddepcontrol.wait) before it reads them.
+template <typename K, typename... Args>
+cudaError_t launch_dependent(K kernel, int grid, int smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(RT, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename K>
 int grid_for(K kernel, int smem, int64_t nchunks) {
   const int occ = cached_occupancy(reinterpret_cast<const void*>(kernel), RT, smem);
@@ -1657,8 +1725,7 @@ cudaError_t launch_amax_rows(const Flat& f, uint64_t seed, Workspace* ws, cudaSt
   constexpr int smem = Ring<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid_for(k, smem, f.nchunks), RT, smem, s>>>(f, seed, ws, kRingTimeoutNs);
-  return cudaGetLastError();
+  return launch_dependent(k, grid_for(k, smem, f.nchunks), smem, s, f, seed, ws, kRingTimeoutNs);
 }
 
 template <int FMT, bool F32, bool RHT, bool SR>
@@ -1668,8 +1735,7 @@ cudaError_t launch_quant_rows(const Flat& f, uint64_t seed, const CopyOut& o, Wo
   constexpr int smem = Ring<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid_for(k, smem, f.nchunks), RT, smem, s>>>(f, seed, o, ws, kRingTimeoutNs);
-  return cudaGetLastError();
+  return launch_dependent(k, grid_for(k, smem, f.nchunks), smem, s, f, seed, o, ws, kRingTimeoutNs);
 }
 
 template <int FMT, bool F32>
@@ -1688,8 +1754,7 @@ cudaError_t launch_amax_tiles(const CUtensorMap& map, const TileGeom& g, uint64_
   constexpr int smem = TileRing<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid_for(k, smem, g.ntiles), RT, smem, s>>>(map, g, seed, ws, kRingTimeoutNs);
-  return cudaGetLastError();
+  return launch_dependent(k, grid_for(k, smem, g.ntiles), smem, s, map, g, seed, ws, kRingTimeoutNs);
 }
 
 template <int FMT, bool F32, bool RHT, bool SR>
@@ -1699,8 +1764,7 @@ cudaError_t launch_quant_tiles(const CUtensorMap& map, const TileGeom& g, uint64
   constexpr int smem = TileRing<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid_for(k, smem, g.ntiles), RT, smem, s>>>(map, g, seed, r, c, ws, kRingTimeoutNs);
-  return cudaGetLastError();
+  return launch_dependent(k, grid_for(k, smem, g.ntiles), smem, s, map, g, seed, r, c, ws, kRingTimeoutNs);
 }
 
 template <int FMT, bool F32>
@@ -1753,14 +1817,10 @@ cudaError_t launch_dequant_rows(const Flat& f, const CopyOut& q, int irht, uint6
   const int64_t gmax = (int64_t)sm_count() * 8;
   if (grid > gmax) grid = gmax;
   if (grid < 1) grid = 1;
-  if (f32) {
-    if (irht) dequant_rows_kernel<FMT, true, true><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
-    else dequant_rows_kernel<FMT, true, false><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
-  } else {
-    if (irht) dequant_rows_kernel<FMT, false, true><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
-    else dequant_rows_kernel<FMT, false, false><<<(int)grid, 256, 0, s>>>(f, q, seed, dst);
-  }
-  return cudaGetLastError();
+  if (f32) return irht ? launch_dependent(dequant_rows_kernel<FMT, true, true>, (int)grid, 0, s, f, q, seed, dst)
+                      : launch_dependent(dequant_rows_kernel<FMT, true, false>, (int)grid, 0, s, f, q, seed, dst);
+  return irht ? launch_dependent(dequant_rows_kernel<FMT, false, true>, (int)grid, 0, s, f, q, seed, dst)
+              : launch_dependent(dequant_rows_kernel<FMT, false, false>, (int)grid, 0, s, f, q, seed, dst);
 }
 
 template <int FMT, bool F32, bool RHT, bool SR>
