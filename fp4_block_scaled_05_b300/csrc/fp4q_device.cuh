@@ -52,6 +52,36 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
   return c;
 }
 
+// The ten round keys of one seed: round i uses (k0 + i * 0x9E3779B9,
+// k1 + i * 0xBB67AE85) mod 2^32. Computed once on the host and passed as a
+// kernel argument, they sit in the constant bank, so a round costs only its
+// two multiplies and two XORs.
+struct PhiloxKey {
+  uint32_t k0[10], k1[10];
+};
+
+inline PhiloxKey philox_key(uint64_t seed) {
+  PhiloxKey k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+  for (int i = 0; i < 10; ++i) {
+    k.k0[i] = a;
+    k.k1[i] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxKey& k) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k.k0[i], lo1, hi0 ^ c.w ^ k.k1[i], lo0);
+  }
+  return c;
+}
+
 // 16-bit RHT sign mask: bit j set <=> sigma_j = -1.
 __device__ __forceinline__ uint32_t rht_sign_mask(uint64_t seed) {
   const uint4 w = philox4x32_10(make_uint4(0u, 0u, 0u, 0xFFFFFFFFu), (uint32_t)seed,

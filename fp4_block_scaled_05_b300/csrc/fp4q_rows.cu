@@ -462,7 +462,7 @@ __device__ __forceinline__ uint32_t sr_pair(f2 Y, uint32_t w0, uint32_t w1, f2& 
 // words and returns the scale code; adds the block's sums to bsum/ssum/esum
 // (NVFP4/UFP4: grid units times s^2; MXFP4: FP64 absolute in sig64/err64).
 template <int FMT, bool SR, int NP>
-__device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint64_t e0, uint64_t seed,
+__device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint64_t e0, const PhiloxKey& pk,
                                                 uint32_t* cw, float& bsum, float& ssum, float& esum,
                                                 Sums& acc, uint32_t& nonfinite, uint32_t axis = 0u) {
   float m = 0.f;
@@ -508,8 +508,7 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
     uint4 rw = make_uint4(0u, 0u, 0u, 0u);
     if constexpr (SR) {   // one Philox call per 4 elements (e0 is a multiple of 16)
       const uint64_t q = (e0 >> 2) + (uint64_t)(j0 >> 1);
-      rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), (uint32_t)seed,
-                         (uint32_t)(seed >> 32));
+      rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), pk);
     }
 #pragma unroll
     for (int j = j0; j < j0 + 2; ++j) {
@@ -566,14 +565,14 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
 template <int FMT, bool SR>
 __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1, const Ctx& cx,
                                                  const Divider& dv, const float2* tab, uint64_t e0,
-                                                 uint64_t e1, uint64_t seed, uint32_t axis,
+                                                 uint64_t e1, const PhiloxKey& pk, uint32_t axis,
                                                  uint32_t (&cw)[4], uint32_t (&sc)[2], f2& bias2,
                                                  f2& sig2, f2& err2, uint32_t& nonfinite);
 
 template <int FMT, bool F32, bool RHT, bool SR, class Seg>
 __device__ __forceinline__ void quant_two16(const Seg& sg, const uint32_t (&sgn)[16], const Ctx& cx,
                                             const Divider& dv, const float2* tab, uint64_t e,
-                                            uint64_t seed, uint32_t (&cw)[4], uint32_t (&sc)[2],
+                                            const PhiloxKey& pk, uint32_t (&cw)[4], uint32_t (&sc)[2],
                                             f2& bias2, f2& sig2, f2& err2, uint32_t& nonfinite) {
   f2 Q[16];
   float m0 = 0.f, m1 = 0.f;
@@ -606,7 +605,7 @@ __device__ __forceinline__ void quant_two16(const Seg& sg, const uint32_t (&sgn)
       m1 = max3_abs_nan(m1, a, b);
     }
   }
-  quant_two16_vals<FMT, SR>(Q, m0, m1, cx, dv, tab, e, e + 16, seed, 0u, cw, sc, bias2, sig2, err2,
+  quant_two16_vals<FMT, SR>(Q, m0, m1, cx, dv, tab, e, e + 16, pk, 0u, cw, sc, bias2, sig2, err2,
                             nonfinite);
 }
 
@@ -617,7 +616,7 @@ __device__ __forceinline__ void quant_two16(const Seg& sg, const uint32_t (&sgn)
 template <int FMT, bool SR>
 __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1, const Ctx& cx,
                                                  const Divider& dv, const float2* tab, uint64_t e0,
-                                                 uint64_t e1, uint64_t seed, uint32_t axis,
+                                                 uint64_t e1, const PhiloxKey& pk, uint32_t axis,
                                                  uint32_t (&cw)[4], uint32_t (&sc)[2], f2& bias2,
                                                  f2& sig2, f2& err2, uint32_t& nonfinite) {
   nonfinite |= (max(__float_as_uint(m0), __float_as_uint(m1)) >= 0x7F800000u) ? 1u : 0u;
@@ -645,8 +644,7 @@ __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1
       uint4 rw = make_uint4(0u, 0u, 0u, 0u);
       if constexpr (SR) {   // one Philox call per 4 elements
         const uint64_t q = ((b ? e1 : e0) >> 2) + (uint64_t)(j0 >> 1);
-        rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), (uint32_t)seed,
-                           (uint32_t)(seed >> 32));
+        rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), pk);
       }
 #pragma unroll
       for (int j = j0; j < j0 + 2; ++j) {
@@ -761,7 +759,7 @@ __device__ __forceinline__ float amax_result(float m, uint32_t m2) {
 template <int FMT, bool F32, bool RHT, bool SR>
 __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const Flat& f, const CopyOut& o,
                                               const uint32_t (&sgn)[16], const Ctx& cx, const Divider& dv,
-                                              const float2* tab, uint64_t seed, Sums& acc, Kahan2& kb,
+                                              const float2* tab, const PhiloxKey& pk, Sums& acc, Kahan2& kb,
                                               Kahan2& ks, Kahan2& ke, uint32_t& nonfinite) {
   const int nb16 = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
   if constexpr (FMT == 1) {
@@ -771,7 +769,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
       load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
       uint32_t cw[4];
-      const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+      const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, pk, cw, bsum, ssum, esum,
                                                     acc, nonfinite);
       *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
       put_scale(o, f, (uint64_t)e / 32, sc);
@@ -780,7 +778,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
   } else if (nb16 == 2) {
     uint32_t cw[4], sc[2];
     f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
-    quant_two16<FMT, F32, RHT, SR>(LinearSeg{p}, sgn, cx, dv, tab, (uint64_t)e, seed, cw, sc, b2, s2, e2,
+    quant_two16<FMT, F32, RHT, SR>(LinearSeg{p}, sgn, cx, dv, tab, (uint64_t)e, pk, cw, sc, b2, s2, e2,
                                    nonfinite);
     *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
     put_scale(o, f, (uint64_t)e / 16, sc[0]);
@@ -794,7 +792,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
     f2 Q[8];
     load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
     uint32_t cw[2];
-    const uint32_t sc = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+    const uint32_t sc = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, pk, cw, bsum, ssum, esum,
                                                  acc, nonfinite);
     *reinterpret_cast<uint2*>(o.codes + e / 2) = make_uint2(cw[0], cw[1]);
     put_scale(o, f, (uint64_t)e / 16, sc);
@@ -859,7 +857,7 @@ __global__ void __launch_bounds__(RT, 2) amax_rows_kernel(Flat f, uint64_t seed,
 
 // ---- K2: quantise the row-wise copy --------------------------------------------------
 template <int FMT, bool F32, bool RHT, bool SR>
-__global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint64_t seed, CopyOut o,
+__global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint64_t seed, PhiloxKey pk, CopyOut o,
                                                            Workspace* ws, uint64_t timeout_ns) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ __align__(8) uint64_t full[Ring<F32>::kStages], empty[Ring<F32>::kStages];
@@ -901,7 +899,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
     if (ok) {
       const int64_t e = c * CH + (int64_t)tid * EPT;
       quant_segment<FMT, F32, RHT, SR>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, e, f, o, sgn, cx, dv,
-                                       tab, seed, acc, kb, ks, ke, nonfinite);
+                                       tab, pk, acc, kb, ks, ke, nonfinite);
     }
     timed_out = __syncthreads_or(!ok);
     if (timed_out) break;
@@ -1227,7 +1225,7 @@ __global__ void __launch_bounds__(RT, 2) amax_tiles_kernel(const __grid_constant
 // ---- K2 for tiles: quantise the row-wise and/or the column-wise copy ------------------
 template <int FMT, bool F32, bool RHT, bool SR, bool ROWS>
 __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constant__ CUtensorMap tmap, TileGeom g,
-                                                            uint64_t seed, CopyOut orow, CopyOut ocol,
+                                                            uint64_t seed, PhiloxKey pk, CopyOut orow, CopyOut ocol,
                                                             Workspace* ws, uint64_t timeout_ns) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[TileRing<F32>::kStages], empty[TileRing<F32>::kStages];
@@ -1291,7 +1289,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
             load_block16<F32, RHT>(sg, 0, sgn, Q);
             load_block16<F32, RHT>(sg, F32 ? 4 : 2, sgn, Q + 8);
             uint32_t cw[4];
-            const uint32_t sc = quant_block<FMT, SR, 16>(Q, cr.cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+            const uint32_t sc = quant_block<FMT, SR, 16>(Q, cr.cx, (uint64_t)e, pk, cw, bsum, ssum, esum,
                                                           cr.acc, nonfinite, 0u);
             store_codes16(orow.codes + row * orow.ld + col / 2, cw);
             put_scale_rk(orow, row, col / 32, sc);
@@ -1300,7 +1298,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
         } else if (nb16 == 2) {
           uint32_t cw[4], sc[2];
           f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
-          quant_two16<FMT, F32, RHT, SR>(sg, sgn, cr.cx, cr.dv, tab[0], (uint64_t)e, seed, cw, sc, b2, s2, e2,
+          quant_two16<FMT, F32, RHT, SR>(sg, sgn, cr.cx, cr.dv, tab[0], (uint64_t)e, pk, cw, sc, b2, s2, e2,
                                          nonfinite);
           store_codes16(orow.codes + row * orow.ld + col / 2, cw);
           put_scale_rk(orow, row, col / 16, sc[0]);
@@ -1313,7 +1311,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
           f2 Q[8];
           load_block16<F32, RHT>(sg, 0, sgn, Q);
           uint32_t cw[2];
-          const uint32_t sc = quant_block<FMT, SR, 8>(Q, cr.cx, (uint64_t)e, seed, cw, bsum, ssum, esum,
+          const uint32_t sc = quant_block<FMT, SR, 8>(Q, cr.cx, (uint64_t)e, pk, cw, bsum, ssum, esum,
                                                        cr.acc, nonfinite, 0u);
           *reinterpret_cast<uint2*>(orow.codes + row * orow.ld + col / 2) = make_uint2(cw[0], cw[1]);
           put_scale_rk(orow, row, col / 16, sc);
@@ -1331,7 +1329,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
           load_col32<F32, RHT>(slot, 32 * cb, col, smask, Q);
           const int64_t crow = c0 + col, ccol = r0 + 32 * cb;
           uint32_t cw[4];
-          const uint32_t sc = quant_block<FMT, SR, 16>(Q, cc.cx, (uint64_t)(crow * g.rows + ccol), seed, cw,
+          const uint32_t sc = quant_block<FMT, SR, 16>(Q, cc.cx, (uint64_t)(crow * g.rows + ccol), pk, cw,
                                                         bsum, ssum, esum, cc.acc, nonfinite, 1u);
           *reinterpret_cast<uint4*>(ocol.codes + crow * ocol.ld + ccol / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
           put_scale_rk(ocol, crow, ccol / 32, sc);
@@ -1366,7 +1364,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
           uint32_t cw[4], sc[2];
           f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
           quant_two16_vals<FMT, SR>(Q, m0, m1, cc.cx, cc.dv, tab[1], (uint64_t)(ca * g.rows + rw),
-                                    (uint64_t)((ca + 1) * g.rows + rw), seed, 1u, cw, sc, b2, s2, e2, nonfinite);
+                                    (uint64_t)((ca + 1) * g.rows + rw), pk, 1u, cw, sc, b2, s2, e2, nonfinite);
           *reinterpret_cast<uint2*>(ocol.codes + ca * ocol.ld + rw / 2) = make_uint2(cw[0], cw[1]);
           *reinterpret_cast<uint2*>(ocol.codes + (ca + 1) * ocol.ld + rw / 2) = make_uint2(cw[2], cw[3]);
           put_scale_rk(ocol, ca, rw / 16, sc[0]);
@@ -1429,7 +1427,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
 // the quantisation pass. The ring runs on across the barrier, so the second
 // pass's first chunks are already in flight while the first pass finishes.
 template <int FMT, bool F32, bool RHT, bool SR>
-__global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uint64_t seed, CopyOut o,
+__global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uint64_t seed, PhiloxKey pk, CopyOut o,
                                                                      Workspace* ws, uint64_t timeout_ns) {
   static_assert(FMT != 1, "MXFP4 has no tensor amax");
   extern __shared__ __align__(128) uint8_t ring[];
@@ -1501,7 +1499,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uin
       if (ok) {
         const int64_t e = chunk_of(it) * CH + (int64_t)tid * EPT;
         quant_segment<FMT, F32, RHT, SR>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, e, f, o, sgn, cx,
-                                         dv, tab, seed, acc, kb, ks, ke, nonfinite);
+                                         dv, tab, pk, acc, kb, ks, ke, nonfinite);
       }
       timed_out = __syncthreads_or(!ok);
       if (timed_out) break;
@@ -1735,7 +1733,8 @@ cudaError_t launch_quant_rows(const Flat& f, uint64_t seed, const CopyOut& o, Wo
   constexpr int smem = Ring<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(k, grid_for(k, smem, f.nchunks), smem, s, f, seed, o, ws, kRingTimeoutNs);
+  return launch_dependent(k, grid_for(k, smem, f.nchunks), smem, s, f, seed, philox_key(seed), o, ws,
+                          kRingTimeoutNs);
 }
 
 template <int FMT, bool F32>
@@ -1764,7 +1763,8 @@ cudaError_t launch_quant_tiles(const CUtensorMap& map, const TileGeom& g, uint64
   constexpr int smem = TileRing<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(k, grid_for(k, smem, g.ntiles), smem, s, map, g, seed, r, c, ws, kRingTimeoutNs);
+  return launch_dependent(k, grid_for(k, smem, g.ntiles), smem, s, map, g, seed, philox_key(seed), r, c, ws,
+                          kRingTimeoutNs);
 }
 
 template <int FMT, bool F32>
@@ -1833,9 +1833,10 @@ cudaError_t launch_quant_fused(const Flat& f, uint64_t seed, const CopyOut& o, W
   const int grid = grid_for(k, smem, f.nchunks);    // at most the co-resident CTAs
   Flat fa = f;
   uint64_t sd = seed, to = kRingTimeoutNs;
+  PhiloxKey pk = philox_key(seed);
   CopyOut oa = o;
   Workspace* wa = ws;
-  void* args[] = {&fa, &sd, &oa, &wa, &to};
+  void* args[] = {&fa, &sd, &pk, &oa, &wa, &to};
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k), dim3(grid), dim3(RT), args, smem, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
