@@ -104,44 +104,8 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
            : __fmul_rn((float)m, 0.001953125f);
 }
 
-// Two FP32 values -> one byte of E2M1 codes (nearest-even, saturating at 6):
-// `lo` lands in bits 0-3, `hi` in bits 4-7.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// One byte of E2M1 codes -> the two magnitudes (bits 0-3 -> lo, bits 4-7 -> hi).
-__device__ __forceinline__ void e2m1x2_abs(uint32_t byte, float& lo, float& hi) {
-  uint32_t h2;
-  asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(h2) : "r"(byte));
-  lo = fabsf(__half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu))));
-  hi = fabsf(__half2float(__ushort_as_half((unsigned short)(h2 >> 16))));
-}
-
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// In-place 16-point RHT of w (already sign-flipped): stages h = 1, 2, 4, 8 of
-// (a + b, a - b), then * 0.25, every step one FP32 rounding.
-__device__ __forceinline__ void fwht16_quarter(float* w) {
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if ((i & h) == 0) {
-        const float a = w[i], b = w[i + h];
-        w[i] = __fadd_rn(a, b);
-        w[i + h] = __fsub_rn(a, b);
-      }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 16; ++i) w[i] = __fmul_rn(w[i], 0.25f);
-}
 
 // Byte offset of scale (row r, block kb) in the tensor-core tiled layout
 // (128 rows x 4 blocks per 512-byte tile, block index fastest between tiles).
@@ -227,29 +191,8 @@ __device__ __forceinline__ uint32_t cta_max(uint32_t v, uint32_t* sh) {
   return r;
 }
 
-// Thread 0 publishes, then every thread learns whether this CTA finished last.
-__device__ __forceinline__ bool arrive_last(unsigned int* counter, bool* s_flag) {
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int prev = atomicInc(counter, gridDim.x - 1);
-    *s_flag = (prev == gridDim.x - 1);
-  }
-  __syncthreads();
-  const bool last = *s_flag;
-  if (last) __threadfence();
-  return last;
-}
-
-
 // SR uniform of one Philox word: its top 24 bits times 2^-24 (exact in FP32).
 __device__ __forceinline__ float sr_u(uint32_t w) { return __uint2float_rz(w >> 8) * 5.9604644775390625e-08f; }
-
-__device__ __forceinline__ void store_scale(const CopyOut& o, int64_t row, int64_t kb, uint32_t sc) {
-  const int64_t off = o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb;
-  o.scales[off] = (uint8_t)sc;
-}
-
-
 
 // Tensor amax (FP32 bits) of copy c, folded from the amax pass's per-CTA
 // partials; every thread of the CTA gets it.

@@ -1,5 +1,7 @@
-// Row-wise block-scaled 4-bit quantisation as a flat stream (sm_103a): the
-// tensor-amax pass and the quantisation pass for the row-wise copy.
+// Block-scaled 4-bit quantisation kernels (sm_103a): the tensor-amax pass and
+// the quantisation pass, as a flat stream for row-wise copies and as a tile
+// stream for requests with the transposed copy; the one-launch quantiser for
+// small row-wise tensors; the dequantiser.
 //
 // Method: "Replanteamiento del Sesgo de Contraccion en el Preentrenamiento de
 // LLM en FP4" (Metodologia §1-2: E2M1 / uniform E1M2 grids, RTNE, stochastic
@@ -19,6 +21,11 @@
 // chunk (two 16-blocks, or one MXFP4 32-block) in registers, using packed
 // FP32x2 operations where the lanes are independent; every value-deciding step
 // is one IEEE round-to-nearest-even operation in the order of the method.
+//
+// Requests with the transposed copy (TetraJet-v2, Riepilogo Tecnico §2A) walk
+// 64 x 128 tiles instead, brought in by 2-D TMA with the 128-byte swizzle, so
+// that one read of the source serves the row-wise and the column-wise copy
+// (see the tile section below).
 #include <cfloat>
 #include <cstdint>
 
