@@ -45,6 +45,11 @@ design notes of the repository):
      Philox word keyed on (seed) with counter (i / 4, axis, 0) picking word
      i mod 4; i = index of the element inside the copy being produced.
   R6 shrinkage bias = mean over elements of (|q| - |y|) / Qmax.
+  R13 two-level NVFP4 (the double-block scale of [TJ2] §2A): every outer block
+     of 128 consecutive values along the block axis has its own FP32 scale
+     g_o = A_o / (6 * 448), A_o = max |v| over the outer block, in place of the
+     tensor scale; the 16-element inner blocks inside it are scaled and rounded
+     exactly as NVFP4 is under a tensor scale, with g replaced by g_o.
 """
 from __future__ import annotations
 
@@ -476,6 +481,84 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
     return out
 
 
+#: outer block of the two-level NVFP4 scale ([TJ2] Riepilogo Tecnico §2A).
+OUTER_BLOCK = 128
+
+
+def quantize_copy_two_level(m32: np.ndarray, rht: bool = False, rounding: str = "rtne",
+                            seed: int = 0, axis: int = 0, rht_mode: str = "butterfly",
+                            rows_subset=None) -> dict:
+    """NVFP4 with the double-block scale ([TJ2] Riepilogo Tecnico §2A, reading
+    R13): "an outer block of 128 elements is scaled globally, the inner blocks
+    of 16 locally", which avoids the whole-tensor amax. Per copy row (blocks
+    along the columns), per outer block o of 128 values and inner block b of 16:
+      v   = RHT(x) or x
+      A_o = max |v| over the outer block;  g_o = A_o / (6 * 448)       (FP32)
+      d_o = 6 * g_o (FP32); t = a_b / d_o (FP32); s_b = E4M3_rne_sat(t);
+      p = s_b * g_o (FP32); r_b = 1 / p (FP32; 0 if p = 0, FLT_MAX if it
+      overflows); y = v * r_b (FP32); if g_o = 0 the outer block's scales and
+      codes are all 0
+      q   = RTNE(y) or SR(y, u_i) on the E2M1 grid
+    Returns codes and inner scales as NVFP4 does, and ``outer_scales`` (FP32,
+    rows x cols/128) in place of the tensor scale. Statistics as for NVFP4
+    with v_hat = q * s_b * g_o (FP64)."""
+    n, k = m32.shape
+    if k % OUTER_BLOCK:
+        raise ValueError("cols must be a multiple of the outer block (128)")
+    sel = np.arange(n) if rows_subset is None else np.asarray(rows_subset, dtype=np.int64)
+    v = transform_copy(np.ascontiguousarray(m32[sel]), "nvfp4", rht, seed, rht_mode)
+    rows = v.shape[0]
+    no, nb = k // OUTER_BLOCK, OUTER_BLOCK // 16
+    vb = v.reshape(rows, no, nb, 16)
+    a_o = np.max(np.abs(vb), axis=(2, 3)).astype(np.float32) if rows else np.zeros((0, no), np.float32)
+    g_o = (a_o / F32(6.0 * E4M3_MAX)).astype(np.float32)
+    d_o = (F32(6.0) * g_o).astype(np.float32)
+    a_b = np.max(np.abs(vb), axis=3).astype(np.float32) if rows else np.zeros((0, no, nb), np.float32)
+    zero = (g_o == 0.0)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = (a_b / d_o[..., None]).astype(np.float32)
+    s_code = np.where(zero, 0, e4m3_encode_rne_sat(np.where(zero, F32(0.0), t))).astype(np.uint8)
+    s_val = e4m3_decode(s_code).astype(np.float32)
+    p = (s_val * g_o[..., None]).astype(np.float32)
+    with np.errstate(divide="ignore", over="ignore"):
+        r_b = np.where(p == 0.0, F32(0.0), (F32(1.0) / p)).astype(np.float32)
+    r_b = np.where(np.isinf(r_b), np.finfo(np.float32).max, r_b).astype(np.float32)
+    y = (vb * r_b[..., None]).astype(np.float32).reshape(rows, k)
+    if rounding == "rtne":
+        c = round_rtne(y, "nvfp4")
+    elif rounding == "sr":
+        idx = sel[:, None] * k + np.arange(k, dtype=np.int64)[None, :]
+        c = round_sr(y, "nvfp4", sr_uniforms(idx, seed, axis))
+    else:
+        raise ValueError(rounding)
+    qv = code_value(c, "nvfp4")
+    term = np.abs(qv) - np.abs(y.astype(np.float64))
+    step64 = s_val.astype(np.float64) * g_o.astype(np.float64)[..., None]
+    vhat = (qv.reshape(rows, no, nb, 16) * step64[..., None]).reshape(rows, k)
+    v64 = v.astype(np.float64)
+    stats = stats_from_sums(float(np.sum(term)), float(np.sum(np.abs(term))), float(np.sum(v64 * v64)),
+                            float(np.sum((v64 - vhat) ** 2)), rows * k, QMAX["nvfp4"])
+    return {"fmt": "nvfp4_2l", "block": 16, "rows": rows, "cols": k, "rows_subset": rows_subset,
+            "codes": pack_nibbles(c), "scales": s_code.reshape(rows, k // 16),
+            "outer_scales": g_o, "stats": stats}
+
+
+def dequantize_two_level(codes_packed: np.ndarray, scales: np.ndarray, outer_scales: np.ndarray,
+                         inverse_rht: bool = False, seed: int = 0) -> np.ndarray:
+    """v_hat = (q * s_b) * g_o in FP32, two round-to-nearest products in that
+    order, g_o the scale of the element's outer block of 128; optionally
+    followed by R^T (FP32 butterfly)."""
+    c = unpack_nibbles(codes_packed)
+    n, k = c.shape
+    q = code_value(c, "nvfp4").astype(np.float32).reshape(n, k // 16, 16)
+    s_val = e4m3_decode(scales).astype(np.float32)
+    g = np.repeat(np.asarray(outer_scales, dtype=np.float32), OUTER_BLOCK // 16, axis=1)
+    v = ((q * s_val[..., None]).astype(np.float32) * g[..., None]).astype(np.float32).reshape(n, k)
+    if inverse_rht:
+        v = rht_inverse_butterfly(v.reshape(n, k // 16, 16), rht_signs(seed)).reshape(n, k)
+    return v
+
+
 def stats_from_sums(sum_bias, sum_abs_bias, sum_sig2, sum_err2, nel, qmax) -> dict:
     """Shrinkage bias (mean signed error in magnitude, normalised by Qmax;
     [UFP4] Metodología §1) and quantisation SNR in dB ([UFP4] Resultados;
@@ -506,6 +589,13 @@ def quantize(x, fmt: str, rht: bool = False, rounding: str = "rtne", seed: int =
     """
     m = _as_f32_matrix(x)
     out = {"nonfinite": bool(not np.all(np.isfinite(m)))}
+    if fmt == "nvfp4_2l":
+        if axis in ("row", "both"):
+            out["row"] = quantize_copy_two_level(m, rht, rounding, seed, 0, rht_mode, rows_subset)
+        if axis in ("col", "both"):
+            out["col"] = quantize_copy_two_level(np.ascontiguousarray(m.T), rht, rounding, seed, 1,
+                                                 rht_mode, cols_subset)
+        return out
     if axis in ("row", "both"):
         out["row"] = quantize_copy(m, fmt, rht, rounding, seed, 0, rht_mode, keep_y=keep_y,
                                    rows_subset=rows_subset)
