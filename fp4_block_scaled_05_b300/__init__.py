@@ -26,8 +26,9 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-FORMATS = {"nvfp4": 0, "mxfp4": 1, "ufp4": 2}
-BLOCKS = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16}
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "ufp4": 2, "nvfp4_2l": 3}
+BLOCKS = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16, "nvfp4_2l": 16}
+OUTER_BLOCK = 128   # two-level NVFP4: one FP32 scale per 128 elements of a row
 ROUNDING = {"rtne": 0, "sr": 1}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 AXES = {"row": 1, "col": 2, "both": 3}
@@ -132,7 +133,7 @@ class QCopy:
     """One quantised copy (device buffers) of a rows x cols matrix."""
     codes: torch.Tensor          # uint8 [rows, cols/2]
     scales: torch.Tensor         # uint8 [rows, cols/block] (linear) or flat (mma)
-    tensor_scale: torch.Tensor   # float32 [1]
+    tensor_scale: torch.Tensor   # float32 [1]; two-level NVFP4: [rows, cols/128] outer-block scales
     fmt: str
     rows: int
     cols: int
@@ -155,7 +156,10 @@ def alloc_copy(rows: int, cols: int, fmt: str, layout: str = "linear", device=No
         scales = torch.empty(rows, cols // b, dtype=torch.uint8, device=dev)
     else:
         scales = torch.empty(fp4q_scales_bytes(rows, cols, b, 1), dtype=torch.uint8, device=dev)
-    ts = torch.empty(1, dtype=torch.float32, device=dev)
+    if fmt == "nvfp4_2l":
+        ts = torch.empty(rows, cols // OUTER_BLOCK, dtype=torch.float32, device=dev)
+    else:
+        ts = torch.empty(1, dtype=torch.float32, device=dev)
     return QCopy(codes, scales, ts, fmt, rows, cols, layout)
 
 

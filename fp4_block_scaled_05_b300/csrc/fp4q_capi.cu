@@ -105,7 +105,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int block_for(int fmt) { return fmt == FP4Q_MXFP4 ? 32 : 16; }
 
 int check_format(int fmt, int block) {
-  if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4 && fmt != FP4Q_UFP4) return FP4Q_EINVAL;
+  if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4 && fmt != FP4Q_UFP4 && fmt != FP4Q_NVFP4_2L) return FP4Q_EINVAL;
   if (block != block_for(fmt)) return FP4Q_ENOTSUP;
   return FP4Q_OK;
 }
@@ -149,6 +149,10 @@ int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt
   if (cols % 16) return FP4Q_EINVAL;     // source rows start on 32-byte boundaries
   if ((axis & FP4Q_ROWWISE) && cols % block) return FP4Q_EINVAL;
   if ((axis & FP4Q_COLWISE) && rows % block) return FP4Q_EINVAL;
+  if (fmt == FP4Q_NVFP4_2L) {
+    if (axis & FP4Q_COLWISE) return FP4Q_ENOTSUP;     // row-wise copy only in this version
+    if (cols % 128) return FP4Q_EINVAL;               // whole outer blocks per row
+  }
   return FP4Q_OK;
 }
 
@@ -178,7 +182,9 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
               uint64_t seed, int axis, void* workspace, size_t ws_bytes, void* stream) {
   const int rc = check_source(src, dtype, rows, cols, fmt, block, rht, axis, workspace, ws_bytes);
   if (rc) return rc;
-  if (fmt == FP4Q_MXFP4) return FP4Q_OK;   // power-of-two block scales only: no tensor amax
+  // power-of-two block scales (MXFP4) or per-outer-block scales (two-level
+  // NVFP4): no tensor amax
+  if (fmt == FP4Q_MXFP4 || fmt == FP4Q_NVFP4_2L) return FP4Q_OK;
   fp4q::QuantArgs a{};
   a.src = src;
   a.dtype = dtype;
@@ -239,6 +245,7 @@ int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, 
   if (inverse_rht != 0 && inverse_rht != 1) return FP4Q_EINVAL;
   if (dst_dtype != FP4Q_BF16 && dst_dtype != FP4Q_F32) return FP4Q_EINVAL;
   if (rows < 0 || cols < 0 || cols % block) return FP4Q_EINVAL;
+  if (fmt == FP4Q_NVFP4_2L && cols % 128) return FP4Q_EINVAL;
   if (rows == 0 || cols == 0) return FP4Q_OK;
   if (!dst || !aligned(dst, 16)) return FP4Q_EINVAL;
   fp4q::DequantArgs a{};
@@ -327,7 +334,7 @@ namespace {
 int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K, int fmt,
                 void* Y, int out_dtype, void* workspace, size_t ws_bytes, uint64_t timeout_ns, int skip,
                 void* stream) {
-  if (fmt == FP4Q_UFP4) return FP4Q_ENOTSUP;
+  if (fmt == FP4Q_UFP4 || fmt == FP4Q_NVFP4_2L) return FP4Q_ENOTSUP;
   if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4) return FP4Q_EINVAL;
   if (fmt == FP4Q_MXFP4) return FP4Q_ENOTSUP;
   int rc;

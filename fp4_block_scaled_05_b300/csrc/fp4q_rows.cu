@@ -294,7 +294,40 @@ __device__ __forceinline__ void make_sign_words(uint32_t smask, uint32_t (&sgn)[
 struct Sums {        // per-thread running sums of one copy
   Kahan bias, sig, err;
   double sig64 = 0.0, err64 = 0.0;
+  int e_ref = 0;     // two-level NVFP4: sig / err are in units of 2^(2 (e_ref - 127)); 0 = not set yet
 };
+
+// Two-level NVFP4: add a thread's signal and error sums, in units of g_o^2, to
+// its running sums. FP32 Kahan sums in units of a power of two fixed by the
+// first outer scale the thread meets (the exact power-of-two rescaling keeps
+// them far from overflow and underflow); an outer scale more than 2^60 away
+// from it, or subnormal, goes to the FP64 sums instead.
+__device__ __forceinline__ void add_outer_stats(Sums& acc, float g, float ss, float es) {
+  const int E = (int)((__float_as_uint(g) >> 23) & 0xFFu);
+  if (acc.e_ref == 0 && E != 0 && E != 255) acc.e_ref = E;
+  const int dE = E - acc.e_ref;
+  if (E != 0 && E != 255 && dE >= -60 && dE <= 60) {
+    const float w = __uint_as_float((uint32_t)((int)__float_as_uint(g) - (acc.e_ref - 127) * (1 << 23)));
+    const float w2 = __fmul_rn(w, w);
+    acc.sig.add(__fmul_rn(ss, w2));
+    acc.err.add(__fmul_rn(es, w2));
+  } else if (g != 0.f) {
+    const double g2 = (double)g * (double)g;
+    acc.sig64 += (double)ss * g2;
+    acc.err64 += (double)es * g2;
+  }
+}
+
+// The running sums of add_outer_stats in absolute units (FP64).
+__device__ __forceinline__ void outer_stats_value(const Sums& acc, double& sig, double& err) {
+  sig = acc.sig64;
+  err = acc.err64;
+  if (acc.e_ref != 0) {
+    const double u = __longlong_as_double((long long)(1023 + 2 * (acc.e_ref - 127)) << 52);
+    sig += acc.sig.value() * u;
+    err += acc.err.value() * u;
+  }
+}
 
 // Two independent Kahan-compensated FP32 sums, one per lane of a pair.
 struct Kahan2 {
@@ -326,14 +359,16 @@ __device__ __forceinline__ float max3_abs_nan(float m, float a, float b) {
 // FLT_MAX when it overflows; the NaN code 127 maps to 0) and s^2, s the
 // code's value. A block's normaliser and statistics weight are then one table
 // read instead of a decode, a product and a reciprocal per block.
+__device__ __forceinline__ float2 scale_entry(uint32_t c, float g) {
+  const float s = (c < 127) ? e4m3_to_f32(c) : 0.f;
+  const float p = __fmul_rn(s, g);
+  float r = (p == 0.f) ? 0.f : __frcp_rn(p);
+  if (r > FLT_MAX) r = FLT_MAX;
+  return make_float2(r, __fmul_rn(s, s));
+}
+
 __device__ __forceinline__ void fill_scale_table(float2* tab, float g) {
-  for (int c = threadIdx.x; c < 128; c += blockDim.x) {
-    const float s = (c < 127) ? e4m3_to_f32((uint32_t)c) : 0.f;
-    const float p = __fmul_rn(s, g);
-    float r = (p == 0.f) ? 0.f : __frcp_rn(p);
-    if (r > FLT_MAX) r = FLT_MAX;
-    tab[c] = make_float2(r, __fmul_rn(s, s));
-  }
+  for (int c = threadIdx.x; c < 128; c += blockDim.x) tab[c] = scale_entry((uint32_t)c, g);
 }
 
 // t = RN(m / d) for both lanes. With y = RN(1/d) two correction steps
@@ -569,7 +604,7 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
 // two lanes of FP32 pairs. Writes four code words and two scale codes; adds
 // the blocks' bias / signal / error sums (grid units, signal and error times
 // s^2) to the lanes of bias2 / sig2 / err2.
-template <int FMT, bool SR>
+template <int FMT, bool SR, bool TAB = true>
 __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1, const Ctx& cx,
                                                  const Divider& dv, const float2* tab, uint64_t e0,
                                                  uint64_t e1, const PhiloxKey& pk, uint32_t axis,
@@ -619,8 +654,10 @@ __device__ __forceinline__ void quant_two16(const Seg& sg, const uint32_t (&sgn)
 // Quantise two 16-blocks given as FP32 pairs (block 0 in Q[0..7], block 1 in
 // Q[8..15], pair j holding elements 2j and 2j+1) with their maxima |v| m0, m1;
 // e0, e1 are the blocks' first element indices in the copy, `axis` the copy
-// (0 row-wise, 1 column-wise) for the SR counter.
-template <int FMT, bool SR>
+// (0 row-wise, 1 column-wise) for the SR counter. TAB: the normaliser and s^2
+// of a scale code come from the CTA's table `tab`; else they are computed from
+// cx.g, as the table computes them (the scale g differs between threads).
+template <int FMT, bool SR, bool TAB>
 __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1, const Ctx& cx,
                                                  const Divider& dv, const float2* tab, uint64_t e0,
                                                  uint64_t e1, const PhiloxKey& pk, uint32_t axis,
@@ -637,7 +674,14 @@ __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1
     sc[0] = c2 & 0xFFu;
     sc[1] = (uint32_t)c2 >> 8;
   }
-  const float2 T0 = tab[sc[0]], T1 = tab[sc[1]];
+  float2 T0, T1;
+  if constexpr (TAB) {
+    T0 = tab[sc[0]];
+    T1 = tab[sc[1]];
+  } else {
+    T0 = scale_entry(sc[0], cx.g);
+    T1 = scale_entry(sc[1], cx.g);
+  }
 
   float bs[2], ys[2], es[2];
 #pragma unroll
@@ -782,6 +826,47 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       put_scale(o, f, (uint64_t)e / 32, sc);
       acc.bias.add(bsum);
     }
+  } else if constexpr (FMT == 3) {
+    // Two-level NVFP4 (TetraJet-v2, Riepilogo Tecnico §2A): the four threads of
+    // a 128-element outer block (lanes 4k .. 4k+3; rows hold whole outer
+    // blocks) share its amax, which sets the block's own scale g_o in place
+    // of the tensor scale. Every lane takes part in the shuffles.
+    f2 Q[16];
+    float m0 = 0.f, m1 = 0.f;
+    if (nb16 == 2) {
+      load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
+      load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float a, b;
+        f2_split(Q[j], a, b);
+        m0 = max3_abs_nan(m0, a, b);
+        f2_split(Q[j + 8], a, b);
+        m1 = max3_abs_nan(m1, a, b);
+      }
+    }
+    float m = max_abs_nan(m0, m1);
+    m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    if (nb16 == 2) {
+      const Ctx co = make_ctx(__float_as_uint(m), 6.f, 2688.f);
+      Divider dvo;
+      dvo.init(co.d);
+      uint32_t cw[4], sc[2];
+      f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
+      quant_two16_vals<0, SR, false>(Q, m0, m1, co, dvo, nullptr, (uint64_t)e, (uint64_t)e + 16, pk, 0u, cw, sc,
+                                     b2, s2, e2, nonfinite);
+      *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      put_scale(o, f, (uint64_t)e / 16, sc[0]);
+      put_scale(o, f, (uint64_t)e / 16 + 1, sc[1]);
+      float x0, x1, y0, y1;
+      f2_split(b2, x0, x1);
+      acc.bias.add(__fadd_rn(x0, x1));
+      f2_split(s2, x0, x1);
+      f2_split(e2, y0, y1);
+      add_outer_stats(acc, co.g, __fadd_rn(x0, x1), __fadd_rn(y0, y1));
+      if ((threadIdx.x & 3u) == 0u) o.tensor_scale[e / 128] = co.g;
+    }
   } else if (nb16 == 2) {
     uint32_t cw[4], sc[2];
     f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
@@ -886,7 +971,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   grid_dependency_wait();
   Ctx cx{1.f, 0.f, 0.f};
   Divider dv{};
-  if constexpr (FMT != 1) {
+  if constexpr (FMT == 0 || FMT == 2) {
     cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
     dv.init(cx.d);
     fill_scale_table(tab, cx.g);
@@ -927,8 +1012,9 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
 
   // ---- statistics: one partial per CTA (summed on the host by fp4q_stats) ----
   if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
-  if constexpr (FMT == 1) {
-    const double p[3] = {acc.bias.value(), acc.sig64, acc.err64};
+  if constexpr (FMT == 1 || FMT == 3) {   // FP64 sums (absolute units)
+    double p[3] = {acc.bias.value(), acc.sig64, acc.err64};
+    if constexpr (FMT == 3) outer_stats_value(acc, p[1], p[2]);
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const double v = cta_sum<RT>(p[k], sh_sum);
@@ -945,10 +1031,10 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   if (blockIdx.x == 0 && tid == 0) {
     ws->stat_nparts = gridDim.x;
     ws->copies = 1u;
-    ws->tensor_scale[0] = (FMT == 1) ? 1.f : cx.g;
+    ws->tensor_scale[0] = (FMT == 1 || FMT == 3) ? 1.f : cx.g;
     ws->qmax = kQmax;
     ws->n = (double)f.n;
-    if (o.tensor_scale) *o.tensor_scale = (FMT == 1) ? 1.f : cx.g;
+    if (FMT != 3 && o.tensor_scale) *o.tensor_scale = (FMT == 1) ? 1.f : cx.g;
   }
 }
 
@@ -1649,7 +1735,7 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
   }
   constexpr int B = (FMT == 1) ? 32 : 16;
   constexpr int ES = OUT_F32 ? 4 : 2;
-  const float g = (FMT == 1) ? 1.f : __ldg(q.tensor_scale);
+  const float g = (FMT == 1 || FMT == 3) ? 1.f : __ldg(q.tensor_scale);
   const int64_t nseg = (f.n + 31) / 32;
   uint8_t* out = static_cast<uint8_t*>(dst);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -1667,13 +1753,15 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
       } else {
         const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16));
         const float s1 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16 + 1));
-        deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, g, sgn, out + e * ES);
-        deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, s1, g, sgn, out + (e + 16) * ES);
+        const float gs = (FMT == 3) ? __ldg(q.tensor_scale + e / 128) : g;   // two-level: outer-block scale
+        deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
+        deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, s1, gs, sgn, out + (e + 16) * ES);
       }
     } else {   // a lone 16-block at the very end (16-element formats only)
       const uint2 cw = __ldg(reinterpret_cast<const uint2*>(q.codes + e / 2));
       const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / B));
-      deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, g, sgn, out + e * ES);
+      const float gs = (FMT == 3) ? __ldg(q.tensor_scale + e / 128) : g;
+      deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
     }
   }
 }
@@ -1886,8 +1974,11 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
                        : dispatch_quant_rows<0, false>(a.rht, sr, f, a.seed, o, ws, s);
     case 1: return f32 ? dispatch_quant_rows<1, true>(a.rht, sr, f, a.seed, o, ws, s)
                        : dispatch_quant_rows<1, false>(a.rht, sr, f, a.seed, o, ws, s);
-    default: return f32 ? dispatch_quant_rows<2, true>(a.rht, sr, f, a.seed, o, ws, s)
-                        : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 2: return f32 ? dispatch_quant_rows<2, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 3: return f32 ? dispatch_quant_rows<3, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<3, false>(a.rht, sr, f, a.seed, o, ws, s);
+    default: return cudaErrorNotSupported;
   }
 }
 
@@ -1905,7 +1996,9 @@ cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s) {
   switch (a.fmt) {
     case 0: return launch_dequant_rows<0>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 1: return launch_dequant_rows<1>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
-    default: return launch_dequant_rows<2>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 2: return launch_dequant_rows<2>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 3: return launch_dequant_rows<3>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    default: return cudaErrorNotSupported;
   }
 }
 
@@ -1955,8 +2048,9 @@ cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s) {
                        : dispatch_quant_tiles<0, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
     case 1: return f32 ? dispatch_quant_tiles<1, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
                        : dispatch_quant_tiles<1, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
-    default: return f32 ? dispatch_quant_tiles<2, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
-                        : dispatch_quant_tiles<2, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+    case 2: return f32 ? dispatch_quant_tiles<2, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
+                       : dispatch_quant_tiles<2, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+    default: return cudaErrorNotSupported;     // the two-level format is row-wise only
   }
 }
 

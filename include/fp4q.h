@@ -49,7 +49,10 @@ extern "C" {
 typedef enum {
   FP4Q_NVFP4 = 0, /* E2M1 elements, 16-element blocks, E4M3 block scale, FP32 tensor scale [TJ2 §2A, MXFP4 §2] */
   FP4Q_MXFP4 = 1, /* E2M1 elements, 32-element blocks, E8M0 (power-of-two) block scale [MXFP4 §2]          */
-  FP4Q_UFP4  = 2  /* uniform E1M2 levels 0..7, 16-element blocks, E4M3 block scale, FP32 tensor scale [UFP4 §2] */
+  FP4Q_UFP4  = 2, /* uniform E1M2 levels 0..7, 16-element blocks, E4M3 block scale, FP32 tensor scale [UFP4 §2] */
+  FP4Q_NVFP4_2L = 3 /* NVFP4 with the double-block scale [TJ2 §2A]: E2M1 elements, 16-element inner blocks with
+                       an E4M3 scale, and an FP32 scale g_o = A_o / (6 * 448) per 128-element outer block along
+                       the row (A_o = max |v| over it) in place of the tensor scale: one pass, no tensor amax */
 } fp4q_format;
 
 typedef enum { FP4Q_RTNE = 0, FP4Q_SR = 1 } fp4q_rounding;
@@ -85,6 +88,8 @@ enum {
  *                codes (exponent + 127).
  *   tensor_scale one FP32 (device): g = amax / (Qmax * 448) for NVFP4 (Qmax 6)
  *                and UFP4 (Qmax 7, levels in integer units), 1.0 for MXFP4.
+ *                FP4Q_NVFP4_2L: rows x cols/128 FP32 values (row-major), the
+ *                outer-block scales g_o; element (r, c) uses g_o(r, c / 128).
  *   scale_layout FP4Q_SCALES_LINEAR or FP4Q_SCALES_MMA.
  * The value of element (r, c) is level(code) * scale(r, c / block) * g. */
 typedef struct {
@@ -164,8 +169,9 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  * Arguments
  *   src          device, rows x cols elements of `dtype` (FP4Q_BF16 or
  *                FP4Q_F32), row-major, 16-byte aligned.
- *   fmt, block   FP4Q_NVFP4/FP4Q_UFP4 with block 16, FP4Q_MXFP4 with block 32
- *                (else FP4Q_ENOTSUP).
+ *   fmt, block   FP4Q_NVFP4/FP4Q_UFP4/FP4Q_NVFP4_2L with block 16, FP4Q_MXFP4
+ *                with block 32 (else FP4Q_ENOTSUP). FP4Q_NVFP4_2L: row-wise
+ *                copy only (FP4Q_COLWISE -> FP4Q_ENOTSUP), cols % 128 == 0.
  *   rht          0 or 1. rounding: FP4Q_RTNE or FP4Q_SR. seed: RHT signs and SR.
  *   axis         FP4Q_ROWWISE: blocks along rows, copy row_out (rows x cols).
  *                FP4Q_COLWISE: blocks along columns, emitted transposed into
@@ -221,7 +227,8 @@ int fp4q_quantize_noalloc(const void* src, int dtype, int64_t rows, int64_t cols
  * cols elements of `dst_dtype` (BF16 rounded to nearest-even, or FP32) to the
  * device buffer `dst` (16-byte aligned). q is a host pointer to a descriptor of
  * device buffers laid out as fp4q_quantize wrote them for a copy of rows x
- * cols. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
+ * cols. FP4Q_NVFP4_2L: g is the outer-block scale of the element, cols %
+ * 128 == 0. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
 int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, int block,
                     int inverse_rht, uint64_t seed, void* dst, int dst_dtype, void* stream);
 

@@ -68,6 +68,10 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, -1, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     # column-wise only still needs source rows of a multiple of 16 elements
     assert q(fake, 0, 32, 100, 0, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
+    # two-level NVFP4 (format 3): row-wise only, whole 128-element outer blocks per row
+    assert q(fake, 0, 32, 256, 3, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 32, 144, 3, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 32, 256, 3, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
 
 
 def test_amax_validation_without_gpu(so):
