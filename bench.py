@@ -641,6 +641,39 @@ def run_grad_leg(fq, torch, device, steps, warmup):
     return out
 
 
+def run_two_level_leg(fq, torch, device, steps, warmup, peaks):
+    """Two-level NVFP4 (double-block scale: FP32 scale per 128-element outer
+    block, E4M3 per 16-element inner block; one pass, no tensor amax) on the
+    activation tensor with the 16-point RHT, RTNE, row-wise, against the
+    two-pass NVFP4 + RHT call on the same tensor: time per fp4q_quantize call
+    (L2 flushed before each)."""
+    import synth
+    x = synth.activation(ROWS, COLS).to(device)
+    ws = fq.workspace(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    n = ROWS * COLS
+    out = {}
+    for fmt, byts in (("nvfp4_2l", (2.0 + 0.5 + 1.0 / 16 + 4.0 / 128) * n), ("nvfp4", (B_AMAX + B_QUANT) * n)):
+        q = fq.alloc_copy(ROWS, COLS, fmt, "linear", device)
+        evs = []
+        for k in range(warmup + steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fq.fp4q_quantize(x, fmt=fmt, rht=True, seed=SEED, ws=ws, row_out=q)
+            e1.record(stream)
+            if k >= warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        gbs = byts / (us * 1e-6) / 1e9
+        out[fmt + "+rht"] = {"us": us, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"],
+                             "bytes_per_element": byts / n, "launches": len(evs) * (1 if fmt == "nvfp4_2l" else 2),
+                             "status": fq.fp4q_status(ws)}
+    return out
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
     if args.impl == "reference":
@@ -665,6 +698,7 @@ def main(argv=None) -> int:
     main_r = run_main_leg(fq, torch, device, args.steps, args.warmup)
     gemm_r = None if args.no_gemm else run_gemm_leg(fq, torch, device, args.steps, args.warmup)
     grad_r = run_grad_leg(fq, torch, device, min(args.steps, 50), args.warmup)
+    tl_r = run_two_level_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     e2e_steps = min(args.steps, 100)
     e2e_r = None if args.no_e2e else run_e2e_leg(fq, torch, device, e2e_steps, args.warmup)
     clocks = sampler.stop()
@@ -745,6 +779,11 @@ def main(argv=None) -> int:
         "workload": "4096x14336 and 14336x4096 BF16 N(0,1e-6) with 0.1% x100, NVFP4 + RHT16 + Philox "
                     "SR (seed 1234), row-wise and column-wise copies from one read",
         "bytes_per_element": B_AMAX + 2.0 + 2 * (0.5 + 1.0 / 16), **grad_r}
+    line["two_level_leg"] = {
+        "workload": "activation 8192x4096 BF16, RHT16, RTNE, row-wise: two-level NVFP4 (FP32 scale per "
+                    "128-element outer block, E4M3 per 16; one pass) vs NVFP4 with a tensor scale (amax "
+                    "pass + quantisation pass), time per fp4q_quantize call, L2 flushed before each",
+        **tl_r}
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
