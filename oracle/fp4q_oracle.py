@@ -45,6 +45,11 @@ design notes of the repository):
      Philox word keyed on (seed) with counter (i / 4, axis, 0) picking word
      i mod 4; i = index of the element inside the copy being produced.
   R6 shrinkage bias = mean over elements of (|q| - |y|) / Qmax.
+  R14 code utilisation ("effective bucket ratio", [UFP4] Resultados): the
+     histogram of the 16 codes of a copy; the effective bucket ratio is
+     exp(H) / 8, H the Shannon entropy (natural log) of the distribution of
+     the 8 magnitude levels, i.e. the effective number of levels in use over
+     the number available.
   R13 two-level NVFP4 (the double-block scale of [TJ2] §2A): every outer block
      of 128 consecutive values along the block axis has its own FP32 scale
      g_o = A_o / (6 * 448), A_o = max |v| over the outer block, in place of the
@@ -557,6 +562,26 @@ def dequantize_two_level(codes_packed: np.ndarray, scales: np.ndarray, outer_sca
     if inverse_rht:
         v = rht_inverse_butterfly(v.reshape(n, k // 16, 16), rht_signs(seed)).reshape(n, k)
     return v
+
+
+def code_histogram(codes_packed: np.ndarray) -> np.ndarray:
+    """Number of elements carrying each 4-bit code 0..15 in a packed copy
+    (reading R14)."""
+    c = unpack_nibbles(codes_packed).ravel()
+    return np.bincount(c, minlength=16).astype(np.int64)
+
+
+def effective_bucket_ratio(hist16: np.ndarray) -> float:
+    """exp(H) / 8, H = -sum p_l ln p_l over the 8 magnitude levels (codes c and
+    c + 8 fold together): 1 when all levels are used equally, 1/8 when one
+    level holds everything ([UFP4] Resultados, reading R14)."""
+    h = np.asarray(hist16, dtype=np.float64)
+    m = h[:8] + h[8:]
+    tot = m.sum()
+    if tot == 0:
+        return 0.0
+    p = m[m > 0] / tot
+    return float(np.exp(-np.sum(p * np.log(p))) / 8.0)
 
 
 def stats_from_sums(sum_bias, sum_abs_bias, sum_sig2, sum_err2, nel, qmax) -> dict:
