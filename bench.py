@@ -674,6 +674,39 @@ def run_two_level_leg(fq, torch, device, steps, warmup, peaks):
     return out
 
 
+def run_histogram_leg(fq, torch, device, steps, warmup, peaks):
+    """Code utilisation of the activation's three quantised copies ([UFP4]
+    Resultados: the RHT raises the effective bucket ratio): the histogram
+    kernel's time over the E2M1 + RHT copy (0.5 B/element read) and the
+    effective bucket ratio of each way."""
+    import synth
+    x = synth.activation(ROWS, COLS).to(device)
+    ws = fq.workspace(device)
+    stream = torch.cuda.current_stream(device)
+    ratios, copies = {}, {}
+    for fmt, rht in WAYS:
+        q = fq.alloc_copy(ROWS, COLS, fmt, "linear", device)
+        fq.fp4q_quantize(x, fmt=fmt, rht=rht, seed=SEED, ws=ws, row_out=q)
+        name = f"{fmt}{'+rht' if rht else ''}"
+        ratios[name] = fq.fp4q_effective_bucket_ratio(fq.fp4q_code_histogram(q))
+        copies[name] = q
+    q = copies["nvfp4+rht"]
+    counts = torch.empty(16, dtype=torch.int64, device=device)
+    evs = []
+    for k in range(warmup + steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fq.fp4q_code_histogram(q, out=counts)
+        e1.record(stream)
+        if k >= warmup:
+            evs.append((e0, e1))
+    torch.cuda.synchronize(device)
+    us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+    gbs = 0.5 * ROWS * COLS / (us * 1e-6) / 1e9
+    return {"us": us, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "launches": len(evs),
+            "effective_bucket_ratio": ratios}
+
+
 def main(argv=None) -> int:
     args = parse_args(argv)
     if args.impl == "reference":
@@ -699,6 +732,7 @@ def main(argv=None) -> int:
     gemm_r = None if args.no_gemm else run_gemm_leg(fq, torch, device, args.steps, args.warmup)
     grad_r = run_grad_leg(fq, torch, device, min(args.steps, 50), args.warmup)
     tl_r = run_two_level_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
+    hist_r = run_histogram_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     e2e_steps = min(args.steps, 100)
     e2e_r = None if args.no_e2e else run_e2e_leg(fq, torch, device, e2e_steps, args.warmup)
     clocks = sampler.stop()
@@ -784,6 +818,9 @@ def main(argv=None) -> int:
                     "128-element outer block, E4M3 per 16; one pass) vs NVFP4 with a tensor scale (amax "
                     "pass + quantisation pass), time per fp4q_quantize call, L2 flushed before each",
         **tl_r}
+    line["code_histogram"] = {
+        "workload": "16-code histogram of the activation's E2M1 + RHT copy (16.8 MB of codes); effective "
+                    "bucket ratio exp(H)/8 of each way's copy", **hist_r}
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

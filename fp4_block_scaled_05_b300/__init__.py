@@ -67,6 +67,8 @@ _SIGS = {
     "fp4q_status": ([_P, _P], _I),
     "fp4q_gemm": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
     "fp4q_gemm_selftest_timeout": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, ctypes.c_uint64, _P], _I),
+    "fp4q_code_histogram": ([_QP, _I64, _I64, _P, _P], _I),
+    "fp4q_effective_bucket_ratio": ([ctypes.POINTER(ctypes.c_ulonglong)], ctypes.c_double),
     "fp4q_strerror": ([_I], ctypes.c_char_p),
     "fp4q_version": ([], _I),
 }
@@ -246,6 +248,23 @@ def fp4q_dequantize(q: QCopy, inverse_rht: bool = False, seed: int = 0,
                               DTYPES[out.dtype], _stream(out.device))
     _check("fp4q_dequantize", rc)
     return out
+
+
+def fp4q_code_histogram(q: QCopy, out: torch.Tensor = None) -> torch.Tensor:
+    """Counts of the 16 codes of a copy (int64 [16], on the copy's device)."""
+    if out is None:
+        out = torch.empty(16, dtype=torch.int64, device=q.codes.device)
+    s = q.c_struct()
+    rc = _lib.fp4q_code_histogram(ctypes.byref(s), q.rows, q.cols, ctypes.c_void_p(out.data_ptr()),
+                                  _stream(q.codes.device))
+    _check("fp4q_code_histogram", rc)
+    return out
+
+
+def fp4q_effective_bucket_ratio(counts) -> float:
+    """exp(H)/8 of a 16-code histogram (see fp4q.h)."""
+    h = (ctypes.c_ulonglong * 16)(*[int(v) for v in torch.as_tensor(counts).cpu().tolist()])
+    return float(_lib.fp4q_effective_bucket_ratio(h))
 
 
 def _stats_dict(st: fp4q_stats_t) -> dict:

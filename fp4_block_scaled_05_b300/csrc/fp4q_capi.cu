@@ -260,6 +260,35 @@ int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, 
   return fp4q::run_dequantize(a, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
 }
 
+int fp4q_code_histogram(const fp4q_qtensor* q, int64_t rows, int64_t cols, unsigned long long* counts,
+                        void* stream) {
+  if (!q || !counts || !aligned(counts, 8)) return FP4Q_EINVAL;
+  if (rows < 0 || cols < 0 || (cols & 1)) return FP4Q_EINVAL;
+  if (rows && cols > (int64_t(1) << 46) / rows) return FP4Q_EINVAL;
+  const int64_t nbytes = rows * (cols / 2);
+  if (nbytes && (!q->codes || !aligned(q->codes, 16))) return FP4Q_EINVAL;
+  return fp4q::run_code_histogram(q->codes, nbytes, counts, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK
+                                                                                                  : FP4Q_ECUDA;
+}
+
+double fp4q_effective_bucket_ratio(const unsigned long long* counts) {
+  if (!counts) return 0.0;
+  double m[8], tot = 0.0;
+  for (int l = 0; l < 8; ++l) {
+    m[l] = (double)counts[l] + (double)counts[l + 8];
+    tot += m[l];
+  }
+  if (tot == 0.0) return 0.0;
+  double h = 0.0;
+  for (int l = 0; l < 8; ++l) {
+    if (m[l] > 0.0) {
+      const double p = m[l] / tot;
+      h -= p * std::log(p);
+    }
+  }
+  return std::exp(h) / 8.0;
+}
+
 int fp4q_stats(const void* workspace, fp4q_stats_t* row_stats, fp4q_stats_t* col_stats,
                void* stream) {
   if (!workspace) return FP4Q_EINVAL;

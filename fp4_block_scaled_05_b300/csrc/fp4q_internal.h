@@ -71,6 +71,9 @@ cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s);
 // Both passes of a row-wise NVFP4/UFP4 request in one cooperative launch.
 cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
+// Counts of the 16 four-bit codes in `nbytes` bytes of packed codes (zeroes `counts` first).
+cudaError_t run_code_histogram(const uint8_t* codes, int64_t nbytes, unsigned long long* counts,
+                               cudaStream_t s);
 // Returns cudaErrorNotSupported when no GEMM kernel covers the request.
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s);
 // run_gemm with an explicit bound on every wait and, when `skip_first_stage`,

@@ -245,6 +245,25 @@ int fp4q_stats(const void* workspace, fp4q_stats_t* row_stats, fp4q_stats_t* col
  * timeout wins) and clear it. FP4Q_ECUDA if the synchronisation failed. */
 int fp4q_status(void* workspace, void* stream);
 
+/* ---- code utilisation ----------------------------------------------------------- */
+
+/* Histogram of the 4-bit codes of one copy ([UFP4] Resultados: the RHT raises
+ * the effective bucket ratio of both grids). q->codes: device, rows x cols/2
+ * packed bytes as fp4q_quantize wrote them (16-byte aligned; q's scales and
+ * tensor scale are not read). counts: device array of 16 unsigned 64-bit
+ * integers, 8-byte aligned, overwritten with the number of elements carrying
+ * each code 0..15 (bit 3 the sign, bits 0-2 the level). Asynchronous on
+ * `stream`. Errors: FP4Q_EINVAL (null or misaligned pointers, negative sizes,
+ * odd cols), FP4Q_ECUDA. */
+int fp4q_code_histogram(const fp4q_qtensor* q, int64_t rows, int64_t cols, unsigned long long* counts,
+                        void* stream);
+
+/* Effective bucket ratio of a code histogram (host array of 16 counts):
+ * exp(H) / 8, H = -sum p_l ln p_l over the 8 levels (a code and its negative
+ * count together): 1 when the 8 levels are used equally, 1/8 when one level
+ * holds every element, 0 for an empty histogram. */
+double fp4q_effective_bucket_ratio(const unsigned long long* counts);
+
 /* ---- block-scaled GEMM --------------------------------------------------------- */
 
 /* Y = dequant(A) * dequant(B)^T on the tensor cores ([NGPT] Metodologia: NVFP4

@@ -113,3 +113,28 @@ def test_gemm_selftest_validation_without_gpu(so):
     assert f(fake, fake, 128, 128, 256, 0, fake, 0, fake, ws, 100, None) == 1           # bound too short
     assert f(fake, fake, 128, 128, 256, 0, fake, 0, fake, ws, 10**11, None) == 1        # bound too long
     assert f(fake, fake, 128, 128, 256, 2, fake, 0, fake, ws, 10**7, None) == 2         # UFP4 GEMM
+
+
+def test_effective_bucket_ratio_host(so):
+    """The host-side ratio of the C library against the oracle's closed forms."""
+    import numpy as np
+    from oracle import fp4q_oracle as o
+    f = so.fp4q_effective_bucket_ratio
+    f.argtypes = [ctypes.POINTER(ctypes.c_ulonglong)]
+    f.restype = ctypes.c_double
+    for h in ([10] * 8 + [0] * 8, [0, 0, 0, 100] + [0] * 12, [5, 0, 3, 7, 1, 0, 0, 2, 4, 0, 6, 0, 0, 1, 0, 3],
+              [0] * 16):
+        arr = (ctypes.c_ulonglong * 16)(*h)
+        assert abs(f(arr) - o.effective_bucket_ratio(np.array(h))) < 1e-15
+
+
+def test_code_histogram_validation_without_gpu(so):
+    f = so.fp4q_code_histogram
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    fake = ctypes.c_void_p(1 << 20)
+    assert f(None, 4, 32, fake, None) == 1                 # no descriptor
+    assert f(fake, 4, 32, None, None) == 1                 # no counts
+    assert f(fake, 4, 31, fake, None) == 1                 # odd cols
+    assert f(fake, -1, 32, fake, None) == 1                # negative rows
+    assert f(fake, 4, 32, ctypes.c_void_p((1 << 20) + 4), None) == 1   # counts not 8-byte aligned
