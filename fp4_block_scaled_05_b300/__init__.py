@@ -68,6 +68,8 @@ _SIGS = {
     "fp4q_gemm": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
     "fp4q_gemm_selftest_timeout": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, ctypes.c_uint64, _P], _I),
     "fp4q_code_histogram": ([_QP, _I64, _I64, _P, _P], _I),
+    "fp4q_gemm_via_bf16_scratch_bytes": ([_I64, _I64, _I64], _SZ),
+    "fp4q_gemm_via_bf16": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
     "fp4q_effective_bucket_ratio": ([ctypes.POINTER(ctypes.c_ulonglong)], ctypes.c_double),
     "fp4q_strerror": ([_I], ctypes.c_char_p),
     "fp4q_version": ([], _I),
@@ -306,6 +308,26 @@ def fp4q_gemm(a: QCopy, b: QCopy, out_dtype=torch.bfloat16, out: torch.Tensor = 
                         out.data_ptr(), DTYPES[out.dtype], ws.data_ptr(), ws.numel(),
                         _stream(out.device))
     _check("fp4q_gemm", rc)
+    return out
+
+
+def fp4q_gemm_via_bf16(a: QCopy, b: QCopy, out_dtype=torch.bfloat16, out: torch.Tensor = None,
+                       scratch: torch.Tensor = None) -> torch.Tensor:
+    """Y = dequant(a) @ dequant(b)^T through BF16 operands (UFP4, MXFP4 or
+    NVFP4 row-wise copies a (M x K), b (N x K))."""
+    if a.cols != b.cols or a.fmt != b.fmt:
+        raise ValueError("K or format mismatch")
+    dev = a.codes.device
+    if scratch is None:
+        scratch = torch.empty(_lib.fp4q_gemm_via_bf16_scratch_bytes(a.rows, b.rows, a.cols), dtype=torch.uint8,
+                              device=dev)
+    if out is None:
+        out = torch.empty(a.rows, b.rows, dtype=out_dtype, device=dev)
+    sa, sb = a.c_struct(), b.c_struct()
+    rc = _lib.fp4q_gemm_via_bf16(ctypes.byref(sa), ctypes.byref(sb), a.rows, b.rows, a.cols, FORMATS[a.fmt],
+                                 out.data_ptr(), DTYPES[out.dtype], scratch.data_ptr(), scratch.numel(),
+                                 _stream(dev))
+    _check("fp4q_gemm_via_bf16", rc)
     return out
 
 

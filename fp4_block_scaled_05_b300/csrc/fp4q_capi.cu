@@ -260,6 +260,35 @@ int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, 
   return fp4q::run_dequantize(a, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
 }
 
+size_t fp4q_gemm_via_bf16_scratch_bytes(int64_t M, int64_t N, int64_t K) {
+  if (M < 0 || N < 0 || K < 0) return 0;
+  return fp4q::gemm_bf16_scratch_bytes(M, N, K);
+}
+
+int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+                       int fmt, void* Y, int out_dtype, void* scratch, size_t scratch_bytes, void* stream) {
+  int rc = check_format(fmt, block_for(fmt));
+  if (rc) return rc;
+  if (fmt == FP4Q_NVFP4_2L) return FP4Q_ENOTSUP;
+  if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
+  if (out_dtype != FP4Q_BF16 && out_dtype != FP4Q_F32) return FP4Q_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || K % block_for(fmt)) return FP4Q_EINVAL;
+  if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP4Q_EINVAL;
+  if (!Y || !aligned(Y, 16)) return FP4Q_EINVAL;
+  if (!scratch || !aligned(scratch, 256) || scratch_bytes < fp4q::gemm_bf16_scratch_bytes(M, N, K))
+    return FP4Q_EINVAL;
+  fp4q::GemmArgs a{};
+  a.a = to_qout(A);
+  a.b = to_qout(B);
+  a.m = M;
+  a.n = N;
+  a.k = K;
+  a.fmt = fmt;
+  a.y = Y;
+  a.out_dtype = out_dtype;
+  return fp4q::run_gemm_bf16(a, scratch, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+}
+
 int fp4q_code_histogram(const fp4q_qtensor* q, int64_t rows, int64_t cols, unsigned long long* counts,
                         void* stream) {
   if (!q || !counts || !aligned(counts, 8)) return FP4Q_EINVAL;

@@ -71,6 +71,10 @@ cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s);
 // Both passes of a row-wise NVFP4/UFP4 request in one cooperative launch.
 cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
+// Block-scaled operands dequantised to BF16, then a BF16 GEMM (FP32
+// accumulation) scaled by g_A * g_B; `scratch` holds gemm_bf16_scratch_bytes().
+size_t gemm_bf16_scratch_bytes(int64_t m, int64_t n, int64_t k);
+cudaError_t run_gemm_bf16(const GemmArgs& a, void* scratch, cudaStream_t s);
 // Counts of the 16 four-bit codes in `nbytes` bytes of packed codes (zeroes `counts` first).
 cudaError_t run_code_histogram(const uint8_t* codes, int64_t nbytes, unsigned long long* counts,
                                cudaStream_t s);

@@ -286,6 +286,30 @@ double fp4q_effective_bucket_ratio(const unsigned long long* counts);
 int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
               int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of scratch fp4q_gemm_via_bf16 needs for M x K and N x K operands:
+ * 256 + (M + N) * K * 2 + 32 MiB (the BF16 operands and the GEMM library's
+ * workspace). */
+size_t fp4q_gemm_via_bf16_scratch_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Y = dequant(A) * dequant(B)^T for block-scaled formats without a native
+ * tensor-core GEMM here: UFP4 ([UFP4] Metodologia §2 and Resultados: the
+ * uniform grid with the RHT on every training GEMM) and MXFP4; NVFP4 is
+ * accepted too. Each operand is dequantised on the GPU to its BF16 block
+ * values level * s_b (exact in BF16), then a BF16 GEMM with FP32 accumulation
+ * (the CUDA GEMM library) forms the product, scaled by g_A * g_B (FP32
+ * product; 1 for MXFP4). When both operands were quantised with the RHT along
+ * K under the same seed, the transforms cancel.
+ *   A, B       host pointers to descriptors of row-wise copies (M x K, N x K),
+ *              linear or tiled scales, of format `fmt`.
+ *   Y          device, M x N row-major, FP4Q_BF16 or FP4Q_F32, 16-byte aligned.
+ *   scratch    device, 256-byte aligned, scratch_bytes >=
+ *              fp4q_gemm_via_bf16_scratch_bytes(M, N, K); owned by the caller.
+ * Calls from different host threads must not share a stream at the same time.
+ * Shapes: M, N, K > 0, K % block == 0 (else FP4Q_EINVAL).
+ * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP (FP4Q_NVFP4_2L), FP4Q_ECUDA. */
+int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+                       int fmt, void* Y, int out_dtype, void* scratch, size_t scratch_bytes, void* stream);
+
 /* Test hook for the device-side failure path (not a step of the method): runs
  * fp4q_gemm with the producer of the first CTA withholding the first stage of
  * its first tile and every wait bounded by `timeout_ns`, so the waits that
