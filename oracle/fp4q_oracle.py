@@ -50,6 +50,19 @@ design notes of the repository):
      exp(H) / 8, H the Shannon entropy (natural log) of the distribution of
      the 8 magnitude levels, i.e. the effective number of levels in use over
      the number available.
+  R15 the E8M0 variants of [MXFP4] §2A-§2B sit on 16-element blocks (the page
+     applies both techniques at block size 16): ``mxfp4_b16`` keeps the OCP
+     exponent rule; ``mxfp4_oas`` (overflow-aware scaling) takes the smallest
+     power of two 2^e with alpha_max / 2^e <= 7, i.e. e = ceil(log2(alpha_max
+     / 7)), which puts alpha_max / 2^e in (3.5, 7] instead of [4, 8).
+  R16 MBS-static ([MXFP4] §2B): every macro block of 128 consecutive values
+     along the block axis has a scale S with 8 mantissa bits, S = alpha_M / 6
+     rounded to nearest (ties to even) on FP32's grid with 8 fraction bits
+     (alpha_M = max |v| over the macro block), so the macro block's maximum
+     lands on the top level; inside it, each 16-element block gets an E8M0
+     exponent by the OCP rule applied to a_b * (1/S), and y = (v * (1/S)) *
+     2^-e_b; 1/S is one FP32 reciprocal (0 when S = 0, FLT_MAX if it
+     overflows), as r_b is under R3.
   R13 two-level NVFP4 (the double-block scale of [TJ2] §2A): every outer block
      of 128 consecutive values along the block axis has its own FP32 scale
      g_o = A_o / (6 * 448), A_o = max |v| over the outer block, in place of the
@@ -72,9 +85,11 @@ E2M1_LEVELS = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float6
 #: [UFP4] Metodología §2 "Rejilla Uniforme": equal left/right bin widths.
 UFP4_LEVELS = np.arange(8, dtype=np.float64)
 
-FORMATS = ("nvfp4", "mxfp4", "ufp4")
-QMAX = {"nvfp4": 6.0, "mxfp4": 6.0, "ufp4": 7.0}
-BLOCK = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16}
+FORMATS = ("nvfp4", "mxfp4", "ufp4", "mxfp4_b16", "mxfp4_oas")
+QMAX = {"nvfp4": 6.0, "mxfp4": 6.0, "ufp4": 7.0, "mxfp4_b16": 6.0, "mxfp4_oas": 6.0}
+BLOCK = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16, "mxfp4_b16": 16, "mxfp4_oas": 16}
+#: formats whose block scale is an E8M0 power of two (no tensor scale)
+E8M0_FORMATS = ("mxfp4", "mxfp4_b16", "mxfp4_oas")
 E4M3_MAX = 448.0
 
 F32 = np.float32
@@ -155,6 +170,38 @@ def e8m0_exponent(amax) -> np.ndarray:
     e = ex.astype(np.int64) - 1 - 2
     e = np.where(a == 0.0, -127, e)
     return np.clip(e, -127, 127)
+
+
+def e8m0_exponent_oas(amax) -> np.ndarray:
+    """Overflow-aware shared exponent ([MXFP4] §2A, reading R15): the smallest
+    e with amax / 2^e <= 7, so that amax / 2^e lies in (3.5, 7]. With amax =
+    m * 2^ex (frexp, m in [0.5, 1)): amax / 2^(ex-3) = 8m <= 7 iff m <= 7/8,
+    giving e = ex - 3, else e = ex - 2. Clamped to [-127, 127]; amax = 0 gives
+    -127."""
+    a = np.asarray(amax, dtype=np.float64)
+    m, ex = np.frexp(a)
+    e = np.where(m <= 0.875, ex.astype(np.int64) - 3, ex.astype(np.int64) - 2)
+    e = np.where(a == 0.0, -127, e)
+    return np.clip(e, -127, 127)
+
+
+def block_exponent(amax, fmt: str) -> np.ndarray:
+    """E8M0 exponent of a block under the format's rule."""
+    return e8m0_exponent_oas(amax) if fmt == "mxfp4_oas" else e8m0_exponent(amax)
+
+
+def mbs_macro_scale(alpha) -> np.ndarray:
+    """MBS-static macro-block scale ([MXFP4] §2B, reading R16): alpha / 6
+    rounded to nearest, ties to even, on the FP32 grid with 8 fraction bits
+    (quantum 2^(E - 8) for alpha / 6 in [2^E, 2^(E+1)), E >= -126; 2^-134 below
+    2^-126). alpha / 6 is formed in FP64: for an FP32 alpha it is either exact
+    or has a non-terminating binary expansion (alternating bits from the 24th
+    significant bit on), so it is never a tie of the 8-bit grid unless exactly
+    one, and the FP64 rounding cannot cross one. Returns FP32."""
+    t = np.asarray(alpha, dtype=np.float32).astype(np.float64) / 6.0
+    _, ex = np.frexp(t)
+    quantum = np.exp2((np.maximum(ex.astype(np.int64) - 1, -126) - 8).astype(np.float64))
+    return (np.rint(t / quantum) * quantum).astype(np.float32)
 
 
 # --------------------------------------------------------------------------- #
@@ -366,9 +413,9 @@ def tensor_amax(v: np.ndarray) -> np.float32:
 
 def tensor_scale(amax: np.float32, fmt: str) -> np.float32:
     """NVFP4 per-tensor FP32 scale g = A / (Qmax * 448), one FP32 division
-    by the exact constant 2688 (NVFP4) or 3136 (UFP4, reading R2); MXFP4 has
-    no tensor scale (1.0)."""
-    if fmt == "mxfp4":
+    by the exact constant 2688 (NVFP4) or 3136 (UFP4, reading R2); the E8M0
+    formats have no tensor scale (1.0)."""
+    if fmt in E8M0_FORMATS:
         return F32(1.0)
     return F32(F32(amax) / F32(QMAX[fmt] * E4M3_MAX))
 
@@ -390,7 +437,8 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
                   y = v * r_b (FP32)                                  (reading R3)
                   if g = 0 every scale and code is 0.
       MXFP4:      e_b = floor(log2 a_b) - 2 in [-127, 127]; scale code e_b + 127;
-                  y = v * 2^-e_b (FP32)
+                  y = v * 2^-e_b (FP32); mxfp4_b16 the same on 16-element
+                  blocks, mxfp4_oas with e_b = ceil(log2(a_b / 7)) (R15)
       q   = RTNE(y) or SR(y, u_i)
     ``rows_subset`` (row indices of the copy) restricts the codes, scales and
     statistics to those rows; the tensor amax still covers the whole copy.
@@ -432,8 +480,8 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
         rows = v.shape[0]
         vb = v.reshape(rows, k // b, b)
         a_b = np.max(np.abs(vb), axis=2).astype(np.float32)
-        if fmt == "mxfp4":
-            e_b = e8m0_exponent(a_b)
+        if fmt in E8M0_FORMATS:
+            e_b = block_exponent(a_b, fmt)
             scales[r0:r0 + rows] = (e_b + 127).astype(np.uint8)
             mult = np.exp2(-e_b.astype(np.float64)).astype(np.float32)
             y = (vb * mult[..., None]).astype(np.float32)
@@ -564,6 +612,84 @@ def dequantize_two_level(codes_packed: np.ndarray, scales: np.ndarray, outer_sca
     return v
 
 
+#: macro block of MBS-static ([MXFP4] Résumé technique §2B)
+MACRO_BLOCK = 128
+
+
+def quantize_copy_mbs(m32: np.ndarray, rht: bool = False, rounding: str = "rtne",
+                      seed: int = 0, axis: int = 0, rht_mode: str = "butterfly",
+                      rows_subset=None) -> dict:
+    """MXFP4 with the static macro-block scale ([MXFP4] Résumé technique §2B,
+    reading R16): a scale with 8 mantissa bits per macro block of 128 values,
+    E8M0 scales per 16-element block under it. Per copy row, macro block M and
+    16-element block b inside it:
+      v   = RHT(x) or x
+      alpha_M = max |v| over M;  S = RN8(alpha_M / 6)                  (FP32)
+      rS  = 1 / S (FP32; 0 if S = 0, FLT_MAX if it overflows)
+      a_b = max |v| over b;  a1 = a_b * rS (FP32);  e_b = floor(log2 a1) - 2
+            in [-127, 127] (a1 = 0 gives -127); scale code e_b + 127
+      w   = v * rS (FP32);  y = w * 2^-e_b (exact)
+      q   = RTNE(y) or SR(y, u_i) on the E2M1 grid
+    Returns codes and E8M0 scale codes, and ``macro_scales`` (FP32, rows x
+    cols/128). Statistics as for MXFP4 with v_hat = q * 2^e_b * S (FP64)."""
+    n, k = m32.shape
+    if k % MACRO_BLOCK:
+        raise ValueError("cols must be a multiple of the macro block (128)")
+    sel = np.arange(n) if rows_subset is None else np.asarray(rows_subset, dtype=np.int64)
+    v = transform_copy(np.ascontiguousarray(m32[sel]), "mxfp4", rht, seed, rht_mode)
+    rows = v.shape[0]
+    nm, nb = k // MACRO_BLOCK, MACRO_BLOCK // 16
+    vb = v.reshape(rows, nm, nb, 16)
+    if rows:
+        alpha = np.max(np.abs(vb), axis=(2, 3)).astype(np.float32)
+        a_b = np.max(np.abs(vb), axis=3).astype(np.float32)
+    else:
+        alpha = np.zeros((0, nm), np.float32)
+        a_b = np.zeros((0, nm, nb), np.float32)
+    S = mbs_macro_scale(alpha)
+    with np.errstate(divide="ignore", over="ignore"):
+        rS = np.where(S == 0.0, F32(0.0), F32(1.0) / S).astype(np.float32)
+    rS = np.where(np.isinf(rS), np.finfo(np.float32).max, rS).astype(np.float32)
+    a1 = (a_b * rS[..., None]).astype(np.float32)
+    e_b = e8m0_exponent(a1)
+    w = (vb * rS[..., None, None]).astype(np.float32)
+    y = (w.astype(np.float64) * np.exp2(-e_b.astype(np.float64))[..., None]).astype(np.float32)
+    y = y.reshape(rows, k)
+    if rounding == "rtne":
+        c = round_rtne(y, "mxfp4")
+    elif rounding == "sr":
+        idx = sel[:, None] * k + np.arange(k, dtype=np.int64)[None, :]
+        c = round_sr(y, "mxfp4", sr_uniforms(idx, seed, axis))
+    else:
+        raise ValueError(rounding)
+    qv = code_value(c, "mxfp4")
+    term = np.abs(qv) - np.abs(y.astype(np.float64))
+    step64 = np.exp2(e_b.astype(np.float64)) * S.astype(np.float64)[..., None]
+    vhat = (qv.reshape(rows, nm, nb, 16) * step64[..., None]).reshape(rows, k)
+    v64 = v.astype(np.float64)
+    stats = stats_from_sums(float(np.sum(term)), float(np.sum(np.abs(term))), float(np.sum(v64 * v64)),
+                            float(np.sum((v64 - vhat) ** 2)), rows * k, 6.0)
+    return {"fmt": "mxfp4_mbs", "block": 16, "rows": rows, "cols": k, "rows_subset": rows_subset,
+            "codes": pack_nibbles(c), "scales": (e_b + 127).astype(np.uint8).reshape(rows, k // 16),
+            "macro_scales": S, "stats": stats}
+
+
+def dequantize_mbs(codes_packed: np.ndarray, scales: np.ndarray, macro_scales: np.ndarray,
+                   inverse_rht: bool = False, seed: int = 0) -> np.ndarray:
+    """v_hat = (q * 2^e_b) * S in FP32, two round-to-nearest products in that
+    order (the first is exact), S the scale of the element's macro block;
+    optionally followed by R^T (FP32 butterfly)."""
+    c = unpack_nibbles(codes_packed)
+    n, k = c.shape
+    q = code_value(c, "mxfp4").astype(np.float32).reshape(n, k // 16, 16)
+    mult = np.exp2((np.asarray(scales, dtype=np.int64) - 127).astype(np.float64)).astype(np.float32)
+    S = np.repeat(np.asarray(macro_scales, dtype=np.float32), MACRO_BLOCK // 16, axis=1)
+    v = ((q * mult[..., None]).astype(np.float32) * S[..., None]).astype(np.float32).reshape(n, k)
+    if inverse_rht:
+        v = rht_inverse_butterfly(v.reshape(n, k // 16, 16), rht_signs(seed)).reshape(n, k)
+    return v
+
+
 def code_histogram(codes_packed: np.ndarray) -> np.ndarray:
     """Number of elements carrying each 4-bit code 0..15 in a packed copy
     (reading R14)."""
@@ -614,12 +740,12 @@ def quantize(x, fmt: str, rht: bool = False, rounding: str = "rtne", seed: int =
     """
     m = _as_f32_matrix(x)
     out = {"nonfinite": bool(not np.all(np.isfinite(m)))}
-    if fmt == "nvfp4_2l":
+    outer = {"nvfp4_2l": quantize_copy_two_level, "mxfp4_mbs": quantize_copy_mbs}.get(fmt)
+    if outer is not None:
         if axis in ("row", "both"):
-            out["row"] = quantize_copy_two_level(m, rht, rounding, seed, 0, rht_mode, rows_subset)
+            out["row"] = outer(m, rht, rounding, seed, 0, rht_mode, rows_subset)
         if axis in ("col", "both"):
-            out["col"] = quantize_copy_two_level(np.ascontiguousarray(m.T), rht, rounding, seed, 1,
-                                                 rht_mode, cols_subset)
+            out["col"] = outer(np.ascontiguousarray(m.T), rht, rounding, seed, 1, rht_mode, cols_subset)
         return out
     if axis in ("row", "both"):
         out["row"] = quantize_copy(m, fmt, rht, rounding, seed, 0, rht_mode, keep_y=keep_y,
@@ -637,12 +763,13 @@ def quantize(x, fmt: str, rht: bool = False, rounding: str = "rtne", seed: int =
 def dequantize(codes_packed: np.ndarray, scales: np.ndarray, g, fmt: str,
                inverse_rht: bool = False, seed: int = 0) -> np.ndarray:
     """v_hat = (q * s_b) * g in FP32, two round-to-nearest products in that
-    order (MXFP4: q * 2^e_b); optionally followed by R^T (FP32 butterfly)."""
+    order (E8M0 formats: q * 2^e_b); optionally followed by R^T (FP32
+    butterfly)."""
     b = BLOCK[fmt]
     c = unpack_nibbles(codes_packed)
     n, k = c.shape
     q = code_value(c, fmt).astype(np.float32).reshape(n, k // b, b)
-    if fmt == "mxfp4":
+    if fmt in E8M0_FORMATS:
         e_b = np.asarray(scales, dtype=np.int64) - 127
         mult = np.exp2(e_b.astype(np.float64)).astype(np.float32)
         v = (q * mult[..., None]).astype(np.float32)
@@ -657,14 +784,15 @@ def dequantize(codes_packed: np.ndarray, scales: np.ndarray, g, fmt: str,
 
 def dequantize_f64(codes_packed: np.ndarray, scales: np.ndarray, g, fmt: str,
                    rows=None) -> np.ndarray:
-    """Exact FP64 value of each element: q * s_b * g (MXFP4: q * 2^e_b)."""
+    """Exact FP64 value of each element: q * s_b * g (E8M0 formats:
+    q * 2^e_b)."""
     b = BLOCK[fmt]
     cp = codes_packed if rows is None else codes_packed[rows]
     sc = scales if rows is None else scales[rows]
     c = unpack_nibbles(cp)
     n, k = c.shape
     q = code_value(c, fmt).reshape(n, k // b, b)
-    if fmt == "mxfp4":
+    if fmt in E8M0_FORMATS:
         step = np.exp2((np.asarray(sc, dtype=np.int64) - 127).astype(np.float64))
     else:
         step = e4m3_decode(sc) * np.float64(g)
@@ -709,10 +837,14 @@ def mma_scale_offset(r, kb, nkb: int) -> np.ndarray:
     return tile * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + kb % 4
 
 
-def scales_to_mma_layout(scales: np.ndarray) -> np.ndarray:
+def scales_to_mma_layout(scales: np.ndarray, block: int = 16) -> np.ndarray:
     """Linear [rows][nkb] scales -> the tiled layout (rows padded to 128,
-    blocks to 4, padding bytes 0), as a flat uint8 array."""
+    blocks to 4, padding bytes 0), as a flat uint8 array. The tensor cores read
+    one scale per 16 elements along K: a 32-element block's scale is written
+    for both of its 16-element halves."""
     s = np.asarray(scales, dtype=np.uint8)
+    if block == 32:
+        s = np.repeat(s, 2, axis=1)
     n, nkb = s.shape
     n_p = -(-n // 128) * 128
     nkb_p = -(-nkb // 4) * 4
