@@ -711,6 +711,70 @@ def run_two_level_leg(fq, torch, device, steps, warmup, peaks):
     return out
 
 
+def run_mx_leg(fq, torch, device, steps, warmup, peaks):
+    """The E8M0 formats of the MXFP4 page (Resume technique §2, §2A-§2B) on the
+    activation tensor, RTNE, no RHT, row-wise: MXFP4 on 32- and on 16-element
+    blocks, the overflow-aware rule (OAS), the static macro-block scale (MBS),
+    beside NVFP4: time per fp4q_quantize call (L2 flushed before each) and the
+    SNR of each copy. Then the native block-scaled GEMM at 8192^3 with E8M0
+    scales (MXFP4 32-element blocks, and OAS on 16-element blocks), operands
+    quantised with the RHT along K."""
+    import synth
+    x = synth.activation(ROWS, COLS).to(device)
+    ws = fq.workspace(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    n = ROWS * COLS
+    quant = {}
+    for fmt, bpe, launches in (("mxfp4", 2.5 + 1.0 / 32, 1), ("mxfp4_b16", 2.5 + 1.0 / 16, 1),
+                               ("mxfp4_oas", 2.5 + 1.0 / 16, 1), ("mxfp4_mbs", 2.5 + 1.0 / 16 + 4.0 / 128, 1),
+                               ("nvfp4", B_AMAX + B_QUANT, 2)):
+        q = fq.alloc_copy(ROWS, COLS, fmt, "linear", device)
+        fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q)
+        st, _ = fq.fp4q_stats(ws)
+        evs = []
+        for k in range(warmup + steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q)
+            e1.record(stream)
+            if k >= warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+        us = statistics.fmean(a.elapsed_time(b) for a, b in evs) * 1e3
+        gbs = bpe * n / (us * 1e-6) / 1e9
+        quant[fmt] = {"us": us, "GB/s": gbs, "frac_hbm": gbs / peaks["hbm_gbs"], "bytes_per_element": bpe,
+                      "snr_db": st["snr_db"], "shrink_bias": st["shrink_bias"], "launches": len(evs) * launches,
+                      "status": fq.fp4q_status(ws)}
+    gemm = {}
+    m = GEMM_N
+    a = synth.gemm_operand("a", m, m).to(device)
+    b = synth.gemm_operand("b", m, m).to(device)
+    y = torch.empty(m, m, dtype=torch.bfloat16, device=device)
+    rows = torch.arange(0, m, 64, device=device)
+    ref = a[rows].double() @ b.double().T
+    for fmt in ("mxfp4", "mxfp4_oas"):
+        qa, _ = fq.fp4q_quantize(a, fmt=fmt, rht=True, seed=SEED, layout="mma", ws=ws)
+        qb, _ = fq.fp4q_quantize(b, fmt=fmt, rht=True, seed=SEED, layout="mma", ws=ws)
+        evs = []
+        for k in range(warmup + min(steps, 100)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fq.fp4q_gemm(qa, qb, out=y, ws=ws)
+            e1.record(stream)
+            if k >= warmup:
+                evs.append((e0, e1))
+        torch.cuda.synchronize(device)
+        us = statistics.fmean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3
+        tflops = 2.0 * m ** 3 / (us * 1e-6) / 1e12
+        got = y[rows].double()
+        snr = 10 * math.log10(float((ref * ref).sum()) / float(((got - ref) ** 2).sum()))
+        gemm[fmt] = {"us": us, "tflops": tflops, "frac_of_fp4_peak": tflops / (peaks["bf16_tflops"] * FP4_OVER_BF16),
+                     "snr_db_vs_bf16_product": snr, "launches": len(evs), "status": fq.fp4q_status(ws)}
+    return {"quantize": quant, "gemm_8192": gemm}
+
+
 def run_histogram_leg(fq, torch, device, steps, warmup, peaks):
     """Code utilisation of the activation's three quantised copies ([UFP4]
     Resultados: the RHT raises the effective bucket ratio): the histogram
@@ -772,6 +836,7 @@ def main(argv=None) -> int:
     grad_r = run_grad_leg(fq, torch, device, min(args.steps, 50), args.warmup)
     tl_r = run_two_level_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     hist_r = run_histogram_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
+    mx_r = run_mx_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     e2e_steps = min(args.steps, 100)
     e2e_r = None if args.no_e2e else run_e2e_leg(fq, torch, device, e2e_steps, args.warmup)
     clocks = sampler.stop()
@@ -861,6 +926,12 @@ def main(argv=None) -> int:
     line["code_histogram"] = {
         "workload": "16-code histogram of the activation's E2M1 + RHT copy (16.8 MB of codes); effective "
                     "bucket ratio exp(H)/8 of each way's copy", **hist_r}
+    line["mx_formats_leg"] = {
+        "workload": "activation 8192x4096 BF16, RTNE, no RHT, row-wise: MXFP4 (32-element E8M0 blocks), MXFP4 "
+                    "on 16-element blocks, OAS (16, E8M0), MBS-static (16, E8M0, 8-bit-mantissa scale per "
+                    "128), NVFP4; time per fp4q_quantize call, L2 flushed before each, and each copy's SNR. "
+                    "GEMM 8192^3 with E8M0 scales on the tensor cores (operands + RHT16 along K)",
+        **mx_r}
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -26,9 +26,11 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-FORMATS = {"nvfp4": 0, "mxfp4": 1, "ufp4": 2, "nvfp4_2l": 3}
-BLOCKS = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16, "nvfp4_2l": 16}
-OUTER_BLOCK = 128   # two-level NVFP4: one FP32 scale per 128 elements of a row
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "ufp4": 2, "nvfp4_2l": 3, "mxfp4_b16": 4, "mxfp4_oas": 5, "mxfp4_mbs": 6}
+BLOCKS = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16, "nvfp4_2l": 16, "mxfp4_b16": 16, "mxfp4_oas": 16,
+          "mxfp4_mbs": 16}
+OUTER_BLOCK = 128   # two-level NVFP4 and MBS: one FP32 scale per 128 elements of a row
+OUTER_SCALED = ("nvfp4_2l", "mxfp4_mbs")
 ROUNDING = {"rtne": 0, "sr": 1}
 DTYPES = {torch.bfloat16: 0, torch.float32: 1}
 AXES = {"row": 1, "col": 2, "both": 3}
@@ -137,7 +139,7 @@ class QCopy:
     """One quantised copy (device buffers) of a rows x cols matrix."""
     codes: torch.Tensor          # uint8 [rows, cols/2]
     scales: torch.Tensor         # uint8 [rows, cols/block] (linear) or flat (mma)
-    tensor_scale: torch.Tensor   # float32 [1]; two-level NVFP4: [rows, cols/128] outer-block scales
+    tensor_scale: torch.Tensor   # float32 [1]; two-level NVFP4 and MBS: [rows, cols/128] per-128 scales
     fmt: str
     rows: int
     cols: int
@@ -160,7 +162,7 @@ def alloc_copy(rows: int, cols: int, fmt: str, layout: str = "linear", device=No
         scales = torch.empty(rows, cols // b, dtype=torch.uint8, device=dev)
     else:
         scales = torch.empty(fp4q_scales_bytes(rows, cols, b, 1), dtype=torch.uint8, device=dev)
-    if fmt == "nvfp4_2l":
+    if fmt in OUTER_SCALED:
         ts = torch.empty(rows, cols // OUTER_BLOCK, dtype=torch.float32, device=dev)
     else:
         ts = torch.empty(1, dtype=torch.float32, device=dev)

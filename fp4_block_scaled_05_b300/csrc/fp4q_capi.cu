@@ -105,10 +105,15 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int block_for(int fmt) { return fmt == FP4Q_MXFP4 ? 32 : 16; }
 
 int check_format(int fmt, int block) {
-  if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4 && fmt != FP4Q_UFP4 && fmt != FP4Q_NVFP4_2L) return FP4Q_EINVAL;
+  if (fmt < FP4Q_NVFP4 || fmt > FP4Q_MXFP4_MBS) return FP4Q_EINVAL;
   if (block != block_for(fmt)) return FP4Q_ENOTSUP;
   return FP4Q_OK;
 }
+
+// formats with one FP32 scale per 128 elements of a row in place of the tensor scale
+bool outer_scaled(int fmt) { return fmt == FP4Q_NVFP4_2L || fmt == FP4Q_MXFP4_MBS; }
+// formats with a per-tensor FP32 scale, set by an amax pass
+bool tensor_scaled(int fmt) { return fmt == FP4Q_NVFP4 || fmt == FP4Q_UFP4; }
 
 int check_qtensor(const fp4q_qtensor* q, bool empty = false) {
   if (!q || !q->tensor_scale) return FP4Q_EINVAL;
@@ -149,7 +154,7 @@ int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt
   if (cols % 16) return FP4Q_EINVAL;     // source rows start on 32-byte boundaries
   if ((axis & FP4Q_ROWWISE) && cols % block) return FP4Q_EINVAL;
   if ((axis & FP4Q_COLWISE) && rows % block) return FP4Q_EINVAL;
-  if (fmt == FP4Q_NVFP4_2L) {
+  if (outer_scaled(fmt)) {
     if (axis & FP4Q_COLWISE) return FP4Q_ENOTSUP;     // row-wise copy only in this version
     if (cols % 128) return FP4Q_EINVAL;               // whole outer blocks per row
   }
@@ -172,8 +177,8 @@ int fp4q_workspace_init(void* workspace, void* stream) {
 size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout) {
   if (rows < 0 || cols < 0 || block <= 0) return 0;
   const int64_t nkb = cols / block;
-  if (scale_layout == FP4Q_SCALES_MMA) {
-    return (size_t)(((rows + 127) / 128) * 128) * (size_t)(((nkb + 3) / 4) * 4);
+  if (scale_layout == FP4Q_SCALES_MMA) {     // one scale per 16 elements along the row
+    return (size_t)(((rows + 127) / 128) * 128) * (size_t)(((cols / 16 + 3) / 4) * 4);
   }
   return (size_t)rows * (size_t)nkb;
 }
@@ -182,9 +187,9 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
               uint64_t seed, int axis, void* workspace, size_t ws_bytes, void* stream) {
   const int rc = check_source(src, dtype, rows, cols, fmt, block, rht, axis, workspace, ws_bytes);
   if (rc) return rc;
-  // power-of-two block scales (MXFP4) or per-outer-block scales (two-level
-  // NVFP4): no tensor amax
-  if (fmt == FP4Q_MXFP4 || fmt == FP4Q_NVFP4_2L) return FP4Q_OK;
+  // power-of-two block scales (the MXFP4 formats) or per-128-element scales
+  // (two-level NVFP4, MBS): no tensor amax
+  if (!tensor_scaled(fmt)) return FP4Q_OK;
   fp4q::QuantArgs a{};
   a.src = src;
   a.dtype = dtype;
@@ -212,11 +217,11 @@ int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols, int fm
   if ((axis & FP4Q_COLWISE) && (rc = check_qtensor(col_out, empty))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   // padding bytes of the tiled scale layout are defined as 0
-  if (!empty && (axis & FP4Q_ROWWISE) && row_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(rows, cols / block)) {
+  if (!empty && (axis & FP4Q_ROWWISE) && row_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(rows, cols / 16)) {
     if (cudaMemsetAsync(row_out->scales, 0, fp4q_scales_bytes(rows, cols, block, FP4Q_SCALES_MMA), s) != cudaSuccess)
       return FP4Q_ECUDA;
   }
-  if (!empty && (axis & FP4Q_COLWISE) && col_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(cols, rows / block)) {
+  if (!empty && (axis & FP4Q_COLWISE) && col_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(cols, rows / 16)) {
     if (cudaMemsetAsync(col_out->scales, 0, fp4q_scales_bytes(cols, rows, block, FP4Q_SCALES_MMA), s) != cudaSuccess)
       return FP4Q_ECUDA;
   }
@@ -245,7 +250,7 @@ int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, 
   if (inverse_rht != 0 && inverse_rht != 1) return FP4Q_EINVAL;
   if (dst_dtype != FP4Q_BF16 && dst_dtype != FP4Q_F32) return FP4Q_EINVAL;
   if (rows < 0 || cols < 0 || cols % block) return FP4Q_EINVAL;
-  if (fmt == FP4Q_NVFP4_2L && cols % 128) return FP4Q_EINVAL;
+  if (outer_scaled(fmt) && cols % 128) return FP4Q_EINVAL;
   if (rows == 0 || cols == 0) return FP4Q_OK;
   if (!dst || !aligned(dst, 16)) return FP4Q_EINVAL;
   fp4q::DequantArgs a{};
@@ -269,7 +274,8 @@ int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, 
                        int fmt, void* Y, int out_dtype, void* scratch, size_t scratch_bytes, void* stream) {
   int rc = check_format(fmt, block_for(fmt));
   if (rc) return rc;
-  if (fmt == FP4Q_NVFP4_2L) return FP4Q_ENOTSUP;
+  // per-128-element scales: no single alpha; MBS values also need more than BF16's 8 significant bits
+  if (outer_scaled(fmt)) return FP4Q_ENOTSUP;
   if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
   if (out_dtype != FP4Q_BF16 && out_dtype != FP4Q_F32) return FP4Q_EINVAL;
   if (M <= 0 || N <= 0 || K <= 0 || K % block_for(fmt)) return FP4Q_EINVAL;
@@ -392,9 +398,10 @@ namespace {
 int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K, int fmt,
                 void* Y, int out_dtype, void* workspace, size_t ws_bytes, uint64_t timeout_ns, int skip,
                 void* stream) {
-  if (fmt == FP4Q_UFP4 || fmt == FP4Q_NVFP4_2L) return FP4Q_ENOTSUP;
-  if (fmt != FP4Q_NVFP4 && fmt != FP4Q_MXFP4) return FP4Q_EINVAL;
-  if (fmt == FP4Q_MXFP4) return FP4Q_ENOTSUP;
+  if (fmt < FP4Q_NVFP4 || fmt > FP4Q_MXFP4_MBS) return FP4Q_EINVAL;
+  // E2M1 operands with E4M3 or E8M0 block scales; UFP4 has no FP4 tensor-core
+  // type and per-128-element scales vary along K
+  if (fmt == FP4Q_UFP4 || outer_scaled(fmt)) return FP4Q_ENOTSUP;
   int rc;
   if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
   if (A->scale_layout != FP4Q_SCALES_MMA || B->scale_layout != FP4Q_SCALES_MMA) return FP4Q_EINVAL;

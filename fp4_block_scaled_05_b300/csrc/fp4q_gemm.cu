@@ -1,11 +1,14 @@
-// Block-scaled NVFP4 GEMM on the 5th-generation tensor cores (sm_103a).
+// Block-scaled FP4 GEMM on the 5th-generation tensor cores (sm_103a).
 //
 // Y[M][N] = (sum_k A[m][k] * B[n][k]) * g_A * g_B, with A, B row-wise NVFP4
 // copies (E2M1 codes, one E4M3 scale per 16 elements along K, one FP32 tensor
 // scale each): "Le Architetture Normalizzate sono Nativamente a 4 Bit",
 // Metodologia (NVFP4 consumed natively by Blackwell tensor cores); "Unveiling
 // the Potential of Quantization with MXFP4 ...", Resume technique §2B (scale
-// factors handled beside the dense tensor-core math).
+// factors handled beside the dense tensor-core math). The same kernel takes
+// the MXFP4 formats (E8M0 scales, g = 1): the instruction's scale type
+// switches to UE8M0, and a 32-element block's scale sits in the scale layout
+// once for each of its 16-element halves.
 //
 // Structure (one persistent CTA per SM, 192 threads, clusters of up to 4 CTAs
 // that share each B tile through TMA multicast):
@@ -126,10 +129,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor for kind::mxf4nvf4 (dense, K = 64): A and B E2M1
-// (format 1) K-major, scale type UE4M3, N >> 3 in bits 17-22, M >> 4 in 24-28,
-// scale-factor IDs 0.
-__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n) {
-  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+// (format 1) K-major, N >> 3 in bits 17-22, the scale type in bit 23 (0 UE4M3,
+// 1 UE8M0), M >> 4 in 24-28, scale-factor IDs 0. With scale_vec::4X every 16
+// elements along K carry a scale of either type.
+__host__ __device__ constexpr uint32_t idesc_nvf4(int m, int n, bool ue8m0 = false) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) |
+         ((uint32_t)(m >> 4) << 24);
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -190,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
                  const float* __restrict__ g_a, const float* __restrict__ g_b, void* __restrict__ y,
-                 int M, int N, int K, Workspace* ws, uint64_t timeout_ns, int skip_first_stage) {
+                 int M, int N, int K, Workspace* ws, uint64_t timeout_ns, int skip_first_stage,
+                 int ue8m0) {
   using C = Cfg<BN>;
   constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
   constexpr int kBPiece = BN / CL;                  // rows of B each CTA loads
@@ -309,7 +315,7 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_nvf4(BM, BN);
+      const uint32_t idesc = ue8m0 ? idesc_nvf4(BM, BN, true) : idesc_nvf4(BM, BN);
       // Descriptors of stage 0; a stage's descriptors differ only in the start
       // address field (bits 0-13, address >> 4), so each is this base plus the
       // stage offset >> 4 (shared addresses stay below 2^18: no carry out).
@@ -455,7 +461,8 @@ cudaError_t launch(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStream_
   cfg.gridDim = dim3(clusters * CL, 1, 1);
   e = cudaLaunchKernelEx(&cfg, k, ma, mb, (const uint8_t*)a.a.scales, (const uint8_t*)a.b.scales,
                          (const float*)a.a.tensor_scale, (const float*)a.b.tensor_scale, a.y, (int)a.m,
-                         (int)a.n, (int)a.k, static_cast<Workspace*>(a.ws), timeout_ns, skip);
+                         (int)a.n, (int)a.k, static_cast<Workspace*>(a.ws), timeout_ns, skip,
+                         a.fmt == 0 ? 0 : 1);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -480,7 +487,9 @@ cudaError_t launch_cl(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStre
 }  // namespace
 
 cudaError_t run_gemm_ex(const GemmArgs& a, uint64_t timeout_ns, int skip_first_stage, cudaStream_t s) {
-  if (a.fmt != 0) return cudaErrorNotSupported;
+  // NVFP4 (E4M3 scales) or the MXFP4 formats on 32- or 16-element blocks
+  // (E8M0 scales; a 32-element block's scale is stored for both halves)
+  if (a.fmt != 0 && a.fmt != 1 && a.fmt != 4 && a.fmt != 5) return cudaErrorNotSupported;
   const bool f32 = a.out_dtype == 1;
   if (a.n % 256 == 0) return f32 ? launch_cl<256, true>(a, timeout_ns, skip_first_stage, s)
                                  : launch_cl<256, false>(a, timeout_ns, skip_first_stage, s);

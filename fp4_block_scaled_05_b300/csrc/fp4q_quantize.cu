@@ -17,9 +17,10 @@
 //    memory ring, one read of the source serving both copies
 //    (amax_tiles_kernel when the RHT makes the two copies' amax differ,
 //    quant_tiles_kernel).
-// MXFP4 (power-of-two block scales) and two-level NVFP4 (a scale per
-// 128-element outer block, row-wise only) have no tensor scale, so they skip
-// the amax pass.
+// The E8M0 formats (MXFP4 on 32- or 16-element blocks, its overflow-aware
+// variant, MBS with its 128-element macro scale) and two-level NVFP4 (a scale
+// per 128-element outer block) have no tensor scale, so they skip the amax
+// pass.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -33,8 +34,8 @@ namespace {
 
 // Empty input: write the tensor scales and empty statistics, nothing else.
 __global__ void quantize_empty_kernel(int fmt, int axis, float* ts_row, float* ts_col, Workspace* ws) {
-  const float g = (fmt == 1) ? 1.f : 0.f;
-  if (fmt == 3) ts_row = ts_col = nullptr;     // two-level: the outer-scale array is empty
+  const float g = (fmt == 0 || fmt == 2) ? 0.f : 1.f;       // 1.0 for the E8M0 formats
+  if (fmt == 3 || fmt == 6) ts_row = ts_col = nullptr;     // per-128-element scales: the array is empty
   ws->stat_nparts = 0u;
   ws->copies = (unsigned)axis;
   ws->tensor_scale[0] = g;
@@ -75,8 +76,7 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
   // launch cost less; measured on B300: 12.4 vs 14.4 us at 1M elements) and
   // ties at 2^25; above that the two launches are faster, because the second
   // launch's grid restarts on chunks the amax pass left in L2.
-  // MXFP4 (power-of-two block scales) and two-level NVFP4 (outer-block
-  // scales) have no tensor amax: one pass
+  // the E8M0 formats and two-level NVFP4 have no tensor amax: one pass
   const bool tensor_scaled = a.fmt == 0 || a.fmt == 2;
   if (tensor_scaled && !a.amax_ready && a.axis == 1 && a.rows * a.cols < (int64_t(1) << 25)) {
     // the two-launch path if a co-resident grid cannot be had

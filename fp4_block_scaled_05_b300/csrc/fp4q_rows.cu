@@ -291,6 +291,16 @@ __device__ __forceinline__ void make_sign_words(uint32_t smask, uint32_t (&sgn)[
 }
 
 // ---- per-block quantisation --------------------------------------------------------
+// Formats (template argument FMT): 0 NVFP4, 1 MXFP4 (32-element blocks),
+// 2 UFP4, 3 two-level NVFP4, 4 MXFP4 on 16-element blocks, 5 the same with the
+// overflow-aware exponent rule, 6 MBS-static (16-element E8M0 blocks under a
+// 128-element macro scale).
+template <int FMT> constexpr bool kE8M0 = FMT == 1 || FMT == 4 || FMT == 5 || FMT == 6;
+// formats with a per-tensor FP32 scale (and so an amax pass)
+template <int FMT> constexpr bool kTensorScaled = FMT == 0 || FMT == 2;
+// formats whose "tensor scale" array holds one FP32 scale per 128 elements
+template <int FMT> constexpr bool kOuterScaled = FMT == 3 || FMT == 6;
+
 struct Sums {        // per-thread running sums of one copy
   Kahan bias, sig, err;
   double sig64 = 0.0, err64 = 0.0;
@@ -499,6 +509,20 @@ __device__ __forceinline__ uint32_t sr_pair(f2 Y, uint32_t w0, uint32_t w1, f2& 
   else return sr_pair_e2m1(Y, w0, w1, D);
 }
 
+// MBS-static macro scale: alpha / 6 rounded to nearest, ties to even, on
+// FP32's grid with 8 fraction bits (the low 15 bits of the FP32 encoding zero).
+// The quotient q is correctly rounded and alpha - 6 q is exact (fma), so when
+// q falls on a tie of the 8-bit grid the remainder's sign says on which side
+// the exact quotient lies.
+__device__ __forceinline__ float mbs_macro_scale(float alpha) {
+  const float q = __fdiv_rn(alpha, 6.f);
+  const float rem = __fmaf_rn(-6.f, q, alpha);
+  const uint32_t b = __float_as_uint(q);
+  const uint32_t low = b & 0x7FFFu, base = b - low;
+  const bool up = low > 0x4000u || (low == 0x4000u && (rem > 0.f || (rem == 0.f && (base & 0x8000u))));
+  return __uint_as_float(base + (up ? 0x8000u : 0u));
+}
+
 // Quantise one block of NP pairs (NP = 8: a 16-block, NP = 16: an MXFP4
 // 32-block) whose first element has index e0 in the copy. Writes NP/4 code
 // words and returns the scale code; adds the block's sums to bsum/ssum/esum
@@ -506,7 +530,8 @@ __device__ __forceinline__ uint32_t sr_pair(f2 Y, uint32_t w0, uint32_t w1, f2& 
 template <int FMT, bool SR, int NP>
 __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint64_t e0, const PhiloxKey& pk,
                                                 uint32_t* cw, float& bsum, float& ssum, float& esum,
-                                                Sums& acc, uint32_t& nonfinite, uint32_t axis = 0u) {
+                                                Sums& acc, uint32_t& nonfinite, uint32_t axis = 0u,
+                                                float s_macro = 1.f) {
   float m = 0.f;
 #pragma unroll
   for (int j = 0; j < NP; ++j) {
@@ -519,13 +544,21 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
   uint32_t scode;
   float r, s2 = 0.f;
   int e2 = 0;
-  if constexpr (FMT == 1) {
+  if constexpr (kE8M0<FMT>) {
+    // OCP rule: e = floor(log2 m) - 2 puts m / 2^e in [4, 8); the overflow-aware
+    // rule (FMT 5) adds one when m's significand is above 1.75, which puts
+    // m / 2^e in (3.5, 7]
     const uint32_t mb = __float_as_uint(m);
     const uint32_t E = mb >> 23;
-    const int fl = E ? (int)E - 127 : (mb ? (31 - __clz((int)mb)) - 149 : -200);
+    const int msb = mb ? 31 - __clz((int)mb) : 0;
+    int fl = E ? (int)E - 127 : (mb ? msb - 149 : -200);
+    if constexpr (FMT == 5) {
+      const uint32_t frac = E ? (mb & 0x7FFFFFu) : ((mb << (23 - msb)) & 0x7FFFFFu);
+      if (frac > 0x600000u) ++fl;
+    }
     const int e = max(-127, min(127, fl - 2));
     scode = (uint32_t)(e + 127);
-    r = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 125]
+    r = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 126]
     e2 = 2 * e;
   } else {
     if (cx.g == 0.f) {
@@ -576,8 +609,9 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
   f2_split(S2, s0, s1);
   const float bs = __fadd_rn(b0, b1), es = __fadd_rn(e0f, e1f), ys = __fadd_rn(s0, s1);
   bsum = __fadd_rn(bsum, bs);
-  if constexpr (FMT == 1) {
-    const double sc = __longlong_as_double((long long)(1023 + e2) << 52);
+  if constexpr (kE8M0<FMT>) {
+    double sc = __longlong_as_double((long long)(1023 + e2) << 52);
+    if constexpr (FMT == 6) sc *= (double)s_macro * (double)s_macro;
     acc.sig64 += (double)ys * sc;
     acc.err64 += (double)es * sc;
   } else if (scode == 0 && cx.g > 0.f) {
@@ -749,6 +783,10 @@ __device__ __forceinline__ void quant_two16_vals(const f2* Q, float m0, float m1
   }
 }
 
+// The tensor cores read one scale per 16 elements along K: in the MMA layout a
+// 32-element block's scale (DUP) is written for both of its halves, as one
+// 2-byte store (the pair starts on an even byte).
+template <bool DUP = false>
 __device__ __forceinline__ void put_scale(const CopyOut& o, const Flat& f, uint64_t blk, uint32_t sc) {
   if (!o.mma) {
     o.scales[blk] = (uint8_t)sc;
@@ -761,7 +799,12 @@ __device__ __forceinline__ void put_scale(const CopyOut& o, const Flat& f, uint6
     r = blk / f.nkb.d;
   }
   const uint64_t kb = blk - r * f.nkb.d;
-  o.scales[mma_scale_offset((int64_t)r, (int64_t)kb, o.nkb_p)] = (uint8_t)sc;
+  if constexpr (DUP) {
+    *reinterpret_cast<uint16_t*>(o.scales + mma_scale_offset((int64_t)r, (int64_t)(2 * kb), o.nkb_p)) =
+        (uint16_t)(sc | (sc << 8));
+  } else {
+    o.scales[mma_scale_offset((int64_t)r, (int64_t)kb, o.nkb_p)] = (uint8_t)sc;
+  }
 }
 
 // ---- per-thread work on its 32 elements of a ring slot ---------------------------------
@@ -823,8 +866,65 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       const uint32_t sc = quant_block<FMT, SR, 16>(Q, cx, (uint64_t)e, pk, cw, bsum, ssum, esum,
                                                     acc, nonfinite);
       *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      put_scale(o, f, (uint64_t)e / 32, sc);
+      put_scale<true>(o, f, (uint64_t)e / 32, sc);
       acc.bias.add(bsum);
+    }
+  } else if constexpr (FMT == 4 || FMT == 5) {
+    // E8M0 scales on 16-element blocks
+    float bsum = 0.f, ssum = 0.f, esum = 0.f;
+    f2 Q[16];
+    if (nb16 >= 1) load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
+    if (nb16 == 2) load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (h < nb16) {
+        uint32_t cw[2];
+        const uint32_t sc = quant_block<FMT, SR, 8>(Q + 8 * h, cx, (uint64_t)(e + 16 * h), pk, cw, bsum, ssum,
+                                                     esum, acc, nonfinite);
+        *reinterpret_cast<uint2*>(o.codes + (e + 16 * h) / 2) = make_uint2(cw[0], cw[1]);
+        put_scale(o, f, (uint64_t)e / 16 + h, sc);
+      }
+    }
+    acc.bias.add(bsum);
+  } else if constexpr (FMT == 6) {
+    // MBS-static ("Unveiling the Potential of Quantization with MXFP4 ...",
+    // Resume technique §2B): the four threads of a 128-element macro block
+    // (lanes 4k .. 4k+3; rows hold whole macro blocks) share its amax, which
+    // sets the macro scale S (8 mantissa bits); the values are taken to units
+    // of S (w = v * (1/S)) and quantised as 16-element E8M0 blocks. Every lane
+    // takes part in the shuffles.
+    f2 Q[16];
+    float m = 0.f;
+    if (nb16 == 2) {
+      load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
+      load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float a, b;
+        f2_split(Q[j], a, b);
+        m = max3_abs_nan(m, a, b);
+      }
+    }
+    m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    if (nb16 == 2) {
+      const float S = mbs_macro_scale(m);
+      float rs = (S == 0.f) ? 0.f : __frcp_rn(S);
+      if (rs > FLT_MAX) rs = FLT_MAX;
+      const f2 RS = f2_make(rs, rs);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) Q[j] = f2_mul(Q[j], RS);
+      float bsum = 0.f, ssum = 0.f, esum = 0.f;
+      uint32_t cw[4];
+      const uint32_t s0 = quant_block<FMT, SR, 8>(Q, cx, (uint64_t)e, pk, cw, bsum, ssum, esum, acc, nonfinite,
+                                                   0u, S);
+      const uint32_t s1 = quant_block<FMT, SR, 8>(Q + 8, cx, (uint64_t)e + 16, pk, cw + 2, bsum, ssum, esum, acc,
+                                                   nonfinite, 0u, S);
+      *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      put_scale(o, f, (uint64_t)e / 16, s0);
+      put_scale(o, f, (uint64_t)e / 16 + 1, s1);
+      acc.bias.add(bsum);
+      if ((threadIdx.x & 3u) == 0u) o.tensor_scale[e / 128] = S;
     }
   } else if constexpr (FMT == 3) {
     // Two-level NVFP4 (TetraJet-v2, Riepilogo Tecnico §2A): the four threads of
@@ -1012,7 +1112,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
 
   // ---- statistics: one partial per CTA (summed on the host by fp4q_stats) ----
   if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
-  if constexpr (FMT == 1 || FMT == 3) {   // FP64 sums (absolute units)
+  if constexpr (!kTensorScaled<FMT>) {   // FP64 sums (absolute units)
     double p[3] = {acc.bias.value(), acc.sig64, acc.err64};
     if constexpr (FMT == 3) outer_stats_value(acc, p[1], p[2]);
 #pragma unroll
@@ -1031,10 +1131,10 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   if (blockIdx.x == 0 && tid == 0) {
     ws->stat_nparts = gridDim.x;
     ws->copies = 1u;
-    ws->tensor_scale[0] = (FMT == 1 || FMT == 3) ? 1.f : cx.g;
+    ws->tensor_scale[0] = kTensorScaled<FMT> ? cx.g : 1.f;
     ws->qmax = kQmax;
     ws->n = (double)f.n;
-    if (FMT != 3 && o.tensor_scale) *o.tensor_scale = (FMT == 1) ? 1.f : cx.g;
+    if (!kOuterScaled<FMT> && o.tensor_scale) *o.tensor_scale = kTensorScaled<FMT> ? cx.g : 1.f;
   }
 }
 
@@ -1218,8 +1318,13 @@ __device__ __forceinline__ void load_col32(const uint8_t* slot, int row0, int co
   }
 }
 
+template <bool DUP = false>
 __device__ __forceinline__ void put_scale_rk(const CopyOut& o, int64_t row, int64_t kb, uint32_t sc) {
-  o.scales[o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb] = (uint8_t)sc;
+  if (DUP && o.mma) {
+    *reinterpret_cast<uint16_t*>(o.scales + mma_scale_offset(row, 2 * kb, o.nkb_p)) = (uint16_t)(sc | (sc << 8));
+  } else {
+    o.scales[o.mma ? mma_scale_offset(row, kb, o.nkb_p) : row * o.nkb + kb] = (uint8_t)sc;
+  }
 }
 
 // 16 code bytes of one row of a copy. A row starts on an 8-byte boundary (its
@@ -1344,7 +1449,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
   cc.cx = Ctx{1.f, 0.f, 0.f};
   cr.dv = Divider{};
   cc.dv = Divider{};
-  if constexpr (FMT != 1) {
+  if constexpr (kTensorScaled<FMT>) {
     if (ROWS) {
       cr.cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
       cr.dv.init(cr.cx.d);
@@ -1385,9 +1490,25 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
             const uint32_t sc = quant_block<FMT, SR, 16>(Q, cr.cx, (uint64_t)e, pk, cw, bsum, ssum, esum,
                                                           cr.acc, nonfinite, 0u);
             store_codes16(orow.codes + row * orow.ld + col / 2, cw);
-            put_scale_rk(orow, row, col / 32, sc);
+            put_scale_rk<true>(orow, row, col / 32, sc);
             cr.acc.bias.add(bsum);
           }
+        } else if constexpr (FMT == 4 || FMT == 5) {
+          float bsum = 0.f, ssum = 0.f, esum = 0.f;
+          f2 Q[16];
+          if (nb16 >= 1) load_block16<F32, RHT>(sg, 0, sgn, Q);
+          if (nb16 == 2) load_block16<F32, RHT>(sg, F32 ? 4 : 2, sgn, Q + 8);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h < nb16) {
+              uint32_t cw[2];
+              const uint32_t sc = quant_block<FMT, SR, 8>(Q + 8 * h, cr.cx, (uint64_t)(e + 16 * h), pk, cw, bsum,
+                                                           ssum, esum, cr.acc, nonfinite, 0u);
+              *reinterpret_cast<uint2*>(orow.codes + row * orow.ld + col / 2 + 8 * h) = make_uint2(cw[0], cw[1]);
+              put_scale_rk(orow, row, col / 16 + h, sc);
+            }
+          }
+          cr.acc.bias.add(bsum);
         } else if (nb16 == 2) {
           uint32_t cw[4], sc[2];
           f2 b2 = 0ull, s2 = 0ull, e2 = 0ull;
@@ -1425,7 +1546,35 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
           const uint32_t sc = quant_block<FMT, SR, 16>(Q, cc.cx, (uint64_t)(crow * g.rows + ccol), pk, cw,
                                                         bsum, ssum, esum, cc.acc, nonfinite, 1u);
           *reinterpret_cast<uint4*>(ocol.codes + crow * ocol.ld + ccol / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-          put_scale_rk(ocol, crow, ccol / 32, sc);
+          put_scale_rk<true>(ocol, crow, ccol / 32, sc);
+          cc.acc.bias.add(bsum);
+        }
+      } else if constexpr (FMT == 4 || FMT == 5) {
+        const int pair = tid & 63, cb = tid >> 6;         // two columns x 16 rows, a block each
+        if (16 * cb < vr && 2 * pair < vc) {
+          float a[16], b[16];
+          load_col_pair<F32, RHT>(slot, 16 * cb, pair, smask, a, b);
+          f2 Q[16];
+          if constexpr (RHT) {
+            rht16_pairs(a, Q);
+            rht16_pairs(b, Q + 8);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              Q[j] = f2_make(a[2 * j], a[2 * j + 1]);
+              Q[j + 8] = f2_make(b[2 * j], b[2 * j + 1]);
+            }
+          }
+          const int64_t ca = c0 + 2 * pair, rw = r0 + 16 * cb;
+          float bsum = 0.f, ssum = 0.f, esum = 0.f;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t cw[2];
+            const uint32_t sc = quant_block<FMT, SR, 8>(Q + 8 * h, cc.cx, (uint64_t)((ca + h) * g.rows + rw), pk,
+                                                         cw, bsum, ssum, esum, cc.acc, nonfinite, 1u);
+            *reinterpret_cast<uint2*>(ocol.codes + (ca + h) * ocol.ld + rw / 2) = make_uint2(cw[0], cw[1]);
+            put_scale_rk(ocol, ca + h, rw / 16, sc);
+          }
           cc.acc.bias.add(bsum);
         }
       } else {
@@ -1482,7 +1631,7 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
 
   // ---- statistics: one partial per CTA and copy (summed on the host) ----
   if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
-  if constexpr (FMT == 1) {
+  if constexpr (kE8M0<FMT>) {
     const double p[2][3] = {{cr.acc.bias.value(), cr.acc.sig64, cr.acc.err64},
                             {cc.acc.bias.value(), cc.acc.sig64, cc.acc.err64}};
 #pragma unroll
@@ -1505,12 +1654,12 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
   if (blockIdx.x == 0 && tid == 0) {
     ws->stat_nparts = gridDim.x;
     ws->copies = (ROWS ? 1u : 0u) | 2u;
-    ws->tensor_scale[0] = (FMT == 1) ? 1.f : cr.cx.g;
-    ws->tensor_scale[1] = (FMT == 1) ? 1.f : cc.cx.g;
+    ws->tensor_scale[0] = kE8M0<FMT> ? 1.f : cr.cx.g;
+    ws->tensor_scale[1] = kE8M0<FMT> ? 1.f : cc.cx.g;
     ws->qmax = kQmax;
     ws->n = (double)g.rows * (double)g.cols;
-    if (ROWS && orow.tensor_scale) *orow.tensor_scale = (FMT == 1) ? 1.f : cr.cx.g;
-    if (ocol.tensor_scale) *ocol.tensor_scale = (FMT == 1) ? 1.f : cc.cx.g;
+    if (ROWS && orow.tensor_scale) *orow.tensor_scale = kE8M0<FMT> ? 1.f : cr.cx.g;
+    if (ocol.tensor_scale) *ocol.tensor_scale = kE8M0<FMT> ? 1.f : cc.cx.g;
   }
 }
 
@@ -1658,7 +1807,7 @@ __device__ __forceinline__ void levels2(uint32_t byte, float& lo, float& hi) {
 
 template <int FMT>
 __device__ __forceinline__ float block_scale_value(uint32_t sc) {
-  if constexpr (FMT == 1) {   // E8M0: 2^(sc - 127); code 0 is 2^-127 (subnormal)
+  if constexpr (kE8M0<FMT>) {   // E8M0: 2^(sc - 127); code 0 is 2^-127 (subnormal)
     return sc ? __uint_as_float(sc << 23) : __uint_as_float(0x00400000u);
   } else {
     return e4m3_to_f32(sc);
@@ -1679,7 +1828,7 @@ __device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float 
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       f2 r = f2_mul(f2_make(q[2 * j], q[2 * j + 1]), S);
-      if (FMT != 1) r = f2_mul(r, G);
+      if (FMT != 1 && FMT != 4 && FMT != 5) r = f2_mul(r, G);
       f2_split(r, v[2 * j], v[2 * j + 1]);
     }
   }
@@ -1713,11 +1862,13 @@ __device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float 
   }
 }
 
+// DUP: a 32-element block, whose scale the MMA layout holds for both halves
+template <bool DUP = false>
 __device__ __forceinline__ uint32_t get_scale(const CopyOut& q, const Flat& f, uint64_t blk) {
   if (!q.mma) return __ldg(q.scales + blk);
   const uint64_t r = f.small ? (uint64_t)f.nkb.div((uint32_t)blk) : blk / f.nkb.d;
   const uint64_t kb = blk - r * f.nkb.d;
-  return __ldg(q.scales + mma_scale_offset((int64_t)r, (int64_t)kb, q.nkb_p));
+  return __ldg(q.scales + mma_scale_offset((int64_t)r, (int64_t)(DUP ? 2 * kb : kb), q.nkb_p));
 }
 
 template <int FMT, bool OUT_F32, bool IRHT>
@@ -1735,7 +1886,7 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
   }
   constexpr int B = (FMT == 1) ? 32 : 16;
   constexpr int ES = OUT_F32 ? 4 : 2;
-  const float g = (FMT == 1 || FMT == 3) ? 1.f : __ldg(q.tensor_scale);
+  const float g = kTensorScaled<FMT> ? __ldg(q.tensor_scale) : 1.f;
   const int64_t nseg = (f.n + 31) / 32;
   uint8_t* out = static_cast<uint8_t*>(dst);
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -1747,26 +1898,30 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
     if (f.n - e >= 32) {
       const uint4 cw = __ldg(reinterpret_cast<const uint4*>(q.codes + e / 2));
       if constexpr (B == 32) {
-        const float sv = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 32));
+        const float sv = block_scale_value<FMT>(get_scale<true>(q, f, (uint64_t)e / 32));
         deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, sv, g, sgn, out + e * ES);
         deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, sv, g, sgn, out + (e + 16) * ES);
       } else {
         const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16));
         const float s1 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16 + 1));
-        const float gs = (FMT == 3) ? __ldg(q.tensor_scale + e / 128) : g;   // two-level: outer-block scale
+        // two-level NVFP4 and MBS: the scale of the element's 128-element block
+        const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + e / 128) : g;
         deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
         deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, s1, gs, sgn, out + (e + 16) * ES);
       }
     } else {   // a lone 16-block at the very end (16-element formats only)
       const uint2 cw = __ldg(reinterpret_cast<const uint2*>(q.codes + e / 2));
       const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / B));
-      const float gs = (FMT == 3) ? __ldg(q.tensor_scale + e / 128) : g;
+      const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + e / 128) : g;
       deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
     }
   }
 }
 
 // ---- host side ---------------------------------------------------------------------
+// Scale vectors per row in the MMA layout (one per 16 elements, padded to 4).
+int64_t mma_vectors_padded(int64_t cols) { return (cols / 16 + 3) / 4 * 4; }
+
 Flat make_flat(const void* src, int64_t rows, int64_t cols, int block) {
   Flat f{};
   f.src = static_cast<const uint8_t*>(src);
@@ -1898,7 +2053,7 @@ CopyOut tile_copy(const QOut& q, int64_t crows, int64_t ccols, int block) {
   o.mma = q.scale_layout;
   o.ld = ccols / 2;
   o.nkb = ccols / block;
-  o.nkb_p = (o.nkb + 3) / 4 * 4;
+  o.nkb_p = mma_vectors_padded(ccols);
   return o;
 }
 
@@ -1965,7 +2120,7 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
   o.mma = a.row.scale_layout;
   o.ld = a.cols / 2;
   o.nkb = a.cols / block;
-  o.nkb_p = (o.nkb + 3) / 4 * 4;
+  o.nkb_p = mma_vectors_padded(a.cols);
   Workspace* ws = static_cast<Workspace*>(a.ws);
   const bool f32 = a.dtype == 1;
   const int sr = a.rounding == 1;
@@ -1978,6 +2133,12 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
                        : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s);
     case 3: return f32 ? dispatch_quant_rows<3, true>(a.rht, sr, f, a.seed, o, ws, s)
                        : dispatch_quant_rows<3, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 4: return f32 ? dispatch_quant_rows<4, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<4, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 5: return f32 ? dispatch_quant_rows<5, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<5, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 6: return f32 ? dispatch_quant_rows<6, true>(a.rht, sr, f, a.seed, o, ws, s)
+                       : dispatch_quant_rows<6, false>(a.rht, sr, f, a.seed, o, ws, s);
     default: return cudaErrorNotSupported;
   }
 }
@@ -1992,12 +2153,15 @@ cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s) {
   q.mma = a.q.scale_layout;
   q.ld = a.cols / 2;
   q.nkb = a.cols / block;
-  q.nkb_p = (q.nkb + 3) / 4 * 4;
+  q.nkb_p = mma_vectors_padded(a.cols);
   switch (a.fmt) {
     case 0: return launch_dequant_rows<0>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 1: return launch_dequant_rows<1>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 2: return launch_dequant_rows<2>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 3: return launch_dequant_rows<3>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 4: return launch_dequant_rows<4>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 5: return launch_dequant_rows<5>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 6: return launch_dequant_rows<6>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     default: return cudaErrorNotSupported;
   }
 }
@@ -2011,7 +2175,7 @@ cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s) {
   o.mma = a.row.scale_layout;
   o.ld = a.cols / 2;
   o.nkb = a.cols / 16;
-  o.nkb_p = (o.nkb + 3) / 4 * 4;
+  o.nkb_p = mma_vectors_padded(a.cols);
   Workspace* ws = static_cast<Workspace*>(a.ws);
   const bool f32 = a.dtype == 1;
   const int sr = a.rounding == 1;
@@ -2050,7 +2214,11 @@ cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s) {
                        : dispatch_quant_tiles<1, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
     case 2: return f32 ? dispatch_quant_tiles<2, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
                        : dispatch_quant_tiles<2, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
-    default: return cudaErrorNotSupported;     // the two-level format is row-wise only
+    case 4: return f32 ? dispatch_quant_tiles<4, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
+                       : dispatch_quant_tiles<4, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+    case 5: return f32 ? dispatch_quant_tiles<5, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
+                       : dispatch_quant_tiles<5, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
+    default: return cudaErrorNotSupported;     // the two-level and MBS formats are row-wise only
   }
 }
 

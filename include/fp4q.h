@@ -50,9 +50,17 @@ typedef enum {
   FP4Q_NVFP4 = 0, /* E2M1 elements, 16-element blocks, E4M3 block scale, FP32 tensor scale [TJ2 §2A, MXFP4 §2] */
   FP4Q_MXFP4 = 1, /* E2M1 elements, 32-element blocks, E8M0 (power-of-two) block scale [MXFP4 §2]          */
   FP4Q_UFP4  = 2, /* uniform E1M2 levels 0..7, 16-element blocks, E4M3 block scale, FP32 tensor scale [UFP4 §2] */
-  FP4Q_NVFP4_2L = 3 /* NVFP4 with the double-block scale [TJ2 §2A]: E2M1 elements, 16-element inner blocks with
+  FP4Q_NVFP4_2L = 3, /* NVFP4 with the double-block scale [TJ2 §2A]: E2M1 elements, 16-element inner blocks with
                        an E4M3 scale, and an FP32 scale g_o = A_o / (6 * 448) per 128-element outer block along
                        the row (A_o = max |v| over it) in place of the tensor scale: one pass, no tensor amax */
+  FP4Q_MXFP4_B16 = 4, /* MXFP4 on 16-element blocks [MXFP4 §2, point 1]: E2M1 elements, E8M0 scale
+                       2^e, e = floor(log2 a_b) - 2 (a_b = max |v| over the block), no tensor scale */
+  FP4Q_MXFP4_OAS = 5, /* overflow-aware scaling [MXFP4 §2A] on 16-element blocks: E8M0 scale with
+                       e = ceil(log2(a_b / 7)), which puts a_b / 2^e in (3.5, 7] instead of [4, 8) */
+  FP4Q_MXFP4_MBS = 6  /* static macro-block scaling [MXFP4 §2B]: an FP32 scale S with 8 mantissa bits per
+                       128-element macro block along the row, S = A_M / 6 rounded to nearest (ties to even) on
+                       the 8-fraction-bit grid (A_M = max |v| over the macro block), and 16-element E8M0 blocks
+                       under it: e = floor(log2(a_b * (1/S))) - 2, y = (v * (1/S)) * 2^-e; row-wise only */
 } fp4q_format;
 
 typedef enum { FP4Q_RTNE = 0, FP4Q_SR = 1 } fp4q_rounding;
@@ -78,18 +86,23 @@ enum {
  *   codes        rows x cols/2 bytes (packed nibbles, row-major).
  *   scales       FP4Q_SCALES_LINEAR: rows x cols/block bytes, row-major.
  *                FP4Q_SCALES_MMA: the tiled layout read by the block-scaled
- *                tensor-core MMA: tiles of 128 rows x 4 blocks stored as 512
- *                contiguous bytes, tiles ordered block-index fastest; inside a
- *                tile the scale of (row r, block kb) sits at byte
- *                (r % 32) * 16 + ((r % 128) / 32) * 4 + kb % 4. Rows are padded
- *                to a multiple of 128 and blocks per row to a multiple of 4;
- *                padding bytes are written as 0. Size: fp4q_scales_bytes().
- *                NVFP4/UFP4 scales are E4M3 codes; MXFP4 scales are E8M0
- *                codes (exponent + 127).
+ *                tensor-core MMA, one scale per 16 elements along the row
+ *                (vector kv = c / 16): tiles of 128 rows x 4 vectors stored as
+ *                512 contiguous bytes, tiles ordered vector-index fastest;
+ *                inside a tile the scale of (row r, vector kv) sits at byte
+ *                (r % 32) * 16 + ((r % 128) / 32) * 4 + kv % 4. Rows are padded
+ *                to a multiple of 128 and vectors per row to a multiple of 4;
+ *                padding bytes are written as 0. A 32-element block (FP4Q_MXFP4)
+ *                has its scale at both of its vectors. Size: fp4q_scales_bytes().
+ *                NVFP4/UFP4/NVFP4_2L scales are E4M3 codes; the MXFP4 formats'
+ *                scales are E8M0 codes (exponent + 127).
  *   tensor_scale one FP32 (device): g = amax / (Qmax * 448) for NVFP4 (Qmax 6)
- *                and UFP4 (Qmax 7, levels in integer units), 1.0 for MXFP4.
+ *                and UFP4 (Qmax 7, levels in integer units), 1.0 for
+ *                FP4Q_MXFP4, FP4Q_MXFP4_B16 and FP4Q_MXFP4_OAS.
  *                FP4Q_NVFP4_2L: rows x cols/128 FP32 values (row-major), the
  *                outer-block scales g_o; element (r, c) uses g_o(r, c / 128).
+ *                FP4Q_MXFP4_MBS: rows x cols/128 FP32 macro scales S, used the
+ *                same way.
  *   scale_layout FP4Q_SCALES_LINEAR or FP4Q_SCALES_MMA.
  * The value of element (r, c) is level(code) * scale(r, c / block) * g. */
 typedef struct {
@@ -130,7 +143,8 @@ size_t fp4q_workspace_size(void);
 int fp4q_workspace_init(void* workspace, void* stream);
 
 /* Bytes of the scale array of one copy with `rows` rows of `cols` elements in
- * blocks of `block`, for the given layout. */
+ * blocks of `block`, for the given layout (FP4Q_SCALES_MMA counts one scale
+ * per 16 elements whatever the block). */
 size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout);
 
 /* ---- quantisation ------------------------------------------------------------ */
@@ -142,8 +156,8 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout
  * The amaxes are recorded in `workspace`; a following fp4q_quantize call on
  * the same workspace with FP4Q_AMAX_READY in its `axis` then skips this pass.
  * Splitting the call lets a caller time or schedule the two passes apart.
- * MXFP4 has no tensor scale: the call validates its arguments and launches
- * nothing. Arguments and errors as for fp4q_quantize (no outputs). */
+ * The MXFP4 formats and FP4Q_NVFP4_2L have no tensor scale: the call
+ * validates its arguments and launches nothing. Arguments and errors as for fp4q_quantize (no outputs). */
 int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block,
               int rht, uint64_t seed, int axis, void* workspace, size_t ws_bytes, void* stream);
 
@@ -157,7 +171,8 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  * butterfly with stages 1, 2, 4, 8 then * 0.25. NVFP4/UFP4: A = max |v| over
  * the copy, g = A / (Qmax * 448), per block t = a_b / (Qmax * g) rounded to
  * E4M3 (nearest-even, saturating at 448), r_b = 1 / (s_b * g), y = v * r_b.
- * MXFP4: e_b = floor(log2 a_b) - 2 clamped to [-127, 127], y = v * 2^-e_b.
+ * MXFP4: e_b = floor(log2 a_b) - 2 clamped to [-127, 127], y = v * 2^-e_b
+ * (FP4Q_MXFP4_OAS: e_b = ceil(log2(a_b / 7)); FP4Q_MXFP4_MBS: see the enum).
  * y is rounded onto the grid: FP4Q_RTNE nearest level ties to the even code,
  * values beyond the top level saturate; FP4Q_SR rounds |y| up from its lower
  * neighbouring level iff u < f, f the fractional position between the two
@@ -169,8 +184,8 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  * Arguments
  *   src          device, rows x cols elements of `dtype` (FP4Q_BF16 or
  *                FP4Q_F32), row-major, 16-byte aligned.
- *   fmt, block   FP4Q_NVFP4/FP4Q_UFP4/FP4Q_NVFP4_2L with block 16, FP4Q_MXFP4
- *                with block 32 (else FP4Q_ENOTSUP). FP4Q_NVFP4_2L: row-wise
+ *   fmt, block   FP4Q_MXFP4 with block 32, every other format with block 16
+ *                (else FP4Q_ENOTSUP). FP4Q_NVFP4_2L and FP4Q_MXFP4_MBS: row-wise
  *                copy only (FP4Q_COLWISE -> FP4Q_ENOTSUP), cols % 128 == 0.
  *   rht          0 or 1. rounding: FP4Q_RTNE or FP4Q_SR. seed: RHT signs and SR.
  *   axis         FP4Q_ROWWISE: blocks along rows, copy row_out (rows x cols).
@@ -221,14 +236,15 @@ int fp4q_quantize_noalloc(const void* src, int dtype, int64_t rows, int64_t cols
 
 /* Dequantise one copy ([UFP4] §2: UFP4 has no tensor-core format and is
  * consumed through this call): v_hat = (level * s_b) * g in FP32, two
- * round-to-nearest products in that order (MXFP4: level * 2^e_b); if
+ * round-to-nearest products in that order (MXFP4 formats: level * 2^e_b,
+ * FP4Q_MXFP4_MBS: (level * 2^e_b) * S); if
  * `inverse_rht`, apply R^T = (1/4) diag(sigma) H16 per 16-block along the row
  * (the same FP32 butterfly, then * 0.25, then the sign flip). Writes rows x
  * cols elements of `dst_dtype` (BF16 rounded to nearest-even, or FP32) to the
  * device buffer `dst` (16-byte aligned). q is a host pointer to a descriptor of
  * device buffers laid out as fp4q_quantize wrote them for a copy of rows x
  * cols. FP4Q_NVFP4_2L: g is the outer-block scale of the element, cols %
- * 128 == 0. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
+ * 128 == 0; FP4Q_MXFP4_MBS likewise with the macro scale. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
 int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, int block,
                     int inverse_rht, uint64_t seed, void* dst, int dst_dtype, void* stream);
 
@@ -269,14 +285,17 @@ double fp4q_effective_bucket_ratio(const unsigned long long* counts);
 /* Y = dequant(A) * dequant(B)^T on the tensor cores ([NGPT] Metodologia: NVFP4
  * consumed natively by Blackwell tensor cores; [MXFP4] §2B: scale factors
  * applied beside the dense MMA; [UFP4] Resultados: single-GEMM output of the
- * quantised operands). A is M x K and B is N x K, both row-wise NVFP4 copies
- * (blocks along K) with FP4Q_SCALES_MMA scales; the K-block products are
- * accumulated in FP32 by tcgen05 block-scaled MMAs and the result is
- * multiplied by g_A * g_B. When both operands were quantised with the RHT
+ * quantised operands). A is M x K and B is N x K, both row-wise copies of
+ * format `fmt` (blocks along K) with FP4Q_SCALES_MMA scales; the K-block
+ * products are accumulated in FP32 by tcgen05 block-scaled MMAs (E4M3 or E8M0
+ * scale per 16 elements) and the result is multiplied by g_A * g_B. When both operands were quantised with the RHT
  * along K under the same seed, the transforms cancel (R R^T = I).
  *   A, B       host pointers to descriptors of device buffers.
- *   fmt        FP4Q_NVFP4 (FP4Q_UFP4 -> FP4Q_ENOTSUP: no tensor-core format;
- *              FP4Q_MXFP4 -> FP4Q_ENOTSUP in this version).
+ *   fmt        FP4Q_NVFP4, FP4Q_MXFP4, FP4Q_MXFP4_B16 or FP4Q_MXFP4_OAS
+ *              ([MXFP4] §2: the MX formats' E8M0 scales on the same MMA).
+ *              FP4Q_UFP4 -> FP4Q_ENOTSUP (no tensor-core format);
+ *              FP4Q_NVFP4_2L, FP4Q_MXFP4_MBS -> FP4Q_ENOTSUP (their FP32
+ *              per-128 scales change along K).
  *   Y          device, M x N row-major, `out_dtype` FP4Q_BF16 (nearest-even)
  *              or FP4Q_F32, 16-byte aligned.
  *   workspace  as for fp4q_quantize (the status word records a bounded wait
@@ -293,11 +312,11 @@ size_t fp4q_gemm_via_bf16_scratch_bytes(int64_t M, int64_t N, int64_t K);
 
 /* Y = dequant(A) * dequant(B)^T for block-scaled formats without a native
  * tensor-core GEMM here: UFP4 ([UFP4] Metodologia §2 and Resultados: the
- * uniform grid with the RHT on every training GEMM) and MXFP4; NVFP4 is
- * accepted too. Each operand is dequantised on the GPU to its BF16 block
+ * uniform grid with the RHT on every training GEMM); NVFP4 and the MXFP4
+ * formats with E8M0 block scales are accepted too. Each operand is dequantised on the GPU to its BF16 block
  * values level * s_b (exact in BF16), then a BF16 GEMM with FP32 accumulation
  * (the CUDA GEMM library) forms the product, scaled by g_A * g_B (FP32
- * product; 1 for MXFP4). When both operands were quantised with the RHT along
+ * product; 1 for the MXFP4 formats). When both operands were quantised with the RHT along
  * K under the same seed, the transforms cancel.
  *   A, B       host pointers to descriptors of row-wise copies (M x K, N x K),
  *              linear or tiled scales, of format `fmt`.
@@ -306,7 +325,7 @@ size_t fp4q_gemm_via_bf16_scratch_bytes(int64_t M, int64_t N, int64_t K);
  *              fp4q_gemm_via_bf16_scratch_bytes(M, N, K); owned by the caller.
  * Calls from different host threads must not share a stream at the same time.
  * Shapes: M, N, K > 0, K % block == 0 (else FP4Q_EINVAL).
- * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP (FP4Q_NVFP4_2L), FP4Q_ECUDA. */
+ * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP (FP4Q_NVFP4_2L, FP4Q_MXFP4_MBS), FP4Q_ECUDA. */
 int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
                        int fmt, void* Y, int out_dtype, void* scratch, size_t scratch_bytes, void* stream);
 

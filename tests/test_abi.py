@@ -52,6 +52,9 @@ def test_host_validation_without_gpu(so):
     so.fp4q_scales_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int]
     assert so.fp4q_scales_bytes(100, 96, 16, 0) == 600
     assert so.fp4q_scales_bytes(100, 96, 16, 1) == 128 * 8
+    # the tiled layout holds one scale per 16 elements: a 32-element block's twice
+    assert so.fp4q_scales_bytes(100, 96, 32, 0) == 300
+    assert so.fp4q_scales_bytes(100, 96, 32, 1) == 128 * 8
     q = so.fp4q_quantize
     q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int,
@@ -72,6 +75,13 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, 32, 256, 3, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
     assert q(fake, 0, 32, 144, 3, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 256, 3, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
+    # the MXFP4 variants on 16-element blocks (4, 5) and MBS (6): block 16 only;
+    # MBS row-wise only with whole 128-element macro blocks; 7 is no format
+    for fmt in (4, 5, 6):
+        assert q(fake, 0, 32, 256, fmt, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 32, 256, 6, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 32, 144, 6, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 32, 256, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
 
 
 def test_amax_validation_without_gpu(so):

@@ -43,7 +43,7 @@ def check_copy(gq, oq, layout):
     if layout == "linear":
         assert np.array_equal(sc, oq["scales"])
     else:
-        assert np.array_equal(sc.ravel(), o.scales_to_mma_layout(oq["scales"]))
+        assert np.array_equal(sc.ravel(), o.scales_to_mma_layout(oq["scales"], oq["block"]))
     ts = gq.tensor_scale.cpu().numpy().view(np.uint32)[0]
     assert ts == np.float32(oq["tensor_scale"]).view(np.uint32)
 
@@ -280,7 +280,8 @@ RAGGED = [(1, 16), (3, 48), (207, 272), (129, 8208), (33, 4096 + 32)]
 @pytest.mark.parametrize("fmt,rht,rounding,layout", [
     ("nvfp4", False, "rtne", "linear"), ("nvfp4", True, "rtne", "mma"), ("nvfp4", True, "sr", "linear"),
     ("ufp4", True, "rtne", "mma"), ("ufp4", False, "sr", "linear"),
-    ("mxfp4", False, "rtne", "mma"), ("mxfp4", True, "sr", "linear")])
+    ("mxfp4", False, "rtne", "mma"), ("mxfp4", True, "sr", "linear"),
+    ("mxfp4_b16", True, "sr", "mma"), ("mxfp4_oas", False, "rtne", "linear"), ("mxfp4_oas", True, "sr", "mma")])
 def test_rowwise_stream_ragged(lib, shape, fmt, rht, rounding, layout):
     """Row-wise copies whose element count leaves a partial chunk and, where
     rows x cols is an odd multiple of 16, a half-filled last thread segment;
