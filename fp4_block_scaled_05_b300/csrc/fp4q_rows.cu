@@ -304,14 +304,16 @@ template <int FMT> constexpr bool kOuterScaled = FMT == 3 || FMT == 6;
 struct Sums {        // per-thread running sums of one copy
   Kahan bias, sig, err;
   double sig64 = 0.0, err64 = 0.0;
-  int e_ref = 0;     // two-level NVFP4: sig / err are in units of 2^(2 (e_ref - 127)); 0 = not set yet
+  int e_ref = 0;     // per-block scales: sig / err are in units of 2^(2 (e_ref - 127)); 0 = not set yet
 };
 
-// Two-level NVFP4: add a thread's signal and error sums, in units of g_o^2, to
-// its running sums. FP32 Kahan sums in units of a power of two fixed by the
-// first outer scale the thread meets (the exact power-of-two rescaling keeps
-// them far from overflow and underflow); an outer scale more than 2^60 away
-// from it, or subnormal, goes to the FP64 sums instead.
+// Two-level NVFP4 and the E8M0 formats: add a thread's signal and error sums,
+// in units of g^2 (g the outer scale, or the block's scale), to its running
+// sums. FP32 Kahan sums in units of a power of two fixed by the first scale the
+// thread meets (the exact power-of-two rescaling keeps them far from overflow
+// and underflow); a scale more than 2^60 away from it, or subnormal, goes to
+// the FP64 sums instead (FP64 arithmetic is slow on this GPU: the common case
+// stays in FP32).
 __device__ __forceinline__ void add_outer_stats(Sums& acc, float g, float ss, float es) {
   const int E = (int)((__float_as_uint(g) >> 23) & 0xFFu);
   if (acc.e_ref == 0 && E != 0 && E != 255) acc.e_ref = E;
@@ -543,7 +545,6 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
   nonfinite |= (__float_as_uint(m) >= 0x7F800000u) ? 1u : 0u;
   uint32_t scode;
   float r, s2 = 0.f;
-  int e2 = 0;
   if constexpr (kE8M0<FMT>) {
     // OCP rule: e = floor(log2 m) - 2 puts m / 2^e in [4, 8); the overflow-aware
     // rule (FMT 5) adds one when m's significand is above 1.75, which puts
@@ -559,7 +560,6 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
     const int e = max(-127, min(127, fl - 2));
     scode = (uint32_t)(e + 127);
     r = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, e in [-127, 126]
-    e2 = 2 * e;
   } else {
     if (cx.g == 0.f) {
       scode = 0;
@@ -610,10 +610,17 @@ __device__ __forceinline__ uint32_t quant_block(const f2* Q, const Ctx& cx, uint
   const float bs = __fadd_rn(b0, b1), es = __fadd_rn(e0f, e1f), ys = __fadd_rn(s0, s1);
   bsum = __fadd_rn(bsum, bs);
   if constexpr (kE8M0<FMT>) {
-    double sc = __longlong_as_double((long long)(1023 + e2) << 52);
-    if constexpr (FMT == 6) sc *= (double)s_macro * (double)s_macro;
-    acc.sig64 += (double)ys * sc;
-    acc.err64 += (double)es * sc;
+    // in units of the block's scale squared: 2^e (2^-127 for code 0), times S
+    // under a macro scale (exact unless it underflows; then in FP64)
+    const float sv = scode ? __uint_as_float(scode << 23) : __uint_as_float(0x00400000u);
+    const float g = (FMT == 6) ? __fmul_rn(sv, s_macro) : sv;
+    if (FMT == 6 && g < FLT_MIN && s_macro != 0.f) {
+      const double w = (double)sv * (double)s_macro;
+      acc.sig64 += (double)ys * w * w;
+      acc.err64 += (double)es * w * w;
+    } else {
+      add_outer_stats(acc, g, ys, es);
+    }
   } else if (scode == 0 && cx.g > 0.f) {
     // the scale rounded to 0: every element becomes 0 and its error is v itself
     float z = 0.f;
@@ -1114,7 +1121,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
   if constexpr (!kTensorScaled<FMT>) {   // FP64 sums (absolute units)
     double p[3] = {acc.bias.value(), acc.sig64, acc.err64};
-    if constexpr (FMT == 3) outer_stats_value(acc, p[1], p[2]);
+    outer_stats_value(acc, p[1], p[2]);
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const double v = cta_sum<RT>(p[k], sh_sum);
@@ -1632,8 +1639,10 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
   // ---- statistics: one partial per CTA and copy (summed on the host) ----
   if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
   if constexpr (kE8M0<FMT>) {
-    const double p[2][3] = {{cr.acc.bias.value(), cr.acc.sig64, cr.acc.err64},
-                            {cc.acc.bias.value(), cc.acc.sig64, cc.acc.err64}};
+    double p[2][3] = {{cr.acc.bias.value(), cr.acc.sig64, cr.acc.err64},
+                      {cc.acc.bias.value(), cc.acc.sig64, cc.acc.err64}};
+    outer_stats_value(cr.acc, p[0][1], p[0][2]);
+    outer_stats_value(cc.acc, p[1][1], p[1][2]);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
 #pragma unroll
