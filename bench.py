@@ -716,9 +716,11 @@ def run_mx_leg(fq, torch, device, steps, warmup, peaks):
     activation tensor, RTNE, no RHT, row-wise: MXFP4 on 32- and on 16-element
     blocks, the overflow-aware rule (OAS), the static macro-block scale (MBS),
     beside NVFP4: time per fp4q_quantize call (L2 flushed before each) and the
-    SNR of each copy. Then the native block-scaled GEMM at 8192^3 with E8M0
-    scales (MXFP4 32-element blocks, and OAS on 16-element blocks), operands
-    quantised with the RHT along K."""
+    SNR of each copy. Then the block-scaled GEMM at 8192^3 on the tensor cores
+    with E8M0 scales (MXFP4 32-element blocks, OAS on 16-element blocks) and
+    with per-128 FP32 scales along K (two-level NVFP4, MBS: a TMEM product per
+    128-element chunk, scaled in the epilogue), operands quantised with the
+    RHT along K."""
     import synth
     x = synth.activation(ROWS, COLS).to(device)
     ws = fq.workspace(device)
@@ -754,7 +756,7 @@ def run_mx_leg(fq, torch, device, steps, warmup, peaks):
     y = torch.empty(m, m, dtype=torch.bfloat16, device=device)
     rows = torch.arange(0, m, 64, device=device)
     ref = a[rows].double() @ b.double().T
-    for fmt in ("mxfp4", "mxfp4_oas"):
+    for fmt in ("mxfp4", "mxfp4_oas", "nvfp4_2l", "mxfp4_mbs"):
         qa, _ = fq.fp4q_quantize(a, fmt=fmt, rht=True, seed=SEED, layout="mma", ws=ws)
         qb, _ = fq.fp4q_quantize(b, fmt=fmt, rht=True, seed=SEED, layout="mma", ws=ws)
         evs = []
@@ -930,7 +932,8 @@ def main(argv=None) -> int:
         "workload": "activation 8192x4096 BF16, RTNE, no RHT, row-wise: MXFP4 (32-element E8M0 blocks), MXFP4 "
                     "on 16-element blocks, OAS (16, E8M0), MBS-static (16, E8M0, 8-bit-mantissa scale per "
                     "128), NVFP4; time per fp4q_quantize call, L2 flushed before each, and each copy's SNR. "
-                    "GEMM 8192^3 with E8M0 scales on the tensor cores (operands + RHT16 along K)",
+                    "GEMM 8192^3 on the tensor cores with E8M0 scales (MXFP4, OAS) and with per-128 FP32 "
+                    "scales along K (two-level NVFP4, MBS); operands + RHT16 along K",
         **mx_r}
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

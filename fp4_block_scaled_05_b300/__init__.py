@@ -140,6 +140,7 @@ class QCopy:
     codes: torch.Tensor          # uint8 [rows, cols/2]
     scales: torch.Tensor         # uint8 [rows, cols/block] (linear) or flat (mma)
     tensor_scale: torch.Tensor   # float32 [1]; two-level NVFP4 and MBS: [rows, cols/128] per-128 scales
+                                 # ([cols/128, rows] with the tiled "mma" layout)
     fmt: str
     rows: int
     cols: int
@@ -163,7 +164,9 @@ def alloc_copy(rows: int, cols: int, fmt: str, layout: str = "linear", device=No
     else:
         scales = torch.empty(fp4q_scales_bytes(rows, cols, b, 1), dtype=torch.uint8, device=dev)
     if fmt in OUTER_SCALED:
-        ts = torch.empty(rows, cols // OUTER_BLOCK, dtype=torch.float32, device=dev)
+        # the tiled layout keeps the per-128 scales column-major (one K chunk's rows contiguous)
+        shape = (cols // OUTER_BLOCK, rows) if layout == "mma" else (rows, cols // OUTER_BLOCK)
+        ts = torch.empty(shape, dtype=torch.float32, device=dev)
     else:
         ts = torch.empty(1, dtype=torch.float32, device=dev)
     return QCopy(codes, scales, ts, fmt, rows, cols, layout)

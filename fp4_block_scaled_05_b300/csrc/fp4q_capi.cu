@@ -399,9 +399,10 @@ int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t
                 void* Y, int out_dtype, void* workspace, size_t ws_bytes, uint64_t timeout_ns, int skip,
                 void* stream) {
   if (fmt < FP4Q_NVFP4 || fmt > FP4Q_MXFP4_MBS) return FP4Q_EINVAL;
-  // E2M1 operands with E4M3 or E8M0 block scales; UFP4 has no FP4 tensor-core
-  // type and per-128-element scales vary along K
-  if (fmt == FP4Q_UFP4 || outer_scaled(fmt)) return FP4Q_ENOTSUP;
+  // E2M1 operands with E4M3 or E8M0 block scales; UFP4 has no FP4 tensor-core type
+  if (fmt == FP4Q_UFP4) return FP4Q_ENOTSUP;
+  // per-128 scales: their own kernel, without the bounded-wait self-test
+  if (outer_scaled(fmt) && skip) return FP4Q_ENOTSUP;
   int rc;
   if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
   if (A->scale_layout != FP4Q_SCALES_MMA || B->scale_layout != FP4Q_SCALES_MMA) return FP4Q_EINVAL;
@@ -410,6 +411,7 @@ int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t
   if (M > (int64_t(1) << 20) || N > (int64_t(1) << 20) || K > (int64_t(1) << 20)) return FP4Q_EINVAL;
   if (!Y || !aligned(Y, 16)) return FP4Q_EINVAL;
   if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
+  if (outer_scaled(fmt) && (!aligned(A->tensor_scale, 16) || !aligned(B->tensor_scale, 16))) return FP4Q_EINVAL;
   fp4q::GemmArgs a{};
   a.a = to_qout(A);
   a.b = to_qout(B);
@@ -420,6 +422,10 @@ int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t
   a.y = Y;
   a.out_dtype = out_dtype;
   a.ws = workspace;
+  if (outer_scaled(fmt)) {
+    const cudaError_t e = fp4q::run_gemm_outer(a, (cudaStream_t)stream);
+    return e == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+  }
   const cudaError_t e = timeout_ns ? fp4q::run_gemm_ex(a, timeout_ns, skip, (cudaStream_t)stream)
                                    : fp4q::run_gemm(a, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return FP4Q_ENOTSUP;

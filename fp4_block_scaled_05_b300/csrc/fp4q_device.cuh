@@ -136,6 +136,7 @@ struct CopyOut {
   int64_t ld;       // bytes per row of codes = (elements per row of the copy) / 2
   int64_t nkb;      // blocks per row of the copy
   int64_t nkb_p;    // blocks per row padded to 4 (tiled layout)
+  int64_t rows;     // rows of the copy (per-128 scales in the tiled layout are column-major)
 };
 
 

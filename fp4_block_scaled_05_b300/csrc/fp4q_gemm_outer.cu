@@ -1,0 +1,314 @@
+// Block-scaled FP4 GEMM for operands with an FP32 scale per 128 elements along
+// K (sm_103a): two-level NVFP4 ("TetraJet-v2 ...", Riepilogo Tecnico §2A: an
+// FP32 scale per 128-element outer block over 16-element E4M3 blocks) and
+// MBS-static ("Unveiling the Potential of Quantization with MXFP4 ...", Resume
+// technique §2B: a scale with 8 mantissa bits per 128-element macro block over
+// 16-element E8M0 blocks, the scale math beside the dense tensor-core math).
+//
+// Y[m][n] = sum_c gA[m][c] gB[n][c] P_c[m][n], where P_c is the block-scaled
+// product of K chunk c (128 elements). The per-128 scales change along K, so
+// they cannot be applied once after the accumulation: each chunk's P_c is
+// accumulated on its own in TMEM (two MMAs of K = 64), and the epilogue warps
+// take it out of TMEM, scale it by gA gB and add it to FP32 accumulators held
+// in registers, while the tensor cores work on the next chunk in the other of
+// two TMEM buffers.
+//
+// Structure (one persistent CTA per SM, 320 threads):
+//   warp 0      TMA producer: per K stage of 256 elements, the A and B code
+//               tiles (2-D TMA, 128B swizzle) and their scale tiles (1-D bulk
+//               copies) into a 4-deep shared-memory ring.
+//   warp 1      allocates 512 TMEM columns; one thread copies each stage's
+//               scale tiles into TMEM (tcgen05.cp 32x128b.warpx4) and, per
+//               128-element chunk, issues two block-scaled MMAs (M = N = 128,
+//               K = 64) into accumulator buffer (chunk & 1), then commits the
+//               buffer to the epilogue.
+//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 and
+//               columns 64 ((w - 2) / 4) .. +63 of the buffer, releases it,
+//               and accumulates P gA gB in registers; after a tile's last chunk
+//               each thread stores the 64 values of its row (BF16 or FP32).
+// The per-128 scales are read in the tiled layout: column-major, (K/128) x
+// rows, so one chunk's scales of consecutive rows are contiguous. Every wait
+// is bounded by a global-timer deadline; on expiry the kernel records
+// FP4Q_ETIMEOUT in the workspace, drains what it issued and returns.
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "fp4q_device.cuh"
+#include "fp4q_ptx.cuh"
+#include "fp4q_tc.cuh"
+#include "fp4q_internal.h"
+
+namespace fp4q {
+namespace {
+
+constexpr int BM = 128;                 // rows of A per tile (= MMA M)
+constexpr int BN = 128;                 // rows of B per tile (= MMA N)
+constexpr int BK = 256;                 // K elements per stage
+constexpr int BK_BYTES = 128;           // code bytes per row per stage
+constexpr int CHUNK = 128;              // K elements per outer scale
+constexpr int kStages = 4;
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr int kTmemCols = 512;
+constexpr int kABytes = BM * BK_BYTES;
+constexpr int kBBytes = BN * BK_BYTES;
+constexpr int kSfBytes = 2048;          // 128 rows x 16 scales (one stage)
+constexpr int kStageBytes = kABytes + kBBytes + 2 * kSfBytes;
+constexpr int kSfStageCols = 32;        // A: 4 x 4 TMEM columns, then B: 4 x 4
+constexpr int kSfBase = 2 * BN;         // accumulator buffers in columns [0, 256)
+constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s
+static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
+static_assert(kStageBytes % 1024 == 0, "stage alignment");
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                  const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
+                  const float* __restrict__ ga, const float* __restrict__ gb, void* __restrict__ y,
+                  int M, int N, int K, Workspace* ws, uint32_t idesc, uint64_t timeout_ns) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  // bars[0..S): full, [S..2S): empty, 2S + b: acc_full[b], 2S + 2 + b: acc_empty[b], 2S + 4: drain
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto acc_full = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
+  auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (uint32_t b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), kEpiThreads);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&s_tmem_base)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  const int num_n = N / BN;
+  const int tiles = (M / BM) * num_n;
+  const int nk = K / BK;
+  const int nch = K / CHUNK;
+  const int64_t sf_row_stride = (int64_t)(K / 64) * 512;   // bytes per 128-row scale tile row
+
+  auto fail = [&]() {
+    if (!s_abort) {
+      s_abort = 1;
+      atomicOr(&ws->status, kStatusTimeout);
+    }
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0, pending = 0, pend_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m = t / num_n, n = t % num_n;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          uint8_t* st = smem + s * kStageBytes;
+          const uint32_t fb = full_bar(s);
+          pending &= ~(1u << s);
+          mbar_arrive_expect_tx(fb, kStageBytes);
+          tma_load_2d(smem_u32(st), &tmap_a, fb, ks * BK_BYTES, m * BM);
+          tma_load_2d(smem_u32(st + kABytes), &tmap_b, fb, ks * BK_BYTES, n * BN);
+          bulk_load(smem_u32(st + kABytes + kBBytes), sfa + (int64_t)m * sf_row_stride + (int64_t)ks * 2048,
+                    kSfBytes, fb);
+          bulk_load(smem_u32(st + kABytes + kBBytes + kSfBytes),
+                    sfb + (int64_t)n * sf_row_stride + (int64_t)ks * 2048, kSfBytes, fb);
+          pending |= 1u << s;
+          pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (ok) {
+        // every slot released: no commit arrival is still on its way when the CTA exits
+        for (int i = 0; i < kStages && ok; ++i) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // drain: the copies issued here land before the CTA exits
+        const uint64_t t0 = globaltimer();
+        for (int ss = 0; ss < kStages; ++ss) {
+          if (!(pending & (1u << ss))) continue;
+          const uint32_t par = (pend_ph >> ss) & 1u;
+          while (!mbar_try_wait(full_bar(ss), par) && globaltimer() - t0 < 50000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      const uint32_t base = smem_u32(smem);
+      const uint64_t da0 = smem_desc(base, 16, 1024, 2);
+      const uint64_t db0 = smem_desc(base + kABytes, 16, 1024, 2);
+      const uint64_t dsa0 = smem_desc(base + kABytes + kBBytes, 128, 128, 0);
+      const uint64_t dsb0 = smem_desc(base + kABytes + kBBytes + kSfBytes, 128, 128, 0);
+      int s = 0;
+      uint32_t ph = 0, gc = 0;
+      bool ok = true, issued_any = false;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int ks = 0; ks < nk && ok; ++ks) {
+          if (!mbar_wait(full_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint64_t off = (uint64_t)(s * (kStageBytes >> 4));
+          const uint32_t sf_col = tmem + kSfBase + s * kSfStageCols;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            tc_cp_sf(sf_col + 4 * j, dsa0 + off + 32 * j);
+            tc_cp_sf(sf_col + 16 + 4 * j, dsb0 + off + 32 * j);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t b = gc & 1u;
+            if (!mbar_wait(acc_empty(b), ((gc >> 1) & 1u) ^ 1u, &s_abort, timeout_ns)) {
+              fail();
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = 2 * h + jj;
+              tc_mma_nvf4(tmem + (uint32_t)(BN * b), da0 + off + 2 * j, db0 + off + 2 * j, idesc, sf_col + 4 * j,
+                          sf_col + 16 + 4 * j, (uint32_t)jj);
+            }
+            issued_any = true;
+            tc_commit(acc_full(b));
+            ++gc;
+          }
+          if (!ok) break;
+          tc_commit(empty_bar(s));
+          if (++s == kStages) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok && issued_any) {
+        // drain: wait (bounded) until every MMA issued so far has completed
+        tc_commit(drain_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 50000000ull) {
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..9) ----------------
+    const int q = warp & 3;                       // TMEM lane quadrant this warp may access
+    const int hc = (warp - 2) >> 2;               // column half of the tile
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    uint32_t gc = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+      const int m = t / num_n, n = t % num_n;
+      const int row = m * BM + q * 32 + lane;
+      const int col0 = n * BN + hc * 64;
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      bool ok = true;
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t b = gc & 1u;
+        if (!mbar_wait(acc_full(b), (gc >> 1) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        tc_fence_after();
+        uint32_t r[64];
+        tmem_ld32(tmem + lane_base + (uint32_t)(BN * b + hc * 64), *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(tmem + lane_base + (uint32_t)(BN * b + hc * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+        tc_fence_before();
+        mbar_arrive(acc_empty(b));
+        ++gc;
+        const float a = __ldg(ga + (int64_t)c * M + row);
+        const float4* g4 = reinterpret_cast<const float4*>(gb + (int64_t)c * N + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 w = __ldg(g4 + i);
+          acc[4 * i] = __fmaf_rn(__uint_as_float(r[4 * i]), __fmul_rn(a, w.x), acc[4 * i]);
+          acc[4 * i + 1] = __fmaf_rn(__uint_as_float(r[4 * i + 1]), __fmul_rn(a, w.y), acc[4 * i + 1]);
+          acc[4 * i + 2] = __fmaf_rn(__uint_as_float(r[4 * i + 2]), __fmul_rn(a, w.z), acc[4 * i + 2]);
+          acc[4 * i + 3] = __fmaf_rn(__uint_as_float(r[4 * i + 3]), __fmul_rn(a, w.w), acc[4 * i + 3]);
+        }
+      }
+      if (!ok) break;
+      if constexpr (OUT_F32) {
+        float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) out[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+      } else {
+        uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint32_t h[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+            h[k] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+template <bool OUT_F32>
+cudaError_t launch_outer(const GemmArgs& a, uint32_t idesc, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!encode_tiled_2d(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.a.codes, (uint64_t)(a.k / 2), (uint64_t)a.m,
+                       (uint64_t)(a.k / 2), BK_BYTES, BM) ||
+      !encode_tiled_2d(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.b.codes, (uint64_t)(a.k / 2), (uint64_t)a.n,
+                       (uint64_t)(a.k / 2), BK_BYTES, BN))
+    return cudaErrorInvalidValue;
+  auto k = gemm_outer_kernel<OUT_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  const int tiles = (int)((a.m / BM) * (a.n / BN));
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  k<<<grid, kThreads, kSmem, s>>>(ma, mb, static_cast<const uint8_t*>(a.a.scales),
+                                  static_cast<const uint8_t*>(a.b.scales), static_cast<const float*>(a.a.tensor_scale),
+                                  static_cast<const float*>(a.b.tensor_scale), a.y, (int)a.m, (int)a.n, (int)a.k,
+                                  static_cast<Workspace*>(a.ws), idesc, kTimeoutNs);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t run_gemm_outer(const GemmArgs& a, cudaStream_t s) {
+  // two-level NVFP4 (E4M3 inner scales) or MBS (E8M0 inner scales)
+  if (a.fmt != 3 && a.fmt != 6) return cudaErrorNotSupported;
+  const uint32_t idesc = idesc_nvf4(BM, BN, a.fmt == 6);
+  return a.out_dtype == 1 ? launch_outer<true>(a, idesc, s) : launch_outer<false>(a, idesc, s);
+}
+
+}  // namespace fp4q

@@ -75,6 +75,9 @@ cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
 // accumulation) scaled by g_A * g_B; `scratch` holds gemm_bf16_scratch_bytes().
 size_t gemm_bf16_scratch_bytes(int64_t m, int64_t n, int64_t k);
 cudaError_t run_gemm_bf16(const GemmArgs& a, void* scratch, cudaStream_t s);
+// The GEMM on operands with an FP32 scale per 128 elements along K (two-level
+// NVFP4, MBS), per-128 scales column-major (K/128 x rows).
+cudaError_t run_gemm_outer(const GemmArgs& a, cudaStream_t s);
 // Counts of the 16 four-bit codes in `nbytes` bytes of packed codes (zeroes `counts` first).
 cudaError_t run_code_histogram(const uint8_t* codes, int64_t nbytes, unsigned long long* counts,
                                cudaStream_t s);

@@ -814,6 +814,18 @@ __device__ __forceinline__ void put_scale(const CopyOut& o, const Flat& f, uint6
   }
 }
 
+// Index of the FP32 scale of element e's 128-element outer (or macro) block:
+// rows x cols/128 row-major, or, with the tiled scale layout, column-major
+// (cols/128 x rows), so that the scales of one 128-element K chunk of
+// consecutive rows are contiguous for the GEMM.
+__device__ __forceinline__ int64_t outer_index(const CopyOut& o, const Flat& f, int64_t e) {
+  if (!o.mma) return e / 128;
+  const uint64_t blk = (uint64_t)e / 16;
+  const uint64_t r = f.small ? (uint64_t)f.nkb.div((uint32_t)blk) : blk / f.nkb.d;
+  const uint64_t kc = (blk - r * f.nkb.d) / 8;
+  return (int64_t)(kc * (uint64_t)o.rows + r);
+}
+
 // ---- per-thread work on its 32 elements of a ring slot ---------------------------------
 // Running max |v| of the (up to two) 16-blocks at p: `m` (FP32 values; |w| = 4|v|
 // with the RHT) or `m2` (BF16 pairs, no RHT).
@@ -931,7 +943,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       put_scale(o, f, (uint64_t)e / 16, s0);
       put_scale(o, f, (uint64_t)e / 16 + 1, s1);
       acc.bias.add(bsum);
-      if ((threadIdx.x & 3u) == 0u) o.tensor_scale[e / 128] = S;
+      if ((threadIdx.x & 3u) == 0u) o.tensor_scale[outer_index(o, f, e)] = S;
     }
   } else if constexpr (FMT == 3) {
     // Two-level NVFP4 (TetraJet-v2, Riepilogo Tecnico §2A): the four threads of
@@ -972,7 +984,7 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       f2_split(s2, x0, x1);
       f2_split(e2, y0, y1);
       add_outer_stats(acc, co.g, __fadd_rn(x0, x1), __fadd_rn(y0, y1));
-      if ((threadIdx.x & 3u) == 0u) o.tensor_scale[e / 128] = co.g;
+      if ((threadIdx.x & 3u) == 0u) o.tensor_scale[outer_index(o, f, e)] = co.g;
     }
   } else if (nb16 == 2) {
     uint32_t cw[4], sc[2];
@@ -1914,14 +1926,14 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
         const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16));
         const float s1 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / 16 + 1));
         // two-level NVFP4 and MBS: the scale of the element's 128-element block
-        const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + e / 128) : g;
+        const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + outer_index(q, f, e)) : g;
         deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
         deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, s1, gs, sgn, out + (e + 16) * ES);
       }
     } else {   // a lone 16-block at the very end (16-element formats only)
       const uint2 cw = __ldg(reinterpret_cast<const uint2*>(q.codes + e / 2));
       const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / B));
-      const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + e / 128) : g;
+      const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + outer_index(q, f, e)) : g;
       deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
     }
   }
@@ -2054,7 +2066,6 @@ TileGeom make_tile_geom(const QuantArgs& a) {
 }
 
 CopyOut tile_copy(const QOut& q, int64_t crows, int64_t ccols, int block) {
-  (void)crows;
   CopyOut o{};
   o.codes = q.codes;
   o.scales = q.scales;
@@ -2063,6 +2074,7 @@ CopyOut tile_copy(const QOut& q, int64_t crows, int64_t ccols, int block) {
   o.ld = ccols / 2;
   o.nkb = ccols / block;
   o.nkb_p = mma_vectors_padded(ccols);
+  o.rows = crows;
   return o;
 }
 
@@ -2130,6 +2142,7 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
   o.ld = a.cols / 2;
   o.nkb = a.cols / block;
   o.nkb_p = mma_vectors_padded(a.cols);
+  o.rows = a.rows;
   Workspace* ws = static_cast<Workspace*>(a.ws);
   const bool f32 = a.dtype == 1;
   const int sr = a.rounding == 1;
@@ -2163,6 +2176,7 @@ cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s) {
   q.ld = a.cols / 2;
   q.nkb = a.cols / block;
   q.nkb_p = mma_vectors_padded(a.cols);
+  q.rows = a.rows;
   switch (a.fmt) {
     case 0: return launch_dequant_rows<0>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 1: return launch_dequant_rows<1>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
@@ -2185,6 +2199,7 @@ cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s) {
   o.ld = a.cols / 2;
   o.nkb = a.cols / 16;
   o.nkb_p = mma_vectors_padded(a.cols);
+  o.rows = a.rows;
   Workspace* ws = static_cast<Workspace*>(a.ws);
   const bool f32 = a.dtype == 1;
   const int sr = a.rounding == 1;

@@ -102,7 +102,10 @@ enum {
  *                FP4Q_NVFP4_2L: rows x cols/128 FP32 values (row-major), the
  *                outer-block scales g_o; element (r, c) uses g_o(r, c / 128).
  *                FP4Q_MXFP4_MBS: rows x cols/128 FP32 macro scales S, used the
- *                same way.
+ *                same way. With FP4Q_SCALES_MMA these per-128 scales are stored
+ *                column-major instead: cols/128 x rows, (r, c) at c * rows + r
+ *                (one K chunk's scales of consecutive rows contiguous, as the
+ *                GEMM reads them).
  *   scale_layout FP4Q_SCALES_LINEAR or FP4Q_SCALES_MMA.
  * The value of element (r, c) is level(code) * scale(r, c / block) * g. */
 typedef struct {
@@ -292,10 +295,13 @@ double fp4q_effective_bucket_ratio(const unsigned long long* counts);
  * along K under the same seed, the transforms cancel (R R^T = I).
  *   A, B       host pointers to descriptors of device buffers.
  *   fmt        FP4Q_NVFP4, FP4Q_MXFP4, FP4Q_MXFP4_B16 or FP4Q_MXFP4_OAS
- *              ([MXFP4] §2: the MX formats' E8M0 scales on the same MMA).
- *              FP4Q_UFP4 -> FP4Q_ENOTSUP (no tensor-core format);
- *              FP4Q_NVFP4_2L, FP4Q_MXFP4_MBS -> FP4Q_ENOTSUP (their FP32
- *              per-128 scales change along K).
+ *              ([MXFP4] §2: the MX formats' E8M0 scales on the same MMA);
+ *              FP4Q_NVFP4_2L and FP4Q_MXFP4_MBS ([TJ2] §2A, [MXFP4] §2B):
+ *              their FP32 per-128 scales change along K, so each 128-element
+ *              K chunk's product is formed apart in TMEM and scaled by
+ *              g_A(m, c) g_B(n, c) into FP32 accumulators (tensor_scale:
+ *              the column-major per-128 scales, 16-byte aligned).
+ *              FP4Q_UFP4 -> FP4Q_ENOTSUP (no tensor-core format).
  *   Y          device, M x N row-major, `out_dtype` FP4Q_BF16 (nearest-even)
  *              or FP4Q_F32, 16-byte aligned.
  *   workspace  as for fp4q_quantize (the status word records a bounded wait

@@ -803,15 +803,32 @@ def dequantize_f64(codes_packed: np.ndarray, scales: np.ndarray, g, fmt: str,
 # Block-scaled GEMM                                                           #
 # --------------------------------------------------------------------------- #
 
+def dequantize_outer_f64(copy: dict, rows=None) -> np.ndarray:
+    """Exact FP64 value of each element of a two-level NVFP4 copy (q * s_b *
+    g_o) or an MBS copy (q * 2^e_b * S), S / g_o the element's per-128 scale."""
+    sel = slice(None) if rows is None else rows
+    c = unpack_nibbles(copy["codes"][sel])
+    n, k = c.shape
+    q = code_value(c, "nvfp4").reshape(n, k // 16, 16)
+    if copy["fmt"] == "nvfp4_2l":
+        step = e4m3_decode(copy["scales"][sel])
+        outer = copy["outer_scales"][sel]
+    else:
+        step = np.exp2((np.asarray(copy["scales"][sel], dtype=np.int64) - 127).astype(np.float64))
+        outer = copy["macro_scales"][sel]
+    step = step * np.repeat(np.asarray(outer, dtype=np.float64), OUTER_BLOCK // 16, axis=1)
+    return (q * step[..., None]).reshape(n, k)
+
+
 def gemm(a_copy: dict, b_copy: dict, rows=None, cols=None) -> np.ndarray:
     """Y = dequant(A) @ dequant(B)^T in FP64 ([UFP4] Resultados, single-GEMM
     output; [NGPT] Metodologia, Y = WX), optionally for a subset of output
     rows (of A) and columns (rows of B)."""
-    fa = a_copy["fmt"]
-    fb = b_copy["fmt"]
-    a = dequantize_f64(a_copy["codes"], a_copy["scales"], a_copy["tensor_scale"], fa, rows)
-    b = dequantize_f64(b_copy["codes"], b_copy["scales"], b_copy["tensor_scale"], fb, cols)
-    return a @ b.T
+    def deq(cp, sel):
+        if cp["fmt"] in ("nvfp4_2l", "mxfp4_mbs"):
+            return dequantize_outer_f64(cp, sel)
+        return dequantize_f64(cp["codes"], cp["scales"], cp["tensor_scale"], cp["fmt"], sel)
+    return deq(a_copy, rows) @ deq(b_copy, cols).T
 
 
 def snr_db(ref: np.ndarray, approx: np.ndarray) -> float:

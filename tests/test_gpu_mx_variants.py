@@ -64,6 +64,8 @@ def check_mbs(gq, oq, layout):
     else:
         assert np.array_equal(sc.ravel(), o.scales_to_mma_layout(oq["scales"]))
     S = gq.tensor_scale.cpu().numpy()
+    if layout == "mma":                 # the tiled layout keeps the macro scales column-major
+        S = np.ascontiguousarray(S.T)
     assert S.shape == oq["macro_scales"].shape
     assert np.array_equal(S.view(np.uint32), oq["macro_scales"].view(np.uint32))
 
@@ -144,9 +146,6 @@ def test_mx_rejections(lib):
         lib.fp4q_quantize(y, fmt="mxfp4_mbs")
     assert e.value.code == 1                        # cols % 128
     a, _ = lib.fp4q_quantize(torch.randn(128, 256, device="cuda"), fmt="mxfp4_mbs", layout="mma")
-    with pytest.raises(lib.FP4QError) as e:
-        lib.fp4q_gemm(a, a)
-    assert e.value.code == 2
     with pytest.raises(lib.FP4QError) as e:
         lib.fp4q_gemm_via_bf16(a, a)
     assert e.value.code == 2

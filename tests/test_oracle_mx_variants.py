@@ -231,3 +231,13 @@ def test_mma_layout_repeats_32_element_scales():
         for kb in range(6):
             for h in range(2):
                 assert flat[o.mma_scale_offset(r, 2 * kb + h, 12)] == s[r, kb]
+
+
+def test_mbs_gemm_reduces_to_b16_when_macro_scales_are_powers_of_two():
+    """The oracle's GEMM on MBS copies equals its GEMM on the 16-element E8M0
+    copies of the same tensors when every macro scale is a power of two."""
+    a = _planted_pow2(4, 256, 21)
+    b = _planted_pow2(3, 256, 22)
+    mbs = o.gemm(o.quantize(a, "mxfp4_mbs")["row"], o.quantize(b, "mxfp4_mbs")["row"])
+    b16 = o.gemm(o.quantize(a, "mxfp4_b16")["row"], o.quantize(b, "mxfp4_b16")["row"])
+    assert np.array_equal(mbs, b16)

@@ -109,3 +109,28 @@ def test_zero_outer_block():
     assert np.all(res["scales"][1, :OB // 16] == 0)
     assert np.all(o.unpack_nibbles(res["codes"])[1, :OB] == 0)
     assert res["outer_scales"][1, 1] == np.float32(1.0) / np.float32(2688.0)
+
+
+def test_gemm_reduces_to_nvfp4_when_outer_amax_is_the_tensor_amax():
+    """The oracle's GEMM on two-level copies equals its (separately pinned)
+    NVFP4 GEMM when every outer scale is the tensor scale."""
+    a = _planted(6, 512, 3.75, 11)
+    b = _planted(5, 512, 3.75, 12)
+    two = o.gemm(o.quantize(a, "nvfp4_2l")["row"], o.quantize(b, "nvfp4_2l")["row"])
+    one = o.gemm(o.quantize(a, "nvfp4")["row"], o.quantize(b, "nvfp4")["row"])
+    assert np.array_equal(two, one)
+
+
+def test_gemm_of_power_of_two_outer_scales_matches_the_fp32_dequantisation():
+    """With power-of-two outer scales every dequantised value is exact in FP32,
+    so the FP64 GEMM equals the product of the FP32 dequantised operands."""
+    rng = np.random.default_rng(13)
+    ca = {"fmt": "nvfp4_2l", "codes": o.pack_nibbles(rng.integers(0, 16, (4, 256)).astype(np.uint8)),
+          "scales": ((rng.integers(-3, 3, (4, 16)) + 7) << 3).astype(np.uint8),
+          "outer_scales": np.exp2(rng.integers(-4, 4, (4, 2))).astype(np.float32)}
+    cb = {"fmt": "nvfp4_2l", "codes": o.pack_nibbles(rng.integers(0, 16, (3, 256)).astype(np.uint8)),
+          "scales": ((rng.integers(-3, 3, (3, 16)) + 7) << 3).astype(np.uint8),
+          "outer_scales": np.exp2(rng.integers(-4, 4, (3, 2))).astype(np.float32)}
+    da = o.dequantize_two_level(ca["codes"], ca["scales"], ca["outer_scales"]).astype(np.float64)
+    db = o.dequantize_two_level(cb["codes"], cb["scales"], cb["outer_scales"]).astype(np.float64)
+    assert np.array_equal(o.gemm(ca, cb), da @ db.T)
