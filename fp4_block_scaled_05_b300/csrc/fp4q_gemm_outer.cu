@@ -10,24 +10,33 @@
 // they cannot be applied once after the accumulation: each chunk's P_c is
 // accumulated on its own in TMEM (two MMAs of K = 64), and the epilogue warps
 // take it out of TMEM, scale it by gA gB and add it to FP32 accumulators held
-// in registers, while the tensor cores work on the next chunk in the other of
-// two TMEM buffers.
+// in registers, while the tensor cores work on the next chunks in the others
+// of three TMEM buffers.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Structure (one persistent CTA per SM, 576 threads):
 //   warp 0      TMA producer: per K stage of 256 elements, the A and B code
-//               tiles (2-D TMA, 128B swizzle) and their scale tiles (1-D bulk
-//               copies) into a 4-deep shared-memory ring.
+//               tiles (2-D TMA, 128B swizzle), their block-scale tiles and the
+//               per-128 scales of the tile's rows for the stage's two chunks
+//               (1-D bulk copies) into a 4-deep shared-memory ring. A slot is
+//               refilled once the MMAs (a commit) and the epilogue (which
+//               reads the per-128 scales there) have both released it.
 //   warp 1      allocates 512 TMEM columns; one thread copies each stage's
 //               scale tiles into TMEM (tcgen05.cp 32x128b.warpx4) and, per
 //               128-element chunk, issues two block-scaled MMAs (M = N = 128,
-//               K = 64) into accumulator buffer (chunk & 1), then commits the
+//               K = 64) into accumulator buffer (chunk % 3), then commits the
 //               buffer to the epilogue.
-//   warps 2-9   epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 and
-//               columns 64 ((w - 2) / 4) .. +63 of the buffer, releases it,
-//               and accumulates P gA gB in registers; after a tile's last chunk
-//               each thread stores the 64 values of its row (BF16 or FP32).
+//   warps 2-17  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 and
+//               columns 32 ((w - 2) / 4) .. +31 of the buffer, releases it,
+//               and accumulates P gA gB in registers (packed FP32x2); after a
+//               tile's last chunk each thread stores the 32 values of its row
+//               (BF16 or FP32).
 // The per-128 scales are read in the tiled layout: column-major, (K/128) x
-// rows, so one chunk's scales of consecutive rows are contiguous. Every wait
+// rows, so one chunk's scales of consecutive rows are contiguous. Bound: each
+// thread holds one output row, so every chunk it needs the scales g_B of all
+// its 32 columns from shared memory, about 32 shared-memory wavefronts per
+// warp and chunk against about 93 cycles of tensor-core work per chunk at the
+// FP4 rate (measured on B300: the shared-memory pipe 77% busy, the tensor
+// pipe 15%). Every wait
 // is bounded by a global-timer deadline; on expiry the kernel records
 // FP4Q_ETIMEOUT in the workspace, drains what it issued and returns.
 #include <cstdint>
@@ -50,19 +59,26 @@ constexpr int BK = 256;                 // K elements per stage
 constexpr int BK_BYTES = 128;           // code bytes per row per stage
 constexpr int CHUNK = 128;              // K elements per outer scale
 constexpr int kStages = 4;
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
+constexpr int kEpiWarps = 16;           // four per TMEM lane quadrant
+constexpr int kEpiCols = BN * 4 / kEpiWarps;   // accumulator columns per epilogue warp (32)
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 constexpr int kABytes = BM * BK_BYTES;
 constexpr int kBBytes = BN * BK_BYTES;
 constexpr int kSfBytes = 2048;          // 128 rows x 16 scales (one stage)
-constexpr int kStageBytes = kABytes + kBBytes + 2 * kSfBytes;
+constexpr int kGBytes = 2 * 128 * 4;    // the per-128 scales of the stage's two chunks, 128 rows
+constexpr int kGaOff = kABytes + kBBytes + 2 * kSfBytes;
+constexpr int kGbOff = kGaOff + kGBytes;
+constexpr int kStageBytes = kGbOff + kGBytes;
 constexpr int kSfStageCols = 32;        // A: 4 x 4 TMEM columns, then B: 4 x 4
-constexpr int kSfBase = 2 * BN;         // accumulator buffers in columns [0, 256)
+constexpr int kAccBufs = 3;             // chunk accumulators: the MMAs run up to two chunks ahead
+constexpr int kSfBase = kAccBufs * BN;  // accumulator buffers in columns [0, 384)
 constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
 constexpr uint64_t kTimeoutNs = 2000000000ull;   // 2 s
 static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
+static_assert(kEpiCols % 32 == 0 && kEpiWarps % 4 == 0, "epilogue split");
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -73,7 +89,7 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-  // bars[0..S): full, [S..2S): empty, 2S + b: acc_full[b], 2S + 2 + b: acc_empty[b], 2S + 4: drain
+  // bars[0..S): full, [S..2S): empty, 2S + b: acc_full[b], 2S + 3 + b: acc_empty[b], 2S + 6: drain
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
 
@@ -82,16 +98,16 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
   auto acc_full = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + b); };
-  auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  auto acc_empty = [&](uint32_t b) { return bar0 + 8u * (2 * kStages + kAccBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 2 * kAccBufs);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + kEpiThreads);     // the MMAs' commit and every epilogue thread
     }
-    for (uint32_t b = 0; b < 2; ++b) {
+    for (uint32_t b = 0; b < (uint32_t)kAccBufs; ++b) {
       mbar_init(acc_full(b), 1);
       mbar_init(acc_empty(b), kEpiThreads);
     }
@@ -141,6 +157,12 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
                     kSfBytes, fb);
           bulk_load(smem_u32(st + kABytes + kBBytes + kSfBytes),
                     sfb + (int64_t)n * sf_row_stride + (int64_t)ks * 2048, kSfBytes, fb);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t c = 2 * (int64_t)ks + h;
+            bulk_load(smem_u32(st + kGaOff + 512 * h), ga + c * M + (int64_t)m * BM, 512, fb);
+            bulk_load(smem_u32(st + kGbOff + 512 * h), gb + c * N + (int64_t)n * BN, 512, fb);
+          }
           pending |= 1u << s;
           pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
           if (++s == kStages) { s = 0; ph ^= 1u; }
@@ -188,8 +210,8 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
           }
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t b = gc & 1u;
-            if (!mbar_wait(acc_empty(b), ((gc >> 1) & 1u) ^ 1u, &s_abort, timeout_ns)) {
+            const uint32_t b = gc % kAccBufs;
+            if (!mbar_wait(acc_empty(b), ((gc / kAccBufs) & 1u) ^ 1u, &s_abort, timeout_ns)) {
               fail();
               ok = false;
               break;
@@ -219,53 +241,70 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..9) ----------------
+    // ---------------- epilogue (warps 2..17) ----------------
     const int q = warp & 3;                       // TMEM lane quadrant this warp may access
-    const int hc = (warp - 2) >> 2;               // column half of the tile
+    const int hc = (warp - 2) >> 2;               // column group of the tile
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     uint32_t gc = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       const int m = t / num_n, n = t % num_n;
       const int row = m * BM + q * 32 + lane;
-      const int col0 = n * BN + hc * 64;
-      float acc[64];
+      const int col0 = n * BN + hc * kEpiCols;
+      f2 acc[kEpiCols / 2];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      for (int i = 0; i < kEpiCols / 2; ++i) acc[i] = f2_make(0.f, 0.f);
       bool ok = true;
       for (int c = 0; c < nch; ++c) {
-        const uint32_t b = gc & 1u;
-        if (!mbar_wait(acc_full(b), (gc >> 1) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        const uint32_t b = gc % kAccBufs;
+        if (!mbar_wait(acc_full(b), (gc / kAccBufs) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
         tc_fence_after();
-        uint32_t r[64];
-        tmem_ld32(tmem + lane_base + (uint32_t)(BN * b + hc * 64), *reinterpret_cast<uint32_t(*)[32]>(r));
-        tmem_ld32(tmem + lane_base + (uint32_t)(BN * b + hc * 64 + 32), *reinterpret_cast<uint32_t(*)[32]>(r + 32));
+        uint32_t r[kEpiCols];
+#pragma unroll
+        for (int k = 0; k < kEpiCols / 32; ++k)
+          tmem_ld32_async(tmem + lane_base + (uint32_t)(BN * b + hc * kEpiCols + 32 * k), r + 32 * k);
+        tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(acc_empty(b));
+        // this chunk's per-128 scales, staged with its codes: stage sequence
+        // number gc / 2, half gc % 2. That stage's load has completed
+        // (the MMAs read it); waiting on its phase makes the copy's writes
+        // visible here, and the slot cannot be refilled before this thread
+        // releases it below.
+        const uint32_t sq = gc >> 1, half = gc & 1u;
+        const int stg = (int)(sq % kStages);
         ++gc;
-        const float a = __ldg(ga + (int64_t)c * M + row);
-        const float4* g4 = reinterpret_cast<const float4*>(gb + (int64_t)c * N + col0);
+        if (!mbar_wait(full_bar(stg), (sq / kStages) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        const uint8_t* st = smem + stg * kStageBytes;
+        const float a = *reinterpret_cast<const float*>(st + kGaOff + 512 * (int)half + 4 * (q * 32 + lane));
+        const float4* g4 = reinterpret_cast<const float4*>(st + kGbOff + 512 * (int)half + 4 * (hc * kEpiCols));
+        const f2 A2 = f2_make(a, a);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float4 w = __ldg(g4 + i);
-          acc[4 * i] = __fmaf_rn(__uint_as_float(r[4 * i]), __fmul_rn(a, w.x), acc[4 * i]);
-          acc[4 * i + 1] = __fmaf_rn(__uint_as_float(r[4 * i + 1]), __fmul_rn(a, w.y), acc[4 * i + 1]);
-          acc[4 * i + 2] = __fmaf_rn(__uint_as_float(r[4 * i + 2]), __fmul_rn(a, w.z), acc[4 * i + 2]);
-          acc[4 * i + 3] = __fmaf_rn(__uint_as_float(r[4 * i + 3]), __fmul_rn(a, w.w), acc[4 * i + 3]);
+        for (int i = 0; i < kEpiCols / 4; ++i) {
+          const float4 w = g4[i];
+          acc[2 * i] = f2_fma(f2_make(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
+                              f2_mul(A2, f2_make(w.x, w.y)), acc[2 * i]);
+          acc[2 * i + 1] = f2_fma(f2_make(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])),
+                                  f2_mul(A2, f2_make(w.z, w.w)), acc[2 * i + 1]);
         }
+        // the stage's second chunk: its per-128 scales are no longer needed
+        if (half == 1u) mbar_arrive(empty_bar(stg));
       }
       if (!ok) break;
+      float v[kEpiCols];
+#pragma unroll
+      for (int i = 0; i < kEpiCols / 2; ++i) f2_split(acc[i], v[2 * i], v[2 * i + 1]);
       if constexpr (OUT_F32) {
         float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) out[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+        for (int i = 0; i < kEpiCols / 4; ++i) out[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       } else {
         uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < kEpiCols / 8; ++i) {
           uint32_t h[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[8 * i + 2 * k], acc[8 * i + 2 * k + 1]);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * k], v[8 * i + 2 * k + 1]);
             h[k] = *reinterpret_cast<const uint32_t*>(&b2);
           }
           out[i] = make_uint4(h[0], h[1], h[2], h[3]);
