@@ -26,17 +26,18 @@
 //               K = 64) into accumulator buffer (chunk % 3), then commits the
 //               buffer to the epilogue.
 //   warps 2-17  epilogue: warp w reads TMEM lanes 32 (w % 4) .. +31 and
-//               columns 32 ((w - 2) / 4) .. +31 of the buffer, releases it,
-//               and accumulates P gA gB in registers (packed FP32x2); after a
-//               tile's last chunk each thread stores the 32 values of its row
-//               (BF16 or FP32).
+//               columns 32 ((w - 2) / 4) .. +31 of the buffer (16x256b
+//               shape: a thread holds 4 rows x 8 columns), releases it, and
+//               accumulates P gA gB in registers (packed FP32x2); after a
+//               tile's last chunk each thread stores its 32 values (BF16 or
+//               FP32).
 // The per-128 scales are read in the tiled layout: column-major, (K/128) x
-// rows, so one chunk's scales of consecutive rows are contiguous. Bound: each
-// thread holds one output row, so every chunk it needs the scales g_B of all
-// its 32 columns from shared memory, about 32 shared-memory wavefronts per
-// warp and chunk against about 93 cycles of tensor-core work per chunk at the
-// FP4 rate (measured on B300: the shared-memory pipe 77% busy, the tensor
-// pipe 15%). Every wait
+// rows, so one chunk's scales of consecutive rows are contiguous. Bound
+// (measured on B300 at 8192^3): the mainloop with 128 x 128 tiles and a commit
+// per chunk takes 643 us even with no epilogue arithmetic; the epilogue adds
+// about 100 us. Register accumulators cap the tile at 128 x 128 (a 128 x 256
+// tile would need the whole register file), and wider TMEM accumulators leave
+// no room for two buffers. Every wait
 // is bounded by a global-timer deadline; on expiry the kernel records
 // FP4Q_ETIMEOUT in the workspace, drains what it issued and returns.
 #include <cstdint>
@@ -242,72 +243,84 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
     }
   } else {
     // ---------------- epilogue (warps 2..17) ----------------
+    // Each warp covers the 32 rows of its TMEM lane quadrant and 32 columns of
+    // the tile, read as two 16-lane halves with the 16x256b shape: thread t
+    // holds rows (t / 4, t / 4 + 8) of each half and columns 8j + 2 (t % 4) +
+    // {0, 1}, so it needs 8 column scales per chunk rather than 32.
     const int q = warp & 3;                       // TMEM lane quadrant this warp may access
     const int hc = (warp - 2) >> 2;               // column group of the tile
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int tr = lane >> 2, tc = 2 * (lane & 3);
     uint32_t gc = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
       const int m = t / num_n, n = t % num_n;
-      const int row = m * BM + q * 32 + lane;
-      const int col0 = n * BN + hc * kEpiCols;
-      f2 acc[kEpiCols / 2];
+      const int row0 = q * 32 + tr;               // rows row0 + {0, 8, 16, 24} of the tile
+      const int c0 = hc * kEpiCols + tc;          // columns c0 + 8j + {0, 1} of the tile
+      f2 acc[16];                                 // [half][j][row offset 0 / 8]
 #pragma unroll
-      for (int i = 0; i < kEpiCols / 2; ++i) acc[i] = f2_make(0.f, 0.f);
+      for (int i = 0; i < 16; ++i) acc[i] = f2_make(0.f, 0.f);
       bool ok = true;
       for (int c = 0; c < nch; ++c) {
         const uint32_t b = gc % kAccBufs;
         if (!mbar_wait(acc_full(b), (gc / kAccBufs) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
         tc_fence_after();
-        uint32_t r[kEpiCols];
+        uint32_t r[32];
 #pragma unroll
-        for (int k = 0; k < kEpiCols / 32; ++k)
-          tmem_ld32_async(tmem + lane_base + (uint32_t)(BN * b + hc * kEpiCols + 32 * k), r + 32 * k);
+        for (int hh = 0; hh < 2; ++hh)
+          tmem_ld16x256_x4_async(tmem + ((uint32_t)(q * 32 + 16 * hh) << 16) + (uint32_t)(BN * b + hc * kEpiCols),
+                                 r + 16 * hh);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(acc_empty(b));
         // this chunk's per-128 scales, staged with its codes: stage sequence
-        // number gc / 2, half gc % 2. That stage's load has completed
-        // (the MMAs read it); waiting on its phase makes the copy's writes
-        // visible here, and the slot cannot be refilled before this thread
-        // releases it below.
+        // number gc / 2, half gc % 2. That stage's load has completed (the MMAs
+        // read it); waiting on its phase makes the copy's writes visible here,
+        // and the slot cannot be refilled before this thread releases it below.
         const uint32_t sq = gc >> 1, half = gc & 1u;
         const int stg = (int)(sq % kStages);
         ++gc;
         if (!mbar_wait(full_bar(stg), (sq / kStages) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
         const uint8_t* st = smem + stg * kStageBytes;
-        const float a = *reinterpret_cast<const float*>(st + kGaOff + 512 * (int)half + 4 * (q * 32 + lane));
-        const float4* g4 = reinterpret_cast<const float4*>(st + kGbOff + 512 * (int)half + 4 * (hc * kEpiCols));
-        const f2 A2 = f2_make(a, a);
+        const float* ga_s = reinterpret_cast<const float*>(st + kGaOff + 512 * (int)half);
+        const float* gb_s = reinterpret_cast<const float*>(st + kGbOff + 512 * (int)half);
+        float a[4];
 #pragma unroll
-        for (int i = 0; i < kEpiCols / 4; ++i) {
-          const float4 w = g4[i];
-          acc[2 * i] = f2_fma(f2_make(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
-                              f2_mul(A2, f2_make(w.x, w.y)), acc[2 * i]);
-          acc[2 * i + 1] = f2_fma(f2_make(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])),
-                                  f2_mul(A2, f2_make(w.z, w.w)), acc[2 * i + 1]);
+        for (int k = 0; k < 4; ++k) a[k] = ga_s[row0 + 8 * k];
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const float2 w = *reinterpret_cast<const float2*>(gb_s + c0 + 8 * jj);
+          const f2 W = f2_make(w.x, w.y);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const float ak = a[2 * hh + k];
+              const uint32_t* rr = r + 16 * hh + 4 * jj + 2 * k;
+              f2& A = acc[8 * hh + 2 * jj + k];
+              A = f2_fma(f2_make(__uint_as_float(rr[0]), __uint_as_float(rr[1])), f2_mul(f2_make(ak, ak), W), A);
+            }
+          }
         }
         // the stage's second chunk: its per-128 scales are no longer needed
         if (half == 1u) mbar_arrive(empty_bar(stg));
       }
       if (!ok) break;
-      float v[kEpiCols];
 #pragma unroll
-      for (int i = 0; i < kEpiCols / 2; ++i) f2_split(acc[i], v[2 * i], v[2 * i + 1]);
-      if constexpr (OUT_F32) {
-        float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
+      for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-        for (int i = 0; i < kEpiCols / 4; ++i) out[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-      } else {
-        uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+        for (int k = 0; k < 2; ++k) {
+          const int64_t row = (int64_t)m * BM + row0 + 16 * hh + 8 * k;
 #pragma unroll
-        for (int i = 0; i < kEpiCols / 8; ++i) {
-          uint32_t h[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * i + 2 * k], v[8 * i + 2 * k + 1]);
-            h[k] = *reinterpret_cast<const uint32_t*>(&b2);
+          for (int jj = 0; jj < 4; ++jj) {
+            float v0, v1;
+            f2_split(acc[8 * hh + 2 * jj + k], v0, v1);
+            const int64_t col = (int64_t)n * BN + c0 + 8 * jj;
+            if constexpr (OUT_F32) {
+              *reinterpret_cast<float2*>(static_cast<float*>(y) + row * N + col) = make_float2(v0, v1);
+            } else {
+              *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(y) + row * N + col) =
+                  __floats2bfloat162_rn(v0, v1);
+            }
           }
-          out[i] = make_uint4(h[0], h[1], h[2], h[3]);
         }
       }
     }
