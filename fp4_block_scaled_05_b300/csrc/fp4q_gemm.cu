@@ -10,7 +10,7 @@
 // switches to UE8M0, and a 32-element block's scale sits in the scale layout
 // once for each of its 16-element halves.
 //
-// Structure (one persistent CTA per SM, 192 threads, clusters of up to 4 CTAs
+// Structure (one persistent CTA per SM, 320 threads, clusters of up to 4 CTAs
 // that share each B tile through TMA multicast):
 //   warp 0      TMA producer: per K stage of 256 elements, one 2-D tiled TMA
 //               load (128B swizzle) of the A and B code tiles and 1-D bulk
@@ -22,8 +22,10 @@
 //               (M = 128, N = BN, K = 64) into an FP32 accumulator in TMEM;
 //               tcgen05.commit frees the ring slot and, after the last stage,
 //               hands the accumulator to the epilogue.
-//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns at a time, times
-//               g_A * g_B, BF16 (nearest-even) or FP32 stores.
+//   warps 2-9   epilogue: each warp reads its 32 TMEM lanes x BN/2 columns
+//               into registers, releases the accumulator (the next tile's
+//               MMAs start), then multiplies by g_A * g_B and stores BF16
+//               (nearest-even) or FP32.
 // Every mbarrier wait is bounded by a global-timer deadline; on expiry the
 // kernel records FP4Q_ETIMEOUT in the workspace, drains what it issued and
 // returns.
@@ -44,7 +46,8 @@ namespace {
 constexpr int BM = 128;           // rows of A per tile (= MMA M)
 constexpr int BK_BYTES = 128;     // bytes of codes per row per stage (256 FP4 values)
 constexpr int BK = 256;           // K elements per stage
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;              // two per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 
@@ -145,7 +148,7 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       mbar_init(empty_bar(s), CL);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 128);
+    mbar_init(tmem_empty, 32 * kEpiWarps);
     mbar_init(drain_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -288,8 +291,10 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       }
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
+    // ---------------- epilogue (warps 2..9) ----------------
     const int q = warp & 3;                    // TMEM lane quadrant this warp may access
+    const int hcol = (warp - 2) >> 2;          // which half of the tile's columns
+    constexpr int kCols = BN / 2;
     const float alpha = __fmul_rn(__ldg(g_a), __ldg(g_b));
     uint32_t acc_ph = 0;
     for (int gi = cid; gi < num_groups; gi += ncl) {
@@ -297,35 +302,40 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       if (!mbar_wait(tmem_full, acc_ph, &s_abort, timeout_ns)) { fail(); break; }
       tc_fence_after();
       const int row = m * BM + q * 32 + lane;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-        const int col = n * BN + c * 32;
-        if constexpr (OUT_F32) {
-          float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col);
+      uint32_t r[kCols];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
-        } else {
-          uint32_t h[16];
+      for (int c = 0; c < kCols / 32; ++c)
+        tmem_ld32_async(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hcol * kCols + c * 32), r + 32 * c);
+      tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * i]), alpha),
-                                                            __fmul_rn(__uint_as_float(r[2 * i + 1]), alpha));
-            h[i] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) out[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-        }
-      }
+      for (int c = 0; c < kCols / 32; ++c) reg_fence32(r + 32 * c);
+      // the accumulator is in registers: the next tile's MMAs may overwrite it
       tc_fence_before();
       mbar_arrive(tmem_empty);
       acc_ph ^= 1u;
+      const int col0 = n * BN + hcol * kCols;
+      if constexpr (OUT_F32) {
+        float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+        for (int i = 0; i < kCols / 4; ++i)
+          out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+      } else {
+        uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+        for (int i = 0; i < kCols / 8; ++i) {
+          uint32_t h[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * i + 2 * k]), alpha),
+                                                            __fmul_rn(__uint_as_float(r[8 * i + 2 * k + 1]), alpha));
+            h[k] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      }
     }
   }
 

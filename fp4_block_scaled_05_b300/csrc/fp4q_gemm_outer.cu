@@ -269,6 +269,8 @@ gemm_outer_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_const
           tmem_ld16x256_x4_async(tmem + ((uint32_t)(q * 32 + 16 * hh) << 16) + (uint32_t)(BN * b + hc * kEpiCols),
                                  r + 16 * hh);
         tmem_ld_wait();
+        reg_fence16(r);
+        reg_fence16(r + 16);
         tc_fence_before();
         mbar_arrive(acc_empty(b));
         // this chunk's per-128 scales, staged with its codes: stage sequence
