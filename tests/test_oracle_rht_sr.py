@@ -81,29 +81,27 @@ def test_philox_properties():
     one flipped counter or key bit flips about half of the 128 output bits; the
     output words are uniform."""
     k0, k1 = 0x1234ABCD, 0x0F0F0F0F
-    outs = set()
-    for c in range(1 << 12):
-        outs.add(tuple(int(v) for v in o.philox4x32_10(c, 0, 0, 0, k0, k1)))
-    assert len(outs) == 1 << 12
+    c = np.arange(1 << 14, dtype=np.uint64)
+    w = np.stack([np.asarray(v, dtype=np.uint64) for v in o.philox4x32_10(c, 0, 0, 0, k0, k1)], axis=1)
+    assert np.unique(w, axis=0).shape[0] == 1 << 14
     rng = np.random.default_rng(3)
-    flips = []
-    for _ in range(200):
-        c = [int(v) for v in rng.integers(0, 1 << 32, 4, dtype=np.uint64)]
-        base = [int(v) for v in o.philox4x32_10(*c, k0, k1)]
-        w, b = int(rng.integers(0, 4)), int(rng.integers(0, 32))
-        c2 = list(c)
-        c2[w] ^= 1 << b
-        other = [int(v) for v in o.philox4x32_10(*c2, k0, k1)]
-        flips.append(sum(bin(x ^ y).count("1") for x, y in zip(base, other)))
-        kk = int(rng.integers(0, 64))
-        k0b, k1b = (k0 ^ (1 << kk), k1) if kk < 32 else (k0, k1 ^ (1 << (kk - 32)))
-        other = [int(v) for v in o.philox4x32_10(*c, k0b, k1b)]
-        flips.append(sum(bin(x ^ y).count("1") for x, y in zip(base, other)))
-    m = np.mean(flips)
-    assert abs(m - 64.0) < 2.0          # 400 samples of Binomial(128, 1/2): sd of the mean 0.28
-    words = np.array([int(v) for c in range(1024) for v in o.philox4x32_10(c, 7, 0, 0, k0, k1)])
-    h, _ = np.histogram(words >> 26, bins=64, range=(0, 64))
-    e = words.size / 64
+    n = 400
+    ctr = rng.integers(0, 1 << 32, (4, n), dtype=np.uint64)
+    base = np.stack(o.philox4x32_10(*ctr, k0, k1))
+    word, bit = rng.integers(0, 4, n), rng.integers(0, 32, n).astype(np.uint64)
+    ctr2 = ctr.copy()
+    ctr2[word, np.arange(n)] ^= np.uint64(1) << bit
+    flipped = np.stack(o.philox4x32_10(*ctr2, k0, k1))
+    kb = rng.integers(0, 64, n).astype(np.uint64)
+    k0v = np.where(kb < 32, np.uint64(k0) ^ (np.uint64(1) << (kb % np.uint64(32))), np.uint64(k0))
+    k1v = np.where(kb >= 32, np.uint64(k1) ^ (np.uint64(1) << (kb % np.uint64(32))), np.uint64(k1))
+    keyed = np.stack(o.philox4x32_10(*ctr, k0v, k1v))
+    def popcount(x):
+        return np.array([bin(int(v)).count("1") for v in x.ravel()]).reshape(x.shape)
+    flips = np.concatenate([popcount(base ^ flipped).sum(axis=0), popcount(base ^ keyed).sum(axis=0)])
+    assert abs(flips.mean() - 64.0) < 2.0    # 800 samples of Binomial(128, 1/2): sd of the mean 0.2
+    h, _ = np.histogram((w[:, 1] >> np.uint64(26)).astype(np.int64), bins=64, range=(0, 64))
+    e = w.shape[0] / 64
     assert np.sum((h - e) ** 2 / e) < 120
 
 
