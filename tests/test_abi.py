@@ -41,6 +41,26 @@ def test_python_binding_uses_the_c_names():
         assert callable(getattr(fq, n)), n
 
 
+def _header_enum(prefix):
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {k: int(v) for k, v in re.findall(r"\b(" + prefix + r"[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+
+
+def test_python_tables_match_the_header():
+    """The binding's format, rounding, layout and axis numbers are the header's."""
+    import fp4_block_scaled_05_b300 as fq
+    fmts = _header_enum("FP4Q_")
+    names = {"nvfp4": "FP4Q_NVFP4", "mxfp4": "FP4Q_MXFP4", "ufp4": "FP4Q_UFP4", "nvfp4_2l": "FP4Q_NVFP4_2L",
+             "mxfp4_b16": "FP4Q_MXFP4_B16", "mxfp4_oas": "FP4Q_MXFP4_OAS", "mxfp4_mbs": "FP4Q_MXFP4_MBS"}
+    assert set(fq.FORMATS) == set(names)
+    for py, c in names.items():
+        assert fq.FORMATS[py] == fmts[c], py
+    assert fq.ROUNDING == {"rtne": fmts["FP4Q_RTNE"], "sr": fmts["FP4Q_SR"]}
+    assert fq.LAYOUTS == {"linear": fmts["FP4Q_SCALES_LINEAR"], "mma": fmts["FP4Q_SCALES_MMA"]}
+    assert fq.AXES["row"] == fmts["FP4Q_ROWWISE"] and fq.AXES["col"] == fmts["FP4Q_COLWISE"]
+    assert fq.BLOCKS["mxfp4"] == 32 and all(b == 16 for f, b in fq.BLOCKS.items() if f != "mxfp4")
+
+
 def test_host_validation_without_gpu(so):
     so.fp4q_workspace_size.restype = ctypes.c_size_t
     ws_size = so.fp4q_workspace_size()
