@@ -18,7 +18,8 @@ def _rel_fro(y, ref):
     return float(np.linalg.norm(y - ref) / np.linalg.norm(ref))
 
 
-@pytest.mark.parametrize("fmt,rht", [("ufp4", True), ("ufp4", False), ("mxfp4", False), ("nvfp4", True)])
+@pytest.mark.parametrize("fmt,rht", [("ufp4", True), ("ufp4", False), ("mxfp4", False), ("nvfp4", True),
+                                     ("mxfp4_b16", False), ("mxfp4_oas", True)])
 @pytest.mark.parametrize("layout", ["linear", "mma"])
 @pytest.mark.parametrize("shape", [(256, 384, 512), (128, 128, 1024), (96, 200, 256)])
 def test_gemm_via_bf16_against_oracle(lib, fmt, rht, layout, shape):
@@ -41,6 +42,20 @@ def test_gemm_via_bf16_matches_native_nvfp4(lib):
     b = synth.gemm_operand("b", 512, 1024)
     qa, _ = lib.fp4q_quantize(a.cuda(), fmt="nvfp4", rht=True, seed=5, layout="mma")
     qb, _ = lib.fp4q_quantize(b.cuda(), fmt="nvfp4", rht=True, seed=5, layout="mma")
+    y1 = lib.fp4q_gemm(qa, qb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    y2 = lib.fp4q_gemm_via_bf16(qa, qb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    assert _rel_fro(y2, y1) < 1e-5
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "mxfp4_oas"])
+def test_gemm_via_bf16_matches_native_e8m0(lib, fmt):
+    """The two routes for E8M0 operands agree: exact BF16 block values with a
+    library GEMM, and the tensor cores with UE8M0 scales (MXFP4's 32-element
+    scales stored for both halves of the tiled layout)."""
+    a = synth.gemm_operand("a", 384, 768)
+    b = synth.gemm_operand("b", 256, 768)
+    qa, _ = lib.fp4q_quantize(a.cuda(), fmt=fmt, rht=True, seed=9, layout="mma")
+    qb, _ = lib.fp4q_quantize(b.cuda(), fmt=fmt, rht=True, seed=9, layout="mma")
     y1 = lib.fp4q_gemm(qa, qb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
     y2 = lib.fp4q_gemm_via_bf16(qa, qb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
     assert _rel_fro(y2, y1) < 1e-5
