@@ -241,3 +241,18 @@ def test_mbs_gemm_reduces_to_b16_when_macro_scales_are_powers_of_two():
     mbs = o.gemm(o.quantize(a, "mxfp4_mbs")["row"], o.quantize(b, "mxfp4_mbs")["row"])
     b16 = o.gemm(o.quantize(a, "mxfp4_b16")["row"], o.quantize(b, "mxfp4_b16")["row"])
     assert np.array_equal(mbs, b16)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4_2l", "mxfp4_mbs"])
+def test_fp32_dequantisation_is_one_rounding_of_the_exact_value(fmt):
+    """level * block scale is exact in FP32, so the FP32 dequantisation rounds
+    the exact value (level * block scale * per-128 scale, exact in FP64) once."""
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal((16, 512)) * np.exp(2 * rng.standard_normal((16, 1)))).astype(np.float32)
+    r = o.quantize(x, fmt, rht=True, seed=2)["row"]
+    exact = o.dequantize_outer_f64(r)
+    if fmt == "nvfp4_2l":
+        got = o.dequantize_two_level(r["codes"], r["scales"], r["outer_scales"])
+    else:
+        got = o.dequantize_mbs(r["codes"], r["scales"], r["macro_scales"])
+    assert np.array_equal(got.view(np.uint32), exact.astype(np.float32).view(np.uint32))
