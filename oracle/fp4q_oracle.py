@@ -29,8 +29,8 @@ Sources (page title, section):
   [OCP-MX] OCP Microscaling Formats (MX) v1.0: shared scale exponent
           floor(log2 amax) - emax_elem, emax_elem = 2 for E2M1.
   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1,
-          2, 3", SC'11: the Philox4x32-10 counter-based generator (parity
-          unpinned for its exact bits: see philox4x32_10).
+          2, 3", SC'11: the Philox4x32-10 counter-based generator (pinned
+          against cuRAND's host generator: see philox4x32_10).
 
 Readings where the pages are silent (each is listed with its reason in the
 design notes of the repository):
@@ -223,10 +223,11 @@ def philox4x32_10(c0, c1, c2, c3, k0, k1):
     products; the new counter is (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0).
     Between rounds the key is bumped by the Weyl constants (W0, W1) mod 2^32.
     Inputs broadcast; returns four uint64 arrays holding 32-bit words.
-    Parity unpinned for the exact output bits: no known-answer vectors are
-    available here; the tests check the construction's properties (distinct
-    outputs for distinct counters, avalanche, uniformity), and the CUDA path
-    implements the generator separately from the same published definition.
+    Pinned word for word against cuRAND's host-side Philox4x32-10 generator
+    (an implementation this oracle shares no code with), over several keys
+    including all-zero and all-ones and counters whose first three words vary
+    (tests/test_oracle_rht_sr.py); the construction's properties (distinct
+    outputs, avalanche, uniformity) are checked as well.
     """
     c0, c1, c2, c3, k0, k1 = np.broadcast_arrays(
         *[np.asarray(v, dtype=np.uint64) & _MASK32 for v in (c0, c1, c2, c3, k0, k1)])

@@ -1,5 +1,7 @@
 """Pins of the oracle's RHT, Philox and stochastic rounding (no GPU)."""
 
+import os
+
 import numpy as np
 import pytest
 
@@ -73,6 +75,68 @@ def test_rht_cancels_in_a_dot_product():
 
 
 # ---- Philox ----------------------------------------------------------------
+
+def _curand_host_philox(seed: int, nwords: int, offset: int):
+    """Words of cuRAND's host-side Philox4x32-10 generator (libcurand, NVIDIA's
+    implementation, run on the CPU: no device needed), default ordering."""
+    import ctypes
+    import ctypes.util
+    names = ["libcurand.so", "libcurand.so.10", ctypes.util.find_library("curand")]
+    for d in ("/usr/local/cuda/lib64", "/usr/local/cuda/targets/x86_64-linux/lib"):
+        names.append(os.path.join(d, "libcurand.so"))
+    lib = None
+    for n in names:
+        if not n:
+            continue
+        try:
+            lib = ctypes.CDLL(n)
+            break
+        except OSError:
+            continue
+    assert lib is not None, "libcurand not found: the Philox pin needs cuRAND's host generator"
+    gen = ctypes.c_void_p()
+    assert lib.curandCreateGeneratorHost(ctypes.byref(gen), 161) == 0   # CURAND_RNG_PSEUDO_PHILOX4_32_10
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(offset)) == 0
+        out = np.zeros(nwords, dtype=np.uint32)
+        assert lib.curandGenerate(gen, out.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(nwords)) == 0
+    finally:
+        lib.curandDestroyGenerator(gen)
+    return out
+
+
+# cuRAND's host Philox generator runs 65536 subsequences side by side: output
+# quadruple q comes from subsequence t = q mod 65536 at step s = q div 65536,
+# i.e. from the counter (s lo, s hi, t, 0) under the key (seed lo, seed hi) --
+# the counter/key assignment its device API documents for curand_init(seed,
+# subsequence t, offset 4 s). A generator offset of 4 q starts at quadruple q.
+_CURAND_THREADS = 65536
+
+
+@pytest.mark.parametrize("seed", [0, 0xFFFFFFFFFFFFFFFF, 1234, 0x0123456789ABCDEF])
+def test_philox_matches_curand_host_generator(seed):
+    """Pins the oracle's Philox4x32-10 word for word against an implementation
+    it does not share code with (cuRAND). Covered: the round function (both
+    multipliers, the output word order), the key schedule (bump before each
+    round after the first), both key words, and the counter words c0, c1
+    (steps past 2^32) and c2 (the subsequence). c3 enters the first round
+    through the same round function that rounds 2-10 exercise with non-zero
+    values in that slot."""
+    k0, k1 = seed & 0xFFFFFFFF, seed >> 32
+    # the first 64 quadruples: subsequences 0..63 at step 0
+    got = _curand_host_philox(seed, 256, 0).reshape(-1, 4)
+    t = np.arange(64, dtype=np.uint64)
+    want = np.stack(o.philox4x32_10(0, 0, t, 0, k0, k1), axis=1).astype(np.uint32)
+    assert np.array_equal(got, want)
+    # step 1 and steps beyond 2^32 (the counter's second word), several subsequences
+    for s, t0 in ((1, 0), (3, 65530), (1 << 32, 0), ((1 << 32) + 5, 7), ((1 << 33) + 3, 65535)):
+        q = s * _CURAND_THREADS + t0
+        got = _curand_host_philox(seed, 4, 4 * q)
+        want = np.array([int(w) for w in o.philox4x32_10(s & 0xFFFFFFFF, s >> 32, t0, 0, k0, k1)],
+                        dtype=np.uint32)
+        assert np.array_equal(got, want), (hex(seed), s, t0)
+
 
 def test_philox_properties():
     """Philox4x32-10 has no known-answer vectors here (parity unpinned for
