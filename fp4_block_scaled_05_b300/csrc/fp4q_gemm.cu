@@ -10,8 +10,7 @@
 // switches to UE8M0, and a 32-element block's scale sits in the scale layout
 // once for each of its 16-element halves.
 //
-// Structure (one persistent CTA per SM, 320 threads, clusters of up to 4 CTAs
-// that share each B tile through TMA multicast):
+// Structure (one persistent CTA per SM, 320 threads):
 //   warp 0      TMA producer: per K stage of 256 elements, one 2-D tiled TMA
 //               load (128B swizzle) of the A and B code tiles and 1-D bulk
 //               copies of their scale tiles into a 4-deep shared-memory ring
@@ -68,53 +67,8 @@ struct Cfg {
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
-// The same load multicast to the CTAs of `mask` in the cluster: the data lands
-// at offset `dst` of each one's shared memory and completes bytes on the
-// mbarrier at offset `bar` of each one.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4}], [%2], %5;"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
-                                             uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1], %2, [%3], %4;"
-      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "h"(mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-// All threads of every CTA of the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Arrive (once the MMAs issued so far complete) on the mbarrier at offset
-// `bar` of every CTA in `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-               ::"r"(bar), "h"(mask) : "memory");
-}
-
 // ---- the kernel -----------------------------------------------------------------
-// CL CTAs form a cluster that works on CL vertically adjacent tiles (m-tiles
-// CL*g .. CL*g + CL-1, one n-tile): CTA r loads its own A tile and A scales,
-// and 1/CL of the shared B tile (plus its share of the B scales), multicast to
-// every CTA of the cluster, so each B byte leaves L2 once per cluster. A slot
-// of the ring is refilled only when the MMAs of all CL CTAs have released it
-// (their commits arrive on every CTA's "empty" barrier).
-template <int BN, bool OUT_F32, int CL>
+template <int BN, bool OUT_F32>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
@@ -122,8 +76,6 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                  int M, int N, int K, Workspace* ws, uint64_t timeout_ns, int skip_first_stage,
                  int ue8m0) {
   using C = Cfg<BN>;
-  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
-  constexpr int kBPiece = BN / CL;                  // rows of B each CTA loads
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -132,8 +84,7 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rank = (CL > 1) ? cluster_rank() : 0u;
-  const int cid = (int)blockIdx.x / CL, ncl = (int)gridDim.x / CL;
+  const int cid = (int)blockIdx.x, ncl = (int)gridDim.x;   // first tile, tile stride
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::kStages + s); };
@@ -145,13 +96,12 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     s_abort = 0;
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), CL);
+      mbar_init(empty_bar(s), 1);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, 32 * kEpiWarps);
     mbar_init(drain_bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    fence_mbarrier_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
@@ -160,12 +110,11 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL > 1) cluster_sync();       // every barrier of the cluster exists before any copy
   tc_fence_after();
   const uint32_t tmem = s_tmem_base;
 
   const int num_n = N / BN;
-  const int num_groups = (M / (BM * CL)) * num_n;  // a group: CL m-tiles x one n-tile
+  const int num_tiles = (M / BM) * num_n;
   const int nk = K / BK;
   const int64_t sf_row_stride = (int64_t)(K / 64) * 512;   // bytes per 128-row scale tile row
 
@@ -184,8 +133,8 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       uint32_t pending = 0;    // bit ss: stage ss has copies whose phase may not have completed
       uint32_t pend_ph = 0;    // bit ss: the parity of that phase
       bool ok = true;
-      for (int gi = cid; gi < num_groups && ok; gi += ncl) {
-        const int m = (gi / num_n) * CL + (int)rank, n = gi % num_n;
+      for (int gi = cid; gi < num_tiles && ok; gi += ncl) {
+        const int m = gi / num_n, n = gi % num_n;
         for (int ks = 0; ks < nk; ++ks) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
           const bool skip = skip_first_stage && blockIdx.x == 0 && gi == cid && ks == 0;
@@ -197,19 +146,12 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             tma_load_2d(smem_u32(st), &tmap_a, fb, ks * BK_BYTES, m * BM);
             bulk_load(smem_u32(st + C::kABytes + C::kBBytes),
                       sfa + (int64_t)m * sf_row_stride + (int64_t)ks * 2048, 2048, fb);
-            const uint32_t b_dst = smem_u32(st + C::kABytes + (int)rank * kBPiece * BK_BYTES);
-            if constexpr (CL > 1) {
-              tma_load_2d_mc(b_dst, &tmap_b, fb, ks * BK_BYTES, n * BN + (int)rank * kBPiece, kMask);
-            } else {
-              tma_load_2d(b_dst, &tmap_b, fb, ks * BK_BYTES, n * BN);
-            }
+            tma_load_2d(smem_u32(st + C::kABytes), &tmap_b, fb, ks * BK_BYTES, n * BN);
 #pragma unroll
             for (int j = 0; j < BN / 128; ++j) {
-              if (j % CL != (int)rank) continue;
               const uint32_t d = smem_u32(st + C::kABytes + C::kBBytes + C::kSfaBytes + 2048 * j);
               const uint8_t* src = sfb + (int64_t)(n * (BN / 128) + j) * sf_row_stride + (int64_t)ks * 2048;
-              if constexpr (CL > 1) bulk_load_mc(d, src, 2048, fb, kMask);
-              else bulk_load(d, src, 2048, fb);
+              bulk_load(d, src, 2048, fb);
             }
             pending |= 1u << s;
             pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
@@ -218,8 +160,8 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
       }
       if (ok) {
-        // every slot released by every CTA of the cluster: no commit arrival is
-        // still on its way to this CTA's barriers when it exits
+        // every slot released: no commit arrival is still on its way to this
+        // CTA's barriers when it exits
         for (int i = 0; i < C::kStages && ok; ++i) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
           if (++s == C::kStages) { s = 0; ph ^= 1u; }
@@ -253,7 +195,7 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       uint32_t ph = 0, acc_ph = 0;
       bool ok = true;
       bool issued_any = false;
-      for (int gi = cid; gi < num_groups && ok; gi += ncl) {
+      for (int gi = cid; gi < num_tiles && ok; gi += ncl) {
         if (!mbar_wait(tmem_empty, acc_ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
         tc_fence_after();
         for (int ks = 0; ks < nk; ++ks) {
@@ -274,8 +216,7 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         sf_col + C::kSfaCols + (BN / 128) * 4 * j, (ks | j) != 0 ? 1u : 0u);
           }
           issued_any = true;
-          if constexpr (CL > 1) tc_commit_mc(empty_bar(s), kMask);
-          else tc_commit(empty_bar(s));
+          tc_commit(empty_bar(s));
           if (++s == C::kStages) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
@@ -297,8 +238,8 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     constexpr int kCols = BN / 2;
     const float alpha = __fmul_rn(__ldg(g_a), __ldg(g_b));
     uint32_t acc_ph = 0;
-    for (int gi = cid; gi < num_groups; gi += ncl) {
-      const int m = (gi / num_n) * CL + (int)rank, n = gi % num_n;
+    for (int gi = cid; gi < num_tiles; gi += ncl) {
+      const int m = gi / num_n, n = gi % num_n;
       if (!mbar_wait(tmem_full, acc_ph, &s_abort, timeout_ns)) { fail(); break; }
       tc_fence_after();
       const int row = m * BM + q * 32 + lane;
@@ -341,7 +282,6 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 
   tc_fence_before();
   __syncthreads();
-  if constexpr (CL > 1) cluster_sync();       // no peer writes into this CTA after it exits
   tc_fence_after();
   if (warp == 1) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
@@ -355,64 +295,23 @@ bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kby
                          (uint64_t)kbytes, BK_BYTES, (uint32_t)box_rows);
 }
 
-template <int BN, bool OUT_F32, int CL>
+template <int BN, bool OUT_F32>
 cudaError_t launch(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStream_t s) {
   using C = Cfg<BN>;
   CUtensorMap ma, mb;
-  if (!make_code_map(&ma, a.a.codes, a.m, a.k / 2, BM) ||
-      !make_code_map(&mb, a.b.codes, a.n, a.k / 2, BN / CL))
+  if (!make_code_map(&ma, a.a.codes, a.m, a.k / 2, BM) || !make_code_map(&mb, a.b.codes, a.n, a.k / 2, BN))
     return cudaErrorInvalidValue;
-  auto k = gemm_nvf4_kernel<BN, OUT_F32, CL>;
+  auto k = gemm_nvf4_kernel<BN, OUT_F32>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  // one persistent CTA per SM, in as many clusters as can be resident at once
-  int max_clusters = sm_count() / CL;
-  cfg.gridDim = dim3(max_clusters * CL, 1, 1);
-  int resident = 0;
-  if (CL > 1) {
-    if (cudaOccupancyMaxActiveClusters(&resident, k, &cfg) == cudaSuccess && resident > 0) {
-      if (resident < max_clusters) max_clusters = resident;
-    } else {
-      cudaGetLastError();
-    }
-  }
-  const int groups = (int)((a.m / (BM * CL)) * (a.n / BN));
-  const int clusters = groups < max_clusters ? groups : max_clusters;
-  cfg.gridDim = dim3(clusters * CL, 1, 1);
-  e = cudaLaunchKernelEx(&cfg, k, ma, mb, (const uint8_t*)a.a.scales, (const uint8_t*)a.b.scales,
-                         (const float*)a.a.tensor_scale, (const float*)a.b.tensor_scale, a.y, (int)a.m,
-                         (int)a.n, (int)a.k, static_cast<Workspace*>(a.ws), timeout_ns, skip,
-                         a.fmt == 0 ? 0 : 1);
-  if (e != cudaSuccess) return e;
+  // one persistent CTA per SM
+  const int tiles = (int)((a.m / BM) * (a.n / BN));
+  const int grid = tiles < sm_count() ? tiles : sm_count();
+  k<<<grid, kThreads, C::kSmem, s>>>(ma, mb, (const uint8_t*)a.a.scales, (const uint8_t*)a.b.scales,
+                                     (const float*)a.a.tensor_scale, (const float*)a.b.tensor_scale, a.y,
+                                     (int)a.m, (int)a.n, (int)a.k, static_cast<Workspace*>(a.ws), timeout_ns,
+                                     skip, a.fmt == 0 ? 0 : 1);
   return cudaGetLastError();
-}
-
-#ifndef FP4Q_GEMM_MAX_CLUSTER
-#define FP4Q_GEMM_MAX_CLUSTER 1
-#endif
-
-// Clusters cut the L2 reads of B but not the bytes each SM must take in (every
-// CTA still receives the whole B tile), which is what bounds this kernel on
-// B300: measured at 8192^3, no cluster 333 us, 2 CTAs 335 us, 4 CTAs 382 us.
-// The multicast path stays available at build time (FP4Q_GEMM_MAX_CLUSTER).
-template <int BN, bool OUT_F32>
-cudaError_t launch_cl(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStream_t s) {
-  // the widest cluster (up to FP4Q_GEMM_MAX_CLUSTER) whose m-tiles divide M
-  const int64_t mt = a.m / BM;
-  if (FP4Q_GEMM_MAX_CLUSTER >= 4 && mt % 4 == 0) return launch<BN, OUT_F32, 4>(a, timeout_ns, skip, s);
-  if (FP4Q_GEMM_MAX_CLUSTER >= 2 && mt % 2 == 0) return launch<BN, OUT_F32, 2>(a, timeout_ns, skip, s);
-  return launch<BN, OUT_F32, 1>(a, timeout_ns, skip, s);
 }
 
 }  // namespace
@@ -422,10 +321,10 @@ cudaError_t run_gemm_ex(const GemmArgs& a, uint64_t timeout_ns, int skip_first_s
   // (E8M0 scales; a 32-element block's scale is stored for both halves)
   if (a.fmt != 0 && a.fmt != 1 && a.fmt != 4 && a.fmt != 5) return cudaErrorNotSupported;
   const bool f32 = a.out_dtype == 1;
-  if (a.n % 256 == 0) return f32 ? launch_cl<256, true>(a, timeout_ns, skip_first_stage, s)
-                                 : launch_cl<256, false>(a, timeout_ns, skip_first_stage, s);
-  return f32 ? launch_cl<128, true>(a, timeout_ns, skip_first_stage, s)
-             : launch_cl<128, false>(a, timeout_ns, skip_first_stage, s);
+  if (a.n % 256 == 0) return f32 ? launch<256, true>(a, timeout_ns, skip_first_stage, s)
+                                 : launch<256, false>(a, timeout_ns, skip_first_stage, s);
+  return f32 ? launch<128, true>(a, timeout_ns, skip_first_stage, s)
+             : launch<128, false>(a, timeout_ns, skip_first_stage, s);
 }
 
 cudaError_t run_gemm(const GemmArgs& a, cudaStream_t s) {
