@@ -31,7 +31,8 @@ struct Workspace {
   unsigned int copies;          // axis bits produced by the last quantisation pass
   float tensor_scale[2];        // g of its row / column copy
   float qmax;                   // its Qmax
-  unsigned int gbar_count;      // grid barrier of the one-launch quantiser: arrivals (wraps to 0)
+  unsigned int gbar_count;      // grid barrier of the one-launch quantiser: arrivals (wraps to 0;
+                                // zeroed before each launch)
   double n;                     // its elements per copy
   unsigned int gbar_gen;        // grid barrier: generation, bumped by the last arrival
   unsigned int reserved;

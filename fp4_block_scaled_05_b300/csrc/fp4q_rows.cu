@@ -2108,6 +2108,11 @@ cudaError_t launch_quant_fused(const Flat& f, uint64_t seed, const CopyOut& o, W
   CopyOut oa = o;
   Workspace* wa = ws;
   void* args[] = {&fa, &sd, &pk, &oa, &wa, &to};
+  // A grid barrier that ran out of time leaves its arrival count part-way; a
+  // stale count would release this launch's barrier early (or never), so the
+  // count starts from zero on every call.
+  e = cudaMemsetAsync(&ws->gbar_count, 0, sizeof(ws->gbar_count), s);
+  if (e != cudaSuccess) return e;
   e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(k), dim3(grid), dim3(RT), args, smem, s);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

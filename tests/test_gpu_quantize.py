@@ -325,3 +325,30 @@ def test_rowwise_nonfinite_sets_status(lib, fmt):
         x[17, 3] = bad
         lib.fp4q_quantize(x.cuda(), fmt=fmt, axis="row", rht=True, seed=1)
         assert lib.fp4q_status() == 4, bad
+
+
+# Byte offset of the one-launch quantiser's grid-barrier arrival count in the
+# workspace header: after status, amax_nparts, stat_nparts, copies (4 x u32),
+# tensor_scale[2] and qmax (3 x f32).
+_GBAR_COUNT_OFFSET = 28
+
+
+@pytest.mark.parametrize("leftover", [3, 100000])
+def test_fused_barrier_ignores_a_stale_arrival_count(lib, leftover):
+    """A grid barrier whose wait ran out leaves its arrival count part-way.
+    Planted here on the host (no kernel is made to time out): the next
+    one-launch quantisation on that workspace must still see every CTA's
+    amax, so its tensor scale, scales and codes match the oracle."""
+    ws = torch.zeros(lib.fp4q_workspace_size(), dtype=torch.uint8, device="cuda")
+    big = synth.normal_with_outliers(512, 1024, 1000.0, 0.01, 20.0, 31)
+    small = synth.normal_with_outliers(512, 1024, 1.0, 0.01, 20.0, 32)
+    lib.fp4q_quantize(big.cuda(), fmt="nvfp4", rht=True, seed=8, axis="row", ws=ws)
+    torch.cuda.synchronize()
+    ws[_GBAR_COUNT_OFFSET:_GBAR_COUNT_OFFSET + 4] = torch.tensor(
+        [leftover], dtype=torch.int32).view(torch.uint8).cuda()
+    r, _ = lib.fp4q_quantize(small.cuda(), fmt="nvfp4", rht=True, seed=8, axis="row", ws=ws)
+    rs, _ = lib.fp4q_stats(ws)
+    assert lib.fp4q_status(ws) == 0
+    ref = o.quantize(_bits(small), "nvfp4", rht=True, seed=8, axis="row")["row"]
+    check_copy(r, ref, "linear")
+    check_stats(rs, ref["stats"])
