@@ -6,7 +6,7 @@ through its C ABI (include/fp4q.h). There is no CPU path: if the shared library
 is missing, importing this package fails.
 
 Function names follow the C ABI: fp4q_amax, fp4q_quantize, fp4q_dequantize, fp4q_stats,
-fp4q_status, fp4q_gemm, fp4q_gemm_selftest_timeout, fp4q_quantize_noalloc, fp4q_workspace_size, fp4q_workspace_init,
+fp4q_status, fp4q_gemm, fp4q_gemm_selftest_timeout, fp4q_quantize_noalloc, fp4q_status_noalloc, fp4q_workspace_size, fp4q_workspace_init,
 fp4q_scales_bytes, fp4q_strerror, fp4q_version.
 """
 from __future__ import annotations
@@ -67,6 +67,7 @@ _SIGS = {
     "fp4q_dequantize": ([_QP, _I64, _I64, _I, _I, _I, ctypes.c_uint64, _P, _I, _P], _I),
     "fp4q_stats": ([_P, _SP, _SP, _P], _I),
     "fp4q_status": ([_P, _P], _I),
+    "fp4q_status_noalloc": ([_P], _I),
     "fp4q_gemm": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
     "fp4q_gemm_selftest_timeout": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, ctypes.c_uint64, _P], _I),
     "fp4q_code_histogram": ([_QP, _I64, _I64, _P, _P], _I),
@@ -296,6 +297,16 @@ def fp4q_status(ws: torch.Tensor = None, device=None) -> int:
     rc = _lib.fp4q_status(ws.data_ptr(), _stream(ws.device))
     if rc not in (0, 4, 5):
         _check("fp4q_status", rc)
+    return rc
+
+
+def fp4q_status_noalloc(device=None) -> int:
+    """Device status of the fp4q_quantize_noalloc calls on the current device
+    (0, 4 = non-finite, 5 = timeout); clears it."""
+    dev = torch.device(device if device is not None else "cuda")
+    rc = _lib.fp4q_status_noalloc(_stream(dev))
+    if rc not in (0, 4, 5):
+        _check("fp4q_status_noalloc", rc)
     return rc
 
 

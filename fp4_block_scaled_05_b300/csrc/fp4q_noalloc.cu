@@ -64,3 +64,10 @@ extern "C" int fp4q_quantize_noalloc(const void* src, int dtype, int64_t rows, i
   return fp4q_quantize(src, dtype, rows, cols, fmt, block, rht, rounding, seed, axis, row_out,
                        col_out, scratch, kNoAllocScratchBytes, stream);
 }
+
+extern "C" int fp4q_status_noalloc(void* stream) {
+  void* scratch = nullptr;
+  const int rc = scratch_address(&scratch);
+  if (rc) return rc;
+  return fp4q_status(scratch, stream);
+}

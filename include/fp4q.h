@@ -224,8 +224,10 @@ int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols,
  * up the array's device address (cudaGetSymbolAddress) with that device
  * current, so make that first call before any stream capture. Every call
  * clears the status word and the counters of the array, then runs exactly
- * what fp4q_quantize runs; the statistics and status it records stay in the
- * array and are not readable (use fp4q_quantize with a workspace for them).
+ * what fp4q_quantize runs; the device status it records (non-finite input,
+ * a bounded wait that ran out) is read by fp4q_status_noalloc, while its
+ * statistics stay in the array and are not readable (use fp4q_quantize with
+ * a workspace for them).
  * All calls on a device share the one array: calls that overlap on the GPU
  * (other streams, other threads) race and must be serialised by the caller.
  * Arguments, outputs and errors as for fp4q_quantize, except that
@@ -236,6 +238,15 @@ int fp4q_quantize_noalloc(const void* src, int dtype, int64_t rows, int64_t cols
                           int fmt, int block, int rht, int rounding, uint64_t seed, int axis,
                           const fp4q_qtensor* row_out, const fp4q_qtensor* col_out,
                           void* stream);
+
+/* fp4q_status for fp4q_quantize_noalloc's library-owned scratch (no paper
+ * counterpart: a calling convention). Synchronises `stream`, returns the
+ * device status the no-allocation calls on the current device recorded since
+ * the previous call of this function or since their last start (each
+ * fp4q_quantize_noalloc call clears it), FP4Q_OK, FP4Q_ENONFINITE or
+ * FP4Q_ETIMEOUT, and clears it. Allocates nothing. FP4Q_ECUDA if the lookup
+ * of the scratch or the synchronisation failed. */
+int fp4q_status_noalloc(void* stream);
 
 /* Dequantise one copy ([UFP4] §2: UFP4 has no tensor-core format and is
  * consumed through this call): v_hat = (level * s_b) * g in FP32, two

@@ -60,6 +60,17 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(lib):
             _same(got_r, want_r)
             _same(got_c, want_c)
     assert lib.fp4q_status() == 0
+    assert lib.fp4q_status_noalloc() == 0
+
+
+def test_noalloc_status_reports_nonfinite_input(lib):
+    """The status of a no-allocation call is readable without a workspace:
+    a NaN in the input is reported once, then cleared."""
+    x = synth.normal(64, 256, 1.0, 45)
+    x[9, 17] = float("nan")
+    lib.fp4q_quantize_noalloc(x.cuda(), fmt="nvfp4", axis="row")
+    assert lib.fp4q_status_noalloc() == 4
+    assert lib.fp4q_status_noalloc() == 0
 
 
 def test_noalloc_binding_and_rejections(lib):
