@@ -256,8 +256,8 @@ def ncu_traffic(kernel: str, units: float) -> float | None:
 # --------------------------------------------------------------------------- #
 
 def oracle_step(bits, seed: int = SEED) -> dict:
-    """One step of the path on the CPU oracle (test infrastructure; used only
-    for the baseline timing)."""
+    """One step of the path on the CPU oracle, one thread (test infrastructure;
+    used only for the baseline timing)."""
     from oracle import fp4q_oracle as o
     out = {}
     for fmt, rht in WAYS:
@@ -267,9 +267,98 @@ def oracle_step(bits, seed: int = SEED) -> dict:
     return out
 
 
+# ---- the oracle on every host core: a process pool over row ranges -------------
+# Each worker holds the whole input; a step runs, per way, pass 1 (the copy's
+# amax) over row ranges in parallel, then pass 2 (scales, codes, statistics;
+# for the UFP4 way also the dequantisation of those rows) over the same ranges
+# with the tensor amax of pass 1. The arithmetic is the oracle's, unchanged.
+
+_POOL_M32 = None
+_POOL_SHM = None
+
+
+def _pool_init(shm_name, shape):
+    import os as _os
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        _os.environ[var] = "1"
+    import numpy as np
+    from multiprocessing import shared_memory
+    global _POOL_M32, _POOL_SHM
+    _POOL_SHM = shared_memory.SharedMemory(name=shm_name)
+    _POOL_M32 = np.ndarray(shape, dtype=np.float32, buffer=_POOL_SHM.buf)
+
+
+def _pool_amax(task):
+    from oracle import fp4q_oracle as o
+    fmt, rht, seed, r0, r1 = task
+    return float(o.copy_amax(_POOL_M32[r0:r1], fmt, rht, seed))
+
+
+def _pool_quant(task):
+    import numpy as np
+    from oracle import fp4q_oracle as o
+    fmt, rht, seed, r0, r1, amax, dequant = task
+    q = o.quantize_copy(_POOL_M32, fmt, rht, "rtne", seed, 0, rows_subset=np.arange(r0, r1),
+                        amax=np.float32(amax))
+    if dequant:
+        o.dequantize(q["codes"], q["scales"], q["tensor_scale"], fmt, True, seed)
+    st = q["stats"]
+    return st["shrink_bias"] * st["n"], st["sum_sig2"], st["sum_err2"]
+
+
+def _row_ranges(rows: int, parts: int):
+    step = max(16, -(-rows // parts) // 16 * 16)
+    return [(r0, min(rows, r0 + step)) for r0 in range(0, rows, step)]
+
+
+def oracle_step_parallel(pool, rows: int, parts: int, seed: int = SEED) -> None:
+    ranges = _row_ranges(rows, parts)
+    for fmt, rht in WAYS:
+        amax = max(pool.map(_pool_amax, [(fmt, rht, seed, r0, r1) for r0, r1 in ranges]))
+        pool.map(_pool_quant, [(fmt, rht, seed, r0, r1, amax, fmt == "ufp4") for r0, r1 in ranges])
+
+
+def host_description() -> dict:
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.startswith("model name"):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+class OraclePool:
+    """A spawn-started pool of one worker per host core (up to 256). The first
+    `rows` rows of the activation tensor, widened to FP32 once by the oracle,
+    sit in shared memory that every worker maps."""
+
+    def __init__(self, rows: int):
+        import multiprocessing as mp
+        from multiprocessing import shared_memory
+        import numpy as np
+        import synth
+        from oracle import fp4q_oracle as o
+        m32 = o._as_f32_matrix(synth.bf16_bits(synth.activation(ROWS, COLS)[:rows]))
+        self.shm = shared_memory.SharedMemory(create=True, size=m32.nbytes)
+        np.ndarray(m32.shape, dtype=np.float32, buffer=self.shm.buf)[...] = m32
+        self.n = min(os.cpu_count() or 1, 256)
+        self.pool = mp.get_context("spawn").Pool(self.n, initializer=_pool_init,
+                                                 initargs=(self.shm.name, m32.shape))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        self.shm.close()
+        self.shm.unlink()
+
+
 def time_oracle(rows: int, reps: int = 1) -> dict:
-    """CPU seconds and wall seconds of `reps` oracle steps on the first `rows`
-    rows of the activation tensor."""
+    """CPU seconds and wall seconds of `reps` one-thread oracle steps on the
+    first `rows` rows of the activation tensor."""
     import synth
     x = synth.activation(ROWS, COLS)[:rows]
     bits = synth.bf16_bits(x)
@@ -282,45 +371,65 @@ def time_oracle(rows: int, reps: int = 1) -> dict:
     return {"wall": wall, "cpu": cpu, "cores": max(1, round(cpu / wall)) if wall > 0 else 1}
 
 
-def cpu_baseline(sample_rows: int = 4096) -> dict:
-    t = time_oracle(sample_rows)
-    gbs = step_bytes(sample_rows, COLS) / t["wall"] / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": t["cores"], "kind": "oracle",
-            "sample": f"one step on the first {sample_rows} of {ROWS} rows "
-                      f"({sample_rows * COLS} elements; tensor amax over the sample), "
-                      f"{t['wall']:.2f} s wall, numpy"}
+def cpu_baseline(single_rows: int = 2048) -> dict:
+    """The oracle on the host: one thread on the first `single_rows` rows, and
+    every core (a spawn-started process pool over row ranges) on the whole
+    8192 x 4096 step. `value` is the all-cores figure."""
+    t1 = time_oracle(single_rows)
+    one = step_bytes(single_rows, COLS) / t1["wall"] / 1e9
+    op = OraclePool(ROWS)
+    n = op.n
+    try:
+        oracle_step_parallel(op.pool, 64, n)         # workers started, imports done
+        w0 = time.perf_counter()
+        oracle_step_parallel(op.pool, ROWS, n)
+        wall = time.perf_counter() - w0
+    finally:
+        op.close()
+    allc = step_bytes(ROWS, COLS) / wall / 1e9
+    return {"value": allc, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "sample": f"one whole step (8192 x 4096, three ways + UFP4 dequantisation) on {n} worker "
+                      f"processes over row ranges (pass 1 amax, then pass 2 with the tensor amax), "
+                      f"{wall:.2f} s wall, numpy",
+            "single_core": {"value": one, "unit": "GB/s", "cores": 1,
+                            "sample": f"one step on the first {single_rows} of {ROWS} rows "
+                                      f"(tensor amax over the sample), {t1['wall']:.2f} s wall"},
+            "host": host_description()}
 
 
 def reference_arm(args) -> int:
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    # each step is a bounded sample sized so the whole run stays near two minutes
-    probe = time_oracle(64)
-    per_row = probe["wall"] / 64
-    budget = 120.0 / (args.steps + args.warmup)
-    rows = int(max(16, min(ROWS, budget / per_row)) // 16 * 16)
-    import synth
-    from oracle import fp4q_oracle  # noqa: F401
-    bits = synth.bf16_bits(synth.activation(ROWS, COLS)[:rows])
-    for _ in range(args.warmup):
-        oracle_step(bits)
-    c0, w0 = time.process_time(), time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(bits)
-    wall = time.perf_counter() - w0
-    cpu = time.process_time() - c0
-    cores = max(1, round(cpu / wall)) if wall > 0 else 1
+    # each step is a bounded sample of rows on every host core, sized so the
+    # whole run stays near two minutes
+    op = OraclePool(ROWS)
+    n, pool = op.n, op.pool
+    try:
+        oracle_step_parallel(pool, 64, n)
+        w0 = time.perf_counter()
+        oracle_step_parallel(pool, min(ROWS, 16 * n), n)
+        per_row = (time.perf_counter() - w0) / min(ROWS, 16 * n)
+        budget = 120.0 / (args.steps + args.warmup)
+        rows = int(max(16, min(ROWS, budget / per_row)) // 16 * 16)
+        for _ in range(args.warmup):
+            oracle_step_parallel(pool, rows, n)
+        w0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_step_parallel(pool, rows, n)
+        wall = time.perf_counter() - w0
+    finally:
+        op.close()
     value = step_bytes(rows, COLS) * args.steps / wall / 1e9
-    sample = (f"each step on the first {rows} of {ROWS} rows ({rows * COLS} elements; "
-              f"tensor amax over the sample), numpy")
+    sample = (f"each step on the first {rows} of {ROWS} rows ({rows * COLS} elements; tensor amax over "
+              f"the sample), {n} worker processes over row ranges, numpy")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": workload_config({"sample_rows": rows}),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle",
+                             "sample": sample, "host": host_description()},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
@@ -590,60 +699,102 @@ def run_gemm_ufp4_leg(fq, torch, device, steps, warmup, peaks):
             "launches": len(evs), "snr_db_vs_bf16_product": snr}
 
 
+def sweep_point(fq, torch, device, x, steps, warmup, peaks, ws, flush) -> dict:
+    """One size of the sweep: MXFP4 (32-element E8M0 blocks, one pass) and
+    NVFP4 (16-element E4M3 blocks, amax pass + quantisation pass) on the R x
+    4096 tensor x, RTNE, no RHT, row-wise: median time per call and GB/s of
+    algorithmic bytes, L2 flushed before each call. NVFP4 is timed as the
+    two-call split (fp4q_amax, then fp4q_quantize with the amax ready) and as
+    one fp4q_quantize call."""
+    stream = torch.cuda.current_stream(device)
+    rows, cols = x.shape
+    n = rows * cols
+    out = {}
+    for fmt in ("mxfp4", "nvfp4"):
+        q = fq.alloc_copy(rows, cols, fmt, "linear", device)
+        times = {"amax": [], "quant": [], "one": []}
+        for k in range(warmup + steps):
+            flush.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            fq.fp4q_amax(x, fmt=fmt, ws=ws)
+            e1.record(stream)
+            fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q, amax_ready=True)
+            e2.record(stream)
+            flush.zero_()
+            e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+            e3.record(stream)
+            fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q)
+            e4.record(stream)
+            if k >= warmup:
+                times["amax"].append((e0, e1))
+                times["quant"].append((e1, e2))
+                times["one"].append((e3, e4))
+        torch.cuda.synchronize(device)
+        t_one = statistics.median(a.elapsed_time(b) for a, b in times["one"])
+        t_a = statistics.median(a.elapsed_time(b) for a, b in times["amax"]) if fmt == "nvfp4" else 0.0
+        t_q = statistics.median(a.elapsed_time(b) for a, b in times["quant"])
+        b_q = (2.0 + 0.5 + (1.0 / 16 if fmt == "nvfp4" else 1.0 / 32)) * n
+        b_a = 2.0 * n if fmt == "nvfp4" else 0.0
+        out[fmt] = {"call_us": (t_a + t_q) * 1e3, "call_GB/s": (b_a + b_q) / ((t_a + t_q) / 1e3) / 1e9,
+                    "quant_us": t_q * 1e3, "quant_GB/s": b_q / (t_q / 1e3) / 1e9,
+                    "quant_frac_hbm": b_q / (t_q / 1e3) / 1e9 / peaks["hbm_gbs"],
+                    "quant_bytes_per_element": b_q / n}
+        if fmt == "nvfp4":
+            out[fmt].update({"amax_us": t_a * 1e3, "amax_GB/s": b_a / (t_a / 1e3) / 1e9,
+                             "amax_frac_hbm": b_a / (t_a / 1e3) / 1e9 / peaks["hbm_gbs"],
+                             "one_launch_us": t_one * 1e3,
+                             "one_launch_GB/s": (b_a + b_q) / (t_one / 1e3) / 1e9,
+                             "call_frac_hbm": (b_a + b_q) / ((t_a + t_q) / 1e3) / 1e9 / peaks["hbm_gbs"]})
+        else:
+            out[fmt]["launches"] = 3 * (warmup + steps)
+        del q
+    return out
+
+
 def run_sweep(fq, torch, device, args, peaks) -> None:
-    """MXFP4 (32-element E8M0 blocks, one pass) vs NVFP4 (16-element E4M3
-    blocks, amax pass + quantisation pass) on R x 4096 N(0,1) BF16 tensors,
-    RTNE, no RHT, row-wise: time per call and GB/s of algorithmic bytes. NVFP4
-    is timed as the two-call split (fp4q_amax, then fp4q_quantize with the amax
-    ready) and as the one-launch fp4q_quantize."""
+    """The size sweep: R x 4096 N(0,1) BF16, R = 2^8 .. 2^18, one JSON line
+    per size (sweep_point)."""
     import synth
     cols = 4096
     ws = fq.workspace(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream(device)
     rows_list = [r for r in synth.sweep_rows() if r <= args.sweep_max_rows]
     x_full = synth.sweep(max(rows_list), cols).to(device)
     for rows in rows_list:
-        x = x_full[:rows]
-        n = rows * cols
-        out = {}
-        for fmt in ("mxfp4", "nvfp4"):
-            q = fq.alloc_copy(rows, cols, fmt, "linear", device)
-            times = {"amax": [], "quant": [], "one": []}
-            for k in range(args.warmup + args.steps):
-                flush.zero_()
-                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-                e0.record(stream)
-                fq.fp4q_amax(x, fmt=fmt, ws=ws)
-                e1.record(stream)
-                fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q, amax_ready=True)
-                e2.record(stream)
-                flush.zero_()
-                e3, e4 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
-                e3.record(stream)
-                fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q)
-                e4.record(stream)
-                if k >= args.warmup:
-                    times["amax"].append((e0, e1))
-                    times["quant"].append((e1, e2))
-                    times["one"].append((e3, e4))
-            torch.cuda.synchronize(device)
-            t_one = statistics.median(a.elapsed_time(b) for a, b in times["one"])
-            t_a = statistics.median(a.elapsed_time(b) for a, b in times["amax"]) if fmt == "nvfp4" else 0.0
-            t_q = statistics.median(a.elapsed_time(b) for a, b in times["quant"])
-            b_q = (2.0 + 0.5 + (1.0 / 16 if fmt == "nvfp4" else 1.0 / 32)) * n
-            b_a = 2.0 * n if fmt == "nvfp4" else 0.0
-            out[fmt] = {"call_us": (t_a + t_q) * 1e3, "call_GB/s": (b_a + b_q) / ((t_a + t_q) / 1e3) / 1e9,
-                        "quant_us": t_q * 1e3, "quant_GB/s": b_q / (t_q / 1e3) / 1e9,
-                        "quant_frac_hbm": b_q / (t_q / 1e3) / 1e9 / peaks["hbm_gbs"]}
-            if fmt == "nvfp4":
-                out[fmt].update({"amax_us": t_a * 1e3, "amax_GB/s": b_a / (t_a / 1e3) / 1e9,
-                                 "one_launch_us": t_one * 1e3,
-                                 "one_launch_GB/s": (b_a + b_q) / (t_one / 1e3) / 1e9})
-            del q
+        out = sweep_point(fq, torch, device, x_full[:rows], args.steps, args.warmup, peaks, ws, flush)
         print(json.dumps({"sweep": "R x 4096 BF16 N(0,1), RTNE, no RHT, row-wise", "rows": rows,
-                          "elements": n, **out}), flush=True)
+                          "elements": rows * cols, **out}), flush=True)
     assert fq.fp4q_status(ws) == 0
+
+
+def run_sweep_largest_leg(fq, torch, device, steps, warmup, peaks) -> dict:
+    """The sweep's largest point (262144 x 4096 = 2^30 elements, 2 GiB of BF16:
+    far above L2), as the default run's keyed entry, with a roofline for each
+    pass."""
+    import synth
+    rows = synth.sweep_rows()[-1]
+    x = synth.sweep(rows, 4096).to(device)
+    ws = fq.workspace(device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    out = sweep_point(fq, torch, device, x, steps, warmup, peaks, ws, flush)
+    status = fq.fp4q_status(ws)
+    del x
+    torch.cuda.empty_cache()
+    n = rows * 4096
+    peak = peaks["hbm_gbs"]
+
+    def roof(gbs, ncu_name):
+        return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                "peak_source": f"{peaks['source']} (copy bandwidth)", "traffic": ncu_traffic(ncu_name, n)}
+
+    return {"workload": f"size sweep, largest point: {rows} x 4096 BF16 N(0,1) ({n} elements), RTNE, no RHT, "
+                        "row-wise; MXFP4 (32-element E8M0, one pass) vs NVFP4 (16-element E4M3, amax pass + "
+                        "quantisation pass); median per call, L2 flushed before each",
+            **out, "device_status": status,
+            "roofline": {"mxfp4_quantize": roof(out["mxfp4"]["quant_GB/s"], "quant_rows_kernel"),
+                         "nvfp4_amax": roof(out["nvfp4"]["amax_GB/s"], "amax_rows_kernel"),
+                         "nvfp4_quantize": roof(out["nvfp4"]["quant_GB/s"], "quant_rows_kernel")}}
 
 
 def run_grad_leg(fq, torch, device, steps, warmup):
@@ -839,6 +990,7 @@ def main(argv=None) -> int:
     tl_r = run_two_level_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     hist_r = run_histogram_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     mx_r = run_mx_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
+    sweep_r = run_sweep_largest_leg(fq, torch, device, min(args.steps, 20), args.warmup, peaks)
     e2e_steps = min(args.steps, 100)
     e2e_r = None if args.no_e2e else run_e2e_leg(fq, torch, device, e2e_steps, args.warmup)
     clocks = sampler.stop()
@@ -935,6 +1087,7 @@ def main(argv=None) -> int:
                     "GEMM 8192^3 on the tensor cores with E8M0 scales (MXFP4, OAS) and with per-128 FP32 "
                     "scales along K (two-level NVFP4, MBS); operands + RHT16 along K",
         **mx_r}
+    line["sweep_largest"] = sweep_r
     line["clocks"] = clocks
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

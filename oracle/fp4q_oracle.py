@@ -426,9 +426,22 @@ def tensor_scale(amax: np.float32, fmt: str) -> np.float32:
     return F32(F32(amax) / F32(QMAX[fmt] * E4M3_MAX))
 
 
+def copy_amax(m32: np.ndarray, fmt: str, rht: bool = False, seed: int = 0,
+              rht_mode: str = "butterfly", chunk_rows: int = 256) -> np.float32:
+    """Pass 1 of a copy: A = max |v| over every (transformed) value of the
+    rows x cols matrix m32, blocks along its columns."""
+    amax = F32(0.0)
+    for r0 in range(0, m32.shape[0], chunk_rows):
+        v = transform_copy(m32[r0:r0 + chunk_rows], fmt, rht, seed, rht_mode)
+        if v.size:
+            amax = max(amax, tensor_amax(v))
+    return amax
+
+
 def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = "rtne",
                   seed: int = 0, axis: int = 0, rht_mode: str = "butterfly",
-                  chunk_rows: int = 256, keep_y: bool = False, rows_subset=None) -> dict:
+                  chunk_rows: int = 256, keep_y: bool = False, rows_subset=None,
+                  amax=None) -> dict:
     """Quantise one copy: a rows x cols FP32 matrix whose blocks run along the
     columns. For the row-wise copy this is X itself; for the column-wise copy it
     is X^T ([TJ2] §2A: the transposed operand of the weight-gradient GEMM).
@@ -448,6 +461,8 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
       q   = RTNE(y) or SR(y, u_i)
     ``rows_subset`` (row indices of the copy) restricts the codes, scales and
     statistics to those rows; the tensor amax still covers the whole copy.
+    ``amax``: the copy's tensor amax when pass 1 already ran (copy_amax over
+    the whole copy); m32 may then hold only some of the copy's rows.
     Statistics (FP64): bias = sum(|q| - |y|) / (Qmax * N)   (reading R6)
                        snr_db = 10 log10(sum v^2 / sum (v - v_hat)^2), v_hat =
                        q * s_b * g (or q * 2^e_b) exactly in FP64.
@@ -463,11 +478,9 @@ def quantize_copy(m32: np.ndarray, fmt: str, rht: bool = False, rounding: str = 
     assert levels_top == qmax
 
     # Pass 1: the tensor amax over every transformed value of the copy.
-    amax = F32(0.0)
-    for r0 in range(0, n, chunk_rows):
-        v = transform_copy(m32[r0:r0 + chunk_rows], fmt, rht, seed, rht_mode)
-        if v.size:
-            amax = max(amax, tensor_amax(v))
+    if amax is None:
+        amax = copy_amax(m32, fmt, rht, seed, rht_mode, chunk_rows)
+    amax = F32(amax)
     g = tensor_scale(amax, fmt)
     d = F32(F32(qmax) * g)
 

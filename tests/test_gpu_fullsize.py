@@ -66,3 +66,34 @@ def test_gradient_both_copies_full_size(lib, which):
         assert np.array_equal(got.scales[idx].cpu().numpy(), want["scales"])
         ts = got.tensor_scale.cpu().numpy().view(np.uint32)[0]
         assert ts == np.float32(want["tensor_scale"]).view(np.uint32)
+
+
+@pytest.fixture(scope="module")
+def sweep_largest():
+    """The size sweep's largest point: 262144 x 4096 BF16 N(0,1) (2^30 elements)."""
+    x = synth.sweep(1 << 18, 4096)
+    return x, synth.bf16_bits(x)
+
+
+@pytest.mark.parametrize("fmt", ["mxfp4", "nvfp4"])
+def test_sweep_largest_size_sampled(lib, sweep_largest, fmt):
+    """2^30 elements in the launch configuration bench.py times for the size
+    sweep: MXFP4 (32-element E8M0 blocks, one pass) and NVFP4 (16-element E4M3
+    blocks, one fp4q_quantize call: amax pass then quantisation pass), RTNE, no
+    RHT, row-wise, linear scales. Sampled rows (both ends, chunk boundaries, a
+    seeded spread) against the oracle; NVFP4's tensor scale comes from the
+    whole tensor on both sides."""
+    import torch
+    x, bits = sweep_largest
+    rows, cols = x.shape
+    xd = x.cuda()
+    r, _ = lib.fp4q_quantize(xd, fmt=fmt, axis="row")
+    assert lib.fp4q_status() == 0
+    del xd
+    sel = np.unique(np.concatenate([_sample(rows, 2, k=60), [rows // 2 - 1, rows // 2]])).astype(np.int64)
+    ref = o.quantize(bits, fmt, rows_subset=sel)["row"]
+    idx = torch.from_numpy(sel).cuda()
+    assert np.array_equal(r.codes[idx].cpu().numpy(), ref["codes"])
+    assert np.array_equal(r.scales[idx].cpu().numpy(), ref["scales"])
+    ts = r.tensor_scale.cpu().numpy().view(np.uint32)[0]
+    assert ts == np.float32(ref["tensor_scale"]).view(np.uint32)

@@ -103,8 +103,17 @@ def test_gemm_full_size_sampled(lib):
     cols = np.sort(rng.choice(n, 64, replace=False))
     ra = o.quantize(_bits(a), "nvfp4", rht=True, seed=1234, rows_subset=rows)["row"]
     rb = o.quantize(_bits(b), "nvfp4", rht=True, seed=1234, rows_subset=cols)["row"]
-    assert ra["tensor_scale"] == qa.tensor_scale.item()
-    ref = ra["codes"], rb["codes"]
+    # the operands themselves: sampled rows of A and of B (codes, tiled scales,
+    # tensor scale from the whole operand) against the oracle, bit for bit
+    for q, r, sel in ((qa, ra, rows), (qb, rb, cols)):
+        idx = torch.from_numpy(sel).cuda()
+        assert np.array_equal(q.codes[idx].cpu().numpy(), r["codes"])
+        nkb = n // 16
+        nkb_p = -(-nkb // 4) * 4
+        rr, kb = np.meshgrid(sel, np.arange(nkb), indexing="ij")
+        off = torch.from_numpy(o.mma_scale_offset(rr, kb, nkb_p).astype(np.int64)).cuda()
+        assert np.array_equal(q.scales[off].cpu().numpy(), r["scales"])
+        assert np.float32(r["tensor_scale"]).view(np.uint32) == q.tensor_scale.cpu().numpy().view(np.uint32)[0]
     yref = o.gemm(ra, rb)                       # the sampled rows x cols block, FP64
     got = y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].float().cpu().numpy()
     ref_bf16 = o.bf16_bits_to_f32(o.f32_to_bf16_bits_rne(yref.astype(np.float32)))
@@ -113,7 +122,6 @@ def test_gemm_full_size_sampled(lib):
     snr = o.snr_db(exact, got)
     assert 15.0 < snr < 40.0, snr
     assert lib.fp4q_status() == 0
-    del ref
 
 
 def test_bounded_wait_runs_out_without_fault(lib):
