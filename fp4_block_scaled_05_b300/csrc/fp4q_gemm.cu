@@ -10,7 +10,11 @@
 // switches to UE8M0, and a 32-element block's scale sits in the scale layout
 // once for each of its 16-element halves.
 //
-// Structure (one persistent CTA per SM, 320 threads):
+// Two kernels: when M and N are multiples of 256, CTA pairs share each
+// 256 x 256 tile through the two-SM MMA (gemm_nvf4_pair_kernel, below);
+// otherwise one CTA per 128 x BN tile (gemm_nvf4_kernel).
+//
+// One-CTA structure (one persistent CTA per SM, 320 threads):
 //   warp 0      TMA producer: per K stage of 256 elements, one 2-D tiled TMA
 //               load (128B swizzle) of the A and B code tiles and 1-D bulk
 //               copies of their scale tiles into a 4-deep shared-memory ring
@@ -288,6 +292,364 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   }
 }
 
+// ---- the CTA-pair kernel (tcgen05 cta_group::2) ----------------------------------------
+// Two CTAs of a cluster (ranks 0 and 1, on the two SMs of a pair) compute one
+// 256 x 256 tile of Y together: rank r holds rows [128 r, 128 r + 128) of the
+// tile's A rows and of its B rows (the B tile is split along N), the scales of
+// its own A rows, and the scales of all 256 B rows. One thread of rank 0 issues
+// every scale copy and MMA for both (cta_group::2): each instruction reads the
+// shared memory of both CTAs at the same offsets and writes both tensor
+// memories, so each SM takes in half of B per multiply-add instead of all of
+// it, and one scale copy serves two SMs. Each CTA's TMEM holds its 128 rows x
+// 256 columns of the accumulator.
+//
+// Hand-offs between the two CTAs (no multicast):
+//   rank 1's stage ready (TMA landed, its scales expanded) -> rank 1 warp 1
+//     relays it to rank 0's pfull[s]
+//   rank 0's MMA thread commits each stage to empty[s] of both CTAs (two
+//     unicast commits) and each finished tile to tfull of both CTAs
+//   every epilogue warp of both CTAs -> rank 0's tempty (accumulator read out)
+// The relays are relaxed arrivals: each hands on an event the relaying thread
+// has observed complete within its own CTA (the stage's TMA bytes counted in
+// by the mbarrier and the helpers' expanded scales stored, fenced for the
+// async proxy and released on a CTA barrier; or a warp's TMEM reads finished,
+// tcgen05.wait::ld). A release at cluster scope measured ~0.8 us per arrival
+// here, which the stage time cannot afford.
+//
+// Scale factors: the block-scaled MMA reads each operand's scales from TMEM,
+// where tcgen05.cp puts them, and every copy instruction costs the tensor
+// pipe a fixed time: twelve 32x128b.warpx4 copies of 512 bytes per stage took
+// about half of the pipe's time. So helper warps in each CTA first expand the
+// stage's scale tiles (512 bytes per 128 rows x 64 K elements, the layout the
+// quantiser writes) in shared memory into 4 KB blocks in which each of the
+// four 32-lane quadrants finds its copy of the 32-row pattern, with two K
+// chunks of A, or both 128-row halves of B's tile, side by side. Six 128x256b
+// copies per stage then fill what twelve copies filled. Two helper warps
+// share the expansion (one alone took most of a stage's time; a third only
+// moved the bound). The expanded blocks sit in a ring of three slots; a slot
+// is reused once the MMAs of the stage three back have completed.
+// Every wait is bounded, as in the one-CTA kernel.
+struct PairCfg {
+  static constexpr int kStages = 4;
+  static constexpr int kABytes = 128 * BK_BYTES;          // this CTA's 128 rows of A
+  static constexpr int kBBytes = 128 * BK_BYTES;          // this CTA's 128 rows of B
+  static constexpr int kSfaBytes = 2048;                  // its A rows' scales: 4 K chunks x 512 B
+  static constexpr int kSfbBytes = 4096;                  // all 256 B rows' scales
+  static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
+  static constexpr int kSfaCols = 16;
+  static constexpr int kSfbCols = 32;
+  static constexpr int kSfStageCols = kSfaCols + kSfbCols;
+  static constexpr int kSfBase = 256;                     // accumulator: columns [0, 256)
+  static constexpr int kRepSlots = 3;
+  static constexpr int kRepBytes = 6 * 4096;             // SFA chunks 0-1, 2-3; SFB chunks 0..3
+  static constexpr int kSmem = kStages * kStageBytes + kRepSlots * kRepBytes + 1024 + 256;
+  static constexpr int kHelperWarps = 2;                   // scale expansion: A + B chunk 0, B chunks 1-3
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kHelperWarps;
+  static constexpr int kHelperWarp = 2 + kEpiWarps;
+  static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+// One 16-byte row of a 32x128b scale tile, expanded into the 128 lanes of a
+// 128x256b copy source (8-row core matrices of 16 bytes: 8-row groups 256
+// bytes apart, the two 16-byte halves of a row 128 bytes apart): lane 32q + l
+// of half `half` gets it for every quadrant q.
+__device__ __forceinline__ void expand_row(uint8_t* blk, int l, int half, uint4 v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int L = 32 * q + l;
+    *reinterpret_cast<uint4*>(blk + (L >> 3) * 256 + half * 128 + (L & 7) * 16) = v;
+  }
+}
+
+__device__ __forceinline__ void tc2_cp_256(uint32_t taddr, uint64_t desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+template <bool OUT_F32>
+__global__ void __launch_bounds__(PairCfg::kThreads, 1)
+gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                      const uint8_t* __restrict__ sfa, const uint8_t* __restrict__ sfb,
+                      const float* __restrict__ g_a, const float* __restrict__ g_b, void* __restrict__ y,
+                      int M, int N, int K, Workspace* ws, uint64_t timeout_ns, int skip_first_stage,
+                      int ue8m0) {
+  using C = PairCfg;
+  constexpr int S = C::kStages;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* rep_ring = smem + S * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(rep_ring + C::kRepSlots * C::kRepBytes);
+  // bars[0..S): full, [S..2S): pfull, [2S..3S): empty, 3S: tfull, 3S+1: tempty, 3S+2: drain,
+  // 3S+3+r: rfull[r] (expanded scales of ring slot r written)
+  __shared__ uint32_t s_tmem_base;
+  __shared__ volatile int s_abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = (int)cluster_id_x(), npairs = (int)cluster_count_x();
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto pfull_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  const uint32_t tfull = bar0 + 8u * (3 * S);
+  const uint32_t tempty = bar0 + 8u * (3 * S + 1);
+  const uint32_t drain_bar = bar0 + 8u * (3 * S + 2);
+  auto rfull_bar = [&](int r) { return bar0 + 8u * (3 * S + 3 + r); };
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(pfull_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * kEpiWarps);
+    mbar_init(drain_bar, 1);
+    for (int r = 0; r < C::kRepSlots; ++r) mbar_init(rfull_bar(r), C::kHelperWarps);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    // one warp of each CTA of the pair allocates, collectively, in both TMEMs
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(&s_tmem_base)), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();          // both CTAs' barriers exist before any cross-CTA arrival
+  tc_fence_after();
+  const uint32_t tmem = s_tmem_base;
+
+  const int num_n = N / 256;
+  const int num_tiles = (M / 256) * num_n;
+  const int nk = K / BK;
+  const int64_t sf_row_stride = (int64_t)(K / 64) * 512;   // bytes per 128-row scale tile row
+
+  auto fail = [&]() {
+    if (!s_abort) {
+      s_abort = 1;
+      atomicOr(&ws->status, kStatusTimeout);
+    }
+  };
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t pending = 0, pend_ph = 0;
+      bool ok = true;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        const int pm = t / num_n, n = t % num_n;
+        const int arow = pm * 256 + (int)rank * 128;
+        const int brow = n * 256 + (int)rank * 128;
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          const bool skip = skip_first_stage && rank == 0 && pair == 0 && t == pair && ks == 0;
+          pending &= ~(1u << s);
+          if (!skip) {
+            uint8_t* st = smem + s * C::kStageBytes;
+            const uint32_t fb = full_bar(s);
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
+            tma_load_2d(smem_u32(st), &tmap_a, fb, ks * BK_BYTES, arow);
+            tma_load_2d(smem_u32(st + C::kABytes), &tmap_b, fb, ks * BK_BYTES, brow);
+            bulk_load(smem_u32(st + C::kABytes + C::kBBytes),
+                      sfa + (int64_t)(arow / 128) * sf_row_stride + (int64_t)ks * 2048, 2048, fb);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              bulk_load(smem_u32(st + C::kABytes + C::kBBytes + C::kSfaBytes + 2048 * h),
+                        sfb + (int64_t)(n * 2 + h) * sf_row_stride + (int64_t)ks * 2048, 2048, fb);
+            pending |= 1u << s;
+            pend_ph = (pend_ph & ~(1u << s)) | (ph << s);
+          }
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (ok) {
+        // every slot released: no commit is still on its way to this CTA's
+        // barriers when it exits
+        for (int i = 0; i < S && ok; ++i) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        const uint64_t t0 = globaltimer();
+        for (int ss = 0; ss < S; ++ss) {
+          if (!(pending & (1u << ss))) continue;
+          const uint32_t par = (pend_ph >> ss) & 1u;
+          while (!mbar_try_wait(full_bar(ss), par) && globaltimer() - t0 < 50000000ull) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 1) {
+      // ---------------- rank 1: hand each landed stage to rank 0 ----------------
+      // (its A, B and expanded scales: the helper waited for the stage's copies)
+      const uint32_t peer_pfull0 = peer_addr(pfull_bar(0), 0);
+      int s = 0;
+      uint32_t g = 0;
+      for (int t = pair; t < num_tiles; t += npairs) {
+        bool ok = true;
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          if (!mbar_wait(rfull_bar((int)(g % C::kRepSlots)), (g / C::kRepSlots) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          mbar_arrive_remote(peer_pfull0 + 8u * s);
+          if (++s == S) s = 0;
+        }
+        if (!ok) break;
+      }
+    } else if (lane == 0) {
+      // ---------------- rank 0: MMA issuer for the pair ----------------
+      const uint32_t idesc = ue8m0 ? idesc_nvf4(256, 256, true) : idesc_nvf4(256, 256);
+      const uint32_t base = smem_u32(smem);
+      const uint64_t da0 = smem_desc(base, 16, 1024, 2);
+      const uint64_t db0 = smem_desc(base + C::kABytes, 16, 1024, 2);
+      const uint64_t drep0 = smem_desc(smem_u32(rep_ring), 128, 256, 0);
+      const uint32_t sf_base = tmem + C::kSfBase;
+      const uint32_t peer_empty0 = peer_addr(empty_bar(0), 1);
+      const uint32_t peer_tfull = peer_addr(tfull, 1);
+      int s = 0;
+      uint32_t ph = 0, acc_ph = 0, g = 0;
+      bool ok = true, issued_any = false;
+      for (int t = pair; t < num_tiles && ok; t += npairs) {
+        if (!mbar_wait_cluster(tempty, acc_ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        tc_fence_after();
+        for (int ks = 0; ks < nk; ++ks, ++g) {
+          // this CTA's expanded scales (its helper saw the stage land), then rank 1's stage
+          if (!mbar_wait(rfull_bar((int)(g % C::kRepSlots)), (g / C::kRepSlots) & 1u, &s_abort, timeout_ns) ||
+              !mbar_wait_cluster(pfull_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          tc_fence_after();
+          const uint64_t off = (uint64_t)(s * (C::kStageBytes >> 4));
+          const uint64_t roff = (uint64_t)((g % C::kRepSlots) * (C::kRepBytes >> 4));
+          const uint32_t sf_col = sf_base + s * C::kSfStageCols;
+          // A: chunks 0-1 and 2-3 (4 columns each); B: per chunk both 128-row halves
+          tc2_cp_256(sf_col, drep0 + roff);
+          tc2_cp_256(sf_col + 8, drep0 + roff + (4096 >> 4));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tc2_cp_256(sf_col + C::kSfaCols + 8 * j, drep0 + roff + ((8192 + 4096 * j) >> 4));
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc2_mma_nvf4(tmem, da0 + off + 2 * j, db0 + off + 2 * j, idesc, sf_col + 4 * j,
+                         sf_col + C::kSfaCols + 8 * j, (ks | j) != 0 ? 1u : 0u);
+          issued_any = true;
+          tc2_commit(empty_bar(s));
+          tc2_commit(peer_empty0 + 8u * s);
+          if (++s == S) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc2_commit(tfull);
+        tc2_commit(peer_tfull);
+        acc_ph ^= 1u;
+      }
+      if (!ok && issued_any) {
+        tc2_commit(drain_bar);
+        const uint64_t t0 = globaltimer();
+        while (!mbar_try_wait(drain_bar, 0) && globaltimer() - t0 < 50000000ull) {
+        }
+      }
+    }
+  } else if (warp >= C::kHelperWarp) {
+    // ---------------- scale expansion (both CTAs) ----------------
+    const int hw = warp - C::kHelperWarp;      // 0: A's four chunks and B's chunk 0; 1: B's chunks 1-3
+    int s = 0;
+    uint32_t ph = 0, g = 0;
+    for (int t = pair; t < num_tiles; t += npairs) {
+      bool ok = true;
+      for (int ks = 0; ks < nk; ++ks, ++g) {
+        if (!mbar_wait(full_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        if (g >= (uint32_t)C::kRepSlots) {
+          // the ring slot was last read by the copies of the stage kRepSlots back
+          const uint32_t gp = g - (uint32_t)C::kRepSlots;
+          if (!mbar_wait(empty_bar((int)(gp % S)), (gp / S) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        }
+        const uint8_t* raw = smem + s * C::kStageBytes + C::kABytes + C::kBBytes;
+        uint8_t* blk = rep_ring + (g % C::kRepSlots) * C::kRepBytes;
+        if (hw == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            expand_row(blk + 4096 * (j >> 1), lane, j & 1, *reinterpret_cast<const uint4*>(raw + 512 * j + 16 * lane));
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if ((j == 0) != (hw == 0)) continue;
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            expand_row(blk + 8192 + 4096 * j, lane, h,
+                       *reinterpret_cast<const uint4*>(raw + C::kSfaBytes + 2048 * h + 512 * j + 16 * lane));
+        }
+        // the expanded blocks become visible to the tensor cores' (async) reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rfull_bar((int)(g % C::kRepSlots)));
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  } else {
+    // ---------------- epilogue (warps 2..9 of both CTAs) ----------------
+    const int q = warp & 3;
+    const int hcol = (warp - 2) >> 2;
+    constexpr int kCols = 128;
+    const float alpha = __fmul_rn(__ldg(g_a), __ldg(g_b));
+    const uint32_t tempty0 = rank == 0 ? tempty : peer_addr(tempty, 0);
+    uint32_t acc_ph = 0;
+    for (int t = pair; t < num_tiles; t += npairs) {
+      const int pm = t / num_n, n = t % num_n;
+      if (!mbar_wait(tfull, acc_ph, &s_abort, timeout_ns)) { fail(); break; }
+      tc_fence_after();
+      const int row = pm * 256 + (int)rank * 128 + q * 32 + lane;
+      uint32_t r[kCols];
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c)
+        tmem_ld32_async(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hcol * kCols + c * 32), r + 32 * c);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < kCols / 32; ++c) reg_fence32(r + 32 * c);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(tempty0);
+        else mbar_arrive_remote(tempty0);
+      }
+      acc_ph ^= 1u;
+      const int col0 = n * 256 + hcol * kCols;
+      if constexpr (OUT_F32) {
+        float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+        for (int i = 0; i < kCols / 4; ++i)
+          out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                               __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+      } else {
+        uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+        for (int i = 0; i < kCols / 8; ++i) {
+          uint32_t h[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * i + 2 * k]), alpha),
+                                                            __fmul_rn(__uint_as_float(r[8 * i + 2 * k + 1]), alpha));
+            h[k] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();          // no cross-CTA arrival or shared-memory read is still under way
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
 // ---- host side ----------------------------------------------------------------------
 // 2-D map over a rows x (K/2)-byte code matrix; box = `box_rows` rows x 128 bytes.
 bool make_code_map(CUtensorMap* map, const void* base, int64_t rows, int64_t kbytes, int box_rows) {
@@ -314,6 +676,46 @@ cudaError_t launch(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStream_
   return cudaGetLastError();
 }
 
+// The pair kernel: clusters of two CTAs, as many pairs as can be resident.
+template <bool OUT_F32>
+cudaError_t launch_pair(const GemmArgs& a, uint64_t timeout_ns, int skip, cudaStream_t s) {
+  using C = PairCfg;
+  CUtensorMap ma, mb;
+  if (!make_code_map(&ma, a.a.codes, a.m, a.k / 2, 128) || !make_code_map(&mb, a.b.codes, a.n, a.k / 2, 128))
+    return cudaErrorInvalidValue;
+  auto k = gemm_nvf4_pair_kernel<OUT_F32>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int pairs = sm_count() / 2;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  int resident = 0;
+  if (cudaOccupancyMaxActiveClusters(&resident, k, &cfg) == cudaSuccess && resident > 0) {
+    if (resident < pairs) pairs = resident;
+  } else {
+    cudaGetLastError();
+  }
+  const int tiles = (int)((a.m / 256) * (a.n / 256));
+  if (tiles < pairs) pairs = tiles;
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  e = cudaLaunchKernelEx(&cfg, k, ma, mb, (const uint8_t*)a.a.scales, (const uint8_t*)a.b.scales,
+                         (const float*)a.a.tensor_scale, (const float*)a.b.tensor_scale, a.y, (int)a.m,
+                         (int)a.n, (int)a.k, static_cast<Workspace*>(a.ws), timeout_ns, skip,
+                         a.fmt == 0 ? 0 : 1);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t run_gemm_ex(const GemmArgs& a, uint64_t timeout_ns, int skip_first_stage, cudaStream_t s) {
@@ -321,6 +723,9 @@ cudaError_t run_gemm_ex(const GemmArgs& a, uint64_t timeout_ns, int skip_first_s
   // (E8M0 scales; a 32-element block's scale is stored for both halves)
   if (a.fmt != 0 && a.fmt != 1 && a.fmt != 4 && a.fmt != 5) return cudaErrorNotSupported;
   const bool f32 = a.out_dtype == 1;
+  if (a.m % 256 == 0 && a.n % 256 == 0)
+    return f32 ? launch_pair<true>(a, timeout_ns, skip_first_stage, s)
+               : launch_pair<false>(a, timeout_ns, skip_first_stage, s);
   if (a.n % 256 == 0) return f32 ? launch<256, true>(a, timeout_ns, skip_first_stage, s)
                                  : launch<256, false>(a, timeout_ns, skip_first_stage, s);
   return f32 ? launch<128, true>(a, timeout_ns, skip_first_stage, s)

@@ -47,8 +47,11 @@ def _rand_copy(rng, rows, k, kexp_lo, kexp_hi):
 
 @pytest.mark.parametrize("variant", ["unit", "a_scales", "b_scales", "both"])
 @pytest.mark.parametrize("shape", [(128, 256, 256), (128, 128, 512), (256, 512, 768), (512, 256, 512),
-                                   (1024, 512, 256)])
+                                   (1024, 512, 256), (384, 768, 512), (256, 256, 256), (4096, 4096, 256),
+                                   (2304, 2560, 512)])
 def test_gemm_exact_power_of_two(lib, variant, shape):
+    """M and N multiples of 256 run on CTA pairs (one 256 x 256 tile per pair,
+    several tiles per pair at 4096 x 4096), other shapes on single CTAs."""
     M, N, K = shape
     rng = np.random.default_rng(M + N + K)
     a = _rand_copy(rng, M, K, 0 if variant in ("unit", "b_scales") else -2,
