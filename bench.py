@@ -665,38 +665,46 @@ def run_gemm_leg(fq, torch, device, steps, warmup):
 def run_gemm_ufp4_leg(fq, torch, device, steps, warmup, peaks):
     """UFP4 on the contraction at 8192^3 (the pages' proposal: the uniform grid
     with the RHT on every GEMM): A, B N(0, 1/8192) BF16 -> UFP4 + RHT16 along
-    K, then fp4q_gemm_via_bf16 (both operands dequantised to exact BF16 block
-    values on the GPU, BF16 GEMM with FP32 accumulation, scaled by g_A g_B).
-    Time per GEMM call (the two dequantisations included)."""
+    K, then fp4q_gemm, which runs UFP4 on the 16-bit tensor-core MMA: converter
+    warps form the exact FP16 block values level * s_b in shared memory, the
+    tensor cores accumulate in FP32, the epilogue applies g_A g_B. Time per
+    GEMM call; the roofline is the dense FP16/BF16 tensor peak."""
     import synth
     n = GEMM_N
     a = synth.gemm_operand("a", n, n).to(device)
     b = synth.gemm_operand("b", n, n).to(device)
-    qa, _ = fq.fp4q_quantize(a, fmt="ufp4", rht=True, seed=SEED)
-    qb, _ = fq.fp4q_quantize(b, fmt="ufp4", rht=True, seed=SEED)
+    qa, _ = fq.fp4q_quantize(a, fmt="ufp4", rht=True, seed=SEED, layout="mma")
+    qb, _ = fq.fp4q_quantize(b, fmt="ufp4", rht=True, seed=SEED, layout="mma")
     y = torch.empty(n, n, dtype=torch.bfloat16, device=device)
-    scratch = torch.empty(fq._lib.fp4q_gemm_via_bf16_scratch_bytes(n, n, n), dtype=torch.uint8, device=device)
+    ws = fq.workspace(device)
     stream = torch.cuda.current_stream(device)
     evs = []
     for k in range(warmup + steps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        fq.fp4q_gemm_via_bf16(qa, qb, out=y, scratch=scratch)
+        fq.fp4q_gemm(qa, qb, out=y, ws=ws)
         e1.record(stream)
         if k >= warmup:
             evs.append((e0, e1))
     torch.cuda.synchronize(device)
     us = statistics.fmean(x.elapsed_time(z) for x, z in evs) * 1e3
+    status = fq.fp4q_status(ws)
     flop = 2.0 * n ** 3
     rows = torch.arange(0, n, 64, device=device)
     ref = a[rows].double() @ b.double().T
     got = y[rows].double()
     snr = 10 * math.log10(float((ref * ref).sum()) / float(((got - ref) ** 2).sum()))
     tflops = flop / (us * 1e-6) / 1e12
-    return {"workload": "A, B 8192x8192 BF16 N(0,1/8192) -> UFP4 + RHT16 along K -> dequantise to BF16 "
-                        "(exact) + BF16 GEMM (FP32 accumulate) x g_A g_B, BF16 Y = A B^T",
-            "us": us, "tflops": tflops, "frac_of_bf16_peak": tflops / peaks["bf16_tflops"],
-            "launches": len(evs), "snr_db_vs_bf16_product": snr}
+    peak = peaks["bf16_tflops"]
+    return {"workload": "A, B 8192x8192 BF16 N(0,1/8192) -> UFP4 + RHT16 along K -> fp4q_gemm: exact FP16 block "
+                        "values formed in shared memory, tcgen05 kind::f16 MMA (FP32 accumulate) x g_A g_B, BF16 "
+                        "Y = A B^T",
+            "us": us, "tflops": tflops, "launches": len(evs), "device_status": status,
+            "snr_db_vs_bf16_product": snr,
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak,
+                         "peak_source": f"{peaks['source']} bf16 burst (the dense FP16 rate is the same)",
+                         "traffic": ncu_traffic("gemm_dq_kernel", flop)}}
 
 
 def sweep_point(fq, torch, device, x, steps, warmup, peaks, ws, flush) -> dict:
@@ -1067,7 +1075,7 @@ def main(argv=None) -> int:
                          "traffic": ncu_traffic("gemm_nvf4_kernel", flop)},
         }
         line["gpu_launches_gemm_leg"] = 3 * args.steps
-        line["gemm_ufp4_via_bf16"] = gemm_u
+        line["gemm_ufp4"] = gemm_u
     line["gradient_leg"] = {
         "workload": "4096x14336 and 14336x4096 BF16 N(0,1e-6) with 0.1% x100, NVFP4 + RHT16 + Philox "
                     "SR (seed 1234), row-wise and column-wise copies from one read",

@@ -6,7 +6,7 @@ through its C ABI (include/fp4q.h). There is no CPU path: if the shared library
 is missing, importing this package fails.
 
 Function names follow the C ABI: fp4q_amax, fp4q_quantize, fp4q_dequantize, fp4q_stats,
-fp4q_status, fp4q_gemm, fp4q_gemm_selftest_timeout, fp4q_quantize_noalloc, fp4q_status_noalloc, fp4q_workspace_size, fp4q_workspace_init,
+fp4q_status, fp4q_gemm, fp4q_gemm_dequant, fp4q_gemm_selftest_timeout, fp4q_quantize_noalloc, fp4q_status_noalloc, fp4q_workspace_size, fp4q_workspace_init,
 fp4q_scales_bytes, fp4q_strerror, fp4q_version.
 """
 from __future__ import annotations
@@ -71,8 +71,7 @@ _SIGS = {
     "fp4q_gemm": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
     "fp4q_gemm_selftest_timeout": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, ctypes.c_uint64, _P], _I),
     "fp4q_code_histogram": ([_QP, _I64, _I64, _P, _P], _I),
-    "fp4q_gemm_via_bf16_scratch_bytes": ([_I64, _I64, _I64], _SZ),
-    "fp4q_gemm_via_bf16": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
+    "fp4q_gemm_dequant": ([_QP, _QP, _I64, _I64, _I64, _I, _P, _I, _P, _SZ, _P], _I),
     "fp4q_effective_bucket_ratio": ([ctypes.POINTER(ctypes.c_ulonglong)], ctypes.c_double),
     "fp4q_strerror": ([_I], ctypes.c_char_p),
     "fp4q_version": ([], _I),
@@ -327,23 +326,22 @@ def fp4q_gemm(a: QCopy, b: QCopy, out_dtype=torch.bfloat16, out: torch.Tensor = 
     return out
 
 
-def fp4q_gemm_via_bf16(a: QCopy, b: QCopy, out_dtype=torch.bfloat16, out: torch.Tensor = None,
-                       scratch: torch.Tensor = None) -> torch.Tensor:
-    """Y = dequant(a) @ dequant(b)^T through BF16 operands (UFP4, MXFP4 or
-    NVFP4 row-wise copies a (M x K), b (N x K))."""
+def fp4q_gemm_dequant(a: QCopy, b: QCopy, out_dtype=torch.bfloat16, out: torch.Tensor = None,
+                      ws: torch.Tensor = None) -> torch.Tensor:
+    """Y = dequant(a) @ dequant(b)^T on the 16-bit tensor-core MMA (UFP4, NVFP4
+    or E8M0 row-wise copies a (M x K), b (N x K)); the block values are formed
+    in shared memory, never in HBM."""
     if a.cols != b.cols or a.fmt != b.fmt:
         raise ValueError("K or format mismatch")
     dev = a.codes.device
-    if scratch is None:
-        scratch = torch.empty(_lib.fp4q_gemm_via_bf16_scratch_bytes(a.rows, b.rows, a.cols), dtype=torch.uint8,
-                              device=dev)
+    if ws is None:
+        ws = workspace(dev)
     if out is None:
         out = torch.empty(a.rows, b.rows, dtype=out_dtype, device=dev)
     sa, sb = a.c_struct(), b.c_struct()
-    rc = _lib.fp4q_gemm_via_bf16(ctypes.byref(sa), ctypes.byref(sb), a.rows, b.rows, a.cols, FORMATS[a.fmt],
-                                 out.data_ptr(), DTYPES[out.dtype], scratch.data_ptr(), scratch.numel(),
-                                 _stream(dev))
-    _check("fp4q_gemm_via_bf16", rc)
+    rc = _lib.fp4q_gemm_dequant(ctypes.byref(sa), ctypes.byref(sb), a.rows, b.rows, a.cols, FORMATS[a.fmt],
+                                out.data_ptr(), DTYPES[out.dtype], ws.data_ptr(), ws.numel(), _stream(dev))
+    _check("fp4q_gemm_dequant", rc)
     return out
 
 

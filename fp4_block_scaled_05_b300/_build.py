@@ -18,7 +18,7 @@ COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler",
           "--expt-relaxed-constexpr", "-I" + os.path.join(ROOT, "include")]
 # the exact path must not contract a*b+c into an FMA
 PER_FILE = {"fp4q_quantize.cu": ["-fmad=false"], "fp4q_rows.cu": ["-fmad=false"]}
-SOURCES = ["fp4q_capi.cu", "fp4q_quantize.cu", "fp4q_rows.cu", "fp4q_gemm.cu", "fp4q_noalloc.cu", "fp4q_hist.cu", "fp4q_gemm_bf16.cu",
+SOURCES = ["fp4q_capi.cu", "fp4q_quantize.cu", "fp4q_rows.cu", "fp4q_gemm.cu", "fp4q_noalloc.cu", "fp4q_hist.cu", "fp4q_gemm_dq.cu",
            "fp4q_gemm_outer.cu"]
 HEADERS = ["fp4q_device.cuh", "fp4q_internal.h", "fp4q_ptx.cuh", "fp4q_tc.cuh"]
 
@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for _, log in results:
             sys.stderr.write(log)
     tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *[o for o, _ in results], "-lcublas", "-o", tmp]
+    cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", *[o for o, _ in results], "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")

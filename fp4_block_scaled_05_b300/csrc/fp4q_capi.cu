@@ -265,24 +265,19 @@ int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, 
   return fp4q::run_dequantize(a, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
 }
 
-size_t fp4q_gemm_via_bf16_scratch_bytes(int64_t M, int64_t N, int64_t K) {
-  if (M < 0 || N < 0 || K < 0) return 0;
-  return fp4q::gemm_bf16_scratch_bytes(M, N, K);
-}
-
-int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
-                       int fmt, void* Y, int out_dtype, void* scratch, size_t scratch_bytes, void* stream) {
+int fp4q_gemm_dequant(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+                      int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream) {
   int rc = check_format(fmt, block_for(fmt));
   if (rc) return rc;
-  // per-128-element scales: no single alpha; MBS values also need more than BF16's 8 significant bits
+  // per-128-element scales: not one 16-bit value per element
   if (outer_scaled(fmt)) return FP4Q_ENOTSUP;
   if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
+  if (!aligned(A->scales, 2) || !aligned(B->scales, 2)) return FP4Q_EINVAL;
   if (out_dtype != FP4Q_BF16 && out_dtype != FP4Q_F32) return FP4Q_EINVAL;
-  if (M <= 0 || N <= 0 || K <= 0 || K % block_for(fmt)) return FP4Q_EINVAL;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 64 || N % 8) return FP4Q_EINVAL;
   if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP4Q_EINVAL;
   if (!Y || !aligned(Y, 16)) return FP4Q_EINVAL;
-  if (!scratch || !aligned(scratch, 256) || scratch_bytes < fp4q::gemm_bf16_scratch_bytes(M, N, K))
-    return FP4Q_EINVAL;
+  if (!workspace || !aligned(workspace, 16) || ws_bytes < fp4q_workspace_size()) return FP4Q_EINVAL;
   fp4q::GemmArgs a{};
   a.a = to_qout(A);
   a.b = to_qout(B);
@@ -292,7 +287,10 @@ int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, 
   a.fmt = fmt;
   a.y = Y;
   a.out_dtype = out_dtype;
-  return fp4q::run_gemm_bf16(a, scratch, (cudaStream_t)stream) == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
+  a.ws = workspace;
+  const cudaError_t e = fp4q::run_gemm_dequant(a, (cudaStream_t)stream);
+  if (e == cudaErrorNotSupported) return FP4Q_ENOTSUP;
+  return e == cudaSuccess ? FP4Q_OK : FP4Q_ECUDA;
 }
 
 int fp4q_code_histogram(const fp4q_qtensor* q, int64_t rows, int64_t cols, unsigned long long* counts,
@@ -399,8 +397,11 @@ int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t
                 void* Y, int out_dtype, void* workspace, size_t ws_bytes, uint64_t timeout_ns, int skip,
                 void* stream) {
   if (fmt < FP4Q_NVFP4 || fmt > FP4Q_MXFP4_MBS) return FP4Q_EINVAL;
-  // E2M1 operands with E4M3 or E8M0 block scales; UFP4 has no FP4 tensor-core type
-  if (fmt == FP4Q_UFP4) return FP4Q_ENOTSUP;
+  // UFP4 has no FP4 tensor-core type: its block values go through the 16-bit MMA
+  if (fmt == FP4Q_UFP4) {
+    if (skip) return FP4Q_ENOTSUP;
+    return fp4q_gemm_dequant(A, B, M, N, K, fmt, Y, out_dtype, workspace, ws_bytes, stream);
+  }
   // per-128 scales: their own kernel, without the bounded-wait self-test
   if (outer_scaled(fmt) && skip) return FP4Q_ENOTSUP;
   int rc;

@@ -71,10 +71,10 @@ cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s);
 // Both passes of a row-wise NVFP4/UFP4 request in one cooperative launch.
 cudaError_t run_quant_fused(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s);
-// Block-scaled operands dequantised to BF16, then a BF16 GEMM (FP32
-// accumulation) scaled by g_A * g_B; `scratch` holds gemm_bf16_scratch_bytes().
-size_t gemm_bf16_scratch_bytes(int64_t m, int64_t n, int64_t k);
-cudaError_t run_gemm_bf16(const GemmArgs& a, void* scratch, cudaStream_t s);
+// Block-scaled operands dequantised in shared memory to exact 16-bit block
+// values, multiplied by tcgen05 kind::f16 MMAs with FP32 accumulation, scaled
+// by g_A * g_B (UFP4, NVFP4, the E8M0 formats; K % 64 == 0, N % 8 == 0).
+cudaError_t run_gemm_dequant(const GemmArgs& a, cudaStream_t s);
 // The GEMM on operands with an FP32 scale per 128 elements along K (two-level
 // NVFP4, MBS), per-128 scales column-major (K/128 x rows).
 cudaError_t run_gemm_outer(const GemmArgs& a, cudaStream_t s);

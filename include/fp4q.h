@@ -312,39 +312,43 @@ double fp4q_effective_bucket_ratio(const unsigned long long* counts);
  *              K chunk's product is formed apart in TMEM and scaled by
  *              g_A(m, c) g_B(n, c) into FP32 accumulators (tensor_scale:
  *              the column-major per-128 scales, 16-byte aligned).
- *              FP4Q_UFP4 -> FP4Q_ENOTSUP (no tensor-core format).
+ *              FP4Q_UFP4 (no tensor-core format holds its levels): runs as
+ *              fp4q_gemm_dequant, with that call's shape rules.
  *   Y          device, M x N row-major, `out_dtype` FP4Q_BF16 (nearest-even)
  *              or FP4Q_F32, 16-byte aligned.
  *   workspace  as for fp4q_quantize (the status word records a bounded wait
  *              that ran out: FP4Q_ETIMEOUT via fp4q_status).
  * Shapes: M % 128 == 0, N % 128 == 0, K % 256 == 0, all > 0 (else FP4Q_EINVAL).
+ * M and N multiples of 256 run on pairs of SMs (the two-SM MMA), others on
+ * single SMs; the results are the same.
  * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
 int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
               int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
 
-/* Bytes of scratch fp4q_gemm_via_bf16 needs for M x K and N x K operands:
- * 256 + (M + N) * K * 2 + 32 MiB (the BF16 operands and the GEMM library's
- * workspace). */
-size_t fp4q_gemm_via_bf16_scratch_bytes(int64_t M, int64_t N, int64_t K);
-
-/* Y = dequant(A) * dequant(B)^T for block-scaled formats without a native
- * tensor-core GEMM here: UFP4 ([UFP4] Metodologia §2 and Resultados: the
- * uniform grid with the RHT on every training GEMM); NVFP4 and the MXFP4
- * formats with E8M0 block scales are accepted too. Each operand is dequantised on the GPU to its BF16 block
- * values level * s_b (exact in BF16), then a BF16 GEMM with FP32 accumulation
- * (the CUDA GEMM library) forms the product, scaled by g_A * g_B (FP32
- * product; 1 for the MXFP4 formats). When both operands were quantised with the RHT along
- * K under the same seed, the transforms cancel.
- *   A, B       host pointers to descriptors of row-wise copies (M x K, N x K),
- *              linear or tiled scales, of format `fmt`.
- *   Y          device, M x N row-major, FP4Q_BF16 or FP4Q_F32, 16-byte aligned.
- *   scratch    device, 256-byte aligned, scratch_bytes >=
- *              fp4q_gemm_via_bf16_scratch_bytes(M, N, K); owned by the caller.
- * Calls from different host threads must not share a stream at the same time.
- * Shapes: M, N, K > 0, K % block == 0 (else FP4Q_EINVAL).
- * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP (FP4Q_NVFP4_2L, FP4Q_MXFP4_MBS), FP4Q_ECUDA. */
-int fp4q_gemm_via_bf16(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
-                       int fmt, void* Y, int out_dtype, void* scratch, size_t scratch_bytes, void* stream);
+/* Y = dequant(A) * dequant(B)^T on the tensor cores for block-scaled formats
+ * whose values the block-scaled MMA cannot take: UFP4 ([UFP4] Metodologia §2
+ * and Resultados: the uniform grid with the RHT on every training GEMM); NVFP4
+ * and the E8M0 formats (FP4Q_MXFP4, FP4Q_MXFP4_B16, FP4Q_MXFP4_OAS) are
+ * accepted too, to compare with fp4q_gemm. The kernel's converter warps turn
+ * each operand's codes and block scales into the 16-bit block values
+ * level * s_b in shared memory -- FP16 for UFP4 and NVFP4 (E4M3 scales; exact:
+ * at most 7 significant bits in [2^-10, 3136]), BF16 for the E8M0 formats
+ * (exact) -- and tcgen05.mma.kind::f16 accumulates their products, exact in
+ * FP32, in FP32; the result is multiplied by g_A * g_B (their FP32 product;
+ * 1 for the E8M0 formats). No dequantised operand is written to memory. When
+ * both operands were quantised with the RHT along K under the same seed, the
+ * transforms cancel.
+ *   A, B       host pointers to descriptors of row-wise copies (M x K, N x K)
+ *              of format `fmt`, linear or tiled scales (2-byte aligned).
+ *   Y          device, M x N row-major, FP4Q_BF16 (nearest-even) or FP4Q_F32,
+ *              16-byte aligned.
+ *   workspace  as for fp4q_gemm (FP4Q_ETIMEOUT via fp4q_status).
+ * Shapes: M, N > 0 (any; rows past a 128 x 256 tile are zeros), N % 8 == 0,
+ * K > 0, K % 64 == 0 (else FP4Q_EINVAL).
+ * Errors: FP4Q_EINVAL, FP4Q_ENOTSUP (FP4Q_NVFP4_2L, FP4Q_MXFP4_MBS: their
+ * per-128 scales are not one 16-bit value per element), FP4Q_ECUDA. */
+int fp4q_gemm_dequant(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K,
+                      int fmt, void* Y, int out_dtype, void* workspace, size_t ws_bytes, void* stream);
 
 /* Test hook for the device-side failure path (not a step of the method): runs
  * fp4q_gemm with the producer of the first CTA withholding the first stage of

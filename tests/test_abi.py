@@ -150,19 +150,26 @@ def test_gemm_selftest_validation_without_gpu(so):
 
 
 def test_gemm_format_validation_without_gpu(so):
-    """fp4q_gemm refuses UFP4 (no FP4 tensor-core type) and unknown formats
-    before touching any pointer, and checks the descriptors of the others."""
+    """fp4q_gemm refuses unknown formats before touching any pointer and checks
+    the descriptors of the others (UFP4 included: it runs on the dequantising
+    kernel); fp4q_gemm_dequant refuses the per-128-scaled formats first."""
     so.fp4q_workspace_size.restype = ctypes.c_size_t
     g = so.fp4q_gemm
     g.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                   ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
     ws = so.fp4q_workspace_size()
-    assert g(fake, fake, 128, 128, 256, 2, fake, 0, fake, ws, None) == 2       # UFP4
     assert g(fake, fake, 128, 128, 256, -1, fake, 0, fake, ws, None) == 1
     assert g(fake, fake, 128, 128, 256, 7, fake, 0, fake, ws, None) == 1
-    for fmt in (0, 1, 3, 4, 5, 6):                                            # null descriptors
+    for fmt in (0, 1, 2, 3, 4, 5, 6):                                         # null descriptors
         assert g(None, None, 128, 128, 256, fmt, fake, 0, fake, ws, None) == 1
+    d = so.fp4q_gemm_dequant
+    d.argtypes = g.argtypes
+    assert d(fake, fake, 128, 128, 256, 3, fake, 0, fake, ws, None) == 2      # two-level NVFP4
+    assert d(fake, fake, 128, 128, 256, 6, fake, 0, fake, ws, None) == 2      # MBS
+    assert d(fake, fake, 128, 128, 256, 7, fake, 0, fake, ws, None) == 1
+    for fmt in (0, 1, 2, 4, 5):
+        assert d(None, None, 128, 128, 256, fmt, fake, 0, fake, ws, None) == 1
 
 
 def test_effective_bucket_ratio_host(so):

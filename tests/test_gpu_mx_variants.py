@@ -147,7 +147,7 @@ def test_mx_rejections(lib):
     assert e.value.code == 1                        # cols % 128
     a, _ = lib.fp4q_quantize(torch.randn(128, 256, device="cuda"), fmt="mxfp4_mbs", layout="mma")
     with pytest.raises(lib.FP4QError) as e:
-        lib.fp4q_gemm_via_bf16(a, a)
+        lib.fp4q_gemm_dequant(a, a)
     assert e.value.code == 2
 
 
