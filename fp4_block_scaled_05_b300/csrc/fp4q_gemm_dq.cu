@@ -16,25 +16,25 @@
 // The FP16 / BF16 products of two such values are exact in FP32, so the only
 // rounding is the FP32 accumulation.
 //
-// Structure: pairs of CTAs (two-CTA clusters, 416 threads each) compute one
+// Structure: pairs of CTAs (two-CTA clusters, 672 threads each) compute one
 // 256 x 256 tile of Y with the two-SM MMA (cta_group::2): CTA r of the pair
 // converts rows [128 r, 128 r + 128) of the tile's A rows and of its B rows,
 // so each SM converts 256 rows per K stage for 128 x 256 x 64 multiply-adds
 // (a one-CTA 128 x 256 tile converts 384).
-//   warps 0-7   converters: per K stage of 64 elements, each thread takes two
-//               half rows (32 elements: one 16-byte load of codes and its
+//   warps 0-15  converters: per K stage of 64 elements, each thread takes one
+//               half row (32 elements: one 16-byte load of codes and its
 //               scales, issued two stages ahead from per-tile pointers), makes
 //               four 16-byte chunks of 16-bit values and stores them in the
 //               128-byte-swizzled K-major layout the MMA reads; then fences
 //               the stores for the async proxy and arrives on the stage's
 //               "full" barrier.
-//   warp 8      allocates 512 TMEM columns in both CTAs (two 256-column
+//   warp 16     allocates 512 TMEM columns in both CTAs (two 256-column
 //               accumulators). In CTA 0 one thread waits for both CTAs' stage
-//               (CTA 1's warp 8 relays its "full" to CTA 0), issues four
+//               (CTA 1's warp 16 relays its "full" to CTA 0), issues four
 //               tcgen05.mma.cta_group::2.kind::f16 (M = 256, N = 256, K = 16)
 //               and commits the stage back to both CTAs' converters and, after
 //               the last stage, the accumulator to both epilogues.
-//   warps 9-12  epilogue, one per TMEM lane quadrant: reads the accumulator in
+//   warps 17-20 epilogue, one per TMEM lane quadrant: reads the accumulator in
 //               32-column chunks, multiplies by g_A * g_B, stores BF16
 //               (nearest-even) or FP32, then frees the accumulator; the other
 //               accumulator already takes the next tile's MMAs.
@@ -65,7 +65,7 @@ constexpr int kStages = 6;
 constexpr int kABytes = kBM * 128;             // 16 KB
 constexpr int kBBytes = kBN * 128;             // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
-constexpr int kConvWarps = 8;
+constexpr int kConvWarps = 16;
 constexpr int kConvThreads = 32 * kConvWarps;
 constexpr int kMmaWarp = kConvWarps;
 constexpr int kEpiWarp0 = kConvWarps + 1;
