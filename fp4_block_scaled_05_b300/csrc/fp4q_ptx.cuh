@@ -120,10 +120,12 @@ __device__ __forceinline__ float max_abs_nan(float m, float v) {
   return d;
 }
 
-// Lane-wise max(m, |w|) over two BF16 values, NaN-propagating.
+// Lane-wise max(|m|, |w|) over two BF16 values, NaN-propagating, in one
+// instruction; the sign bits of the result are not meaningful (the xor of the
+// operands' signs), so the caller takes the magnitude at the end.
 __device__ __forceinline__ uint32_t max_abs_nan_bf16x2(uint32_t m, uint32_t w) {
   uint32_t d;
-  asm("{\n\t.reg .b32 t;\n\tabs.bf16x2 t, %2;\n\tmax.NaN.bf16x2 %0, %1, t;\n\t}" : "=r"(d) : "r"(m), "r"(w));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(m), "r"(w));
   return d;
 }
 

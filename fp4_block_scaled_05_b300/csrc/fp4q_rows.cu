@@ -672,8 +672,8 @@ __device__ __forceinline__ void quant_two16(const Seg& sg, const uint32_t (&sgn)
       a0 = max_abs_nan_bf16x2(a0, w[k]);
       a1 = max_abs_nan_bf16x2(a1, w[k + 8]);
     }
-    m0 = max_abs_nan(bf16lo(a0), bf16hi(a0));
-    m1 = max_abs_nan(bf16lo(a1), bf16hi(a1));
+    m0 = max3_abs_nan(0.f, bf16lo(a0), bf16hi(a0));
+    m1 = max3_abs_nan(0.f, bf16lo(a1), bf16hi(a1));
 #pragma unroll
     for (int j = 0; j < 16; ++j) Q[j] = f2_make(bf16lo(w[j]), bf16hi(w[j]));
   } else {
@@ -861,7 +861,7 @@ __device__ __forceinline__ void amax_segment(const Seg& sg, int nb, const uint32
 template <bool F32, bool RHT>
 __device__ __forceinline__ float amax_result(float m, uint32_t m2) {
   if constexpr (!RHT && !F32) {
-    m = fmaxf(__uint_as_float(m2 << 16), __uint_as_float(m2 & 0xFFFF0000u));
+    m = fmaxf(fabsf(__uint_as_float(m2 << 16)), fabsf(__uint_as_float(m2 & 0xFFFF0000u)));
     if ((m2 & 0x7FFFu) > 0x7F80u || (m2 >> 16 & 0x7FFFu) > 0x7F80u) m = __uint_as_float(0x7FFFFFFFu);
   }
   return RHT ? __fmul_rn(m, 0.25f) : m;
