@@ -155,8 +155,8 @@ int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt
   if ((axis & FP4Q_ROWWISE) && cols % block) return FP4Q_EINVAL;
   if ((axis & FP4Q_COLWISE) && rows % block) return FP4Q_EINVAL;
   if (outer_scaled(fmt)) {
-    if (axis & FP4Q_COLWISE) return FP4Q_ENOTSUP;     // row-wise copy only in this version
-    if (cols % 128) return FP4Q_EINVAL;               // whole outer blocks per row
+    if ((axis & FP4Q_ROWWISE) && cols % 128) return FP4Q_EINVAL;   // whole outer blocks per row
+    if ((axis & FP4Q_COLWISE) && rows % 128) return FP4Q_EINVAL;   // ... and per column
   }
   return FP4Q_OK;
 }

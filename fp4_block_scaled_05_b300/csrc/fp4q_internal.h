@@ -64,7 +64,12 @@ cudaError_t run_amax(const QuantArgs& a, cudaStream_t s);
 // there is no RHT or only the row-wise copy is wanted, and the quantisation
 // pass of a row-wise-only request.
 cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s);
-cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s);
+// grid_out (optional): the number of CTAs launched, i.e. of statistics partials.
+cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s, int* grid_out = nullptr);
+// The column-wise copy of two-level NVFP4 and MBS (rows % 128 == 0): 128-row
+// tiles, outer blocks down the columns. row_np: CTAs of the row kernel that
+// ran before it for the row-wise copy of the same call (0 if none).
+cudaError_t run_quant_cols_outer(const QuantArgs& a, int row_np, cudaStream_t s);
 // Requests with the column-wise copy (rows and cols multiples of 16).
 cudaError_t run_amax_tiles(const QuantArgs& a, cudaStream_t s);
 cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s);

@@ -88,6 +88,16 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
     const cudaError_t e = run_amax(a, s);
     if (e != cudaSuccess) return e;
   }
+  if ((a.fmt == 3 || a.fmt == 6) && (a.axis & 2)) {
+    // scales per 128 elements: the column-wise copy on 128-row tiles (outer
+    // blocks down the columns), the row-wise copy, if wanted, from the row kernel
+    int row_np = 0;
+    if (a.axis & 1) {
+      const cudaError_t e = run_quant_rows(a, s, &row_np);
+      if (e != cudaSuccess) return e;
+    }
+    return run_quant_cols_outer(a, row_np, s);
+  }
   return a.axis == 1 ? run_quant_rows(a, s) : run_quant_tiles(a, s);
 }
 

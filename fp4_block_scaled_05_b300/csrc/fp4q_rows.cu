@@ -1172,12 +1172,15 @@ constexpr int TTR = 64;     // tile rows
 constexpr int TTC = 128;    // tile cols
 constexpr int kBoxBytes = TTR * 128;
 
-template <bool F32>
+// TR: tile rows (64; 128 for the column-wise copies of the formats with a
+// scale per 128 elements, whose outer blocks then run down a tile's columns).
+template <bool F32, int TR = TTR>
 struct TileRing {
   static constexpr int kBoxes = F32 ? 4 : 2;
   static constexpr int kBoxCols = F32 ? 32 : 64;
+  static constexpr int kBoxBytes = TR * 128;
   static constexpr int kTileBytes = kBoxes * kBoxBytes;
-  static constexpr int kStages = F32 ? 3 : 4;
+  static constexpr int kStages = TR == TTR ? (F32 ? 3 : 4) : (F32 ? 2 : 3);
   static constexpr int kSmem = kStages * kTileBytes + 1024;    // + slack to align the ring to 1024
 };
 
@@ -1203,15 +1206,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 
 // Lane 0 of warp 0 fills `slot` with tile t: the byte count (whole boxes, the
 // zero fill included), then one load per box.
-template <bool F32>
+template <bool F32, int TR = TTR>
 __device__ __forceinline__ void tile_issue(const CUtensorMap* map, const TileGeom& g, int64_t t, uint8_t* slot,
                                            uint32_t bar) {
+  using TRg = TileRing<F32, TR>;
   if ((threadIdx.x & 31) != 0) return;
-  const int32_t r0 = (int32_t)((t / g.ntc) * TTR), c0 = (int32_t)((t % g.ntc) * TTC);
-  mbar_arrive_expect_tx(bar, (uint32_t)TileRing<F32>::kTileBytes);
+  const int32_t r0 = (int32_t)((t / g.ntc) * TR), c0 = (int32_t)((t % g.ntc) * TTC);
+  mbar_arrive_expect_tx(bar, (uint32_t)TRg::kTileBytes);
 #pragma unroll
-  for (int b = 0; b < TileRing<F32>::kBoxes; ++b)
-    tma_load_2d(smem_u32(slot + b * kBoxBytes), map, bar, c0 + b * TileRing<F32>::kBoxCols, r0);
+  for (int b = 0; b < TRg::kBoxes; ++b)
+    tma_load_2d(smem_u32(slot + b * TRg::kBoxBytes), map, bar, c0 + b * TRg::kBoxCols, r0);
 }
 
 // Ring protocol. full[s]: the slot's loads have landed (one arrival with the
@@ -1225,10 +1229,10 @@ struct TilePipe {
   int64_t next_it;     // warp 0: the next iteration whose tile is to be issued
 };
 
-template <bool F32>
+template <bool F32, int TR = TTR>
 __device__ __forceinline__ void tile_ring_start(const CUtensorMap* map, const TileGeom& g, uint8_t* ring,
                                                 TilePipe& p) {
-  constexpr int S = TileRing<F32>::kStages;
+  constexpr int S = TileRing<F32, TR>::kStages;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&p.full[s]), 1);
@@ -1242,7 +1246,7 @@ __device__ __forceinline__ void tile_ring_start(const CUtensorMap* map, const Ti
     for (int s = 0; s < S; ++s) {
       const int64_t t = blockIdx.x + (int64_t)s * gridDim.x;
       if (t >= g.ntiles) break;
-      tile_issue<F32>(map, g, t, ring + s * TileRing<F32>::kTileBytes, smem_u32(&p.full[s]));
+      tile_issue<F32, TR>(map, g, t, ring + s * TileRing<F32, TR>::kTileBytes, smem_u32(&p.full[s]));
       p.next_it = s + 1;
     }
   }
@@ -1251,10 +1255,10 @@ __device__ __forceinline__ void tile_ring_start(const CUtensorMap* map, const Ti
 // The calling warp is done with iteration `it` (tile t). Warp 0 then waits for
 // the other warps to be done with the slot too and refills it with the tile
 // kStages iterations later. False if that wait ran out.
-template <bool F32>
+template <bool F32, int TR = TTR>
 __device__ __forceinline__ bool tile_ring_release(const CUtensorMap* map, const TileGeom& g, uint8_t* ring,
                                                   TilePipe& p, int64_t it, int64_t t, uint64_t timeout_ns) {
-  constexpr int S = TileRing<F32>::kStages;
+  constexpr int S = TileRing<F32, TR>::kStages;
   const int s = (int)(it % S);
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(smem_u32(&p.empty[s]));
@@ -1262,7 +1266,7 @@ __device__ __forceinline__ bool tile_ring_release(const CUtensorMap* map, const 
     const int64_t nx = t + (int64_t)S * gridDim.x;
     if (nx < g.ntiles) {
       if (!mbar_wait_bounded(smem_u32(&p.empty[s]), (uint32_t)((it / S) & 1), timeout_ns)) return false;
-      tile_issue<F32>(map, g, nx, ring + s * TileRing<F32>::kTileBytes, smem_u32(&p.full[s]));
+      tile_issue<F32, TR>(map, g, nx, ring + s * TileRing<F32, TR>::kTileBytes, smem_u32(&p.full[s]));
       p.next_it = it + S + 1;
     }
   }
@@ -1282,21 +1286,22 @@ __device__ __forceinline__ SwzSeg tile_row_seg(const uint8_t* slot, int r, int s
   return SwzSeg{slot + box * kBoxBytes + r * 128, 16u * (first ^ (uint32_t)(r & 7))};
 }
 
-// Byte offset, within a slot, of the byte at `b` (0 .. row bytes - 1) of tile
-// row r, for r = r0 + i with r0 a multiple of 8.
+// Byte offset, within a slot of TR-row tiles, of the byte at `b` (0 .. row
+// bytes - 1) of tile row r, for r = r0 + i with r0 a multiple of 8.
+template <int TR = TTR>
 __device__ __forceinline__ uint32_t tile_byte(int r, uint32_t b, int i) {
-  return (b >> 7) * kBoxBytes + (uint32_t)r * 128u + ((b & 127u) ^ (16u * (uint32_t)(i & 7)));
+  return (b >> 7) * (uint32_t)(TR * 128) + (uint32_t)r * 128u + ((b & 127u) ^ (16u * (uint32_t)(i & 7)));
 }
 
 // Two adjacent columns x 16 rows of a slot as FP32 (sign-flipped by sigma
 // along the column when RHT): a[i] = column 2*pair, b[i] = column 2*pair+1.
-template <bool F32, bool RHT>
+template <bool F32, bool RHT, int TR = TTR>
 __device__ __forceinline__ void load_col_pair(const uint8_t* slot, int row0, int pair, uint32_t smask,
                                               float (&a)[16], float (&b)[16]) {
   const uint32_t bo = (uint32_t)pair * (F32 ? 8u : 4u);
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const uint8_t* q = slot + tile_byte(row0 + i, bo, i);
+    const uint8_t* q = slot + tile_byte<TR>(row0 + i, bo, i);
     const uint32_t sg = RHT ? (((smask >> i) & 1u) << 31) : 0u;
     if constexpr (F32) {
       const uint2 w = *reinterpret_cast<const uint2*>(q);
@@ -1684,6 +1689,176 @@ __global__ void __launch_bounds__(RT, 2) quant_tiles_kernel(const __grid_constan
   }
 }
 
+// ---- the column-wise copy of the formats with a scale per 128 elements -----------------
+// Two-level NVFP4 ("TetraJet-v2 ...", Riepilogo Tecnico §2A: the transposed
+// copy for the weight gradient, the double-block scale) and MBS-static
+// ("Unveiling the Potential of Quantization with MXFP4 ...", Resume technique
+// §2B): in the column-wise copy the 16-element blocks and the 128-element outer
+// (macro) blocks run down the source's columns. The source is walked in
+// 128 x 128 tiles, so each tile column holds exactly one outer block. Thread t
+// takes the column pair p = t / 4 (columns 2p, 2p + 1) and the quarter q = t % 4
+// (rows 32q .. 32q + 31: two 16-row blocks per column); the four quarters of a
+// pair are lanes 4k .. 4k + 3, which share the outer maxima by two shuffles.
+// Each column then has its own outer scale, so its blocks go through
+// quant_block one at a time. Rows are a multiple of 128 (whole outer blocks);
+// the row-wise copy, when requested too, comes from the row kernel.
+constexpr int TOR = 128;    // tile rows of this pass
+
+template <int FMT, bool F32, bool RHT, bool SR>
+__global__ void __launch_bounds__(RT, F32 ? 1 : 2) quant_cols_outer_kernel(
+    const __grid_constant__ CUtensorMap tmap, TileGeom g, uint64_t seed, PhiloxKey pk, CopyOut ocol,
+    Workspace* ws, uint64_t timeout_ns, int row_nparts) {
+  static_assert(kOuterScaled<FMT>, "formats with a scale per 128 elements");
+  using TRg = TileRing<F32, TOR>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[TRg::kStages], empty[TRg::kStages];
+  __shared__ double sh_sum[RT / 32];
+  constexpr int S = TRg::kStages;
+  uint8_t* ring = align1024(smem_raw);
+  const int tid = threadIdx.x;
+  const uint32_t smask = RHT ? rht_sign_mask(seed) : 0u;
+  TilePipe pipe{full, empty, 0};
+  tile_ring_start<F32, TOR>(&tmap, g, ring, pipe);
+  grid_dependency_wait();      // the workspace's statistics slots may still be read before this
+  const int pair = tid >> 2, qr = tid & 3;
+  const Ctx unit{1.f, 0.f, 0.f};
+  Sums acc;
+  uint32_t nonfinite = 0;
+  bool timed_out = false;
+  int64_t it = 0;
+  for (int64_t t = blockIdx.x; t < g.ntiles; ++it, t += gridDim.x) {
+    const int s = (int)(it % S);
+    if (!mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+    {
+      const uint8_t* slot = ring + s * TRg::kTileBytes;
+      const int64_t r0 = (t / g.ntc) * TOR, c0 = (t % g.ntc) * TTC;
+      const int vc = (int)min((int64_t)TTC, g.cols - c0);
+      const bool valid = 2 * pair < vc;       // vc is a multiple of 16: pairs are whole
+      // the two 16-row blocks of each column of the pair, transformed
+      f2 Qa[2][8], Qb[2][8];
+      float ma[2] = {0.f, 0.f}, mb[2] = {0.f, 0.f};
+      if (valid) {
+#pragma unroll
+        for (int gi = 0; gi < 2; ++gi) {
+          float a[16], b[16];
+          load_col_pair<F32, RHT, TOR>(slot, 32 * qr + 16 * gi, pair, smask, a, b);
+          if constexpr (RHT) {
+            rht16_pairs(a, Qa[gi]);
+            rht16_pairs(b, Qb[gi]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              Qa[gi][j] = f2_make(a[2 * j], a[2 * j + 1]);
+              Qb[gi][j] = f2_make(b[2 * j], b[2 * j + 1]);
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float x0, x1;
+            f2_split(Qa[gi][j], x0, x1);
+            ma[gi] = max3_abs_nan(ma[gi], x0, x1);
+            f2_split(Qb[gi][j], x0, x1);
+            mb[gi] = max3_abs_nan(mb[gi], x0, x1);
+          }
+        }
+      }
+      // outer maxima of both columns over the pair's four quarters (every lane shuffles)
+      float Ma = max_abs_nan(ma[0], ma[1]), Mb = max_abs_nan(mb[0], mb[1]);
+      Ma = max_abs_nan(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, 1));
+      Ma = max_abs_nan(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, 2));
+      Mb = max_abs_nan(Mb, __shfl_xor_sync(0xFFFFFFFFu, Mb, 1));
+      Mb = max_abs_nan(Mb, __shfl_xor_sync(0xFFFFFFFFu, Mb, 2));
+      if (valid) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {           // column 2p + k: one row of the copy
+          f2 (*Q)[8] = k ? Qb : Qa;
+          const float M = k ? Mb : Ma;
+          const int64_t crow = c0 + 2 * pair + k, ccol = r0 + 32 * qr;
+          uint32_t cw[4];
+          float bsum = 0.f, ssum = 0.f, esum = 0.f;
+          float outer;
+          if constexpr (FMT == 3) {
+            // the outer block's own scale g_o in place of the tensor scale
+            const Ctx co = make_ctx(__float_as_uint(M), 6.f, 2688.f);
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+              const uint32_t sc = quant_block<0, SR, 8>(Q[gi], co, (uint64_t)(crow * g.rows + ccol + 16 * gi), pk,
+                                                        cw + 2 * gi, bsum, ssum, esum, acc, nonfinite, 1u);
+              put_scale_rk(ocol, crow, ccol / 16 + gi, sc);
+            }
+            add_outer_stats(acc, co.g, ssum, esum);
+            outer = co.g;
+          } else {
+            // MBS: values in units of the macro scale S, then E8M0 blocks
+            const float Sm = mbs_macro_scale(M);
+            float rs = (Sm == 0.f) ? 0.f : __frcp_rn(Sm);
+            if (rs > FLT_MAX) rs = FLT_MAX;
+            const f2 RS = f2_make(rs, rs);
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) Q[gi][j] = f2_mul(Q[gi][j], RS);
+              const uint32_t sc = quant_block<6, SR, 8>(Q[gi], unit, (uint64_t)(crow * g.rows + ccol + 16 * gi), pk,
+                                                        cw + 2 * gi, bsum, ssum, esum, acc, nonfinite, 1u, Sm);
+              put_scale_rk(ocol, crow, ccol / 16 + gi, sc);
+            }
+            outer = Sm;
+          }
+          acc.bias.add(bsum);
+          *reinterpret_cast<uint4*>(ocol.codes + crow * ocol.ld + ccol / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+          if (qr == 0) {
+            const int64_t kc = r0 / 128;       // the outer block along the copy's row
+            ocol.tensor_scale[ocol.mma ? kc * ocol.rows + crow : crow * (g.rows / 128) + kc] = outer;
+          }
+        }
+      }
+    }
+    if (!tile_ring_release<F32, TOR>(&tmap, g, ring, pipe, it, t, timeout_ns)) {
+      timed_out = true;
+      break;
+    }
+  }
+  grid_launch_dependents();
+  if (__syncthreads_or(timed_out)) {
+    pipe_drain<S>(pipe.full, pipe.next_it);
+    if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
+  }
+  // ---- statistics of the column-wise copy: one partial per CTA ----
+  if (__syncthreads_or((int)nonfinite) && tid == 0) atomicOr(&ws->status, kStatusNonfinite);
+  double p[3] = {acc.bias.value(), acc.sig64, acc.err64};
+  outer_stats_value(acc, p[1], p[2]);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const double v = cta_sum<RT>(p[k], sh_sum);
+    if (tid == 0) ws->stat_part[1][k][blockIdx.x] = v;
+  }
+  // The statistics header covers both copies: when the row kernel ran before
+  // this one (row_nparts CTAs), each copy's partials past its own grid are zero.
+  const int np = max((int)gridDim.x, row_nparts);
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < np; i += RT) {
+      if (i >= (int)gridDim.x) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) ws->stat_part[1][k][i] = 0.0;
+      }
+      if (row_nparts > 0 && i >= row_nparts) {
+#pragma unroll
+        for (int k = 0; k < 3; ++k) ws->stat_part[0][k][i] = 0.0;
+      }
+    }
+    if (tid == 0) {
+      ws->stat_nparts = (unsigned)np;
+      ws->copies = (row_nparts > 0 ? 1u : 0u) | 2u;
+      ws->tensor_scale[1] = 1.f;
+      ws->qmax = 6.f;
+      ws->n = (double)g.rows * (double)g.cols;
+    }
+  }
+}
+
 // ---- one launch for both passes (NVFP4 / UFP4 row-wise) ------------------------------
 // A cooperatively launched (co-resident) grid streams its chunks twice through
 // one ring: the amax pass, a grid barrier, the fold of the per-CTA maxima, then
@@ -1999,22 +2174,43 @@ cudaError_t launch_amax_rows(const Flat& f, uint64_t seed, Workspace* ws, cudaSt
 
 template <int FMT, bool F32, bool RHT, bool SR>
 cudaError_t launch_quant_rows(const Flat& f, uint64_t seed, const CopyOut& o, Workspace* ws,
-                              cudaStream_t s) {
+                              cudaStream_t s, int* grid_out) {
   auto k = quant_rows_kernel<FMT, F32, RHT, SR>;
   constexpr int smem = Ring<F32>::kSmem;
   cudaError_t e = prepare(k, smem);
   if (e != cudaSuccess) return e;
-  return launch_dependent(k, grid_for(k, smem, f.nchunks), smem, s, f, seed, philox_key(seed), o, ws,
-                          kRingTimeoutNs);
+  const int grid = grid_for(k, smem, f.nchunks);
+  if (grid_out) *grid_out = grid;
+  return launch_dependent(k, grid, smem, s, f, seed, philox_key(seed), o, ws, kRingTimeoutNs);
 }
 
 template <int FMT, bool F32>
 cudaError_t dispatch_quant_rows(int rht, int sr, const Flat& f, uint64_t seed, const CopyOut& o,
-                                Workspace* ws, cudaStream_t s) {
-  if (rht) return sr ? launch_quant_rows<FMT, F32, true, true>(f, seed, o, ws, s)
-                     : launch_quant_rows<FMT, F32, true, false>(f, seed, o, ws, s);
-  return sr ? launch_quant_rows<FMT, F32, false, true>(f, seed, o, ws, s)
-            : launch_quant_rows<FMT, F32, false, false>(f, seed, o, ws, s);
+                                Workspace* ws, cudaStream_t s, int* grid_out) {
+  if (rht) return sr ? launch_quant_rows<FMT, F32, true, true>(f, seed, o, ws, s, grid_out)
+                     : launch_quant_rows<FMT, F32, true, false>(f, seed, o, ws, s, grid_out);
+  return sr ? launch_quant_rows<FMT, F32, false, true>(f, seed, o, ws, s, grid_out)
+            : launch_quant_rows<FMT, F32, false, false>(f, seed, o, ws, s, grid_out);
+}
+
+template <int FMT, bool F32, bool RHT, bool SR>
+cudaError_t launch_cols_outer(const CUtensorMap& map, const TileGeom& g, uint64_t seed, const CopyOut& c,
+                              Workspace* ws, int row_np, cudaStream_t s) {
+  auto k = quant_cols_outer_kernel<FMT, F32, RHT, SR>;
+  constexpr int smem = TileRing<F32, TOR>::kSmem;
+  cudaError_t e = prepare(k, smem);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(k, grid_for(k, smem, g.ntiles), smem, s, map, g, seed, philox_key(seed), c, ws,
+                          kRingTimeoutNs, row_np);
+}
+
+template <int FMT, bool F32>
+cudaError_t dispatch_cols_outer(int rht, int sr, const CUtensorMap& m, const TileGeom& g, uint64_t seed,
+                                const CopyOut& c, Workspace* ws, int row_np, cudaStream_t s) {
+  if (rht) return sr ? launch_cols_outer<FMT, F32, true, true>(m, g, seed, c, ws, row_np, s)
+                     : launch_cols_outer<FMT, F32, true, false>(m, g, seed, c, ws, row_np, s);
+  return sr ? launch_cols_outer<FMT, F32, false, true>(m, g, seed, c, ws, row_np, s)
+            : launch_cols_outer<FMT, F32, false, false>(m, g, seed, c, ws, row_np, s);
 }
 
 template <bool F32, bool ROWS>
@@ -2048,20 +2244,20 @@ cudaError_t dispatch_quant_tiles(int rht, int sr, const CUtensorMap& m, const Ti
 }
 
 // The source as a 2-D TMA map whose box is one 64-row x 128-byte box of a tile.
-bool make_tile_map(CUtensorMap* map, const QuantArgs& a) {
+bool make_tile_map(CUtensorMap* map, const QuantArgs& a, int tile_rows = TTR) {
   const bool f32 = a.dtype == 1;
   return encode_tiled_2d(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.src,
                          (uint64_t)a.cols, (uint64_t)a.rows, (uint64_t)a.cols * (f32 ? 4u : 2u),
                          f32 ? (uint32_t)TileRing<true>::kBoxCols : (uint32_t)TileRing<false>::kBoxCols,
-                         (uint32_t)TTR);
+                         (uint32_t)tile_rows);
 }
 
-TileGeom make_tile_geom(const QuantArgs& a) {
+TileGeom make_tile_geom(const QuantArgs& a, int tile_rows = TTR) {
   TileGeom g;
   g.rows = a.rows;
   g.cols = a.cols;
   g.ntc = (a.cols + TTC - 1) / TTC;
-  g.ntiles = ((a.rows + TTR - 1) / TTR) * g.ntc;
+  g.ntiles = ((a.rows + tile_rows - 1) / tile_rows) * g.ntc;
   return g;
 }
 
@@ -2136,7 +2332,7 @@ cudaError_t run_amax_rows(const QuantArgs& a, cudaStream_t s) {
                : launch_amax_rows<false, false>(f, a.seed, ws, s);
 }
 
-cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
+cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s, int* grid_out) {
   const int block = a.fmt == 1 ? 32 : 16;
   const Flat f = make_flat(a.src, a.rows, a.cols, block);
   CopyOut o{};
@@ -2152,20 +2348,20 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s) {
   const bool f32 = a.dtype == 1;
   const int sr = a.rounding == 1;
   switch (a.fmt) {
-    case 0: return f32 ? dispatch_quant_rows<0, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<0, false>(a.rht, sr, f, a.seed, o, ws, s);
-    case 1: return f32 ? dispatch_quant_rows<1, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<1, false>(a.rht, sr, f, a.seed, o, ws, s);
-    case 2: return f32 ? dispatch_quant_rows<2, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s);
-    case 3: return f32 ? dispatch_quant_rows<3, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<3, false>(a.rht, sr, f, a.seed, o, ws, s);
-    case 4: return f32 ? dispatch_quant_rows<4, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<4, false>(a.rht, sr, f, a.seed, o, ws, s);
-    case 5: return f32 ? dispatch_quant_rows<5, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<5, false>(a.rht, sr, f, a.seed, o, ws, s);
-    case 6: return f32 ? dispatch_quant_rows<6, true>(a.rht, sr, f, a.seed, o, ws, s)
-                       : dispatch_quant_rows<6, false>(a.rht, sr, f, a.seed, o, ws, s);
+    case 0: return f32 ? dispatch_quant_rows<0, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<0, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 1: return f32 ? dispatch_quant_rows<1, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<1, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 2: return f32 ? dispatch_quant_rows<2, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<2, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 3: return f32 ? dispatch_quant_rows<3, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<3, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 4: return f32 ? dispatch_quant_rows<4, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<4, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 5: return f32 ? dispatch_quant_rows<5, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<5, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 6: return f32 ? dispatch_quant_rows<6, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<6, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
     default: return cudaErrorNotSupported;
   }
 }
@@ -2248,6 +2444,23 @@ cudaError_t run_quant_tiles(const QuantArgs& a, cudaStream_t s) {
     case 5: return f32 ? dispatch_quant_tiles<5, true>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s)
                        : dispatch_quant_tiles<5, false>(a.rht, sr, map, g, a.seed, rows, r, c, ws, s);
     default: return cudaErrorNotSupported;     // the two-level and MBS formats are row-wise only
+  }
+}
+
+cudaError_t run_quant_cols_outer(const QuantArgs& a, int row_np, cudaStream_t s) {
+  CUtensorMap map;
+  if (!make_tile_map(&map, a, TOR)) return cudaErrorNotSupported;
+  const TileGeom g = make_tile_geom(a, TOR);
+  const CopyOut c = tile_copy(a.col, a.cols, a.rows, 16);
+  Workspace* ws = static_cast<Workspace*>(a.ws);
+  const bool f32 = a.dtype == 1;
+  const int sr = a.rounding == 1;
+  switch (a.fmt) {
+    case 3: return f32 ? dispatch_cols_outer<3, true>(a.rht, sr, map, g, a.seed, c, ws, row_np, s)
+                       : dispatch_cols_outer<3, false>(a.rht, sr, map, g, a.seed, c, ws, row_np, s);
+    case 6: return f32 ? dispatch_cols_outer<6, true>(a.rht, sr, map, g, a.seed, c, ws, row_np, s)
+                       : dispatch_cols_outer<6, false>(a.rht, sr, map, g, a.seed, c, ws, row_np, s);
+    default: return cudaErrorNotSupported;
   }
 }
 

@@ -91,15 +91,16 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, -1, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     # column-wise only still needs source rows of a multiple of 16 elements
     assert q(fake, 0, 32, 100, 0, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
-    # two-level NVFP4 (format 3): row-wise only, whole 128-element outer blocks per row
-    assert q(fake, 0, 32, 256, 3, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
+    # two-level NVFP4 (format 3): whole 128-element outer blocks along the
+    # block axis: cols % 128 for the row-wise copy, rows % 128 for the column-wise
+    assert q(fake, 0, 32, 256, 3, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 144, 3, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 256, 3, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
     # the MXFP4 variants on 16-element blocks (4, 5) and MBS (6): block 16 only;
-    # MBS row-wise only with whole 128-element macro blocks; 7 is no format
+    # MBS with whole 128-element macro blocks along the block axis; 7 is no format
     for fmt in (4, 5, 6):
         assert q(fake, 0, 32, 256, fmt, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
-    assert q(fake, 0, 32, 256, 6, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 32, 256, 6, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 144, 6, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 256, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
 

@@ -140,7 +140,7 @@ def test_mx_rejections(lib):
     x = torch.randn(64, 384, device="cuda").to(torch.bfloat16)
     with pytest.raises(lib.FP4QError) as e:
         lib.fp4q_quantize(x, fmt="mxfp4_mbs", axis="col")
-    assert e.value.code == 2                        # row-wise only
+    assert e.value.code == 1                        # rows % 128 (outer blocks down the columns)
     y = torch.randn(64, 272, device="cuda").to(torch.bfloat16)
     with pytest.raises(lib.FP4QError) as e:
         lib.fp4q_quantize(y, fmt="mxfp4_mbs")
