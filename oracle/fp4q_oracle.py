@@ -26,6 +26,10 @@ Sources (page title, section):
           Quantization Error Reduction" -- Résumé technique §2 points 1-2
           (MXFP4: 32-element blocks, E8M0 power-of-two scale; NVFP4: 16-element
           blocks, E4M3 scale), §2A (alpha_max mapped to a power-of-two window).
+  [HIF]   "Unleashing Low-Bit Inference on Ascend NPUs: A Comprehensive
+          Evaluation of HiFloat Formats" -- Resumen técnico §2 Metodología
+          (HiF4: one E6M2 scale per 64 elements, E1M0 factors per 8 and per 4
+          elements, E1M2 elements).
   [OCP-MX] OCP Microscaling Formats (MX) v1.0: shared scale exponent
           floor(log2 amax) - emax_elem, emax_elem = 2 for E2M1.
   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1,
@@ -64,6 +68,17 @@ design notes of the repository):
      exponent by the OCP rule applied to a_b * (1/S), and y = (v * (1/S)) *
      2^-e_b; 1/S is one FP32 reciprocal (0 when S = 0, FLT_MAX if it
      overflows), as r_b is under R3.
+  R17 HiF4 ([HIF] §2 gives the structure, not the arithmetic; parity
+     unpinned for the reading itself): elements on the uniform E1M2 grid in
+     integer units 0..7 (as R2); E6M2 = an unsigned float with 6 exponent and
+     2 mantissa bits, bias 31, subnormals, every code finite; per 64-block
+     S = E6M2_rne_sat(a_64 / 7), r = 1/S (FP32; 0 if S = 0); an E1M0 factor
+     is one bit d that halves the step of its group: d_8 = 1 iff
+     RN(a_8 * r) * 2 <= 7, then d_4 = 1 iff RN(a_4 * r) * 2^(d_8 + 1) <= 7
+     (a group halves its step whenever none of its values would then clamp);
+     y = RN(v * r) * 2^(d_8 + d_4), rounded onto the grid. One 32-bit word per
+     64-block: E6M2 code in bits 0-7, d_8 of sub-block j in bit 8 + j, d_4 of
+     micro-block i in bit 16 + i.
   R13 two-level NVFP4 (the double-block scale of [TJ2] §2A): every outer block
      of 128 consecutive values along the block axis has its own FP32 scale
      g_o = A_o / (6 * 448), A_o = max |v| over the outer block, in place of the
@@ -709,6 +724,141 @@ def dequantize_mbs(codes_packed: np.ndarray, scales: np.ndarray, macro_scales: n
     return v
 
 
+# --------------------------------------------------------------------------- #
+# HiF4: three-level hierarchical scale [HIF] §2 Metodología, reading R17      #
+# --------------------------------------------------------------------------- #
+
+#: block, sub-block and micro-block of HiF4 ([HIF] Resumen técnico §2)
+HIF4_BLOCK, HIF4_SUB, HIF4_MICRO = 64, 8, 4
+HIF4_QMAX = 7.0
+E6M2_BIAS = 31
+
+
+def e6m2_decode(code) -> np.ndarray:
+    """Value of an unsigned E6M2 code 0..255 (reading R17), as FP64: exponent
+    field E = code >> 2, mantissa m = code & 3; E = 0 is subnormal,
+    m/4 * 2^(1 - 31); otherwise (1 + m/4) * 2^(E - 31). Largest value
+    1.75 * 2^32 (code 255), smallest positive 2^-32 (code 1)."""
+    c = np.asarray(code, dtype=np.int64) & 0xFF
+    e = c >> 2
+    m = c & 3
+    sub = (m / 4.0) * 2.0 ** (1 - E6M2_BIAS)
+    nrm = (1.0 + m / 4.0) * np.exp2((e - E6M2_BIAS).astype(np.float64))
+    return np.where(e == 0, sub, nrm)
+
+
+#: all 256 E6M2 values, ascending with the code.
+E6M2_VALUES = e6m2_decode(np.arange(256))
+
+
+def e6m2_encode_rne_sat(t) -> np.ndarray:
+    """FP32 t >= 0 -> E6M2 code: nearest value, ties to the even code; values
+    above the largest (1.75 * 2^32) saturate to it."""
+    a = np.minimum(np.asarray(t, dtype=np.float64), E6M2_VALUES[-1])
+    return _nearest_even(a, E6M2_VALUES).astype(np.uint8)
+
+
+def quantize_copy_hif4(m32: np.ndarray, rht: bool = False, rounding: str = "rtne",
+                       seed: int = 0, axis: int = 0, rht_mode: str = "butterfly",
+                       rows_subset=None) -> dict:
+    """HiF4 ([HIF] Resumen técnico §2 Metodología, reading R17): per copy row,
+    64-element block B, 8-element sub-block J inside it and 4-element
+    micro-block I inside J:
+      v    = RHT(x) or x (16-point transforms, four per block)
+      a_64 = max |v| over B;  t = a_64 / 7 (FP32);  S = E6M2_rne_sat(t)
+      r    = 1 / S (FP32; 0 if S = 0)
+      d_J  = 1 iff RN(a_J * r) * 2 <= 7             (a_J = max |v| over J)
+      d_I  = 1 iff RN(a_I * r) * 2^(d_J + 1) <= 7   (a_I = max |v| over I)
+      y    = RN(v * r) * 2^(d_J + d_I)  (the power of two is exact)
+      q    = RTNE(y) or SR(y, u_i) on the integer grid 0..7 (E1M2 in units of
+             1/4), sign kept
+    The element's value is q * S * 2^-(d_J + d_I). Returns the packed codes,
+    ``scales`` = one uint32 word per block (E6M2 code in bits 0-7, d_J of
+    sub-block j in bit 8 + j, d_I of micro-block i in bit 16 + i) and the
+    statistics (Qmax 7; v_hat = q * S * 2^-(d_J + d_I), FP64)."""
+    n, k = m32.shape
+    if k % HIF4_BLOCK:
+        raise ValueError("cols must be a multiple of the HiF4 block (64)")
+    sel = np.arange(n) if rows_subset is None else np.asarray(rows_subset, dtype=np.int64)
+    v = transform_copy(np.ascontiguousarray(m32[sel]), "ufp4", rht, seed, rht_mode)
+    rows = v.shape[0]
+    nb = k // HIF4_BLOCK
+    # block, sub-block (8 per block), micro-block (2 per sub-block), element (4)
+    vb = v.reshape(rows, nb, 8, 2, 4)
+    av = np.abs(vb)
+    a64 = av.max(axis=(2, 3, 4)).astype(np.float32)
+    a8 = av.max(axis=(3, 4)).astype(np.float32)
+    a4 = av.max(axis=4).astype(np.float32)
+    with np.errstate(invalid="ignore"):
+        t = (a64 / F32(HIF4_QMAX)).astype(np.float32)
+        s_code = e6m2_encode_rne_sat(t)
+    S = e6m2_decode(s_code).astype(np.float32)
+    with np.errstate(divide="ignore"):
+        r = np.where(S == 0.0, F32(0.0), F32(1.0) / S).astype(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        w8 = (a8 * r[..., None]).astype(np.float32)
+        d8 = (w8.astype(np.float64) * 2.0) <= HIF4_QMAX
+        w4 = (a4 * r[..., None, None]).astype(np.float32)
+        d4 = (w4.astype(np.float64) * np.exp2(d8[..., None].astype(np.float64) + 1.0)) <= HIF4_QMAX
+        shift = d8[..., None].astype(np.int64) + d4.astype(np.int64)          # rows, nb, 8, 2
+        w = (vb * r[..., None, None, None]).astype(np.float32)
+        y = (w.astype(np.float64) * np.exp2(shift.astype(np.float64))[..., None]).astype(np.float32)
+    y = y.reshape(rows, k)
+    if rounding == "rtne":
+        c = round_rtne(y, "ufp4")
+    elif rounding == "sr":
+        idx = sel[:, None] * k + np.arange(k, dtype=np.int64)[None, :]
+        c = round_sr(y, "ufp4", sr_uniforms(idx, seed, axis))
+    else:
+        raise ValueError(rounding)
+    d8_bits = np.sum(d8.astype(np.uint32) << np.arange(8, dtype=np.uint32), axis=-1, dtype=np.uint32)
+    d4_bits = np.sum(d4.reshape(rows, nb, 16).astype(np.uint32) << np.arange(16, dtype=np.uint32),
+                     axis=-1, dtype=np.uint32)
+    words = (s_code.astype(np.uint32) | (d8_bits << np.uint32(8)) | (d4_bits << np.uint32(16))).astype(np.uint32)
+    qv = code_value(c, "ufp4")
+    term = np.abs(qv) - np.abs(y.astype(np.float64))
+    step = S.astype(np.float64)[..., None, None] * np.exp2(-shift.astype(np.float64))
+    vhat = (qv.reshape(rows, nb, 8, 2, 4) * step[..., None]).reshape(rows, k)
+    v64 = v.astype(np.float64)
+    stats = stats_from_sums(float(np.sum(term)), float(np.sum(np.abs(term))), float(np.sum(v64 * v64)),
+                            float(np.sum((v64 - vhat) ** 2)), rows * k, HIF4_QMAX)
+    return {"fmt": "hif4", "block": HIF4_BLOCK, "rows": rows, "cols": k, "rows_subset": rows_subset,
+            "codes": pack_nibbles(c), "scales": words.reshape(rows, nb), "shift": shift.reshape(rows, nb * 16),
+            "y": y, "stats": stats}
+
+
+def hif4_fields(words: np.ndarray):
+    """Split HiF4 scale words into (E6M2 code, d_8 bits [..., 8], d_4 bits [..., 16])."""
+    w = np.asarray(words, dtype=np.uint32)
+    code = (w & np.uint32(0xFF)).astype(np.uint8)
+    d8 = ((w[..., None] >> (np.uint32(8) + np.arange(8, dtype=np.uint32))) & np.uint32(1)).astype(np.int64)
+    d4 = ((w[..., None] >> (np.uint32(16) + np.arange(16, dtype=np.uint32))) & np.uint32(1)).astype(np.int64)
+    return code, d8, d4
+
+
+def dequantize_hif4_f64(codes_packed: np.ndarray, words: np.ndarray) -> np.ndarray:
+    """Exact value of every element of a HiF4 copy, q * S * 2^-(d_8 + d_4)."""
+    c = unpack_nibbles(codes_packed)
+    n, k = c.shape
+    code, d8, d4 = hif4_fields(words)
+    shift = np.repeat(d8, 2, axis=-1) + d4                                # n, nb, 16
+    step = e6m2_decode(code)[..., None] * np.exp2(-shift.astype(np.float64))
+    q = code_value(c, "ufp4").reshape(n, k // HIF4_BLOCK, 16, HIF4_MICRO)
+    return (q * step[..., None]).reshape(n, k)
+
+
+def dequantize_hif4(codes_packed: np.ndarray, words: np.ndarray, inverse_rht: bool = False,
+                    seed: int = 0) -> np.ndarray:
+    """HiF4 values in FP32 (each is exact there: q * S has at most 6
+    significant bits and the power of two 2^-(d_8 + d_4) stays in range),
+    optionally followed by R^T (FP32 butterfly)."""
+    v = dequantize_hif4_f64(codes_packed, words).astype(np.float32)
+    if inverse_rht:
+        n, k = v.shape
+        v = rht_inverse_butterfly(v.reshape(n, k // 16, 16), rht_signs(seed)).reshape(n, k)
+    return v
+
+
 def code_histogram(codes_packed: np.ndarray) -> np.ndarray:
     """Number of elements carrying each 4-bit code 0..15 in a packed copy
     (reading R14)."""
@@ -759,7 +909,8 @@ def quantize(x, fmt: str, rht: bool = False, rounding: str = "rtne", seed: int =
     """
     m = _as_f32_matrix(x)
     out = {"nonfinite": bool(not np.all(np.isfinite(m)))}
-    outer = {"nvfp4_2l": quantize_copy_two_level, "mxfp4_mbs": quantize_copy_mbs}.get(fmt)
+    outer = {"nvfp4_2l": quantize_copy_two_level, "mxfp4_mbs": quantize_copy_mbs,
+             "hif4": quantize_copy_hif4}.get(fmt)
     if outer is not None:
         if axis in ("row", "both"):
             out["row"] = outer(m, rht, rounding, seed, 0, rht_mode, rows_subset)
