@@ -662,19 +662,22 @@ def run_gemm_leg(fq, torch, device, steps, warmup):
     return {"quant_ms": q_ms, "gemm_ms": g_ms, "status": status, "snr_db_vs_bf16": snr}
 
 
-def run_gemm_ufp4_leg(fq, torch, device, steps, warmup, peaks):
+def run_gemm_ufp4_leg(fq, torch, device, steps, warmup, peaks, fmt="ufp4"):
     """UFP4 on the contraction at 8192^3 (the pages' proposal: the uniform grid
     with the RHT on every GEMM): A, B N(0, 1/8192) BF16 -> UFP4 + RHT16 along
     K, then fp4q_gemm, which runs UFP4 on the 16-bit tensor-core MMA: converter
     warps form the exact FP16 block values level * s_b in shared memory, the
     tensor cores accumulate in FP32, the epilogue applies g_A g_B. Time per
-    GEMM call; the roofline is the dense FP16/BF16 tensor peak."""
+    GEMM call; the roofline is the dense FP16/BF16 tensor peak. fmt="hif4"
+    runs HiF4 operands the same way (exact BF16 block values, a scale per
+    4-element micro-block)."""
     import synth
     n = GEMM_N
     a = synth.gemm_operand("a", n, n).to(device)
     b = synth.gemm_operand("b", n, n).to(device)
-    qa, _ = fq.fp4q_quantize(a, fmt="ufp4", rht=True, seed=SEED, layout="mma")
-    qb, _ = fq.fp4q_quantize(b, fmt="ufp4", rht=True, seed=SEED, layout="mma")
+    layout = "linear" if fmt == "hif4" else "mma"
+    qa, _ = fq.fp4q_quantize(a, fmt=fmt, rht=True, seed=SEED, layout=layout)
+    qb, _ = fq.fp4q_quantize(b, fmt=fmt, rht=True, seed=SEED, layout=layout)
     y = torch.empty(n, n, dtype=torch.bfloat16, device=device)
     ws = fq.workspace(device)
     stream = torch.cuda.current_stream(device)
@@ -696,9 +699,10 @@ def run_gemm_ufp4_leg(fq, torch, device, steps, warmup, peaks):
     snr = 10 * math.log10(float((ref * ref).sum()) / float(((got - ref) ** 2).sum()))
     tflops = flop / (us * 1e-6) / 1e12
     peak = peaks["bf16_tflops"]
-    return {"workload": "A, B 8192x8192 BF16 N(0,1/8192) -> UFP4 + RHT16 along K -> fp4q_gemm: exact FP16 block "
-                        "values formed in shared memory, tcgen05 kind::f16 MMA (FP32 accumulate) x g_A g_B, BF16 "
-                        "Y = A B^T",
+    kind = "FP16" if fmt == "ufp4" else "BF16"
+    return {"workload": f"A, B 8192x8192 BF16 N(0,1/8192) -> {fmt.upper()} + RHT16 along K -> fp4q_gemm: exact "
+                        f"{kind} block values formed in shared memory, tcgen05 kind::f16 MMA (FP32 accumulate) x "
+                        "g_A g_B, BF16 Y = A B^T",
             "us": us, "tflops": tflops, "launches": len(evs), "device_status": status,
             "snr_db_vs_bf16_product": snr,
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
@@ -874,6 +878,7 @@ def run_mx_leg(fq, torch, device, steps, warmup, peaks):
     """The E8M0 formats of the MXFP4 page (Resume technique §2, §2A-§2B) on the
     activation tensor, RTNE, no RHT, row-wise: MXFP4 on 32- and on 16-element
     blocks, the overflow-aware rule (OAS), the static macro-block scale (MBS),
+    and HiF4 from the HiFloat page (E6M2 per 64, halving bits per 8 and 4),
     beside NVFP4: time per fp4q_quantize call (L2 flushed before each) and the
     SNR of each copy. Then the block-scaled GEMM at 8192^3 on the tensor cores
     with E8M0 scales (MXFP4 32-element blocks, OAS on 16-element blocks) and
@@ -889,7 +894,7 @@ def run_mx_leg(fq, torch, device, steps, warmup, peaks):
     quant = {}
     for fmt, bpe, launches in (("mxfp4", 2.5 + 1.0 / 32, 1), ("mxfp4_b16", 2.5 + 1.0 / 16, 1),
                                ("mxfp4_oas", 2.5 + 1.0 / 16, 1), ("mxfp4_mbs", 2.5 + 1.0 / 16 + 4.0 / 128, 1),
-                               ("nvfp4", B_AMAX + B_QUANT, 2)):
+                               ("hif4", 2.5 + 4.0 / 64, 1), ("nvfp4", B_AMAX + B_QUANT, 2)):
         q = fq.alloc_copy(ROWS, COLS, fmt, "linear", device)
         fq.fp4q_quantize(x, fmt=fmt, ws=ws, row_out=q)
         st, _ = fq.fp4q_stats(ws)
@@ -994,6 +999,8 @@ def main(argv=None) -> int:
     gemm_r = None if args.no_gemm else run_gemm_leg(fq, torch, device, args.steps, args.warmup)
     gemm_u = None if args.no_gemm else run_gemm_ufp4_leg(fq, torch, device, min(args.steps, 50), args.warmup,
                                                          peaks)
+    gemm_h = None if args.no_gemm else run_gemm_ufp4_leg(fq, torch, device, min(args.steps, 50), args.warmup,
+                                                         peaks, fmt="hif4")
     grad_r = run_grad_leg(fq, torch, device, min(args.steps, 50), args.warmup)
     tl_r = run_two_level_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
     hist_r = run_histogram_leg(fq, torch, device, min(args.steps, 200), args.warmup, peaks)
@@ -1072,10 +1079,11 @@ def main(argv=None) -> int:
                          "unit": "TFLOP/s", "frac": tflops / fp4_peak,
                          "peak_source": f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} "
                                         "(nominal dense FP4/BF16 ratio)",
-                         "traffic": ncu_traffic("gemm_nvf4_kernel", flop)},
+                         "traffic": ncu_traffic("gemm_nvf4_pair_kernel", flop)},
         }
         line["gpu_launches_gemm_leg"] = 3 * args.steps
         line["gemm_ufp4"] = gemm_u
+        line["gemm_hif4"] = gemm_h
     line["gradient_leg"] = {
         "workload": "4096x14336 and 14336x4096 BF16 N(0,1e-6) with 0.1% x100, NVFP4 + RHT16 + Philox "
                     "SR (seed 1234), row-wise and column-wise copies from one read",
@@ -1091,7 +1099,8 @@ def main(argv=None) -> int:
     line["mx_formats_leg"] = {
         "workload": "activation 8192x4096 BF16, RTNE, no RHT, row-wise: MXFP4 (32-element E8M0 blocks), MXFP4 "
                     "on 16-element blocks, OAS (16, E8M0), MBS-static (16, E8M0, 8-bit-mantissa scale per "
-                    "128), NVFP4; time per fp4q_quantize call, L2 flushed before each, and each copy's SNR. "
+                    "128), HiF4 (E6M2 per 64, halving bits per 8 and per 4, levels 0..7), NVFP4; time per "
+                    "fp4q_quantize call, L2 flushed before each, and each copy's SNR. "
                     "GEMM 8192^3 on the tensor cores with E8M0 scales (MXFP4, OAS) and with per-128 FP32 "
                     "scales along K (two-level NVFP4, MBS); operands + RHT16 along K",
         **mx_r}

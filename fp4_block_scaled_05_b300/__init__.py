@@ -26,9 +26,10 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-FORMATS = {"nvfp4": 0, "mxfp4": 1, "ufp4": 2, "nvfp4_2l": 3, "mxfp4_b16": 4, "mxfp4_oas": 5, "mxfp4_mbs": 6}
+FORMATS = {"nvfp4": 0, "mxfp4": 1, "ufp4": 2, "nvfp4_2l": 3, "mxfp4_b16": 4, "mxfp4_oas": 5, "mxfp4_mbs": 6,
+           "hif4": 7}
 BLOCKS = {"nvfp4": 16, "mxfp4": 32, "ufp4": 16, "nvfp4_2l": 16, "mxfp4_b16": 16, "mxfp4_oas": 16,
-          "mxfp4_mbs": 16}
+          "mxfp4_mbs": 16, "hif4": 64}
 OUTER_BLOCK = 128   # two-level NVFP4 and MBS: one FP32 scale per 128 elements of a row
 OUTER_SCALED = ("nvfp4_2l", "mxfp4_mbs")
 ROUNDING = {"rtne": 0, "sr": 1}
@@ -138,7 +139,8 @@ def workspace(device=None) -> torch.Tensor:
 class QCopy:
     """One quantised copy (device buffers) of a rows x cols matrix."""
     codes: torch.Tensor          # uint8 [rows, cols/2]
-    scales: torch.Tensor         # uint8 [rows, cols/block] (linear) or flat (mma)
+    scales: torch.Tensor         # uint8 [rows, cols/block] (linear) or flat (mma);
+                                 # HiF4: int32 [rows, cols/64], one scale word per block
     tensor_scale: torch.Tensor   # float32 [1]; two-level NVFP4 and MBS: [rows, cols/128] per-128 scales
                                  # ([cols/128, rows] with the tiled "mma" layout)
     fmt: str
@@ -159,7 +161,9 @@ def alloc_copy(rows: int, cols: int, fmt: str, layout: str = "linear", device=No
     dev = device if device is not None else "cuda"
     b = BLOCKS[fmt]
     codes = torch.empty(rows, cols // 2, dtype=torch.uint8, device=dev)
-    if layout == "linear":
+    if fmt == "hif4":
+        scales = torch.empty(rows, cols // b, dtype=torch.int32, device=dev)
+    elif layout == "linear":
         scales = torch.empty(rows, cols // b, dtype=torch.uint8, device=dev)
     else:
         scales = torch.empty(fp4q_scales_bytes(rows, cols, b, 1), dtype=torch.uint8, device=dev)

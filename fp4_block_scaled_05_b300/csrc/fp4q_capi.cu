@@ -102,10 +102,10 @@ namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int block_for(int fmt) { return fmt == FP4Q_MXFP4 ? 32 : 16; }
+int block_for(int fmt) { return fmt == FP4Q_MXFP4 ? 32 : (fmt == FP4Q_HIF4 ? 64 : 16); }
 
 int check_format(int fmt, int block) {
-  if (fmt < FP4Q_NVFP4 || fmt > FP4Q_MXFP4_MBS) return FP4Q_EINVAL;
+  if (fmt < FP4Q_NVFP4 || fmt > FP4Q_HIF4) return FP4Q_EINVAL;
   if (block != block_for(fmt)) return FP4Q_ENOTSUP;
   return FP4Q_OK;
 }
@@ -158,6 +158,14 @@ int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt
     if ((axis & FP4Q_ROWWISE) && cols % 128) return FP4Q_EINVAL;   // whole outer blocks per row
     if ((axis & FP4Q_COLWISE) && rows % 128) return FP4Q_EINVAL;   // ... and per column
   }
+  if (fmt == FP4Q_HIF4 && (axis & FP4Q_COLWISE)) return FP4Q_ENOTSUP;   // row-wise only
+  return FP4Q_OK;
+}
+
+// HiF4 copies: linear scale words (one uint32 per 64-element block), 4-byte aligned.
+int check_hif4_qtensor(const fp4q_qtensor* q, bool empty) {
+  if (q->scale_layout != FP4Q_SCALES_LINEAR) return FP4Q_ENOTSUP;
+  if (!empty && !aligned(q->scales, 4)) return FP4Q_EINVAL;
   return FP4Q_OK;
 }
 
@@ -177,6 +185,9 @@ int fp4q_workspace_init(void* workspace, void* stream) {
 size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout) {
   if (rows < 0 || cols < 0 || block <= 0) return 0;
   const int64_t nkb = cols / block;
+  if (block == 64) {                         // HiF4: a 32-bit word per block, linear only
+    return scale_layout == FP4Q_SCALES_LINEAR ? (size_t)rows * (size_t)nkb * 4 : 0;
+  }
   if (scale_layout == FP4Q_SCALES_MMA) {     // one scale per 16 elements along the row
     return (size_t)(((rows + 127) / 128) * 128) * (size_t)(((cols / 16 + 3) / 4) * 4);
   }
@@ -215,6 +226,7 @@ int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols, int fm
   const bool empty = rows == 0 || cols == 0;
   if ((axis & FP4Q_ROWWISE) && (rc = check_qtensor(row_out, empty))) return rc;
   if ((axis & FP4Q_COLWISE) && (rc = check_qtensor(col_out, empty))) return rc;
+  if (fmt == FP4Q_HIF4 && (rc = check_hif4_qtensor(row_out, empty))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   // padding bytes of the tiled scale layout are defined as 0
   if (!empty && (axis & FP4Q_ROWWISE) && row_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(rows, cols / 16)) {
@@ -251,6 +263,7 @@ int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, 
   if (dst_dtype != FP4Q_BF16 && dst_dtype != FP4Q_F32) return FP4Q_EINVAL;
   if (rows < 0 || cols < 0 || cols % block) return FP4Q_EINVAL;
   if (outer_scaled(fmt) && cols % 128) return FP4Q_EINVAL;
+  if (fmt == FP4Q_HIF4 && (rc = check_hif4_qtensor(q, false))) return rc;
   if (rows == 0 || cols == 0) return FP4Q_OK;
   if (!dst || !aligned(dst, 16)) return FP4Q_EINVAL;
   fp4q::DequantArgs a{};
@@ -273,6 +286,7 @@ int fp4q_gemm_dequant(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, i
   if (outer_scaled(fmt)) return FP4Q_ENOTSUP;
   if ((rc = check_qtensor(A)) || (rc = check_qtensor(B))) return rc;
   if (!aligned(A->scales, 2) || !aligned(B->scales, 2)) return FP4Q_EINVAL;
+  if (fmt == FP4Q_HIF4 && ((rc = check_hif4_qtensor(A, false)) || (rc = check_hif4_qtensor(B, false)))) return rc;
   if (out_dtype != FP4Q_BF16 && out_dtype != FP4Q_F32) return FP4Q_EINVAL;
   if (M <= 0 || N <= 0 || K <= 0 || K % 64 || N % 8) return FP4Q_EINVAL;
   if (M > (int64_t(1) << 24) || N > (int64_t(1) << 24) || K > (int64_t(1) << 24)) return FP4Q_EINVAL;
@@ -396,9 +410,9 @@ namespace {
 int gemm_common(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N, int64_t K, int fmt,
                 void* Y, int out_dtype, void* workspace, size_t ws_bytes, uint64_t timeout_ns, int skip,
                 void* stream) {
-  if (fmt < FP4Q_NVFP4 || fmt > FP4Q_MXFP4_MBS) return FP4Q_EINVAL;
-  // UFP4 has no FP4 tensor-core type: its block values go through the 16-bit MMA
-  if (fmt == FP4Q_UFP4) {
+  if (fmt < FP4Q_NVFP4 || fmt > FP4Q_HIF4) return FP4Q_EINVAL;
+  // UFP4 and HiF4 have no FP4 tensor-core type: their block values go through the 16-bit MMA
+  if (fmt == FP4Q_UFP4 || fmt == FP4Q_HIF4) {
     if (skip) return FP4Q_ENOTSUP;
     return fp4q_gemm_dequant(A, B, M, N, K, fmt, Y, out_dtype, workspace, ws_bytes, stream);
   }

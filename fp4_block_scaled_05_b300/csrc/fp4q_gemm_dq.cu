@@ -13,6 +13,10 @@
 //     product has at most 3 + 4 significant bits and lies in [2^-10, 3136].
 //   The E8M0 formats (MXFP4 on 32- or 16-element blocks, OAS): BF16, whose
 //     exponent range covers 2^e for every E8M0 code.
+//   HiF4 ("Unleashing Low-Bit Inference on Ascend NPUs ...", Resumen tecnico
+//     §2): BF16. A value is level * S * 2^-(d_8 + d_4), levels 0..7 and S an
+//     E6M2 value: at most 3 + 3 significant bits in [2^-34, 7 * 1.75 * 2^32].
+//     One scale word per row and 64-element K stage.
 // The FP16 / BF16 products of two such values are exact in FP32, so the only
 // rounding is the FP32 accumulation.
 //
@@ -78,7 +82,7 @@ static_assert((kBM + kBN) * 2 % kConvThreads == 0, "whole tasks per thread");
 static_assert(kSmem <= 227 * 1024, "shared memory budget");
 
 // Kinds of operand: how a code and a block scale become a 16-bit value.
-enum Kind { kNvfp4F16 = 0, kUfp4F16 = 1, kE8m0Bf16 = 2 };
+enum Kind { kNvfp4F16 = 0, kUfp4F16 = 1, kE8m0Bf16 = 2, kHif4Bf16 = 3 };
 
 // High bytes of the FP16 values of the 8 level magnitudes (their low bytes are
 // all zero): E2M1 {0, 0.5, 1, 1.5, 2, 3, 4, 6}; UFP4 {0, 1, ..., 7}.
@@ -87,6 +91,9 @@ constexpr uint32_t kUfp4F16Lo = 0x42403C00u, kUfp4F16Hi = 0x47464544u;
 // BF16 values of the E2M1 magnitudes, split into high and low bytes.
 constexpr uint32_t kE2m1Bf16HiLo = 0x3F3F3F00u, kE2m1Bf16HiHi = 0x40404040u;
 constexpr uint32_t kE2m1Bf16LoLo = 0xC0800000u, kE2m1Bf16LoHi = 0xC0804000u;
+// BF16 values of the uniform levels 0..7, split the same way.
+constexpr uint32_t kUfp4Bf16HiLo = 0x40403F00u, kUfp4Bf16HiHi = 0x40404040u;
+constexpr uint32_t kUfp4Bf16LoLo = 0x40008000u, kUfp4Bf16LoHi = 0xE0C0A080u;
 
 struct DqArgs {
   const uint8_t* codes;    // rows x K/2
@@ -94,6 +101,7 @@ struct DqArgs {
   int rows;
   int tiled;               // scale layout
   int block32;             // linear MXFP4 scales: one per 32 elements
+  int hif4;                // HiF4: one 32-bit scale word per 64 elements (linear)
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -135,10 +143,28 @@ __device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
   return d;
 }
 
+// HiF4: the eight 4-element micro-blocks of half h of a 64-element block as
+// BF16 scale pairs, S * 2^-(d_8 + d_4) (S = 0 stays 0). S is E6M2 (bias 31):
+// exponent field E >= 1 -> BF16 exponent E + 96 and mantissa m << 5; E = 0 ->
+// m * 2^-32, exact in FP32 and then in BF16.
+__device__ __forceinline__ void hif4_scale_pairs(uint32_t wd, int h, uint32_t (&sp)[8]) {
+  const uint32_t c = wd & 0xFFu, E = c >> 2, m = c & 3u;
+  const uint32_t sb = E ? (((E + 96u) << 7) | (m << 5))
+                        : (__float_as_uint(__fmul_rn((float)m, 2.3283064365386963e-10f)) >> 16);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t sh = ((wd >> (8 + 4 * h + (i >> 1))) & 1u) + ((wd >> (16 + 8 * h + i)) & 1u);
+    const uint32_t v = sb ? sb - (sh << 7) : 0u;
+    sp[i] = v | (v << 16);
+  }
+}
+
 // Eight codes (one 32-bit word: element 2j in the low nibble of byte j) times
-// one scale pair -> four 16-bit pairs (one 16-byte chunk, element order).
+// scale pairs -> four 16-bit pairs (one 16-byte chunk, element order); codes
+// 0-3 take s2lo, codes 4-7 s2hi (the same pair for every block format but
+// HiF4, whose micro-blocks have 4 elements).
 template <int KIND>
-__device__ __forceinline__ uint4 convert8(uint32_t w, uint32_t s2) {
+__device__ __forceinline__ uint4 convert8(uint32_t w, uint32_t s2lo, uint32_t s2hi) {
   const uint32_t t = w << 4;                 // byte j: low code's nibble in bits 4-7
   const uint32_t e4 = t & 0x70707070u;       // byte j, bits 4-6: magnitude of code 2j
   const uint32_t o4 = w & 0x70707070u;       // byte j, bits 4-6: magnitude of code 2j + 1
@@ -147,11 +173,16 @@ __device__ __forceinline__ uint4 convert8(uint32_t w, uint32_t s2) {
   for (int j = 0; j < 4; ++j) {
     // selector nibbles (0, |code 2j|, 0, |code 2j + 1|): entry 0 of every table is 0
     const uint32_t x = prmt(e4, o4, (uint32_t)j | ((uint32_t)(4 + j) << 4));
+    const uint32_t s2 = j < 2 ? s2lo : s2hi;
     uint32_t v;
     if constexpr (KIND == kNvfp4F16) {
       v = hmul2_f16(prmt(kE2m1F16Lo, kE2m1F16Hi, x), s2);
     } else if constexpr (KIND == kUfp4F16) {
       v = hmul2_f16(prmt(kUfp4F16Lo, kUfp4F16Hi, x), s2);
+    } else if constexpr (KIND == kHif4Bf16) {
+      const uint32_t hi = prmt(kUfp4Bf16HiLo, kUfp4Bf16HiHi, x);
+      const uint32_t lo = prmt(kUfp4Bf16LoLo, kUfp4Bf16LoHi, x >> 4);
+      v = hmul2_bf16(hi | lo, s2);
     } else {
       const uint32_t hi = prmt(kE2m1Bf16HiLo, kE2m1Bf16HiHi, x);
       const uint32_t lo = prmt(kE2m1Bf16LoLo, kE2m1Bf16LoHi, x >> 4);
@@ -280,6 +311,9 @@ gemm_dq_kernel(DqArgs A, DqArgs B, int K, const float* __restrict__ g_a, const f
         if (o.tiled) {
           sptr[j] = o.scales + (int64_t)(rr >> 7) * (nkb >> 2) * 512 + (rr & 31) * 16 + ((rr >> 5) & 3) * 4 + 2 * h;
           sstep[j] = 512;
+        } else if (o.hif4) {       // both halves read the block's word
+          sptr[j] = o.scales + (int64_t)rr * (K / 16);
+          sstep[j] = 4;
         } else if (o.block32) {
           sptr[j] = o.scales + (int64_t)rr * (K / 32) + h;
           sstep[j] = 2;
@@ -295,7 +329,9 @@ gemm_dq_kernel(DqArgs A, DqArgs B, int K, const float* __restrict__ g_a, const f
       for (int j = 0; j < kTasks; ++j) {
         if (valid[j]) {
           t[j].codes = __ldg(reinterpret_cast<const uint4*>(cptr[j]));
-          if (sstep[j] == 2) {
+          if constexpr (KIND == kHif4Bf16) {
+            t[j].scales = __ldg(reinterpret_cast<const uint32_t*>(sptr[j]));
+          } else if (sstep[j] == 2) {
             const uint32_t b = __ldg(sptr[j]);
             t[j].scales = b | (b << 8);
           } else {
@@ -321,13 +357,24 @@ gemm_dq_kernel(DqArgs A, DqArgs B, int K, const float* __restrict__ g_a, const f
 #pragma unroll
       for (int j = 0; j < kTasks; ++j) {
         uint8_t* rowp = st + tsmem[j];
-        uint32_t sa, sb;
-        scale_pairs<KIND>(t[j].scales, sa, sb);
         const uint32_t w[4] = {t[j].codes.x, t[j].codes.y, t[j].codes.z, t[j].codes.w};
+        if constexpr (KIND == kHif4Bf16) {
+          uint32_t sp[8];
+          hif4_scale_pairs(t[j].scales, h, sp);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t c = (uint32_t)(4 * h + i);         // 16-byte chunk of the 128-byte row
-          *reinterpret_cast<uint4*>(rowp + ((c ^ tkey[j]) << 4)) = convert8<KIND>(w[i], i < 2 ? sa : sb);
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t c = (uint32_t)(4 * h + i);
+            *reinterpret_cast<uint4*>(rowp + ((c ^ tkey[j]) << 4)) = convert8<KIND>(w[i], sp[2 * i], sp[2 * i + 1]);
+          }
+        } else {
+          uint32_t sa, sb;
+          scale_pairs<KIND>(t[j].scales, sa, sb);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t c = (uint32_t)(4 * h + i);         // 16-byte chunk of the 128-byte row
+            const uint32_t s2 = i < 2 ? sa : sb;
+            *reinterpret_cast<uint4*>(rowp + ((c ^ tkey[j]) << 4)) = convert8<KIND>(w[i], s2, s2);
+          }
         }
       }
       // the stores become visible to the tensor cores' (async) reads
@@ -358,7 +405,7 @@ gemm_dq_kernel(DqArgs A, DqArgs B, int K, const float* __restrict__ g_a, const f
       }
     } else if (lane == 0) {
       // ---------------- rank 0: MMA issuer for the pair ----------------
-      const uint32_t idesc = idesc_f16(2 * kBM, 2 * kBN, KIND == kE8m0Bf16 ? 1u : 0u);
+      const uint32_t idesc = idesc_f16(2 * kBM, 2 * kBN, (KIND == kE8m0Bf16 || KIND == kHif4Bf16) ? 1u : 0u);
       const uint32_t base = smem_u32(smem);
       const uint64_t da0 = smem_desc(base, 16, 1024, 2);
       const uint64_t db0 = smem_desc(base + kABytes, 16, 1024, 2);
@@ -472,8 +519,9 @@ cudaError_t launch_dq(const GemmArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const bool b32 = a.fmt == 1;     // MXFP4: one scale per 32 elements in the linear layout
-  DqArgs da{a.a.codes, a.a.scales, (int)a.m, a.a.scale_layout, b32 && !a.a.scale_layout};
-  DqArgs db{a.b.codes, a.b.scales, (int)a.n, a.b.scale_layout, b32 && !a.b.scale_layout};
+  const int hif4 = a.fmt == 7 ? 1 : 0;
+  DqArgs da{a.a.codes, a.a.scales, (int)a.m, a.a.scale_layout, b32 && !a.a.scale_layout, hif4};
+  DqArgs db{a.b.codes, a.b.scales, (int)a.n, a.b.scale_layout, b32 && !a.b.scale_layout, hif4};
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = kSmem;
@@ -515,6 +563,7 @@ cudaError_t run_gemm_dequant(const GemmArgs& a, cudaStream_t s) {
     case 0: return launch_dq_out<kNvfp4F16>(a, s);
     case 2: return launch_dq_out<kUfp4F16>(a, s);
     case 1: case 4: case 5: return launch_dq_out<kE8m0Bf16>(a, s);
+    case 7: return launch_dq_out<kHif4Bf16>(a, s);
     default: return cudaErrorNotSupported;      // per-128 scales: not one 16-bit value per element
   }
 }

@@ -18,9 +18,10 @@
 //    (amax_tiles_kernel when the RHT makes the two copies' amax differ,
 //    quant_tiles_kernel).
 // The E8M0 formats (MXFP4 on 32- or 16-element blocks, its overflow-aware
-// variant, MBS with its 128-element macro scale) and two-level NVFP4 (a scale
-// per 128-element outer block) have no tensor scale, so they skip the amax
-// pass.
+// variant, MBS with its 128-element macro scale), two-level NVFP4 (a scale
+// per 128-element outer block) and HiF4 (a scale per 64-element block) have no
+// tensor scale, so they skip the amax pass. HiF4 ("Unleashing Low-Bit
+// Inference on Ascend NPUs ...", Resumen tecnico §2) is row-wise only.
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -40,7 +41,7 @@ __global__ void quantize_empty_kernel(int fmt, int axis, float* ts_row, float* t
   ws->copies = (unsigned)axis;
   ws->tensor_scale[0] = g;
   ws->tensor_scale[1] = g;
-  ws->qmax = (fmt == 2) ? 7.f : 6.f;
+  ws->qmax = (fmt == 2 || fmt == 7) ? 7.f : 6.f;
   ws->n = 0.0;
   if ((axis & 1) && ts_row) *ts_row = g;
   if ((axis & 2) && ts_col) *ts_col = g;

@@ -294,7 +294,8 @@ __device__ __forceinline__ void make_sign_words(uint32_t smask, uint32_t (&sgn)[
 // Formats (template argument FMT): 0 NVFP4, 1 MXFP4 (32-element blocks),
 // 2 UFP4, 3 two-level NVFP4, 4 MXFP4 on 16-element blocks, 5 the same with the
 // overflow-aware exponent rule, 6 MBS-static (16-element E8M0 blocks under a
-// 128-element macro scale).
+// 128-element macro scale), 7 HiF4 (an E6M2 scale per 64 elements with
+// halving bits per 8 and per 4 elements, uniform levels 0..7).
 template <int FMT> constexpr bool kE8M0 = FMT == 1 || FMT == 4 || FMT == 5 || FMT == 6;
 // formats with a per-tensor FP32 scale (and so an amax pass)
 template <int FMT> constexpr bool kTensorScaled = FMT == 0 || FMT == 2;
@@ -523,6 +524,25 @@ __device__ __forceinline__ float mbs_macro_scale(float alpha) {
   const uint32_t low = b & 0x7FFFu, base = b - low;
   const bool up = low > 0x4000u || (low == 0x4000u && (rem > 0.f || (rem == 0.f && (base & 0x8000u))));
   return __uint_as_float(base + (up ? 0x8000u : 0u));
+}
+
+// HiF4's block scale: an unsigned E6M2 value (6 exponent bits with bias 31,
+// 2 mantissa bits, subnormals below 2^-30 in steps of 2^-32, every code
+// finite). t >= 0 is rounded to the nearest value, ties to the even code, and
+// saturates at 1.75 * 2^32. In the normal range the rounding keeps 2 of
+// FP32's 23 fraction bits (a carry into the exponent is the correct result);
+// below it, t * 2^32 (exact) is rounded to an integer, ties to even.
+__device__ __forceinline__ float e6m2_rne_sat(float t, uint32_t& code) {
+  if (t >= 9.313225746154785e-10f) {                         // 2^-30
+    const uint32_t b = __float_as_uint(t);
+    uint32_t u = (b + 0x000FFFFFu + ((b >> 21) & 1u)) & ~0x001FFFFFu;
+    if (u > 0x4FE00000u) u = 0x4FE00000u;                    // 1.75 * 2^32 (and +inf)
+    code = (((u >> 23) - 96u) << 2) | ((u >> 21) & 3u);     // E = FP32 exponent - 127 + 31
+    return __uint_as_float(u);
+  }
+  const float k = rintf(__fmul_rn(t, 4294967296.f));         // 0 .. 4 (4 is 2^-30, code 4)
+  code = (uint32_t)k;
+  return __fmul_rn(k, 2.3283064365386963e-10f);              // k * 2^-32
 }
 
 // Quantise one block of NP pairs (NP = 8: a 16-block, NP = 16: an MXFP4
@@ -945,6 +965,119 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       acc.bias.add(bsum);
       if ((threadIdx.x & 3u) == 0u) o.tensor_scale[outer_index(o, f, e)] = S;
     }
+  } else if constexpr (FMT == 7) {
+    // HiF4 ("Unleashing Low-Bit Inference on Ascend NPUs: A Comprehensive
+    // Evaluation of HiFloat Formats", Resumen tecnico §2 Metodologia): the two
+    // threads of a 64-element block (lanes 2k, 2k+1; rows hold whole blocks)
+    // share its amax a, which sets the E6M2 scale S = RN_E6M2(a / 7). Each
+    // thread then decides, for its four 8-element sub-blocks and eight
+    // 4-element micro-blocks, whether the group's step can be halved without
+    // a value clamping at 7 (w = RN(a_group / S) <= 3.5, and <= 1.75 for a
+    // micro-block whose sub-block already halved), and rounds y = RN(v / S)
+    // 2^shift onto the levels 0..7. Every lane takes part in the shuffles.
+    f2 Q[16];
+    float a4[8];
+    if (nb16 == 2) {
+      load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
+      load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float a, b, c, d;
+        f2_split(Q[2 * i], a, b);
+        f2_split(Q[2 * i + 1], c, d);
+        a4[i] = max3_abs_nan(max3_abs_nan(0.f, a, b), c, d);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) a4[i] = 0.f;
+    }
+    float m = max_abs_nan(max_abs_nan(max_abs_nan(a4[0], a4[1]), max_abs_nan(a4[2], a4[3])),
+                          max_abs_nan(max_abs_nan(a4[4], a4[5]), max_abs_nan(a4[6], a4[7])));
+    m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    uint32_t mine = 0u, scode = 0u;
+    if (nb16 == 2) {
+      nonfinite |= (__float_as_uint(m) >= 0x7F800000u) ? 1u : 0u;
+      const float S = e6m2_rne_sat(__fdiv_rn(m, 7.f), scode);
+      const float r = (S == 0.f) ? 0.f : __frcp_rn(S);
+      const f2 R = f2_make(r, r);
+      uint32_t cw[4] = {0u, 0u, 0u, 0u};
+      float bsum = 0.f, ss = 0.f, es = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t d8 = (__fmul_rn(fmaxf(a4[2 * j], a4[2 * j + 1]), r) <= 3.5f) ? 1u : 0u;
+        mine |= d8 << j;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = 2 * j + h;
+          const uint32_t d4 = (__fmul_rn(a4[i], r) <= (d8 ? 1.75f : 3.5f)) ? 1u : 0u;
+          mine |= d4 << (4 + i);
+          const uint32_t sh = d8 + d4;
+          const f2 M = f2_make(__uint_as_float((127u + sh) << 23), __uint_as_float((127u + sh) << 23));
+          const float wt = __uint_as_float((127u - 2u * sh) << 23);     // 4^-shift: units of S^2
+          uint4 rw = make_uint4(0u, 0u, 0u, 0u);
+          if constexpr (SR) {   // the micro-block's four uniforms: one Philox call
+            const uint64_t q = ((uint64_t)e >> 2) + (uint64_t)i;
+            rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), pk);
+          }
+          f2 B2 = f2_make(0.f, 0.f), E2 = B2, S2 = B2;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const f2 Y = f2_mul(f2_mul(Q[2 * i + t], R), M);
+            f2 D;
+            uint32_t byte;
+            if constexpr (SR) {
+              byte = (t == 0) ? sr_pair<2>(Y, rw.x, rw.y, D) : sr_pair<2>(Y, rw.z, rw.w, D);
+            } else {
+              byte = ufp4_pair(Y, D);
+            }
+            cw[i >> 1] |= byte << (8 * ((2 * i + t) & 3));
+            B2 = f2_add(B2, D);
+            E2 = f2_fma(D, D, E2);
+            S2 = f2_fma(Y, Y, S2);
+          }
+          float x0, x1;
+          f2_split(B2, x0, x1);
+          bsum = __fadd_rn(bsum, __fadd_rn(x0, x1));
+          f2_split(S2, x0, x1);
+          ss = __fmaf_rn(__fadd_rn(x0, x1), wt, ss);
+          f2_split(E2, x0, x1);
+          es = __fmaf_rn(__fadd_rn(x0, x1), wt, es);
+        }
+      }
+      *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+      acc.bias.add(bsum);
+      if (S != 0.f && fabsf(ss) <= FLT_MAX && fabsf(es) <= FLT_MAX) {
+        add_outer_stats(acc, S, ss, es);
+      } else if (m > 0.f) {
+        // The scale rounded to 0 (every value became 0: its error is v), or it
+        // saturated so far below the values that their squares overflow FP32:
+        // the sums in FP64 from v and the codes, value = level * S * 2^-shift.
+        double sg = 0.0, er = 0.0;
+#pragma unroll 1
+        for (int j = 0; j < 16; ++j) {
+          float a, b;
+          f2_split(Q[j], a, b);
+          const int i = j >> 1;
+          const uint32_t sh = ((mine >> (i >> 1)) & 1u) + ((mine >> (4 + i)) & 1u);
+          const double st = (double)S * (double)__uint_as_float((127u - sh) << 23);
+          const uint32_t byte = (cw[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+          const double q0 = (double)(byte & 7u) * ((byte & 8u) ? -st : st);
+          const double q1 = (double)((byte >> 4) & 7u) * ((byte & 0x80u) ? -st : st);
+          sg += (double)a * (double)a + (double)b * (double)b;
+          er += ((double)a - q0) * ((double)a - q0) + ((double)b - q1) * ((double)b - q1);
+        }
+        acc.sig64 += sg;
+        acc.err64 += er;
+      }
+    }
+    // the even lane writes the block's word: E6M2 code, then the eight
+    // sub-block bits, then the sixteen micro-block bits (its own half first)
+    const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+    if (nb16 == 2 && (threadIdx.x & 1u) == 0u) {
+      const uint32_t w = scode | ((mine & 0xFu) << 8) | ((other & 0xFu) << 12) | (((mine >> 4) & 0xFFu) << 16) |
+                         (((other >> 4) & 0xFFu) << 24);
+      reinterpret_cast<uint32_t*>(o.scales)[(uint64_t)e >> 6] = w;
+    }
   } else if constexpr (FMT == 3) {
     // Two-level NVFP4 (TetraJet-v2, Riepilogo Tecnico §2A): the four threads of
     // a 128-element outer block (lanes 4k .. 4k+3; rows hold whole outer
@@ -1078,7 +1211,7 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   __shared__ uint32_t sh_max[RT / 32];
   constexpr int S = Ring<F32>::kStages;
   constexpr int ES = F32 ? 4 : 2;
-  constexpr float kQmax = (FMT == 2) ? 7.f : 6.f;
+  constexpr float kQmax = (FMT == 2 || FMT == 7) ? 7.f : 6.f;
   constexpr float kQmax448 = (FMT == 2) ? 3136.f : 2688.f;
   const int tid = threadIdx.x;
   uint32_t sgn[16];
@@ -2010,24 +2143,9 @@ __device__ __forceinline__ float block_scale_value(uint32_t sc) {
   }
 }
 
-// Dequantise one 16-block: `w0`, `w1` its code words, `sv` its scale value.
-// Writes 16 values at `out` (BF16 or FP32).
-template <int FMT, bool OUT_F32, bool IRHT>
-__device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float g, const uint32_t (&sgn)[16],
-                                      void* out) {
-  float q[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) levels2<FMT>(((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu, q[2 * j], q[2 * j + 1]);
-  float v[16];
-  {
-    const f2 S = f2_make(sv, sv), G = f2_make(g, g);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      f2 r = f2_mul(f2_make(q[2 * j], q[2 * j + 1]), S);
-      if (FMT != 1 && FMT != 4 && FMT != 5) r = f2_mul(r, G);
-      f2_split(r, v[2 * j], v[2 * j + 1]);
-    }
-  }
+// 16 dequantised values to `out` (BF16 or FP32), after R^T when IRHT.
+template <bool OUT_F32, bool IRHT>
+__device__ __forceinline__ void store16(float (&v)[16], const uint32_t (&sgn)[16], void* out) {
   if constexpr (IRHT) {
     // R^T = (1/4) diag(sigma) H16: the forward butterfly (stages 1, 2, 4, 8, then
     // * 1/4) without its sign flip, then the sign flip
@@ -2056,6 +2174,57 @@ __device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float 
     o[0] = make_uint4(h[0], h[1], h[2], h[3]);
     o[1] = make_uint4(h[4], h[5], h[6], h[7]);
   }
+}
+
+// Dequantise one 16-block: `w0`, `w1` its code words, `sv` its scale value.
+// Writes 16 values at `out` (BF16 or FP32).
+template <int FMT, bool OUT_F32, bool IRHT>
+__device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float g, const uint32_t (&sgn)[16],
+                                      void* out) {
+  float q[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) levels2<FMT>(((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu, q[2 * j], q[2 * j + 1]);
+  float v[16];
+  const f2 S = f2_make(sv, sv), G = f2_make(g, g);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    f2 r = f2_mul(f2_make(q[2 * j], q[2 * j + 1]), S);
+    if (FMT != 1 && FMT != 4 && FMT != 5) r = f2_mul(r, G);
+    f2_split(r, v[2 * j], v[2 * j + 1]);
+  }
+  store16<OUT_F32, IRHT>(v, sgn, out);
+}
+
+// Value of a HiF4 E6M2 scale code (bias 31; exponent field 0 is subnormal).
+__device__ __forceinline__ float e6m2_value(uint32_t c) {
+  const uint32_t E = c >> 2, m = c & 3u;
+  return E ? __uint_as_float(((E + 96u) << 23) | (m << 21)) : __fmul_rn((float)m, 2.3283064365386963e-10f);
+}
+
+// Dequantise 16 HiF4 elements, the `hb`-th 16 (0..3) of the block whose scale
+// word is `word`: level * S * 2^-(d_8 + d_4) per 4-element micro-block, exact
+// in FP32 (at most 6 significant bits, exponent within range).
+template <bool OUT_F32, bool IRHT>
+__device__ __forceinline__ void deq16_hif4(uint32_t w0, uint32_t w1, uint32_t word, int hb,
+                                           const uint32_t (&sgn)[16], void* out) {
+  float q[16];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) levels2<2>(((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu, q[2 * j], q[2 * j + 1]);
+  const float S = e6m2_value(word & 0xFFu);
+  float v[16];
+#pragma unroll
+  for (int qd = 0; qd < 4; ++qd) {
+    const int i = 4 * hb + qd;                       // micro-block in the block
+    const uint32_t sh = ((word >> (8 + (i >> 1))) & 1u) + ((word >> (16 + i)) & 1u);
+    const float st = __fmul_rn(S, __uint_as_float((127u - sh) << 23));
+    const f2 ST = f2_make(st, st);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int j = 2 * qd + t;
+      f2_split(f2_mul(f2_make(q[2 * j], q[2 * j + 1]), ST), v[2 * j], v[2 * j + 1]);
+    }
+  }
+  store16<OUT_F32, IRHT>(v, sgn, out);
 }
 
 // DUP: a 32-element block, whose scale the MMA layout holds for both halves
@@ -2093,7 +2262,12 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
     if (e2 + 32 <= f.n) asm volatile("prefetch.global.L2 [%0];" ::"l"(q.codes + e2 / 2));
     if (f.n - e >= 32) {
       const uint4 cw = __ldg(reinterpret_cast<const uint4*>(q.codes + e / 2));
-      if constexpr (B == 32) {
+      if constexpr (FMT == 7) {   // rows hold whole 64-element blocks
+        const uint32_t word = __ldg(reinterpret_cast<const uint32_t*>(q.scales) + (e >> 6));
+        const int hb = (int)((e >> 4) & 3);
+        deq16_hif4<OUT_F32, IRHT>(cw.x, cw.y, word, hb, sgn, out + e * ES);
+        deq16_hif4<OUT_F32, IRHT>(cw.z, cw.w, word, hb + 1, sgn, out + (e + 16) * ES);
+      } else if constexpr (B == 32) {
         const float sv = block_scale_value<FMT>(get_scale<true>(q, f, (uint64_t)e / 32));
         deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, sv, g, sgn, out + e * ES);
         deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, sv, g, sgn, out + (e + 16) * ES);
@@ -2105,7 +2279,7 @@ __global__ void __launch_bounds__(256) dequant_rows_kernel(Flat f, CopyOut q, ui
         deq16<FMT, OUT_F32, IRHT>(cw.x, cw.y, s0, gs, sgn, out + e * ES);
         deq16<FMT, OUT_F32, IRHT>(cw.z, cw.w, s1, gs, sgn, out + (e + 16) * ES);
       }
-    } else {   // a lone 16-block at the very end (16-element formats only)
+    } else if constexpr (FMT != 7) {   // a lone 16-block at the very end (16-element formats only)
       const uint2 cw = __ldg(reinterpret_cast<const uint2*>(q.codes + e / 2));
       const float s0 = block_scale_value<FMT>(get_scale(q, f, (uint64_t)e / B));
       const float gs = kOuterScaled<FMT> ? __ldg(q.tensor_scale + outer_index(q, f, e)) : g;
@@ -2362,6 +2536,8 @@ cudaError_t run_quant_rows(const QuantArgs& a, cudaStream_t s, int* grid_out) {
                        : dispatch_quant_rows<5, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
     case 6: return f32 ? dispatch_quant_rows<6, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
                        : dispatch_quant_rows<6, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
+    case 7: return f32 ? dispatch_quant_rows<7, true>(a.rht, sr, f, a.seed, o, ws, s, grid_out)
+                       : dispatch_quant_rows<7, false>(a.rht, sr, f, a.seed, o, ws, s, grid_out);
     default: return cudaErrorNotSupported;
   }
 }
@@ -2386,6 +2562,7 @@ cudaError_t run_dequantize(const DequantArgs& a, cudaStream_t s) {
     case 4: return launch_dequant_rows<4>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 5: return launch_dequant_rows<5>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     case 6: return launch_dequant_rows<6>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
+    case 7: return launch_dequant_rows<7>(f, q, a.inverse_rht, a.seed, a.dst, a.dst_dtype, s);
     default: return cudaErrorNotSupported;
   }
 }

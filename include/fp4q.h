@@ -17,6 +17,10 @@
  *           with E4M3 scales), §2B (scale math beside dense tensor-core math).
  *   [NGPT]  "Le Architetture Normalizzate sono Nativamente a 4 Bit": Metodologia
  *           (NVFP4 consumed natively by Blackwell tensor cores; SNR of Y = WX).
+ *   [HIF]   "Unleashing Low-Bit Inference on Ascend NPUs: A Comprehensive
+ *           Evaluation of HiFloat Formats": Resumen tecnico §2 Metodologia (HiF4:
+ *           E6M2 scale per 64 elements, E1M0 factors per 8 and per 4 elements,
+ *           E1M2 elements).
  *
  * Conventions shared by every entry point
  *   - Every pointer named "device" is a CUDA device pointer owned by the caller.
@@ -57,10 +61,18 @@ typedef enum {
                        2^e, e = floor(log2 a_b) - 2 (a_b = max |v| over the block), no tensor scale */
   FP4Q_MXFP4_OAS = 5, /* overflow-aware scaling [MXFP4 §2A] on 16-element blocks: E8M0 scale with
                        e = ceil(log2(a_b / 7)), which puts a_b / 2^e in (3.5, 7] instead of [4, 8) */
-  FP4Q_MXFP4_MBS = 6  /* static macro-block scaling [MXFP4 §2B]: an FP32 scale S with 8 mantissa bits per
+  FP4Q_MXFP4_MBS = 6, /* static macro-block scaling [MXFP4 §2B]: an FP32 scale S with 8 mantissa bits per
                        128-element macro block along the row, S = A_M / 6 rounded to nearest (ties to even) on
                        the 8-fraction-bit grid (A_M = max |v| over the macro block), and 16-element E8M0 blocks
-                       under it: e = floor(log2(a_b * (1/S))) - 2, y = (v * (1/S)) * 2^-e; row-wise only */
+                       under it: e = floor(log2(a_b * (1/S))) - 2, y = (v * (1/S)) * 2^-e */
+  FP4Q_HIF4 = 7       /* HiF4 three-level scale [HIF §2], block 64, row-wise copy only: per 64-element block an
+                       unsigned E6M2 scale S (bias 31, subnormals, all codes finite) = the value nearest
+                       a_64 / 7 (ties to the even code, saturating at 1.75 * 2^32); per 8-element sub-block a
+                       bit d_8 and per 4-element micro-block a bit d_4 that halve the step, set when no value of
+                       the group would then exceed 7: d_8 = [RN(a_8 / S) <= 3.5], d_4 = [RN(a_4 / S) * 2^(d_8+1)
+                       <= 7], with a_g = max |v| over the group and a / S formed as a * RN(1/S); elements on the
+                       uniform levels 0..7 (E1M2 in units of 1/4), y = RN(v * RN(1/S)) * 2^(d_8 + d_4). The
+                       page gives the structure only: this reading of it is the library's */
 } fp4q_format;
 
 typedef enum { FP4Q_RTNE = 0, FP4Q_SR = 1 } fp4q_rounding;
@@ -96,9 +108,15 @@ enum {
  *                has its scale at both of its vectors. Size: fp4q_scales_bytes().
  *                NVFP4/UFP4/NVFP4_2L scales are E4M3 codes; the MXFP4 formats'
  *                scales are E8M0 codes (exponent + 127).
+ *                FP4Q_HIF4 (linear only): one little-endian uint32 word per
+ *                64-element block, rows x cols/64 words (4-byte aligned): the
+ *                E6M2 code in bits 0-7, d_8 of sub-block j (elements 8j .. 8j+7
+ *                of the block) in bit 8 + j, d_4 of micro-block i (elements
+ *                4i .. 4i+3) in bit 16 + i. Element value: level(code) * S *
+ *                2^-(d_8 + d_4).
  *   tensor_scale one FP32 (device): g = amax / (Qmax * 448) for NVFP4 (Qmax 6)
  *                and UFP4 (Qmax 7, levels in integer units), 1.0 for
- *                FP4Q_MXFP4, FP4Q_MXFP4_B16 and FP4Q_MXFP4_OAS.
+ *                FP4Q_MXFP4, FP4Q_MXFP4_B16, FP4Q_MXFP4_OAS and FP4Q_HIF4.
  *                FP4Q_NVFP4_2L: rows x cols/128 FP32 values (row-major), the
  *                outer-block scales g_o; element (r, c) uses g_o(r, c / 128).
  *                FP4Q_MXFP4_MBS: rows x cols/128 FP32 macro scales S, used the
@@ -147,7 +165,8 @@ int fp4q_workspace_init(void* workspace, void* stream);
 
 /* Bytes of the scale array of one copy with `rows` rows of `cols` elements in
  * blocks of `block`, for the given layout (FP4Q_SCALES_MMA counts one scale
- * per 16 elements whatever the block). */
+ * per 16 elements whatever the block). Block 64 (FP4Q_HIF4): 4 bytes per
+ * block in the linear layout, 0 for FP4Q_SCALES_MMA (not supported). */
 size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout);
 
 /* ---- quantisation ------------------------------------------------------------ */
@@ -159,8 +178,8 @@ size_t fp4q_scales_bytes(int64_t rows, int64_t cols, int block, int scale_layout
  * The amaxes are recorded in `workspace`; a following fp4q_quantize call on
  * the same workspace with FP4Q_AMAX_READY in its `axis` then skips this pass.
  * Splitting the call lets a caller time or schedule the two passes apart.
- * The MXFP4 formats and FP4Q_NVFP4_2L have no tensor scale: the call
- * validates its arguments and launches nothing. Arguments and errors as for fp4q_quantize (no outputs). */
+ * The MXFP4 formats, FP4Q_NVFP4_2L and FP4Q_HIF4 have no tensor scale: the
+ * call validates its arguments and launches nothing. Arguments and errors as for fp4q_quantize (no outputs). */
 int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, int block,
               int rht, uint64_t seed, int axis, void* workspace, size_t ws_bytes, void* stream);
 
@@ -175,7 +194,8 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  * the copy, g = A / (Qmax * 448), per block t = a_b / (Qmax * g) rounded to
  * E4M3 (nearest-even, saturating at 448), r_b = 1 / (s_b * g), y = v * r_b.
  * MXFP4: e_b = floor(log2 a_b) - 2 clamped to [-127, 127], y = v * 2^-e_b
- * (FP4Q_MXFP4_OAS: e_b = ceil(log2(a_b / 7)); FP4Q_MXFP4_MBS: see the enum).
+ * (FP4Q_MXFP4_OAS: e_b = ceil(log2(a_b / 7)); FP4Q_MXFP4_MBS, FP4Q_HIF4: see
+ * the enum).
  * y is rounded onto the grid: FP4Q_RTNE nearest level ties to the even code,
  * values beyond the top level saturate; FP4Q_SR rounds |y| up from its lower
  * neighbouring level iff u < f, f the fractional position between the two
@@ -187,9 +207,13 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  * Arguments
  *   src          device, rows x cols elements of `dtype` (FP4Q_BF16 or
  *                FP4Q_F32), row-major, 16-byte aligned.
- *   fmt, block   FP4Q_MXFP4 with block 32, every other format with block 16
- *                (else FP4Q_ENOTSUP). FP4Q_NVFP4_2L and FP4Q_MXFP4_MBS: row-wise
- *                copy only (FP4Q_COLWISE -> FP4Q_ENOTSUP), cols % 128 == 0.
+ *   fmt, block   FP4Q_MXFP4 with block 32, FP4Q_HIF4 with block 64, every
+ *                other format with block 16 (else FP4Q_ENOTSUP).
+ *                FP4Q_NVFP4_2L and FP4Q_MXFP4_MBS: cols % 128 == 0 for the
+ *                row-wise copy, rows % 128 == 0 for the column-wise copy.
+ *                FP4Q_HIF4: row-wise copy only (FP4Q_COLWISE -> FP4Q_ENOTSUP),
+ *                linear scales only (FP4Q_SCALES_MMA -> FP4Q_ENOTSUP), scale
+ *                words 4-byte aligned.
  *   rht          0 or 1. rounding: FP4Q_RTNE or FP4Q_SR. seed: RHT signs and SR.
  *   axis         FP4Q_ROWWISE: blocks along rows, copy row_out (rows x cols).
  *                FP4Q_COLWISE: blocks along columns, emitted transposed into
@@ -258,7 +282,8 @@ int fp4q_status_noalloc(void* stream);
  * device buffer `dst` (16-byte aligned). q is a host pointer to a descriptor of
  * device buffers laid out as fp4q_quantize wrote them for a copy of rows x
  * cols. FP4Q_NVFP4_2L: g is the outer-block scale of the element, cols %
- * 128 == 0; FP4Q_MXFP4_MBS likewise with the macro scale. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
+ * 128 == 0; FP4Q_MXFP4_MBS likewise with the macro scale. FP4Q_HIF4:
+ * v_hat = level * (S * 2^-(d_8 + d_4)), exact in FP32. Errors: FP4Q_EINVAL, FP4Q_ENOTSUP, FP4Q_ECUDA. */
 int fp4q_dequantize(const fp4q_qtensor* q, int64_t rows, int64_t cols, int fmt, int block,
                     int inverse_rht, uint64_t seed, void* dst, int dst_dtype, void* stream);
 
@@ -313,7 +338,8 @@ double fp4q_effective_bucket_ratio(const unsigned long long* counts);
  *              g_A(m, c) g_B(n, c) into FP32 accumulators (tensor_scale:
  *              the column-major per-128 scales, 16-byte aligned).
  *              FP4Q_UFP4 (no tensor-core format holds its levels): runs as
- *              fp4q_gemm_dequant, with that call's shape rules.
+ *              fp4q_gemm_dequant, with that call's shape rules; so does
+ *              FP4Q_HIF4 ([HIF] §2: no tensor-core format takes its scales).
  *   Y          device, M x N row-major, `out_dtype` FP4Q_BF16 (nearest-even)
  *              or FP4Q_F32, 16-byte aligned.
  *   workspace  as for fp4q_quantize (the status word records a bounded wait
@@ -327,19 +353,22 @@ int fp4q_gemm(const fp4q_qtensor* A, const fp4q_qtensor* B, int64_t M, int64_t N
 
 /* Y = dequant(A) * dequant(B)^T on the tensor cores for block-scaled formats
  * whose values the block-scaled MMA cannot take: UFP4 ([UFP4] Metodologia §2
- * and Resultados: the uniform grid with the RHT on every training GEMM); NVFP4
+ * and Resultados: the uniform grid with the RHT on every training GEMM) and
+ * HiF4 ([HIF] §2; values level * S * 2^-(d_8 + d_4), exact in BF16); NVFP4
  * and the E8M0 formats (FP4Q_MXFP4, FP4Q_MXFP4_B16, FP4Q_MXFP4_OAS) are
  * accepted too, to compare with fp4q_gemm. The kernel's converter warps turn
  * each operand's codes and block scales into the 16-bit block values
  * level * s_b in shared memory -- FP16 for UFP4 and NVFP4 (E4M3 scales; exact:
  * at most 7 significant bits in [2^-10, 3136]), BF16 for the E8M0 formats
- * (exact) -- and tcgen05.mma.kind::f16 accumulates their products, exact in
+ * and HiF4 (exact) -- and tcgen05.mma.kind::f16 accumulates their products, exact in
  * FP32, in FP32; the result is multiplied by g_A * g_B (their FP32 product;
  * 1 for the E8M0 formats). No dequantised operand is written to memory. When
  * both operands were quantised with the RHT along K under the same seed, the
  * transforms cancel.
  *   A, B       host pointers to descriptors of row-wise copies (M x K, N x K)
- *              of format `fmt`, linear or tiled scales (2-byte aligned).
+ *              of format `fmt`, linear or tiled scales (2-byte aligned; HiF4:
+ *              linear scale words, 4-byte aligned, else FP4Q_ENOTSUP /
+ *              FP4Q_EINVAL).
  *   Y          device, M x N row-major, FP4Q_BF16 (nearest-even) or FP4Q_F32,
  *              16-byte aligned.
  *   workspace  as for fp4q_gemm (FP4Q_ETIMEOUT via fp4q_status).

@@ -997,6 +997,9 @@ def gemm(a_copy: dict, b_copy: dict, rows=None, cols=None) -> np.ndarray:
     def deq(cp, sel):
         if cp["fmt"] in ("nvfp4_2l", "mxfp4_mbs"):
             return dequantize_outer_f64(cp, sel)
+        if cp["fmt"] == "hif4":
+            s_ = slice(None) if sel is None else sel
+            return dequantize_hif4_f64(cp["codes"][s_], cp["scales"][s_])
         return dequantize_f64(cp["codes"], cp["scales"], cp["tensor_scale"], cp["fmt"], sel)
     return deq(a_copy, rows) @ deq(b_copy, cols).T
 

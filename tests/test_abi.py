@@ -51,14 +51,16 @@ def test_python_tables_match_the_header():
     import fp4_block_scaled_05_b300 as fq
     fmts = _header_enum("FP4Q_")
     names = {"nvfp4": "FP4Q_NVFP4", "mxfp4": "FP4Q_MXFP4", "ufp4": "FP4Q_UFP4", "nvfp4_2l": "FP4Q_NVFP4_2L",
-             "mxfp4_b16": "FP4Q_MXFP4_B16", "mxfp4_oas": "FP4Q_MXFP4_OAS", "mxfp4_mbs": "FP4Q_MXFP4_MBS"}
+             "mxfp4_b16": "FP4Q_MXFP4_B16", "mxfp4_oas": "FP4Q_MXFP4_OAS", "mxfp4_mbs": "FP4Q_MXFP4_MBS",
+             "hif4": "FP4Q_HIF4"}
     assert set(fq.FORMATS) == set(names)
     for py, c in names.items():
         assert fq.FORMATS[py] == fmts[c], py
     assert fq.ROUNDING == {"rtne": fmts["FP4Q_RTNE"], "sr": fmts["FP4Q_SR"]}
     assert fq.LAYOUTS == {"linear": fmts["FP4Q_SCALES_LINEAR"], "mma": fmts["FP4Q_SCALES_MMA"]}
     assert fq.AXES["row"] == fmts["FP4Q_ROWWISE"] and fq.AXES["col"] == fmts["FP4Q_COLWISE"]
-    assert fq.BLOCKS["mxfp4"] == 32 and all(b == 16 for f, b in fq.BLOCKS.items() if f != "mxfp4")
+    assert fq.BLOCKS["mxfp4"] == 32 and fq.BLOCKS["hif4"] == 64
+    assert all(b == 16 for f, b in fq.BLOCKS.items() if f not in ("mxfp4", "hif4"))
 
 
 def test_host_validation_without_gpu(so):
@@ -75,13 +77,16 @@ def test_host_validation_without_gpu(so):
     # the tiled layout holds one scale per 16 elements: a 32-element block's twice
     assert so.fp4q_scales_bytes(100, 96, 32, 0) == 300
     assert so.fp4q_scales_bytes(100, 96, 32, 1) == 128 * 8
+    # HiF4: one 32-bit word per 64-element block, linear layout only
+    assert so.fp4q_scales_bytes(100, 128, 64, 0) == 100 * 2 * 4
+    assert so.fp4q_scales_bytes(100, 128, 64, 1) == 0
     q = so.fp4q_quantize
     q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int,
                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
     # bad format / block / dtype / axis / workspace size -> EINVAL or ENOTSUP, no launch
-    assert q(fake, 0, 16, 16, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 16, 16, 8, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 16, 16, 0, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
     assert q(fake, 0, 16, 16, 1, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
     assert q(fake, 5, 16, 16, 0, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
@@ -97,12 +102,24 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, 32, 144, 3, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 256, 3, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
     # the MXFP4 variants on 16-element blocks (4, 5) and MBS (6): block 16 only;
-    # MBS with whole 128-element macro blocks along the block axis; 7 is no format
+    # MBS with whole 128-element macro blocks along the block axis; 8 is no format
     for fmt in (4, 5, 6):
         assert q(fake, 0, 32, 256, fmt, 32, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
     assert q(fake, 0, 32, 256, 6, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 144, 6, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
-    assert q(fake, 0, 32, 256, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 32, 256, 8, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    # HiF4 (7): block 64, whole blocks per row, row-wise copy only, linear
+    # 4-byte-aligned scale words
+    from fp4_block_scaled_05_b300 import fp4q_qtensor
+    assert q(fake, 0, 32, 256, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 32, 96, 7, 64, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
+    assert q(fake, 0, 64, 256, 7, 64, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 64, 256, 7, 64, 0, 0, 0, 3, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 32, 256, 7, 64, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1   # row_out NULL
+    mma = fp4q_qtensor(1 << 20, 1 << 20, 1 << 20, 1)
+    assert q(fake, 0, 32, 256, 7, 64, 0, 0, 0, 1, ctypes.addressof(mma), None, fake, ws_size, None) == 2
+    odd = fp4q_qtensor(1 << 20, (1 << 20) + 2, 1 << 20, 0)
+    assert q(fake, 0, 32, 256, 7, 64, 0, 0, 0, 1, ctypes.addressof(odd), None, fake, ws_size, None) == 1
 
 
 def test_amax_validation_without_gpu(so):
@@ -113,7 +130,7 @@ def test_amax_validation_without_gpu(so):
                   ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int, ctypes.c_void_p,
                   ctypes.c_size_t, ctypes.c_void_p]
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
-    assert a(fake, 0, 16, 16, 7, 16, 0, 0, 1, fake, ws_size, None) == 1      # format
+    assert a(fake, 0, 16, 16, 8, 16, 0, 0, 1, fake, ws_size, None) == 1      # format
     assert a(fake, 0, 16, 16, 0, 32, 0, 0, 1, fake, ws_size, None) == 2      # block
     assert a(fake, 0, 16, 24, 0, 16, 0, 0, 1, fake, ws_size, None) == 1      # cols % 16
     assert a(fake, 0, 24, 16, 0, 16, 0, 0, 2, fake, ws_size, None) == 1      # rows % 16
@@ -122,8 +139,10 @@ def test_amax_validation_without_gpu(so):
     assert a(fake, 0, 16, 16, 0, 16, 0, 0, 4, fake, ws_size, None) == 1      # no copy requested
     assert a(fake, 0, 16, 16, 0, 16, 0, 0, 1, fake, 8, None) == 1            # workspace size
     assert a(None, 0, 16, 16, 0, 16, 0, 0, 1, fake, ws_size, None) == 1      # null source
-    # MXFP4 has no tensor amax: valid arguments launch nothing and succeed
+    # MXFP4 and HiF4 have no tensor amax: valid arguments launch nothing and succeed
     assert a(fake, 0, 32, 32, 1, 32, 0, 0, 3, fake, ws_size, None) == 0
+    assert a(fake, 0, 32, 64, 7, 64, 0, 0, 1, fake, ws_size, None) == 0
+    assert a(fake, 0, 64, 64, 7, 64, 0, 0, 2, fake, ws_size, None) == 2      # HiF4 row-wise only
     q = so.fp4q_quantize
     q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int,
@@ -147,7 +166,8 @@ def test_gemm_selftest_validation_without_gpu(so):
     # the per-128-scaled formats have their own kernel, without the bounded-wait self-test
     assert f(fake, fake, 128, 128, 256, 3, fake, 0, fake, ws, 10**7, None) == 2
     assert f(fake, fake, 128, 128, 256, 6, fake, 0, fake, ws, 10**7, None) == 2
-    assert f(fake, fake, 128, 128, 256, 7, fake, 0, fake, ws, 10**7, None) == 1         # no such format
+    assert f(fake, fake, 128, 128, 256, 7, fake, 0, fake, ws, 10**7, None) == 2         # HiF4: dequantising GEMM
+    assert f(fake, fake, 128, 128, 256, 8, fake, 0, fake, ws, 10**7, None) == 1         # no such format
 
 
 def test_gemm_format_validation_without_gpu(so):
@@ -161,16 +181,23 @@ def test_gemm_format_validation_without_gpu(so):
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every call below fails validation first
     ws = so.fp4q_workspace_size()
     assert g(fake, fake, 128, 128, 256, -1, fake, 0, fake, ws, None) == 1
-    assert g(fake, fake, 128, 128, 256, 7, fake, 0, fake, ws, None) == 1
-    for fmt in (0, 1, 2, 3, 4, 5, 6):                                         # null descriptors
+    assert g(fake, fake, 128, 128, 256, 8, fake, 0, fake, ws, None) == 1
+    for fmt in (0, 1, 2, 3, 4, 5, 6, 7):                                         # null descriptors
         assert g(None, None, 128, 128, 256, fmt, fake, 0, fake, ws, None) == 1
     d = so.fp4q_gemm_dequant
     d.argtypes = g.argtypes
     assert d(fake, fake, 128, 128, 256, 3, fake, 0, fake, ws, None) == 2      # two-level NVFP4
     assert d(fake, fake, 128, 128, 256, 6, fake, 0, fake, ws, None) == 2      # MBS
-    assert d(fake, fake, 128, 128, 256, 7, fake, 0, fake, ws, None) == 1
-    for fmt in (0, 1, 2, 4, 5):
+    assert d(fake, fake, 128, 128, 256, 8, fake, 0, fake, ws, None) == 1
+    for fmt in (0, 1, 2, 4, 5, 7):
         assert d(None, None, 128, 128, 256, fmt, fake, 0, fake, ws, None) == 1
+    from fp4_block_scaled_05_b300 import fp4q_qtensor
+    lin = fp4q_qtensor(1 << 20, 1 << 20, 1 << 20, 0)
+    mma = fp4q_qtensor(1 << 20, 1 << 20, 1 << 20, 1)
+    odd = fp4q_qtensor(1 << 20, (1 << 20) + 2, 1 << 20, 0)
+    pa = ctypes.addressof
+    assert d(pa(lin), pa(mma), 128, 128, 256, 7, fake, 0, fake, ws, None) == 2     # tiled HiF4 scales
+    assert d(pa(odd), pa(lin), 128, 128, 256, 7, fake, 0, fake, ws, None) == 1     # words not 4-aligned
 
 
 def test_effective_bucket_ratio_host(so):

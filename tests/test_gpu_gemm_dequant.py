@@ -121,3 +121,52 @@ def test_gemm_dequant_rejections(lib):
     with pytest.raises(lib.FP4QError) as e:          # N % 8
         lib.fp4q_gemm_dequant(qa, qb)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("shape", [(256, 384, 512), (128, 128, 1024), (96, 200, 256), (130, 264, 64)])
+def test_gemm_dequant_hif4_against_oracle(lib, rht, shape):
+    """HiF4 ("Unleashing Low-Bit Inference on Ascend NPUs ...", Resumen técnico
+    §2) on the 16-bit MMA: block values level * S * 2^-(d_8 + d_4) exact in
+    BF16, one scale word per row and 64-element K stage."""
+    M, N, K = shape
+    a = synth.gemm_operand("a", M, K)
+    b = synth.gemm_operand("b", N, K)
+    qa, _ = lib.fp4q_quantize(a.cuda(), fmt="hif4", rht=rht, seed=77)
+    qb, _ = lib.fp4q_quantize(b.cuda(), fmt="hif4", rht=rht, seed=77)
+    y = lib.fp4q_gemm_dequant(qa, qb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    assert lib.fp4q_status() == 0
+    ra = o.quantize(synth.bf16_bits(a), "hif4", rht=rht, seed=77)["row"]
+    rb = o.quantize(synth.bf16_bits(b), "hif4", rht=rht, seed=77)["row"]
+    ref = o.gemm(ra, rb)
+    assert _rel_fro(y, ref) < 1e-5
+    y2 = lib.fp4q_gemm(qa, qb, out_dtype=torch.float32).cpu().numpy().astype(np.float64)
+    assert np.array_equal(y, y2)                       # fp4q_gemm takes HiF4 through the same kernel
+
+
+def test_gemm_dequant_hif4_exact(lib):
+    """HiF4 with scales 2^-1 or 2^0 and random halving bits: every product is
+    k 2^p with k <= 49 and -6 <= p <= 0, every partial sum over K = 512 fits
+    FP32 exactly, so the output equals the FP64 oracle bit for bit. Random
+    codes and words exercise every bit of the scale word."""
+    rng = np.random.default_rng(12)
+    M, N, K = 512, 768, 512
+
+    def copy(rows):
+        codes = rng.integers(0, 16, (rows, K)).astype(np.uint8)
+        e6m2 = np.where(rng.random((rows, K // 64)) < 0.5, 120, 124).astype(np.uint32)     # 2^-1, 2^0
+        bits = rng.integers(0, 1 << 24, (rows, K // 64), dtype=np.int64).astype(np.uint32)
+        words = (e6m2 | (bits << np.uint32(8))).astype(np.uint32)
+        return {"fmt": "hif4", "codes": o.pack_nibbles(codes), "scales": words}
+
+    ca, cb = copy(M), copy(N)
+
+    def dev(c, rows):
+        return lib.QCopy(torch.from_numpy(c["codes"]).cuda(), torch.from_numpy(c["scales"].view(np.int32)).cuda(),
+                         torch.ones(1, dtype=torch.float32, device="cuda"), "hif4", rows, K, "linear")
+
+    y = lib.fp4q_gemm_dequant(dev(ca, M), dev(cb, N), out_dtype=torch.float32).cpu().numpy()
+    ref = o.gemm(ca, cb)
+    assert lib.fp4q_status() == 0
+    bad = np.argwhere(y != ref)
+    assert bad.size == 0, f"{len(bad)} of {y.size} differ; first {bad[:6].tolist()}"
