@@ -223,12 +223,28 @@ def load_peaks() -> dict:
                 "source": "fallback"}
 
 
-def source_digest() -> str:
-    """Digest of the kernel sources: ncu counters apply only to the build they came from."""
+#: the source file that defines each kernel; its digest also covers the shared headers
+KERNEL_SOURCES = {
+    "amax_rows_kernel": "fp4q_rows.cu", "quant_rows_kernel": "fp4q_rows.cu", "dequant_rows_kernel": "fp4q_rows.cu",
+    "amax_tiles_kernel": "fp4q_rows.cu", "quant_tiles_kernel": "fp4q_rows.cu",
+    "quant_cols_outer_kernel": "fp4q_rows.cu", "gemm_nvf4_kernel": "fp4q_gemm.cu",
+    "gemm_nvf4_pair_kernel": "fp4q_gemm.cu", "gemm_dq_kernel": "fp4q_gemm_dq.cu",
+    "gemm_outer_kernel": "fp4q_gemm_outer.cu", "code_hist_kernel": "fp4q_hist.cu",
+}
+
+
+def source_digest(kernel: str) -> str:
+    """Digest of the source a kernel is built from (its .cu file and the shared
+    headers): ncu counters apply only to the build they came from."""
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "fp4_block_scaled_05_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
+    names = sorted(n for n in os.listdir(csrc) if n.endswith((".cuh", ".h")))
+    names.append(KERNEL_SOURCES.get(kernel, ""))
+    for name in names:
+        path = os.path.join(csrc, name)
+        if not os.path.isfile(path):
+            return ""
+        with open(path, "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:12]
 
@@ -236,17 +252,15 @@ def source_digest() -> str:
 def ncu_traffic(kernel: str, units: float) -> float | None:
     """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
     summary, scaled by the elements (or FLOP) a launch processes here; None if
-    the counters were taken on other kernel sources."""
+    the counters were taken on other sources of that kernel."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    if t.get("source_digest") != source_digest():
-        return None
     k = t.get("kernels", {}).get(kernel)
-    if not k:
+    if not k or k.get("source_digest") != source_digest(kernel):
         return None
     return float(k["dram_bytes"]) * units / float(k["units"])
 
