@@ -146,16 +146,21 @@ __device__ __forceinline__ uint32_t hmul2_bf16(uint32_t a, uint32_t b) {
 // HiF4: the eight 4-element micro-blocks of half h of a 64-element block as
 // BF16 scale pairs, S * 2^-(d_8 + d_4) (S = 0 stays 0). S is E6M2 (bias 31):
 // exponent field E >= 1 -> BF16 exponent E + 96 and mantissa m << 5; E = 0 ->
-// m * 2^-32, exact in FP32 and then in BF16.
+// m * 2^-32, exact in FP32 and then in BF16. The three possible pairs (S,
+// S / 2, S / 4: one BF16 exponent step each) are formed once; each micro-block
+// selects one by its two bits.
 __device__ __forceinline__ void hif4_scale_pairs(uint32_t wd, int h, uint32_t (&sp)[8]) {
   const uint32_t c = wd & 0xFFu, E = c >> 2, m = c & 3u;
   const uint32_t sb = E ? (((E + 96u) << 7) | (m << 5))
                         : (__float_as_uint(__fmul_rn((float)m, 2.3283064365386963e-10f)) >> 16);
+  const uint32_t t0 = sb * 0x00010001u;
+  const uint32_t t1 = sb ? t0 - 0x00800080u : 0u;
+  const uint32_t t2 = sb ? t0 - 0x01000100u : 0u;
+  const uint32_t b8 = wd >> (8 + 4 * h), b4 = wd >> (16 + 8 * h);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const uint32_t sh = ((wd >> (8 + 4 * h + (i >> 1))) & 1u) + ((wd >> (16 + 8 * h + i)) & 1u);
-    const uint32_t v = sb ? sb - (sh << 7) : 0u;
-    sp[i] = v | (v << 16);
+    const bool d8 = (b8 >> (i >> 1)) & 1u, d4 = (b4 >> i) & 1u;
+    sp[i] = d4 ? (d8 ? t2 : t1) : (d8 ? t1 : t0);
   }
 }
 
