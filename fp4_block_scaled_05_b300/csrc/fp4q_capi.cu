@@ -158,7 +158,6 @@ int check_source(const void* src, int dtype, int64_t rows, int64_t cols, int fmt
     if ((axis & FP4Q_ROWWISE) && cols % 128) return FP4Q_EINVAL;   // whole outer blocks per row
     if ((axis & FP4Q_COLWISE) && rows % 128) return FP4Q_EINVAL;   // ... and per column
   }
-  if (fmt == FP4Q_HIF4 && (axis & FP4Q_COLWISE)) return FP4Q_ENOTSUP;   // row-wise only
   return FP4Q_OK;
 }
 
@@ -226,7 +225,8 @@ int fp4q_quantize(const void* src, int dtype, int64_t rows, int64_t cols, int fm
   const bool empty = rows == 0 || cols == 0;
   if ((axis & FP4Q_ROWWISE) && (rc = check_qtensor(row_out, empty))) return rc;
   if ((axis & FP4Q_COLWISE) && (rc = check_qtensor(col_out, empty))) return rc;
-  if (fmt == FP4Q_HIF4 && (rc = check_hif4_qtensor(row_out, empty))) return rc;
+  if (fmt == FP4Q_HIF4 && (axis & FP4Q_ROWWISE) && (rc = check_hif4_qtensor(row_out, empty))) return rc;
+  if (fmt == FP4Q_HIF4 && (axis & FP4Q_COLWISE) && (rc = check_hif4_qtensor(col_out, empty))) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   // padding bytes of the tiled scale layout are defined as 0
   if (!empty && (axis & FP4Q_ROWWISE) && row_out->scale_layout == FP4Q_SCALES_MMA && needs_padding(rows, cols / 16)) {

@@ -20,8 +20,8 @@
 // The E8M0 formats (MXFP4 on 32- or 16-element blocks, its overflow-aware
 // variant, MBS with its 128-element macro scale), two-level NVFP4 (a scale
 // per 128-element outer block) and HiF4 (a scale per 64-element block) have no
-// tensor scale, so they skip the amax pass. HiF4 ("Unleashing Low-Bit
-// Inference on Ascend NPUs ...", Resumen tecnico §2) is row-wise only.
+// tensor scale, so they skip the amax pass (HiF4: "Unleashing Low-Bit
+// Inference on Ascend NPUs ...", Resumen tecnico §2).
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -89,9 +89,10 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
     const cudaError_t e = run_amax(a, s);
     if (e != cudaSuccess) return e;
   }
-  if ((a.fmt == 3 || a.fmt == 6) && (a.axis & 2)) {
-    // scales per 128 elements: the column-wise copy on 128-row tiles (outer
-    // blocks down the columns), the row-wise copy, if wanted, from the row kernel
+  if ((a.fmt == 3 || a.fmt == 6 || a.fmt == 7) && (a.axis & 2)) {
+    // scales per 128 (or, HiF4, 64) elements: the column-wise copy on 128-row
+    // tiles (blocks down the columns), the row-wise copy, if wanted, from the
+    // row kernel
     int row_np = 0;
     if (a.axis & 1) {
       const cudaError_t e = run_quant_rows(a, s, &row_np);

@@ -545,6 +545,140 @@ __device__ __forceinline__ float e6m2_rne_sat(float t, uint32_t& code) {
   return __fmul_rn(k, 2.3283064365386963e-10f);              // k * 2^-32
 }
 
+// HiF4's codes and statistics for one half block (see hif4_half), with the
+// halving bits decided from the micro-block maxima a4. The signal and error
+// sums are FP32 in units of a power of two times S^2 (add_outer_stats):
+//   MODE 0  y and y - q as they are, units S^2;
+//   MODE 1  a scale saturated so far below the values that sums of y^2 could
+//           overflow FP32: y 2^-64 and (q - y) 2^-64, units (S 2^64)^2;
+//   MODE 2  a scale that rounded to 0: every value becomes 0 and its error is
+//           v itself; v 2^64 for both sums, units 2^-128.
+// Every scaling is by a power of two, exact but for what underflows next to
+// the block's largest terms.
+template <bool SR, int MODE>
+__device__ __forceinline__ void hif4_codes(const f2 (&Q)[16], const float (&a4)[8], float S, float r,
+                                           uint64_t e0, const PhiloxKey& pk, uint32_t axis, uint32_t (&cw)[4],
+                                           uint32_t& mine, Sums& acc) {
+  const f2 R = f2_make(r, r);
+  const float k = MODE == 1 ? 5.421010862427522e-20f : 1.8446744073709552e19f;     // 2^-64, 2^64
+  const f2 K = f2_make(k, k);
+  float bsum = 0.f, ss = 0.f, es = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t d8 = (__fmul_rn(fmaxf(a4[2 * j], a4[2 * j + 1]), r) <= 3.5f) ? 1u : 0u;
+    mine |= d8 << j;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 2 * j + h;
+      const uint32_t d4 = (__fmul_rn(a4[i], r) <= (d8 ? 1.75f : 3.5f)) ? 1u : 0u;
+      mine |= d4 << (4 + i);
+      const uint32_t sh = d8 + d4;
+      const f2 M = f2_make(__uint_as_float((127u + sh) << 23), __uint_as_float((127u + sh) << 23));
+      uint4 rw = make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (SR) {   // the micro-block's four uniforms: one Philox call
+        const uint64_t q = (e0 >> 2) + (uint64_t)i;
+        rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), axis, 0u), pk);
+      }
+      f2 B2 = f2_make(0.f, 0.f), E2 = B2, S2 = B2;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const f2 Y = f2_mul(f2_mul(Q[2 * i + t], R), M);
+        f2 D;
+        uint32_t byte;
+        if constexpr (SR) {
+          byte = (t == 0) ? sr_pair<2>(Y, rw.x, rw.y, D) : sr_pair<2>(Y, rw.z, rw.w, D);
+        } else {
+          byte = ufp4_pair(Y, D);
+        }
+        cw[i >> 1] |= byte << (8 * ((2 * i + t) & 3));
+        B2 = f2_add(B2, D);
+        if constexpr (MODE == 0) {
+          E2 = f2_fma(D, D, E2);
+          S2 = f2_fma(Y, Y, S2);
+        } else if constexpr (MODE == 1) {
+          const f2 Dk = f2_mul(D, K), Yk = f2_mul(Y, K);
+          E2 = f2_fma(Dk, Dk, E2);
+          S2 = f2_fma(Yk, Yk, S2);
+        } else {
+          const f2 Vk = f2_mul(Q[2 * i + t], K);
+          S2 = f2_fma(Vk, Vk, S2);
+        }
+      }
+      float x0, x1;
+      f2_split(B2, x0, x1);
+      bsum = __fadd_rn(bsum, __fadd_rn(x0, x1));
+      const float wt = MODE == 2 ? 1.f : __uint_as_float((127u - 2u * sh) << 23);   // 4^-shift
+      f2_split(S2, x0, x1);
+      ss = __fmaf_rn(__fadd_rn(x0, x1), wt, ss);
+      if constexpr (MODE != 2) {
+        f2_split(E2, x0, x1);
+        es = __fmaf_rn(__fadd_rn(x0, x1), wt, es);
+      }
+    }
+  }
+  acc.bias.add(bsum);
+  if constexpr (MODE == 0) {
+    add_outer_stats(acc, S, ss, es);
+  } else if constexpr (MODE == 1) {
+    add_outer_stats(acc, __fmul_rn(S, 1.8446744073709552e19f), ss, es);
+  } else {
+    add_outer_stats(acc, 5.421010862427522e-20f, ss, ss);
+  }
+}
+
+// HiF4 ("Unleashing Low-Bit Inference on Ascend NPUs: A Comprehensive
+// Evaluation of HiFloat Formats", Resumen tecnico §2 Metodologia): quantise the
+// calling thread's half of a 64-element block; the other half is held by the
+// lane whose index differs in bit 0. The two share the block's amax a, which
+// sets the E6M2 scale S = RN_E6M2(a / 7). Each thread then decides, for its
+// four 8-element sub-blocks and eight 4-element micro-blocks, whether the
+// group's step can be halved without a value clamping at 7 (w = RN(a_group /
+// S) <= 3.5, and <= 1.75 for a micro-block whose sub-block already halved),
+// and rounds y = RN(v / S) 2^shift onto the levels 0..7.
+//   Q      the half's 32 values in order (16 pairs); read only when `valid`
+//   e0     index of the half's first element in the copy (SR counters)
+// Writes the half's four code words; returns the block's scale word (E6M2
+// code, the eight sub-block bits, the sixteen micro-block bits) to the lane
+// with bit 0 clear. Every lane of the warp must call it (two shuffles).
+template <bool SR>
+__device__ __forceinline__ uint32_t hif4_half(const f2 (&Q)[16], bool valid, uint64_t e0, const PhiloxKey& pk,
+                                              uint32_t axis, uint32_t (&cw)[4], Sums& acc, uint32_t& nonfinite) {
+  float a4[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float a = 0.f, b = 0.f, c = 0.f, d = 0.f;
+    if (valid) {
+      f2_split(Q[2 * i], a, b);
+      f2_split(Q[2 * i + 1], c, d);
+    }
+    a4[i] = max3_abs_nan(max3_abs_nan(0.f, a, b), c, d);
+  }
+  float m = max_abs_nan(max_abs_nan(max_abs_nan(a4[0], a4[1]), max_abs_nan(a4[2], a4[3])),
+                        max_abs_nan(max_abs_nan(a4[4], a4[5]), max_abs_nan(a4[6], a4[7])));
+  m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  uint32_t mine = 0u, scode = 0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) cw[j] = 0u;
+  if (valid) {
+    nonfinite |= (__float_as_uint(m) >= 0x7F800000u) ? 1u : 0u;
+    const float S = e6m2_rne_sat(__fdiv_rn(m, 7.f), scode);
+    const float r = (S == 0.f) ? 0.f : __frcp_rn(S);
+    // y <= 4 RN(a r): past 1e17 the FP32 sums of y^2 could overflow (NaN lands there too)
+    if (S == 0.f) {
+      hif4_codes<SR, 2>(Q, a4, S, r, e0, pk, axis, cw, mine, acc);
+    } else if (__fmul_rn(m, r) <= 1.0e17f) {
+      hif4_codes<SR, 0>(Q, a4, S, r, e0, pk, axis, cw, mine, acc);
+    } else {
+      hif4_codes<SR, 1>(Q, a4, S, r, e0, pk, axis, cw, mine, acc);
+    }
+  }
+  // the block's word: E6M2 code, the eight sub-block bits, then the sixteen
+  // micro-block bits (the lower half's first)
+  const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+  return scode | ((mine & 0xFu) << 8) | ((other & 0xFu) << 12) | (((mine >> 4) & 0xFFu) << 16) |
+         (((other >> 4) & 0xFFu) << 24);
+}
+
 // Quantise one block of NP pairs (NP = 8: a 16-block, NP = 16: an MXFP4
 // 32-block) whose first element has index e0 in the copy. Writes NP/4 code
 // words and returns the scale code; adds the block's sums to bsum/ssum/esum
@@ -966,117 +1100,18 @@ __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const
       if ((threadIdx.x & 3u) == 0u) o.tensor_scale[outer_index(o, f, e)] = S;
     }
   } else if constexpr (FMT == 7) {
-    // HiF4 ("Unleashing Low-Bit Inference on Ascend NPUs: A Comprehensive
-    // Evaluation of HiFloat Formats", Resumen tecnico §2 Metodologia): the two
-    // threads of a 64-element block (lanes 2k, 2k+1; rows hold whole blocks)
-    // share its amax a, which sets the E6M2 scale S = RN_E6M2(a / 7). Each
-    // thread then decides, for its four 8-element sub-blocks and eight
-    // 4-element micro-blocks, whether the group's step can be halved without
-    // a value clamping at 7 (w = RN(a_group / S) <= 3.5, and <= 1.75 for a
-    // micro-block whose sub-block already halved), and rounds y = RN(v / S)
-    // 2^shift onto the levels 0..7. Every lane takes part in the shuffles.
+    // HiF4: the two threads of a 64-element block are lanes 2k, 2k+1 (rows
+    // hold whole blocks); every lane takes part in the shuffles
     f2 Q[16];
-    float a4[8];
     if (nb16 == 2) {
       load_block16<F32, RHT>(LinearSeg{p}, 0, sgn, Q);
       load_block16<F32, RHT>(LinearSeg{p}, F32 ? 4 : 2, sgn, Q + 8);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        float a, b, c, d;
-        f2_split(Q[2 * i], a, b);
-        f2_split(Q[2 * i + 1], c, d);
-        a4[i] = max3_abs_nan(max3_abs_nan(0.f, a, b), c, d);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) a4[i] = 0.f;
     }
-    float m = max_abs_nan(max_abs_nan(max_abs_nan(a4[0], a4[1]), max_abs_nan(a4[2], a4[3])),
-                          max_abs_nan(max_abs_nan(a4[4], a4[5]), max_abs_nan(a4[6], a4[7])));
-    m = max_abs_nan(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    uint32_t mine = 0u, scode = 0u;
+    uint32_t cw[4];
+    const uint32_t w = hif4_half<SR>(Q, nb16 == 2, (uint64_t)e, pk, 0u, cw, acc, nonfinite);
     if (nb16 == 2) {
-      nonfinite |= (__float_as_uint(m) >= 0x7F800000u) ? 1u : 0u;
-      const float S = e6m2_rne_sat(__fdiv_rn(m, 7.f), scode);
-      const float r = (S == 0.f) ? 0.f : __frcp_rn(S);
-      const f2 R = f2_make(r, r);
-      uint32_t cw[4] = {0u, 0u, 0u, 0u};
-      float bsum = 0.f, ss = 0.f, es = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t d8 = (__fmul_rn(fmaxf(a4[2 * j], a4[2 * j + 1]), r) <= 3.5f) ? 1u : 0u;
-        mine |= d8 << j;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int i = 2 * j + h;
-          const uint32_t d4 = (__fmul_rn(a4[i], r) <= (d8 ? 1.75f : 3.5f)) ? 1u : 0u;
-          mine |= d4 << (4 + i);
-          const uint32_t sh = d8 + d4;
-          const f2 M = f2_make(__uint_as_float((127u + sh) << 23), __uint_as_float((127u + sh) << 23));
-          const float wt = __uint_as_float((127u - 2u * sh) << 23);     // 4^-shift: units of S^2
-          uint4 rw = make_uint4(0u, 0u, 0u, 0u);
-          if constexpr (SR) {   // the micro-block's four uniforms: one Philox call
-            const uint64_t q = ((uint64_t)e >> 2) + (uint64_t)i;
-            rw = philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), pk);
-          }
-          f2 B2 = f2_make(0.f, 0.f), E2 = B2, S2 = B2;
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const f2 Y = f2_mul(f2_mul(Q[2 * i + t], R), M);
-            f2 D;
-            uint32_t byte;
-            if constexpr (SR) {
-              byte = (t == 0) ? sr_pair<2>(Y, rw.x, rw.y, D) : sr_pair<2>(Y, rw.z, rw.w, D);
-            } else {
-              byte = ufp4_pair(Y, D);
-            }
-            cw[i >> 1] |= byte << (8 * ((2 * i + t) & 3));
-            B2 = f2_add(B2, D);
-            E2 = f2_fma(D, D, E2);
-            S2 = f2_fma(Y, Y, S2);
-          }
-          float x0, x1;
-          f2_split(B2, x0, x1);
-          bsum = __fadd_rn(bsum, __fadd_rn(x0, x1));
-          f2_split(S2, x0, x1);
-          ss = __fmaf_rn(__fadd_rn(x0, x1), wt, ss);
-          f2_split(E2, x0, x1);
-          es = __fmaf_rn(__fadd_rn(x0, x1), wt, es);
-        }
-      }
       *reinterpret_cast<uint4*>(o.codes + e / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      acc.bias.add(bsum);
-      if (S != 0.f && fabsf(ss) <= FLT_MAX && fabsf(es) <= FLT_MAX) {
-        add_outer_stats(acc, S, ss, es);
-      } else if (m > 0.f) {
-        // The scale rounded to 0 (every value became 0: its error is v), or it
-        // saturated so far below the values that their squares overflow FP32:
-        // the sums in FP64 from v and the codes, value = level * S * 2^-shift.
-        double sg = 0.0, er = 0.0;
-#pragma unroll 1
-        for (int j = 0; j < 16; ++j) {
-          float a, b;
-          f2_split(Q[j], a, b);
-          const int i = j >> 1;
-          const uint32_t sh = ((mine >> (i >> 1)) & 1u) + ((mine >> (4 + i)) & 1u);
-          const double st = (double)S * (double)__uint_as_float((127u - sh) << 23);
-          const uint32_t byte = (cw[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-          const double q0 = (double)(byte & 7u) * ((byte & 8u) ? -st : st);
-          const double q1 = (double)((byte >> 4) & 7u) * ((byte & 0x80u) ? -st : st);
-          sg += (double)a * (double)a + (double)b * (double)b;
-          er += ((double)a - q0) * ((double)a - q0) + ((double)b - q1) * ((double)b - q1);
-        }
-        acc.sig64 += sg;
-        acc.err64 += er;
-      }
-    }
-    // the even lane writes the block's word: E6M2 code, then the eight
-    // sub-block bits, then the sixteen micro-block bits (its own half first)
-    const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
-    if (nb16 == 2 && (threadIdx.x & 1u) == 0u) {
-      const uint32_t w = scode | ((mine & 0xFu) << 8) | ((other & 0xFu) << 12) | (((mine >> 4) & 0xFFu) << 16) |
-                         (((other >> 4) & 0xFFu) << 24);
-      reinterpret_cast<uint32_t*>(o.scales)[(uint64_t)e >> 6] = w;
+      if ((threadIdx.x & 1u) == 0u) reinterpret_cast<uint32_t*>(o.scales)[(uint64_t)e >> 6] = w;
     }
   } else if constexpr (FMT == 3) {
     // Two-level NVFP4 (TetraJet-v2, Riepilogo Tecnico §2A): the four threads of
@@ -1841,7 +1876,7 @@ template <int FMT, bool F32, bool RHT, bool SR>
 __global__ void __launch_bounds__(RT, F32 ? 1 : 2) quant_cols_outer_kernel(
     const __grid_constant__ CUtensorMap tmap, TileGeom g, uint64_t seed, PhiloxKey pk, CopyOut ocol,
     Workspace* ws, uint64_t timeout_ns, int row_nparts) {
-  static_assert(kOuterScaled<FMT>, "formats with a scale per 128 elements");
+  static_assert(kOuterScaled<FMT> || FMT == 7, "formats with a scale per 128 elements, or HiF4");
   using TRg = TileRing<F32, TOR>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[TRg::kStages], empty[TRg::kStages];
@@ -1898,6 +1933,23 @@ __global__ void __launch_bounds__(RT, F32 ? 1 : 2) quant_cols_outer_kernel(
           }
         }
       }
+      if constexpr (FMT == 7) {
+        // HiF4: a 64-row block of a column is held by the threads qr = 2k,
+        // 2k + 1 (lanes differing in bit 0); rows are whole 64-row blocks, so
+        // the block is in the tensor for both or for neither
+        const bool in = valid && r0 + 32 * qr < g.rows;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {           // column 2p + k: one row of the copy
+          const f2 (&Q)[16] = *reinterpret_cast<const f2(*)[16]>(k ? &Qb[0][0] : &Qa[0][0]);
+          const int64_t crow = c0 + 2 * pair + k, ccol = r0 + 32 * qr;
+          uint32_t cw[4];
+          const uint32_t w = hif4_half<SR>(Q, in, (uint64_t)(crow * g.rows + ccol), pk, 1u, cw, acc, nonfinite);
+          if (in) {
+            *reinterpret_cast<uint4*>(ocol.codes + crow * ocol.ld + ccol / 2) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            if ((qr & 1) == 0) reinterpret_cast<uint32_t*>(ocol.scales)[crow * (g.rows / 64) + ccol / 64] = w;
+          }
+        }
+      } else {
       // outer maxima of both columns over the pair's four quarters (every lane shuffles)
       float Ma = max_abs_nan(ma[0], ma[1]), Mb = max_abs_nan(mb[0], mb[1]);
       Ma = max_abs_nan(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, 1));
@@ -1948,6 +2000,7 @@ __global__ void __launch_bounds__(RT, F32 ? 1 : 2) quant_cols_outer_kernel(
           }
         }
       }
+      }
     }
     if (!tile_ring_release<F32, TOR>(&tmap, g, ring, pipe, it, t, timeout_ns)) {
       timed_out = true;
@@ -1986,8 +2039,9 @@ __global__ void __launch_bounds__(RT, F32 ? 1 : 2) quant_cols_outer_kernel(
       ws->stat_nparts = (unsigned)np;
       ws->copies = (row_nparts > 0 ? 1u : 0u) | 2u;
       ws->tensor_scale[1] = 1.f;
-      ws->qmax = 6.f;
+      ws->qmax = FMT == 7 ? 7.f : 6.f;
       ws->n = (double)g.rows * (double)g.cols;
+      if (FMT == 7 && ocol.tensor_scale) *ocol.tensor_scale = 1.f;
     }
   }
 }
@@ -2637,6 +2691,8 @@ cudaError_t run_quant_cols_outer(const QuantArgs& a, int row_np, cudaStream_t s)
                        : dispatch_cols_outer<3, false>(a.rht, sr, map, g, a.seed, c, ws, row_np, s);
     case 6: return f32 ? dispatch_cols_outer<6, true>(a.rht, sr, map, g, a.seed, c, ws, row_np, s)
                        : dispatch_cols_outer<6, false>(a.rht, sr, map, g, a.seed, c, ws, row_np, s);
+    case 7: return f32 ? dispatch_cols_outer<7, true>(a.rht, sr, map, g, a.seed, c, ws, row_np, s)
+                       : dispatch_cols_outer<7, false>(a.rht, sr, map, g, a.seed, c, ws, row_np, s);
     default: return cudaErrorNotSupported;
   }
 }

@@ -65,7 +65,7 @@ typedef enum {
                        128-element macro block along the row, S = A_M / 6 rounded to nearest (ties to even) on
                        the 8-fraction-bit grid (A_M = max |v| over the macro block), and 16-element E8M0 blocks
                        under it: e = floor(log2(a_b * (1/S))) - 2, y = (v * (1/S)) * 2^-e */
-  FP4Q_HIF4 = 7       /* HiF4 three-level scale [HIF §2], block 64, row-wise copy only: per 64-element block an
+  FP4Q_HIF4 = 7       /* HiF4 three-level scale [HIF §2], block 64: per 64-element block along the block axis an
                        unsigned E6M2 scale S (bias 31, subnormals, all codes finite) = the value nearest
                        a_64 / 7 (ties to the even code, saturating at 1.75 * 2^32); per 8-element sub-block a
                        bit d_8 and per 4-element micro-block a bit d_4 that halve the step, set when no value of
@@ -211,9 +211,8 @@ int fp4q_amax(const void* src, int dtype, int64_t rows, int64_t cols, int fmt, i
  *                other format with block 16 (else FP4Q_ENOTSUP).
  *                FP4Q_NVFP4_2L and FP4Q_MXFP4_MBS: cols % 128 == 0 for the
  *                row-wise copy, rows % 128 == 0 for the column-wise copy.
- *                FP4Q_HIF4: row-wise copy only (FP4Q_COLWISE -> FP4Q_ENOTSUP),
- *                linear scales only (FP4Q_SCALES_MMA -> FP4Q_ENOTSUP), scale
- *                words 4-byte aligned.
+ *                FP4Q_HIF4: linear scales only (FP4Q_SCALES_MMA ->
+ *                FP4Q_ENOTSUP), scale words 4-byte aligned.
  *   rht          0 or 1. rounding: FP4Q_RTNE or FP4Q_SR. seed: RHT signs and SR.
  *   axis         FP4Q_ROWWISE: blocks along rows, copy row_out (rows x cols).
  *                FP4Q_COLWISE: blocks along columns, emitted transposed into

@@ -108,13 +108,13 @@ def test_host_validation_without_gpu(so):
     assert q(fake, 0, 32, 256, 6, 16, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 144, 6, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
     assert q(fake, 0, 32, 256, 8, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
-    # HiF4 (7): block 64, whole blocks per row, row-wise copy only, linear
-    # 4-byte-aligned scale words
+    # HiF4 (7): block 64, whole blocks along the block axis, linear 4-byte-aligned
+    # scale words
     from fp4_block_scaled_05_b300 import fp4q_qtensor
     assert q(fake, 0, 32, 256, 7, 16, 0, 0, 0, 1, None, None, fake, ws_size, None) == 2
     assert q(fake, 0, 32, 96, 7, 64, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1
-    assert q(fake, 0, 64, 256, 7, 64, 0, 0, 0, 2, None, None, fake, ws_size, None) == 2
-    assert q(fake, 0, 64, 256, 7, 64, 0, 0, 0, 3, None, None, fake, ws_size, None) == 2
+    assert q(fake, 0, 96, 256, 7, 64, 0, 0, 0, 2, None, None, fake, ws_size, None) == 1   # rows % 64
+    assert q(fake, 0, 64, 256, 7, 64, 0, 0, 0, 3, None, None, fake, ws_size, None) == 1   # outputs NULL
     assert q(fake, 0, 32, 256, 7, 64, 0, 0, 0, 1, None, None, fake, ws_size, None) == 1   # row_out NULL
     mma = fp4q_qtensor(1 << 20, 1 << 20, 1 << 20, 1)
     assert q(fake, 0, 32, 256, 7, 64, 0, 0, 0, 1, ctypes.addressof(mma), None, fake, ws_size, None) == 2
@@ -142,7 +142,8 @@ def test_amax_validation_without_gpu(so):
     # MXFP4 and HiF4 have no tensor amax: valid arguments launch nothing and succeed
     assert a(fake, 0, 32, 32, 1, 32, 0, 0, 3, fake, ws_size, None) == 0
     assert a(fake, 0, 32, 64, 7, 64, 0, 0, 1, fake, ws_size, None) == 0
-    assert a(fake, 0, 64, 64, 7, 64, 0, 0, 2, fake, ws_size, None) == 2      # HiF4 row-wise only
+    assert a(fake, 0, 64, 64, 7, 64, 0, 0, 2, fake, ws_size, None) == 0
+    assert a(fake, 0, 96, 64, 7, 64, 0, 0, 2, fake, ws_size, None) == 1      # rows % 64, column-wise
     q = so.fp4q_quantize
     q.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
                   ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_int,

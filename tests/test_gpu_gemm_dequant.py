@@ -170,3 +170,39 @@ def test_gemm_dequant_hif4_exact(lib):
     assert lib.fp4q_status() == 0
     bad = np.argwhere(y != ref)
     assert bad.size == 0, f"{len(bad)} of {y.size} differ; first {bad[:6].tolist()}"
+
+
+@pytest.mark.parametrize("fmt", ["ufp4", "hif4"])
+def test_gemm_dequant_full_size_sampled(lib, fmt):
+    """The bench's dequantising-GEMM workloads: A, B 8192 x 8192 N(0, 1/8192),
+    UFP4 (tiled scales) or HiF4 (linear scale words) with the RHT along K,
+    Y = A B^T through fp4q_gemm. Sampled rows of both operands bit for bit
+    against the oracle's quantisation, then the 64 x 64 sampled block of Y
+    (FP32 out) within the FP32-accumulation bound at K = 8192 (~sqrt(K) 2^-24)."""
+    n = 8192
+    a = synth.gemm_operand("a", n, n)
+    b = synth.gemm_operand("b", n, n)
+    layout = "linear" if fmt == "hif4" else "mma"
+    qa, _ = lib.fp4q_quantize(a.cuda(), fmt=fmt, rht=True, seed=1234, layout=layout)
+    qb, _ = lib.fp4q_quantize(b.cuda(), fmt=fmt, rht=True, seed=1234, layout=layout)
+    y = lib.fp4q_gemm(qa, qb, out_dtype=torch.float32)
+    rng = np.random.default_rng(1)
+    rows = np.sort(rng.choice(n, 64, replace=False))
+    cols = np.sort(rng.choice(n, 64, replace=False))
+    ra = o.quantize(synth.bf16_bits(a), fmt, rht=True, seed=1234, rows_subset=rows)["row"]
+    rb = o.quantize(synth.bf16_bits(b), fmt, rht=True, seed=1234, rows_subset=cols)["row"]
+    for q, r, sel in ((qa, ra, rows), (qb, rb, cols)):
+        idx = torch.from_numpy(sel).cuda()
+        assert np.array_equal(q.codes[idx].cpu().numpy(), r["codes"])
+        if fmt == "hif4":
+            assert np.array_equal(q.scales[idx].cpu().numpy().view(np.uint32), r["scales"])
+        else:
+            nkb = n // 16
+            rr, kb = np.meshgrid(sel, np.arange(nkb), indexing="ij")
+            off = torch.from_numpy(o.mma_scale_offset(rr, kb, -(-nkb // 4) * 4).astype(np.int64)).cuda()
+            assert np.array_equal(q.scales[off].cpu().numpy(), r["scales"])
+            assert np.float32(r["tensor_scale"]).view(np.uint32) == q.tensor_scale.cpu().numpy().view(np.uint32)[0]
+    ref = o.gemm(ra, rb)
+    got = y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy().astype(np.float64)
+    assert _rel_fro(got, ref) < 2e-5
+    assert lib.fp4q_status() == 0

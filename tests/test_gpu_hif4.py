@@ -148,14 +148,62 @@ def test_hif4_rejections(lib):
     with pytest.raises(lib.FP4QError) as e:
         lib.fp4q_quantize(x, fmt=FMT)
     assert e.value.code == 1                                   # cols % 64
-    y = torch.zeros(64, 128, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(96, 128, dtype=torch.bfloat16, device="cuda")
     for axis in ("col", "both"):
         with pytest.raises(lib.FP4QError) as e:
             lib.fp4q_quantize(y, fmt=FMT, axis=axis)
-        assert e.value.code == 2                               # row-wise only
+        assert e.value.code == 1                               # rows % 64 for the column-wise copy
     with pytest.raises(lib.FP4QError) as e:
         lib.fp4q_quantize(y, fmt=FMT, layout="mma")
     assert e.value.code == 2                                   # linear scale words only
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("rounding", ["rtne", "sr"])
+@pytest.mark.parametrize("rht", [False, True])
+@pytest.mark.parametrize("shape,axis", [((192, 384), "both"), ((256, 320), "col"), ((64, 4160), "both")])
+def test_hif4_column_copy_parity(lib, shape, axis, rht, rounding, dtype):
+    """The transposed copy (blocks of 64 down the columns) from the 128-row
+    tile kernel, with the row-wise copy from the row kernel when both are
+    asked: 192 rows end in half a tile, 4160 columns in a partial one."""
+    x = _grouped(*shape, seed=29, dtype=dtype)
+    r, c = lib.fp4q_quantize(x.cuda(), fmt=FMT, rht=rht, rounding=rounding, seed=77, axis=axis)
+    rs, cs = lib.fp4q_stats()
+    assert lib.fp4q_status() == 0
+    ref = o.quantize(_bits(x), FMT, rht=rht, rounding=rounding, seed=77, axis=axis)
+    check_hif4(c, ref["col"])
+    check_stats(cs, ref["col"]["stats"])
+    if axis == "both":
+        check_hif4(r, ref["row"])
+        check_stats(rs, ref["row"]["stats"])
+
+
+@pytest.mark.parametrize("mag", [1e-30, 1e30])
+def test_hif4_column_copy_extremes(lib, mag):
+    x = (_grouped(128, 256, 31, torch.float32) * mag).float()
+    _, c = lib.fp4q_quantize(x.cuda(), fmt=FMT, axis="col")
+    _, cs = lib.fp4q_stats()
+    ref = o.quantize(x.numpy(), FMT, axis="col")["col"]
+    check_hif4(c, ref)
+    check_stats(cs, ref["stats"])
+
+
+def test_hif4_gradient_both_copies_full_size(lib):
+    """The 4096 x 14336 gradient tensor, HiF4 + RHT + SR, both copies from one
+    call; sampled rows of each copy against the oracle."""
+    x = synth.gradient("a")
+    rows, cols = x.shape
+    r, c = lib.fp4q_quantize(x.cuda(), fmt=FMT, rht=True, rounding="sr", seed=1234, axis="both")
+    assert lib.fp4q_status() == 0
+    rng = np.random.default_rng(3)
+    rsel = np.unique(np.concatenate([[0, 1, 63, 64, rows - 1], rng.integers(0, rows, 30)]))
+    csel = np.unique(np.concatenate([[0, 1, 127, 128, cols - 1], rng.integers(0, cols, 30)]))
+    ref = o.quantize(synth.bf16_bits(x), FMT, rht=True, rounding="sr", seed=1234, axis="both",
+                     rows_subset=rsel, cols_subset=csel)
+    for got, want, sel in ((r, ref["row"], rsel), (c, ref["col"], csel)):
+        idx = torch.from_numpy(sel).cuda()
+        assert np.array_equal(got.codes[idx].cpu().numpy(), want["codes"])
+        assert np.array_equal(got.scales[idx].cpu().numpy().view(np.uint32), want["scales"])
 
 
 def test_hif4_noalloc_matches(lib):
