@@ -127,12 +127,14 @@ def test_gemm_full_size_sampled(lib):
     assert lib.fp4q_status() == 0
 
 
-def test_bounded_wait_runs_out_without_fault(lib):
+@pytest.mark.parametrize("m", [256, 128])
+def test_bounded_wait_runs_out_without_fault(lib, m):
     """Failure detection on the device: the first CTA's producer withholds one
     stage, the waits that depend on it run out after 20 ms, the kernel records
     FP4Q_ETIMEOUT and returns; the context stays usable and the next GEMM on
-    it is correct."""
-    a = synth.gemm_operand("a", 256, 512)
+    it is correct. M = 256 runs the two-SM kernel (the pair's waits, relays and
+    cross-CTA commits), M = 128 the one-SM kernel."""
+    a = synth.gemm_operand("a", m, 512)
     b = synth.gemm_operand("b", 256, 512)
     qa, _ = lib.fp4q_quantize(a.cuda(), fmt="nvfp4", layout="mma")
     qb, _ = lib.fp4q_quantize(b.cuda(), fmt="nvfp4", layout="mma")
