@@ -342,6 +342,21 @@ __device__ __forceinline__ void outer_stats_value(const Sums& acc, double& sig, 
   }
 }
 
+// Two plain FP32 sums, one per lane of a pair. The row-wise quantisation pass
+// adds one partial per chunk to them (about 9 per thread at 2^25 elements, 300
+// at 2^30): the relative error stays below that count times 2^-24 of the sum
+// of magnitudes (typically its square root), and the compensation of Kahan2
+// would cost that kernel register spills.
+struct Sum2 {
+  f2 s = 0ull;
+  __device__ __forceinline__ void add(f2 x) { s = f2_add(s, x); }
+  __device__ __forceinline__ float value_f() const {   // both lanes together
+    float s0, s1;
+    f2_split(s, s0, s1);
+    return __fadd_rn(s0, s1);
+  }
+};
+
 // Two independent Kahan-compensated FP32 sums, one per lane of a pair.
 struct Kahan2 {
   f2 s = 0ull, c = 0ull;
@@ -1023,11 +1038,11 @@ __device__ __forceinline__ float amax_result(float m, uint32_t m2) {
 
 // Quantise the thread's 32 elements at p (elements e .. e+31 of the copy) and
 // add their statistics to the running sums.
-template <int FMT, bool F32, bool RHT, bool SR>
+template <int FMT, bool F32, bool RHT, bool SR, class Acc2>
 __device__ __forceinline__ void quant_segment(const uint8_t* p, int64_t e, const Flat& f, const CopyOut& o,
                                               const uint32_t (&sgn)[16], const Ctx& cx, const Divider& dv,
-                                              const float2* tab, const PhiloxKey& pk, Sums& acc, Kahan2& kb,
-                                              Kahan2& ks, Kahan2& ke, uint32_t& nonfinite) {
+                                              const float2* tab, const PhiloxKey& pk, Sums& acc, Acc2& kb,
+                                              Acc2& ks, Acc2& ke, uint32_t& nonfinite) {
   const int nb16 = (f.n - e >= 32) ? 2 : (f.n - e >= 16 ? 1 : 0);
   if constexpr (FMT == 1) {
     if (nb16 == 2) {
@@ -1256,17 +1271,28 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   // Launched as a programmatic dependent of the amax pass: everything above
   // only reads the source; the amax partials are read after this wait.
   grid_dependency_wait();
-  Ctx cx{1.f, 0.f, 0.f};
-  Divider dv{};
-  if constexpr (FMT == 0 || FMT == 2) {
-    cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
-    dv.init(cx.d);
-    fill_scale_table(tab, cx.g);
-    __syncthreads();
+  // The tensor scale's constants stay in shared memory and are read where
+  // used: held in registers through the loop they made the kernel spill.
+  __shared__ Ctx s_cx;
+  __shared__ Divider s_dv;
+  if (tid == 0) {
+    s_cx = Ctx{1.f, 0.f, 0.f};
+    s_dv = Divider{};
   }
+  if constexpr (FMT == 0 || FMT == 2) {
+    const Ctx c = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
+    if (tid == 0) {
+      s_cx = c;
+      s_dv.init(c.d);
+    }
+    fill_scale_table(tab, c.g);
+  }
+  __syncthreads();
+  const Ctx& cx = s_cx;
+  const Divider& dv = s_dv;
 
   Sums acc;
-  Kahan2 kb, ks, ke;
+  Sum2 kb, ks, ke;
   uint32_t nonfinite = 0;
   bool timed_out = false;
   int64_t it = 0;
