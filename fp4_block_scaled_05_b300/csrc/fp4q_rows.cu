@@ -2125,9 +2125,12 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uin
   }
 
   Sums acc;
-  Kahan2 kb, ks, ke;
+  Sum2 kb, ks, ke;      // plain sums: see Sum2 (compensation made the kernel spill)
   uint32_t nonfinite = 0;
-  Ctx cx{1.f, 0.f, 0.f};
+  // the tensor scale's constants in shared memory, read where used (see quant_rows_kernel)
+  __shared__ Ctx s_cx;
+  __shared__ Divider s_dv;
+  if (tid == 0) s_cx = Ctx{1.f, 0.f, 0.f};
   if (!timed_out) {
     const uint32_t cm = cta_max<RT>(__float_as_uint(amax_result<F32, RHT>(m, m2)), sh_max);
     if (tid == 0) {
@@ -2138,11 +2141,15 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uin
     timed_out = !grid_barrier(ws, timeout_ns);
   }
   if (!timed_out) {
-    cx = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
-    Divider dv{};
-    dv.init(cx.d);
-    fill_scale_table(tab, cx.g);
+    const Ctx c = make_ctx(fold_amax<RT>(ws, 0, sh_max), kQmax, kQmax448);
+    if (tid == 0) {
+      s_cx = c;
+      s_dv.init(c.d);
+    }
+    fill_scale_table(tab, c.g);
     __syncthreads();
+    const Ctx& cx = s_cx;
+    const Divider& dv = s_dv;
     // ---- pass 2: quantise ----
     for (; it < total; ++it) {
       const int s = (int)(it % S);
@@ -2181,10 +2188,10 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_fused_kernel(Flat f, uin
   if (blockIdx.x == 0 && tid == 0) {
     ws->stat_nparts = gridDim.x;
     ws->copies = 1u;
-    ws->tensor_scale[0] = cx.g;
+    ws->tensor_scale[0] = s_cx.g;
     ws->qmax = kQmax;
     ws->n = (double)f.n;
-    if (o.tensor_scale) *o.tensor_scale = cx.g;
+    if (o.tensor_scale) *o.tensor_scale = s_cx.g;
   }
 }
 
