@@ -1296,29 +1296,26 @@ __global__ void __launch_bounds__(RT, SR ? 2 : 3) quant_rows_kernel(Flat f, uint
   uint32_t nonfinite = 0;
   bool timed_out = false;
   int64_t it = 0;
-  // One CTA barrier per chunk (measured faster here than letting warps run
-  // ahead: the quantisation work per chunk is even across warps).
+  // Warps run ahead of one another by up to kStages - 1 chunks, each
+  // releasing a slot on its own (per-slot empty barriers, as the amax pass):
+  // measured 6-7% faster than one CTA barrier per chunk on 8192 x 4096.
   for (int64_t c = blockIdx.x; c < f.nchunks; ++it, c += gridDim.x) {
     const int s = (int)(it % S);
-    const bool ok = mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns);
-    if (ok) {
-      const int64_t e = c * CH + (int64_t)tid * EPT;
-      quant_segment<FMT, F32, RHT, SR>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, e, f, o, sgn, cx, dv,
-                                       tab, pk, acc, kb, ks, ke, nonfinite);
+    if (!mbar_wait_bounded(smem_u32(&full[s]), (uint32_t)((it / S) & 1), timeout_ns)) {
+      timed_out = true;
+      break;
     }
-    timed_out = __syncthreads_or(!ok);
-    if (timed_out) break;
-    if (tid == 0) {
-      const int64_t nx = c + (int64_t)S * gridDim.x;
-      if (nx < f.nchunks) {
-        ring_issue<F32>(f, nx, ring, s, smem_u32(&full[s]));
-        pipe.next_it = it + S + 1;
-      }
+    const int64_t e = c * CH + (int64_t)tid * EPT;
+    quant_segment<FMT, F32, RHT, SR>(ring + s * Ring<F32>::kChunkBytes + tid * EPT * ES, e, f, o, sgn, cx, dv,
+                                     tab, pk, acc, kb, ks, ke, nonfinite);
+    if (!flat_ring_release<F32>(f, ring, pipe, it, c, false, timeout_ns)) {
+      timed_out = true;
+      break;
     }
   }
   // the CTA's last chunk is done: the next kernel on the stream may start
   grid_launch_dependents();
-  if (timed_out) {
+  if (__syncthreads_or(timed_out)) {
     pipe_drain<S>(full, pipe.next_it);
     if (tid == 0) atomicOr(&ws->status, kStatusTimeout);
   }
