@@ -12,7 +12,7 @@
 // Paths (all kernels in fp4q_rows.cu):
 //  * row-wise copy only: the tensor is a flat stream of 8192-element chunks
 //    (amax_rows_kernel, quant_rows_kernel), or one cooperative launch of both
-//    passes for NVFP4 / UFP4 tensors below 2^25 elements (quant_fused_kernel);
+//    passes for NVFP4 / UFP4 tensors below 2^20 elements (quant_fused_kernel);
 //  * any request with the column-wise copy: 64 x 128 tiles through a shared-
 //    memory ring, one read of the source serving both copies
 //    (amax_tiles_kernel when the RHT makes the two copies' amax differ,
@@ -73,13 +73,17 @@ cudaError_t run_quantize(const QuantArgs& a, cudaStream_t s) {
                                           static_cast<Workspace*>(a.ws));
     return cudaGetLastError();
   }
-  // Both passes in one launch pays for tensors up to 2^24 elements (one fixed
-  // launch cost less; measured on B300: 12.4 vs 14.4 us at 1M elements) and
-  // ties at 2^25; above that the two launches are faster, because the second
-  // launch's grid restarts on chunks the amax pass left in L2.
+  // Both passes in one launch pays only for small tensors: measured on B300
+  // (one call, median, L2 flushed / not flushed), 256 x 4096: 15.6 / 16.0 us
+  // one launch against 12.4 / 18.0 us two; from 1024 x 4096 up the two
+  // launches win both ways (22.2 / 18.6 against 16.4 / 18.0 us; 4096 x 4096:
+  // 33.9 / 28.6 against 27.4 / 23.3 us), since the second launch's grid
+  // restarts on the chunks the amax pass left in L2 and its warps run ahead of
+  // one another, which the one-launch kernel's grid barrier and per-chunk CTA
+  // barriers do not allow.
   // the E8M0 formats and two-level NVFP4 have no tensor amax: one pass
   const bool tensor_scaled = a.fmt == 0 || a.fmt == 2;
-  if (tensor_scaled && !a.amax_ready && a.axis == 1 && a.rows * a.cols < (int64_t(1) << 25)) {
+  if (tensor_scaled && !a.amax_ready && a.axis == 1 && a.rows * a.cols < (int64_t(1) << 20)) {
     // the two-launch path if a co-resident grid cannot be had
     const cudaError_t e = run_quant_fused(a, s);
     if (e == cudaSuccess) return e;
