@@ -229,6 +229,7 @@ KERNEL_SOURCES = {
     "amax_tiles_kernel": "fp4q_rows.cu", "quant_tiles_kernel": "fp4q_rows.cu",
     "quant_cols_outer_kernel": "fp4q_rows.cu", "gemm_nvf4_kernel": "fp4q_gemm.cu",
     "gemm_nvf4_pair_kernel": "fp4q_gemm.cu", "gemm_dq_kernel": "fp4q_gemm_dq.cu",
+    "gemm_dq_kernel<3>": "fp4q_gemm_dq.cu",
     "gemm_outer_kernel": "fp4q_gemm_outer.cu", "code_hist_kernel": "fp4q_hist.cu",
 }
 
@@ -722,7 +723,7 @@ def run_gemm_ufp4_leg(fq, torch, device, steps, warmup, peaks, fmt="ufp4"):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                          "frac": tflops / peak,
                          "peak_source": f"{peaks['source']} bf16 burst (the dense FP16 rate is the same)",
-                         "traffic": ncu_traffic("gemm_dq_kernel", flop)}}
+                         "traffic": ncu_traffic("gemm_dq_kernel" if fmt == "ufp4" else "gemm_dq_kernel<3>", flop)}}
 
 
 def sweep_point(fq, torch, device, x, steps, warmup, peaks, ws, flush) -> dict:
