@@ -297,40 +297,39 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 // 256 x 256 tile of Y together: rank r holds rows [128 r, 128 r + 128) of the
 // tile's A rows and of its B rows (the B tile is split along N), the scales of
 // its own A rows, and the scales of all 256 B rows. One thread of rank 0 issues
-// every scale copy and MMA for both (cta_group::2): each instruction reads the
-// shared memory of both CTAs at the same offsets and writes both tensor
-// memories, so each SM takes in half of B per multiply-add instead of all of
-// it, and one scale copy serves two SMs. Each CTA's TMEM holds its 128 rows x
-// 256 columns of the accumulator.
+// every MMA for both (cta_group::2): each instruction reads the shared memory
+// of both CTAs at the same offsets, and the TMEM of both (scales and
+// accumulator), so each SM takes in half of B per multiply-add instead of all
+// of it. Each CTA's TMEM holds its 128 rows x 256 columns of the accumulator
+// and the scales of its stages.
 //
 // Hand-offs between the two CTAs (no multicast):
-//   rank 1's stage ready (TMA landed, its scales expanded) -> rank 1 warp 1
+//   rank 1's stage ready (TMA landed, its scales in its TMEM) -> rank 1 warp 1
 //     relays it to rank 0's pfull[s]
 //   rank 0's MMA thread commits each stage to empty[s] of both CTAs (two
 //     unicast commits) and each finished tile to tfull of both CTAs
 //   every epilogue warp of both CTAs -> rank 0's tempty (accumulator read out)
 // The relays are relaxed arrivals: each hands on an event the relaying thread
 // has observed complete within its own CTA (the stage's TMA bytes counted in
-// by the mbarrier and the helpers' expanded scales stored, fenced for the
-// async proxy and released on a CTA barrier; or a warp's TMEM reads finished,
-// tcgen05.wait::ld). A release at cluster scope measured ~0.8 us per arrival
+// by the mbarrier and the writers' TMEM stores finished (tcgen05.wait::st,
+// then tcgen05.fence::before_thread_sync and an arrival on a CTA barrier); or
+// a warp's TMEM reads finished, tcgen05.wait::ld). A release at cluster scope measured ~0.8 us per arrival
 // here, which the stage time cannot afford.
 //
-// Scale factors: the block-scaled MMA reads each operand's scales from TMEM,
-// where tcgen05.cp puts them, and every copy instruction costs the tensor
-// pipe a fixed time: twelve 32x128b.warpx4 copies of 512 bytes per stage took
-// about half of the pipe's time. So helper warps in each CTA first expand the
-// stage's scale tiles (512 bytes per 128 rows x 64 K elements, the layout the
-// quantiser writes) in shared memory into 4 KB blocks in which each of the
-// four 32-lane quadrants finds its copy of the 32-row pattern, with two K
-// chunks of A, or both 128-row halves of B's tile, side by side. Six 128x256b
-// copies per stage then fill what twelve copies filled. Two helper warps
-// share the expansion (one alone took most of a stage's time; a third only
-// moved the bound). The expanded blocks sit in a ring of three slots; a slot
-// is reused once the MMAs of the stage three back have completed.
+// Scale factors: the block-scaled MMA reads each operand's scales from TMEM.
+// Four writer warps per CTA, one per 32-lane TMEM quadrant (a warp reaches
+// only the lanes of quadrant warp % 4), put each stage's scales there with
+// tcgen05.st once the stage has landed: lane l of each writes the 16-byte row
+// l of every 512-byte scale tile (128 rows x 64 K elements, the layout the
+// quantiser writes) into its own lane of the quadrant, so each quadrant holds
+// the whole 32-row pattern. Moving the scales with tcgen05.cp instead (one
+// thread, in the MMA issuer's stream) measured 292 us at 8192^3 against 212
+// us this way: each copy took tensor-pipe time from the MMAs. A stage's TMEM
+// slot is free when the stage lands, since its TMA was issued only after the
+// MMAs that last read the slot had completed.
 // Every wait is bounded, as in the one-CTA kernel.
 struct PairCfg {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 5;
   static constexpr int kABytes = 128 * BK_BYTES;          // this CTA's 128 rows of A
   static constexpr int kBBytes = 128 * BK_BYTES;          // this CTA's 128 rows of B
   static constexpr int kSfaBytes = 2048;                  // its A rows' scales: 4 K chunks x 512 B
@@ -340,32 +339,35 @@ struct PairCfg {
   static constexpr int kSfbCols = 32;
   static constexpr int kSfStageCols = kSfaCols + kSfbCols;
   static constexpr int kSfBase = 256;                     // accumulator: columns [0, 256)
-  static constexpr int kRepSlots = 3;
-  static constexpr int kRepBytes = 6 * 4096;             // SFA chunks 0-1, 2-3; SFB chunks 0..3
-  static constexpr int kSmem = kStages * kStageBytes + kRepSlots * kRepBytes + 1024 + 256;
-  static constexpr int kHelperWarps = 2;                   // scale expansion: A + B chunk 0, B chunks 1-3
-  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kHelperWarps;
-  static constexpr int kHelperWarp = 2 + kEpiWarps;
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  static constexpr int kScaleWarps = 4;                   // scale writers: one per TMEM lane quadrant
+  static constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kScaleWarps;
+  static constexpr int kScaleWarp = 2 + kEpiWarps;
   static_assert(kSfBase + kStages * kSfStageCols <= kTmemCols, "TMEM budget");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-// One 16-byte row of a 32x128b scale tile, expanded into the 128 lanes of a
-// 128x256b copy source (8-row core matrices of 16 bytes: 8-row groups 256
-// bytes apart, the two 16-byte halves of a row 128 bytes apart): lane 32q + l
-// of half `half` gets it for every quadrant q.
-__device__ __forceinline__ void expand_row(uint8_t* blk, int l, int half, uint4 v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int L = 32 * q + l;
-    *reinterpret_cast<uint4*>(blk + (L >> 3) * 256 + half * 128 + (L & 7) * 16) = v;
-  }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
 }
-
-__device__ __forceinline__ void tc2_cp_256(uint32_t taddr, uint64_t desc) {
-  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
 }
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
@@ -378,10 +380,9 @@ gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_c
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* rep_ring = smem + S * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(rep_ring + C::kRepSlots * C::kRepBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
   // bars[0..S): full, [S..2S): pfull, [2S..3S): empty, 3S: tfull, 3S+1: tempty, 3S+2: drain,
-  // 3S+3+r: rfull[r] (expanded scales of ring slot r written)
+  // 3S+3+s: rfull[s] (the scales of stage s written into this CTA's TMEM)
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
 
@@ -407,7 +408,7 @@ gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_c
     mbar_init(tfull, 1);
     mbar_init(tempty, 2 * kEpiWarps);
     mbar_init(drain_bar, 1);
-    for (int r = 0; r < C::kRepSlots; ++r) mbar_init(rfull_bar(r), C::kHelperWarps);
+    for (int r = 0; r < S; ++r) mbar_init(rfull_bar(r), C::kScaleWarps);
     fence_mbarrier_init();
   }
   if (warp == 1) {
@@ -488,16 +489,16 @@ gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_c
   } else if (warp == 1) {
     if (lane == 0 && rank == 1) {
       // ---------------- rank 1: hand each landed stage to rank 0 ----------------
-      // (its A, B and expanded scales: the helper waited for the stage's copies)
+      // (its A, B and scales: the scale writers waited for the stage's copies)
       const uint32_t peer_pfull0 = peer_addr(pfull_bar(0), 0);
       int s = 0;
-      uint32_t g = 0;
+      uint32_t ph = 0;
       for (int t = pair; t < num_tiles; t += npairs) {
         bool ok = true;
-        for (int ks = 0; ks < nk; ++ks, ++g) {
-          if (!mbar_wait(rfull_bar((int)(g % C::kRepSlots)), (g / C::kRepSlots) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait(rfull_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
           mbar_arrive_remote(peer_pfull0 + 8u * s);
-          if (++s == S) s = 0;
+          if (++s == S) { s = 0; ph ^= 1u; }
         }
         if (!ok) break;
       }
@@ -507,29 +508,22 @@ gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_c
       const uint32_t base = smem_u32(smem);
       const uint64_t da0 = smem_desc(base, 16, 1024, 2);
       const uint64_t db0 = smem_desc(base + C::kABytes, 16, 1024, 2);
-      const uint64_t drep0 = smem_desc(smem_u32(rep_ring), 128, 256, 0);
       const uint32_t sf_base = tmem + C::kSfBase;
       const uint32_t peer_empty0 = peer_addr(empty_bar(0), 1);
       const uint32_t peer_tfull = peer_addr(tfull, 1);
       int s = 0;
-      uint32_t ph = 0, acc_ph = 0, g = 0;
+      uint32_t ph = 0, acc_ph = 0;
       bool ok = true, issued_any = false;
       for (int t = pair; t < num_tiles && ok; t += npairs) {
         if (!mbar_wait_cluster(tempty, acc_ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
         tc_fence_after();
-        for (int ks = 0; ks < nk; ++ks, ++g) {
-          // this CTA's expanded scales (its helper saw the stage land), then rank 1's stage
-          if (!mbar_wait(rfull_bar((int)(g % C::kRepSlots)), (g / C::kRepSlots) & 1u, &s_abort, timeout_ns) ||
+        for (int ks = 0; ks < nk; ++ks) {
+          // this CTA's scales in TMEM (its writers saw the stage land), then rank 1's stage
+          if (!mbar_wait(rfull_bar(s), ph, &s_abort, timeout_ns) ||
               !mbar_wait_cluster(pfull_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint64_t off = (uint64_t)(s * (C::kStageBytes >> 4));
-          const uint64_t roff = (uint64_t)((g % C::kRepSlots) * (C::kRepBytes >> 4));
           const uint32_t sf_col = sf_base + s * C::kSfStageCols;
-          // A: chunks 0-1 and 2-3 (4 columns each); B: per chunk both 128-row halves
-          tc2_cp_256(sf_col, drep0 + roff);
-          tc2_cp_256(sf_col + 8, drep0 + roff + (4096 >> 4));
-#pragma unroll
-          for (int j = 0; j < 4; ++j) tc2_cp_256(sf_col + C::kSfaCols + 8 * j, drep0 + roff + ((8192 + 4096 * j) >> 4));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tc2_mma_nvf4(tmem, da0 + off + 2 * j, db0 + off + 2 * j, idesc, sf_col + 4 * j,
@@ -551,39 +545,42 @@ gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_c
         }
       }
     }
-  } else if (warp >= C::kHelperWarp) {
-    // ---------------- scale expansion (both CTAs) ----------------
-    const int hw = warp - C::kHelperWarp;      // 0: A's four chunks and B's chunk 0; 1: B's chunks 1-3
+  } else if (warp >= C::kScaleWarp) {
+    // ---------------- scale writers (both CTAs) ----------------
+    // Warp w may access TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 only; the
+    // four writers cover the four quadrants. Lane l of each writes, into 48
+    // columns of its lane 32 (w % 4) + l, the 16-byte row l of each 512-byte
+    // scale tile: A's four K chunks (columns 4 j + c), then per K chunk both
+    // 128-row halves of B's (columns 16 + 8 j + 4 h + c). The slot of stage s
+    // is free when the stage lands: its TMA was issued after the MMAs that
+    // read the slot before had completed.
+    const uint32_t quad = (uint32_t)(warp & 3);
     int s = 0;
-    uint32_t ph = 0, g = 0;
+    uint32_t ph = 0;
     for (int t = pair; t < num_tiles; t += npairs) {
       bool ok = true;
-      for (int ks = 0; ks < nk; ++ks, ++g) {
-        if (!mbar_wait(full_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
-        if (g >= (uint32_t)C::kRepSlots) {
-          // the ring slot was last read by the copies of the stage kRepSlots back
-          const uint32_t gp = g - (uint32_t)C::kRepSlots;
-          if (!mbar_wait(empty_bar((int)(gp % S)), (gp / S) & 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
-        }
+      for (int ks = 0; ks < nk; ++ks) {
+        // the warp leaves together (the TMEM stores below are warp-collective)
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), ph, &s_abort, timeout_ns))) { fail(); ok = false; break; }
         const uint8_t* raw = smem + s * C::kStageBytes + C::kABytes + C::kBBytes;
-        uint8_t* blk = rep_ring + (g % C::kRepSlots) * C::kRepBytes;
-        if (hw == 0) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            expand_row(blk + 4096 * (j >> 1), lane, j & 1, *reinterpret_cast<const uint4*>(raw + 512 * j + 16 * lane));
-        }
+        uint32_t va[16], vb[32];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if ((j == 0) != (hw == 0)) continue;
+          const uint4 u = *reinterpret_cast<const uint4*>(raw + 512 * j + 16 * lane);
+          va[4 * j] = u.x; va[4 * j + 1] = u.y; va[4 * j + 2] = u.z; va[4 * j + 3] = u.w;
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            expand_row(blk + 8192 + 4096 * j, lane, h,
-                       *reinterpret_cast<const uint4*>(raw + C::kSfaBytes + 2048 * h + 512 * j + 16 * lane));
+          for (int h = 0; h < 2; ++h) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + C::kSfaBytes + 2048 * h + 512 * j + 16 * lane);
+            vb[8 * j + 4 * h] = w.x; vb[8 * j + 4 * h + 1] = w.y; vb[8 * j + 4 * h + 2] = w.z; vb[8 * j + 4 * h + 3] = w.w;
+          }
         }
-        // the expanded blocks become visible to the tensor cores' (async) reads
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t taddr = tmem + ((32u * quad) << 16) + (uint32_t)(C::kSfBase + s * C::kSfStageCols);
+        tmem_st16(taddr, va);
+        tmem_st32(taddr + C::kSfaCols, vb);
+        tmem_st_wait();
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(rfull_bar((int)(g % C::kRepSlots)));
+        if (lane == 0) mbar_arrive(rfull_bar(s));
         if (++s == S) { s = 0; ph ^= 1u; }
       }
       if (!ok) break;
@@ -601,43 +598,56 @@ gemm_nvf4_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_c
       if (!mbar_wait(tfull, acc_ph, &s_abort, timeout_ns)) { fail(); break; }
       tc_fence_after();
       const int row = pm * 256 + (int)rank * 128 + q * 32 + lane;
-      uint32_t r[kCols];
-#pragma unroll
-      for (int c = 0; c < kCols / 32; ++c)
-        tmem_ld32_async(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hcol * kCols + c * 32), r + 32 * c);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < kCols / 32; ++c) reg_fence32(r + 32 * c);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (rank == 0) mbar_arrive(tempty0);
-        else mbar_arrive_remote(tempty0);
-      }
-      acc_ph ^= 1u;
       const int col0 = n * 256 + hcol * kCols;
-      if constexpr (OUT_F32) {
-        float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hcol * kCols);
+      // two halves of 64 columns (64 registers live at a time): the first is
+      // packed (BF16) or stored (FP32) before the second is read; the
+      // accumulator is released after the second read
+      uint32_t r[64], hpk[32];
 #pragma unroll
-        for (int i = 0; i < kCols / 4; ++i)
-          out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
-      } else {
-        uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+      for (int half = 0; half < 2; ++half) {
+        tmem_ld32_async(tbase + 64 * half, r);
+        tmem_ld32_async(tbase + 64 * half + 32, r + 32);
+        tmem_ld_wait();
+        reg_fence32(r);
+        reg_fence32(r + 32);
+        if (half == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (rank == 0) mbar_arrive(tempty0);
+            else mbar_arrive_remote(tempty0);
+          }
+        }
+        if constexpr (OUT_F32) {
+          float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0 + 64 * half);
 #pragma unroll
-        for (int i = 0; i < kCols / 8; ++i) {
-          uint32_t h[4];
+          for (int i = 0; i < 16; ++i)
+            out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+        } else {
+          uint32_t h[32];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * i + 2 * k]), alpha),
-                                                            __fmul_rn(__uint_as_float(r[8 * i + 2 * k + 1]), alpha));
+          for (int k = 0; k < 32; ++k) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * k]), alpha),
+                                                            __fmul_rn(__uint_as_float(r[2 * k + 1]), alpha));
             h[k] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+          if (half == 0) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) hpk[k] = h[k];
+          } else {
+            uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) out[i] = make_uint4(hpk[4 * i], hpk[4 * i + 1], hpk[4 * i + 2], hpk[4 * i + 3]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) out[8 + i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          }
         }
       }
+      acc_ph ^= 1u;
     }
   }
 
