@@ -14,21 +14,28 @@
 // 256 x 256 tile through the two-SM MMA (gemm_nvf4_pair_kernel, below);
 // otherwise one CTA per 128 x BN tile (gemm_nvf4_kernel).
 //
-// One-CTA structure (one persistent CTA per SM, 320 threads):
+// One-CTA structure (one persistent CTA per SM, 448 threads):
 //   warp 0      TMA producer: per K stage of 256 elements, one 2-D tiled TMA
 //               load (128B swizzle) of the A and B code tiles and 1-D bulk
-//               copies of their scale tiles into a 4-deep shared-memory ring
-//               (mbarrier transaction counts).
-//   warp 1      allocates the 512 TMEM columns; one thread moves each stage's
-//               scale tiles into TMEM (tcgen05.cp 32x128b.warpx4) and issues
-//               four tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               copies of their scale tiles into a shared-memory ring (4
+//               stages for BN = 256, 6 for BN = 128; mbarrier transaction
+//               counts).
+//   warp 1      allocates the 512 TMEM columns; one thread issues, once the
+//               stage's scales are in TMEM, four
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
 //               (M = 128, N = BN, K = 64) into an FP32 accumulator in TMEM;
 //               tcgen05.commit frees the ring slot and, after the last stage,
 //               hands the accumulator to the epilogue.
 //   warps 2-9   epilogue: each warp reads its 32 TMEM lanes x BN/2 columns
-//               into registers, releases the accumulator (the next tile's
-//               MMAs start), then multiplies by g_A * g_B and stores BF16
+//               into registers, 64 columns at a time, releases the
+//               accumulator after the last read (the next tile's MMAs
+//               start), multiplies by g_A * g_B and stores BF16
 //               (nearest-even) or FP32.
+//   warps 10-13 scale writers, one per TMEM lane quadrant: each stage's scale
+//               tiles go from shared memory into TMEM by tcgen05.st (moving
+//               them with tcgen05.cp, in the MMA thread's stream, took tensor-
+//               pipe time from the MMAs: 306 against 227 us at 8064 x 8192 x
+//               8192).
 // Every mbarrier wait is bounded by a global-timer deadline; on expiry the
 // kernel records FP4Q_ETIMEOUT in the workspace, drains what it issued and
 // returns.
@@ -50,13 +57,15 @@ constexpr int BM = 128;           // rows of A per tile (= MMA M)
 constexpr int BK_BYTES = 128;     // bytes of codes per row per stage (256 FP4 values)
 constexpr int BK = 256;           // K elements per stage
 constexpr int kEpiWarps = 8;              // two per TMEM lane quadrant
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kScaleWarps = 4;            // one per TMEM lane quadrant
+constexpr int kScaleWarp = 2 + kEpiWarps; // the first of them
+constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kScaleWarps;
 constexpr int kTmemCols = 512;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s
 
 template <int BN>
 struct Cfg {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = BN == 128 ? 6 : 4;   // as many as shared memory holds
   static constexpr int kABytes = BM * BK_BYTES;
   static constexpr int kBBytes = BN * BK_BYTES;
   static constexpr int kSfaBytes = 2048;                 // 128 rows x 16 scales
@@ -83,7 +92,8 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
-  // bars[0..S): full, bars[S..2S): empty, bars[2S]: tmem_full, bars[2S+1]: tmem_empty, bars[2S+2]: drain
+  // bars[0..S): full, bars[S..2S): empty, bars[2S]: tmem_full, bars[2S+1]: tmem_empty, bars[2S+2]: drain,
+  // bars[2S+3+s]: sfull[s] (the scales of stage s written into TMEM)
   __shared__ uint32_t s_tmem_base;
   __shared__ volatile int s_abort;
 
@@ -95,12 +105,14 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
   const uint32_t tmem_full = bar0 + 8u * (2 * C::kStages);
   const uint32_t tmem_empty = bar0 + 8u * (2 * C::kStages + 1);
   const uint32_t drain_bar = bar0 + 8u * (2 * C::kStages + 2);
+  auto sfull_bar = [&](int s) { return bar0 + 8u * (2 * C::kStages + 3 + s); };
 
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      mbar_init(sfull_bar(s), kScaleWarps);
     }
     mbar_init(tmem_full, 1);
     mbar_init(tmem_empty, 32 * kEpiWarps);
@@ -192,8 +204,6 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       const uint32_t base = smem_u32(smem);
       const uint64_t da0 = smem_desc(base, 16, 1024, 2);
       const uint64_t db0 = smem_desc(base + C::kABytes, 16, 1024, 2);
-      const uint64_t dsa0 = smem_desc(base + C::kABytes + C::kBBytes, 128, 128, 0);
-      const uint64_t dsb0 = smem_desc(base + C::kABytes + C::kBBytes + C::kSfaBytes, 128, 128, 0);
       const uint32_t sf_base = tmem + C::kSfBase;
       int s = 0;
       uint32_t ph = 0, acc_ph = 0;
@@ -203,17 +213,11 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         if (!mbar_wait(tmem_empty, acc_ph ^ 1u, &s_abort, timeout_ns)) { fail(); ok = false; break; }
         tc_fence_after();
         for (int ks = 0; ks < nk; ++ks) {
-          if (!mbar_wait(full_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
+          // the stage's scales in TMEM (their writers saw the stage land)
+          if (!mbar_wait(sfull_bar(s), ph, &s_abort, timeout_ns)) { fail(); ok = false; break; }
           tc_fence_after();
           const uint64_t off = (uint64_t)(s * (C::kStageBytes >> 4));
           const uint32_t sf_col = sf_base + s * C::kSfStageCols;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            tc_cp_sf(sf_col + 4 * j, dsa0 + off + 32 * j);
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              tc_cp_sf(sf_col + C::kSfaCols + (BN / 128) * 4 * j + 4 * h, dsb0 + off + 128 * h + 32 * j);
-          }
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             tc_mma_nvf4(tmem, da0 + off + 2 * j, db0 + off + 2 * j, idesc, sf_col + 4 * j,
@@ -235,11 +239,56 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         }
       }
     }
+  } else if (warp >= kScaleWarp) {
+    // ---------------- scale writers ----------------
+    // Warp w reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 only; lane l of
+    // each writes the 16-byte row l of every 512-byte scale tile of the stage
+    // into its lane: A's four K chunks at columns 4 j + c, then B's (BN / 128
+    // tiles per chunk) at kSfaCols + (BN / 128) 4 j + 4 h + c. The stage's slot
+    // is free when the stage lands (its TMA followed the MMAs that last read it).
+    constexpr int NB = BN / 128;
+    const uint32_t quad = (uint32_t)(warp & 3);
+    int s = 0;
+    uint32_t ph = 0;
+    for (int gi = cid; gi < num_tiles; gi += ncl) {
+      bool ok = true;
+      for (int ks = 0; ks < nk; ++ks) {
+        // the warp leaves together (the TMEM stores below are warp-collective)
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), ph, &s_abort, timeout_ns))) { fail(); ok = false; break; }
+        const uint8_t* raw = smem + s * C::kStageBytes + C::kABytes + C::kBBytes;
+        uint32_t va[16], vb[16 * NB];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint4 u = *reinterpret_cast<const uint4*>(raw + 512 * j + 16 * lane);
+          va[4 * j] = u.x; va[4 * j + 1] = u.y; va[4 * j + 2] = u.z; va[4 * j + 3] = u.w;
+#pragma unroll
+          for (int h = 0; h < NB; ++h) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + C::kSfaBytes + 2048 * h + 512 * j + 16 * lane);
+            uint32_t* d = vb + 4 * NB * j + 4 * h;
+            d[0] = w.x; d[1] = w.y; d[2] = w.z; d[3] = w.w;
+          }
+        }
+        const uint32_t taddr = tmem + ((32u * quad) << 16) + (uint32_t)(C::kSfBase + s * C::kSfStageCols);
+        tmem_st16(taddr, va);
+        if constexpr (NB == 2) {
+          tmem_st32(taddr + C::kSfaCols, vb);
+        } else {
+          tmem_st16(taddr + C::kSfaCols, vb);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sfull_bar(s));
+        if (++s == C::kStages) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+    }
   } else {
     // ---------------- epilogue (warps 2..9) ----------------
     const int q = warp & 3;                    // TMEM lane quadrant this warp may access
     const int hcol = (warp - 2) >> 2;          // which half of the tile's columns
     constexpr int kCols = BN / 2;
+    constexpr int kParts = kCols / 64;         // read 64 columns at a time (64 registers live)
     const float alpha = __fmul_rn(__ldg(g_a), __ldg(g_b));
     uint32_t acc_ph = 0;
     for (int gi = cid; gi < num_tiles; gi += ncl) {
@@ -247,40 +296,53 @@ gemm_nvf4_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
       if (!mbar_wait(tmem_full, acc_ph, &s_abort, timeout_ns)) { fail(); break; }
       tc_fence_after();
       const int row = m * BM + q * 32 + lane;
-      uint32_t r[kCols];
-#pragma unroll
-      for (int c = 0; c < kCols / 32; ++c)
-        tmem_ld32_async(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hcol * kCols + c * 32), r + 32 * c);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < kCols / 32; ++c) reg_fence32(r + 32 * c);
-      // the accumulator is in registers: the next tile's MMAs may overwrite it
-      tc_fence_before();
-      mbar_arrive(tmem_empty);
-      acc_ph ^= 1u;
       const int col0 = n * BN + hcol * kCols;
-      if constexpr (OUT_F32) {
-        float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0);
+      const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(hcol * kCols);
+      uint32_t r[64], hpk[32];
 #pragma unroll
-        for (int i = 0; i < kCols / 4; ++i)
-          out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
-                               __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
-      } else {
-        uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+      for (int part = 0; part < kParts; ++part) {
+        tmem_ld32_async(tbase + 64 * part, r);
+        tmem_ld32_async(tbase + 64 * part + 32, r + 32);
+        tmem_ld_wait();
+        reg_fence32(r);
+        reg_fence32(r + 32);
+        if (part == kParts - 1) {
+          // the accumulator is in registers: the next tile's MMAs may overwrite it
+          tc_fence_before();
+          mbar_arrive(tmem_empty);
+        }
+        if constexpr (OUT_F32) {
+          float4* out = reinterpret_cast<float4*>(static_cast<float*>(y) + (int64_t)row * N + col0 + 64 * part);
 #pragma unroll
-        for (int i = 0; i < kCols / 8; ++i) {
-          uint32_t h[4];
+          for (int i = 0; i < 16; ++i)
+            out[i] = make_float4(__fmul_rn(__uint_as_float(r[4 * i]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 1]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 2]), alpha),
+                                 __fmul_rn(__uint_as_float(r[4 * i + 3]), alpha));
+        } else {
+          uint32_t h[32];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[8 * i + 2 * k]), alpha),
-                                                            __fmul_rn(__uint_as_float(r[8 * i + 2 * k + 1]), alpha));
+          for (int k = 0; k < 32; ++k) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(r[2 * k]), alpha),
+                                                            __fmul_rn(__uint_as_float(r[2 * k + 1]), alpha));
             h[k] = *reinterpret_cast<const uint32_t*>(&b2);
           }
-          out[i] = make_uint4(h[0], h[1], h[2], h[3]);
+          if (part + 1 < kParts) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) hpk[k] = h[k];
+          } else {
+            uint4* out = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(y) + (int64_t)row * N + col0);
+            if (kParts == 2) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) out[i] = make_uint4(hpk[4 * i], hpk[4 * i + 1], hpk[4 * i + 2], hpk[4 * i + 3]);
+              out += 8;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) out[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          }
         }
       }
+      acc_ph ^= 1u;
     }
   }
 
@@ -348,26 +410,6 @@ struct PairCfg {
   static_assert(kSmem <= 227 * 1024, "shared memory budget");
 };
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 template <bool OUT_F32>
 __global__ void __launch_bounds__(PairCfg::kThreads, 1)
