@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -235,18 +236,28 @@ KERNEL_SOURCES = {
 
 
 def source_digest(kernel: str) -> str:
-    """Digest of the source a kernel is built from (its .cu file and the shared
-    headers): ncu counters apply only to the build they came from."""
-    h = hashlib.sha1()
+    """Digest of the source a kernel is built from: its .cu file and every
+    header it includes, directly or through other headers (quoted includes,
+    resolved beside the including file). ncu counters apply only to the build
+    they came from."""
     csrc = os.path.join(ROOT, "fp4_block_scaled_05_b300", "csrc")
-    names = sorted(n for n in os.listdir(csrc) if n.endswith((".cuh", ".h")))
-    names.append(KERNEL_SOURCES.get(kernel, ""))
-    for name in names:
-        path = os.path.join(csrc, name)
+    src = KERNEL_SOURCES.get(kernel)
+    if not src:
+        return ""
+    files, todo = {}, [os.path.normpath(os.path.join(csrc, src))]
+    while todo:
+        path = todo.pop()
+        if path in files:
+            continue
         if not os.path.isfile(path):
             return ""
         with open(path, "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+            files[path] = f.read()
+        for inc in re.findall(rb'#include "([^"]+)"', files[path]):
+            todo.append(os.path.normpath(os.path.join(os.path.dirname(path), inc.decode())))
+    h = hashlib.sha1()
+    for path in sorted(files):
+        h.update(os.path.relpath(path, csrc).encode() + b"\0" + files[path])
     return h.hexdigest()[:12]
 
 
