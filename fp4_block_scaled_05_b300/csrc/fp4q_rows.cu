@@ -2260,21 +2260,55 @@ __device__ __forceinline__ void store16(float (&v)[16], const uint32_t (&sgn)[16
   }
 }
 
+// Byte b of x in the low byte and its sign bit replicated over the high byte
+// (prmt, default mode: a selector nibble with bit 3 set copies the sign of the
+// byte it names into every bit).
+__device__ __forceinline__ uint32_t prmt_sign(uint32_t x, uint32_t b) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(x), "r"(b | ((8u | b) << 12)));
+  return d;
+}
+
 // Dequantise one 16-block: `w0`, `w1` its code words, `sv` its scale value.
 // Writes 16 values at `out` (BF16 or FP32).
 template <int FMT, bool OUT_F32, bool IRHT>
 __device__ __forceinline__ void deq16(uint32_t w0, uint32_t w1, float sv, float g, const uint32_t (&sgn)[16],
                                       void* out) {
-  float q[16];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) levels2<FMT>(((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu, q[2 * j], q[2 * j + 1]);
   float v[16];
-  const f2 S = f2_make(sv, sv), G = f2_make(g, g);
+  const f2 G = f2_make(g, g);
+  if constexpr (FMT == 2 && !OUT_F32) {
+    // UFP4 to BF16 without per-nibble extraction: one prmt puts a code's magnitude
+    // (bits 4-6 of a byte of w << 4 for the low code, of w for the high one)
+    // into the low byte and its sign, replicated, into the high byte; the
+    // magnitude under the FP32 pattern of 2^23 gives 2^23 + 16 k, and
+    // fma(2^23 + 16 k, s / 16, -2^19 s) = k s exactly (k s has at most 7
+    // significant bits; s / 16 and 2^19 s are exact for every E4M3 value).
+    // The sign goes on afterwards, so code 8 still gives -0. Measured on the
+    // 8192 x 4096 activation with the inverse RHT: 24.7 against 26.0 us; the
+    // FP32 output kept the look-up path (71.7 against 79.9 us this way).
+    const f2 S16 = f2_make(__fmul_rn(sv, 0.0625f), __fmul_rn(sv, 0.0625f));
+    const f2 C = f2_make(__fmul_rn(sv, -524288.f), __fmul_rn(sv, -524288.f));
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    f2 r = f2_mul(f2_make(q[2 * j], q[2 * j + 1]), S);
-    if (FMT != 1 && FMT != 4 && FMT != 5) r = f2_mul(r, G);
-    f2_split(r, v[2 * j], v[2 * j + 1]);
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t w = j < 4 ? w0 : w1, b = (uint32_t)(j & 3);
+      const uint32_t xl = prmt_sign(w << 4, b), xh = prmt_sign(w, b);
+      const f2 A = f2_make(__uint_as_float((xl & 0x70u) | 0x4B000000u), __uint_as_float((xh & 0x70u) | 0x4B000000u));
+      float r0, r1;
+      f2_split(f2_mul(f2_fma(A, S16, C), G), r0, r1);
+      v[2 * j] = __uint_as_float(__float_as_uint(r0) ^ (xl & 0x80000000u));
+      v[2 * j + 1] = __uint_as_float(__float_as_uint(r1) ^ (xh & 0x80000000u));
+    }
+  } else {
+    float q[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) levels2<FMT>(((j < 4 ? w0 : w1) >> (8 * (j & 3))) & 0xFFu, q[2 * j], q[2 * j + 1]);
+    const f2 S = f2_make(sv, sv);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      f2 r = f2_mul(f2_make(q[2 * j], q[2 * j + 1]), S);
+      if (FMT != 1 && FMT != 4 && FMT != 5) r = f2_mul(r, G);
+      f2_split(r, v[2 * j], v[2 * j + 1]);
+    }
   }
   store16<OUT_F32, IRHT>(v, sgn, out);
 }
