@@ -89,3 +89,32 @@ def test_two_rank_max_over_ranks_gloo():
 
 def test_reduce_max_without_process_group():
     assert bench.reduce_max(3.5, torch.device("cpu")) == 3.5
+
+
+def test_source_digest_follows_the_translation_unit(tmp_path, monkeypatch):
+    """A kernel's digest covers its .cu file and the headers it includes,
+    directly or through other headers, and nothing else: an edit to a header
+    another kernel includes leaves it unchanged."""
+    csrc = tmp_path / "fp4_block_scaled_05_b300" / "csrc"
+    inc = tmp_path / "include"
+    csrc.mkdir(parents=True)
+    inc.mkdir()
+    (csrc / "a.cu").write_text('#include "h1.cuh"\n#include "../../include/pub.h"\nint a;\n')
+    (csrc / "b.cu").write_text('#include "h2.cuh"\nint b;\n')
+    (csrc / "h1.cuh").write_text('#include "h3.h"\n// h1\n')
+    (csrc / "h2.cuh").write_text("// h2\n")
+    (csrc / "h3.h").write_text("// h3\n")
+    (inc / "pub.h").write_text("// public\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "KERNEL_SOURCES", {"ka": "a.cu", "kb": "b.cu"})
+    da, db = bench.source_digest("ka"), bench.source_digest("kb")
+    assert da and db and da != db
+    (csrc / "h2.cuh").write_text("// h2 edited\n")
+    assert bench.source_digest("ka") == da and bench.source_digest("kb") != db
+    for path in (csrc / "h3.h", inc / "pub.h", csrc / "a.cu"):
+        before = bench.source_digest("ka")
+        path.write_text(path.read_text() + "// edited\n")
+        assert bench.source_digest("ka") != before
+    assert bench.source_digest("unknown") == ""
+    (csrc / "h3.h").unlink()                      # a missing include: no digest, so no stale counters
+    assert bench.source_digest("ka") == ""
